@@ -1,0 +1,211 @@
+"""Acceptance of the longest target-agreeing path (oracle; test infrastructure only).
+
+Rules, as the pages state them:
+
+* Greedy -- "Drafters: ..." (robertz.co), section "Why the answer does not
+  change": a drafted token is kept only if it is the target's own pick; at
+  the first disagreement the target's choice is used.  "Medusa, explained",
+  step 7: a node is valid when its token equals the target's argmax at its
+  parent; the longest valid path is accepted.
+* Typical -- "Medusa and EAGLE ... explained", section "Medusa: heads,
+  losses and trees" and "Medusa, explained", section "Typical acceptance":
+  keep x when p(x) > min(eps, delta * exp(-H(p))), H the entropy of the
+  target's distribution; the step's first token is always the target's
+  greedy choice.
+* Rejection -- "Drafters: ...", section "Why the answer does not change":
+  keep a drafted token with probability min(1, p/q); on rejection draw from
+  the target's distribution with the drafter's probabilities subtracted.
+  "5.3 Medusa、EAGLE 与 MTP", section 9.2: token-level verification from
+  left to right, stopping at the first rejection.
+
+Readings where the pages leave a step open (each is listed in the design
+notes):
+
+* Tree siblings are deterministic top-ranked drafts, so the proposal q of
+  a sibling is a point mass on its token: min(1, p/q) = r(x), and "target
+  minus drafter" renormalised is r with x removed.  Siblings are tried in
+  node order; the next sibling is tested against that residual.
+* Argmax ties go to the lowest token id.  Typical: natural-log entropy;
+  among several valid branches the deepest valid node wins, ties to the
+  lowest node index; the bonus is the greedy token at the stop node.
+* Decisions that compare floats (typical threshold, accept draw, sampling
+  race) are taken in ``dtype`` -- float32 by default, the kernel's
+  precision -- and every decision whose margin is below ``NEAR`` (relative)
+  is counted in ``near_ties``: there, either outcome is a correct result of
+  the rule within rounding.
+* Sampling from the residual uses the exponential race in its log form:
+  argmax over non-removed x of z_x + G_x, z = logits / T and
+  G_x = -log(-log u'_x) with u'_x from the counter-based generator.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import rng
+
+NEAR_REJECT = 1e-5
+NEAR_TYPICAL = 1e-4
+
+
+def _children(first_child, next_sibling, v):
+    out = []
+    c = int(first_child[v])
+    while c != -1:
+        out.append(c)
+        c = int(next_sibling[c])
+    return out
+
+
+def _pack(paths, bonus, path_cap):
+    B = len(paths)
+    acc_len = np.array([len(p) - 1 for p in paths], np.int64)
+    acc_path = np.full((B, path_cap), -1, np.int64)
+    for b, p in enumerate(paths):
+        acc_path[b, : len(p)] = p
+    return acc_len, acc_path, np.asarray(bonus, np.int64)
+
+
+def accept_greedy(logits, tok, first_child, next_sibling, path_cap):
+    """Walk from the root; descend into the first child (node order) whose
+    token is the argmax of the current node's logits; stop when none is.
+    Bonus = that argmax at the stop node."""
+    B = logits.shape[0]
+    paths, bonus = [], []
+    for b in range(B):
+        v, path = 0, [0]
+        while True:
+            a = int(np.argmax(np.asarray(logits[b, v], np.float64)))  # first max = lowest id
+            nxt = [c for c in _children(first_child[b], next_sibling[b], v) if int(tok[b, c]) == a]
+            if not nxt:
+                bonus.append(a)
+                break
+            v = nxt[0]
+            path.append(v)
+        paths.append(path)
+    return _pack(paths, bonus, path_cap)
+
+
+def typical_threshold(row, eps, delta, T, dtype=np.float32):
+    """(p, thr) for one logits row: p = softmax(row / T),
+    thr = min(eps, delta * exp(-H)), H = -sum p ln p = ln S - sum(e z)/S with
+    z = row/T - max, e = exp(z), S = sum e."""
+    z = np.asarray(row, dtype) / dtype(T)
+    z = z - z.max()
+    e = np.exp(z)
+    S = e.sum(dtype=dtype)
+    H = np.log(S) - (e * z).sum(dtype=dtype) / S
+    thr = min(dtype(eps), dtype(delta) * np.exp(-H))
+    return e / S, thr
+
+
+def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, T, path_cap,
+                   dtype=np.float32):
+    """Node c (non-root) is valid iff p_parent(tok_c) > thr_parent; the
+    accepted path is the root path of the deepest node whose whole path is
+    valid (ties: lowest node index); bonus = argmax at that node.
+    Returns (acc_len, acc_path, bonus, near_ties)."""
+    B, N, _ = logits.shape
+    paths, bonus, near = [], [], 0
+    for b in range(B):
+        ok = np.zeros(N, bool)
+        ok[0] = True
+        depth = np.zeros(N, np.int64)
+        for v in range(N):  # parents precede children
+            kids = _children(first_child[b], next_sibling[b], v)
+            if not kids or not ok[v]:
+                for c in kids:
+                    depth[c] = depth[v] + 1
+                continue
+            p, thr = typical_threshold(logits[b, v], eps, delta, T, dtype)
+            for c in kids:
+                depth[c] = depth[v] + 1
+                pc = p[int(tok[b, c])]
+                if abs(float(pc) - float(thr)) <= NEAR_TYPICAL * float(thr):
+                    near += 1
+                ok[c] = bool(pc > thr)
+        reach = [i for i in range(N) if ok[i]]
+        best = max(reach, key=lambda i: (depth[i], -i))
+        path = []
+        u = best
+        while u != -1:
+            path.append(u)
+            u = int(parents[b, u]) if u else -1
+        path.reverse()
+        paths.append(path)
+        bonus.append(int(np.argmax(np.asarray(logits[b, best], np.float64))))
+    acc_len, acc_path, bon = _pack(paths, bonus, path_cap)
+    return acc_len, acc_path, bon, near
+
+
+def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_cap,
+                  dtype=np.float32):
+    """Rejection walk with point-mass sibling proposals and residual
+    resampling.  Returns (acc_len, acc_path, bonus, near_ties)."""
+    B, N, V = logits.shape
+    paths, bonus, near = [], [], 0
+    for b in range(B):
+        v, path = 0, [0]
+        while True:
+            z = np.asarray(logits[b, v], dtype) / dtype(T)
+            e = np.exp(z - z.max())
+            S = e.sum(dtype=dtype)
+            removed = dtype(0)
+            excluded = []
+            chosen = -1
+            for c in _children(first_child[b], next_sibling[b], v):
+                x = int(tok[b, c])
+                r = dtype(0) if x in excluded else e[x] / (S - removed)
+                u = rng.uniform_accept(seed, b, step, c)
+                if abs(float(u) - float(r)) <= NEAR_REJECT * max(float(r), 1e-30):
+                    near += 1
+                if u < r:
+                    chosen = c
+                    break
+                if x not in excluded:
+                    excluded.append(x)
+                    removed = dtype(removed + e[x])
+            if chosen == -1:
+                u = rng.uniform_race(seed, b, step, v, np.arange(V))
+                g = -np.log(-np.log(u.astype(dtype)))
+                key = (z + g).astype(dtype)
+                key[excluded] = -np.inf
+                x = int(np.argmax(key))
+                top2 = np.partition(key, -2)[-2:]
+                if abs(float(top2[1] - top2[0])) <= NEAR_REJECT * max(1.0, abs(float(top2[1]))):
+                    near += 1
+                bonus.append(x)
+                break
+            v = chosen
+            path.append(v)
+        paths.append(path)
+    acc_len, acc_path, bon = _pack(paths, bonus, path_cap)
+    return acc_len, acc_path, bon, near
+
+
+def reject_outcome_probs(probs, tok, first_child, next_sibling):
+    """Exact distribution of (accepted path, bonus token) under the
+    rejection walk for one sequence, by recursion over every accept/reject
+    branch (no random numbers).  ``probs[v]`` is the target distribution at
+    node v (float64 vector).  Returns {(path tuple, bonus): probability}."""
+    out = {}
+
+    def visit(v, path, mass):
+        r = np.array(probs[v], np.float64)
+        r = r / r.sum()
+        for c in _children(first_child, next_sibling, v):
+            x = int(tok[c])
+            a = r[x]
+            if a > 0:
+                visit(c, path + (c,), mass * a)
+            rest = 1.0 - a
+            if rest <= 0:
+                return
+            mass *= rest
+            r[x] = 0.0
+            r /= r.sum()
+        for x in np.nonzero(r)[0]:
+            key = (path, int(x))
+            out[key] = out.get(key, 0.0) + mass * r[x]
+
+    visit(0, (0,), 1.0)
+    return out
