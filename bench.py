@@ -1,0 +1,610 @@
+#!/usr/bin/env python
+"""Throughput of the tree-verification step (Medusa / EAGLE) on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic
+inputs resident in HBM: Medusa heads -> top-s -> static tree -> tree
+attention (one layer) -> LM head over the tree -> greedy acceptance -> KV
+commit, for the Vicuna-7B-shaped workload (batch 1, 32 heads, head_dim 128,
+prefix 2048, 4 heads of hidden 4096, vocabulary 32000, 64-node tree).
+Other workloads: --workload {tiny_exact, vicuna7b_medusa, llama8b_eagle2,
+llama70b_serving, long_context}.
+
+Prints one JSON line (rank 0).  N > 1 (torchrun) runs independent replicas
+(no collective on the data path; weak scaling).  ``--impl reference`` times
+the CPU oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+DEFAULT = "vicuna7b_medusa"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0])); mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the GPU step
+# ----------------------------------------------------------------------------
+class GpuStep:
+    """Device buffers of one workload and the launches of one verify step."""
+
+    def __init__(self, name: str, device):
+        import torch
+        from tree_speculative_decoding_attn_gb300 import specverify as sv
+        from tree_speculative_decoding_attn_gb300 import synth
+        self.torch, self.sv, self.synth = torch, sv, synth
+        w = self.w = synth.WORKLOADS[name]
+        self.name = name
+        dev = self.dev = device
+        bf = torch.bfloat16
+        tdt = self.tdt = bf if w.dtype == "bf16" else torch.float32
+        cu = lambda x, dt=None: (torch.from_numpy(np.ascontiguousarray(x)).to(dt) if dt else
+                                 torch.from_numpy(np.ascontiguousarray(x))).to(dev)
+        i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device=dev)
+        B, N, Hq, Hkv, D, V = w.batch, w.n_nodes, w.hq, w.hkv, w.head_dim, w.vocab
+        self.prefix = synth.prefix_lengths(w)
+        self.max_prefix = int(self.prefix.max())
+        self.s_max = self.max_prefix + 64
+        self.stages = []          # (name, fn, launches, algorithmic bytes or None)
+        self.h2d = []             # (pinned host, device) copied each end-to-end step
+        self.d2h = []
+        # tree
+        if w.tree == "dynamic":
+            dk = w.dynamic
+            par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
+            self.pool = [cu(par), cu(tok), cu(conf)]
+            self.path_cap = dk["rounds"] + 2
+            self.shape = None
+        else:
+            self.shape = synth.tree_shape(w)
+            self.path_cap = self.shape.n_levels + 1
+            self.parents = cu(self.shape.parents)
+            self.rank = cu(self.shape.rank)
+            self.parents_b = cu(np.broadcast_to(self.shape.parents, (B, N)).copy())
+        self.root = cu(synth.root_tokens(w))
+        self.d_prefix = cu(self.prefix)
+        self.tok, self.depth, self.pos = i32(B, N), i32(B, N), i32(B, N)
+        self.fc, self.ns, self.par_out = i32(B, N), i32(B, N), i32(B, N)
+        self.anc = torch.zeros((B, N), dtype=torch.int64, device=dev)
+        self.status = i32(1)
+        # attention inputs
+        q, kc, vc, kt, vt = synth.attention_inputs(w, self.prefix, s_max=self.s_max)
+        self.q, self.kc, self.vc, self.kt, self.vt = (cu(x, tdt) for x in (q, kc, vc, kt, vt))
+        del q, kc, vc, kt, vt
+        self.out = torch.empty((B, N, Hq, D), dtype=tdt, device=dev)
+        wsb = sv.tree_attn_workspace_bytes(tdt, B, N, Hq, Hkv, D, self.max_prefix)
+        self.ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        self.attn_launches = 2 if wsb > 0 else 1
+        esz = 2 if tdt == bf else 4
+        # algorithmic bytes: every prefix and tree K/V row once, Q in, O out
+        self.attn_bytes = int(Hkv * D * 2 * esz * (int(self.prefix.sum()) + B * N) + 2 * B * N * Hq * D * esz)
+        self.attn_flops = int(4 * N * (Hq // Hkv) * D * Hkv * (int(self.prefix.sum()) + B * N))
+        # acceptance outputs
+        self.acc_len, self.acc_path, self.bonus = i32(B), i32(B, self.path_cap), i32(B)
+        self.new_prefix = i32(B)
+        # per-step inputs for the end-to-end leg: this pass's tree Q/K/V and
+        # the per-sequence scalars
+        self.h2d += [(self.q.cpu().pin_memory(), self.q), (self.kt.cpu().pin_memory(), self.kt),
+                     (self.vt.cpu().pin_memory(), self.vt), (self.d_prefix.cpu().pin_memory(), self.d_prefix),
+                     (self.root.cpu().pin_memory(), self.root)]
+        self.d2h += [self.acc_len, self.acc_path, self.bonus, self.new_prefix]
+
+        if w.medusa:
+            self._medusa_stages(cu)
+        else:
+            self._static_or_dynamic_build(cu)
+            self.logits_bytes_row = V * (2 if w.dtype == "bf16" else 4)
+            lg = synth.target_logits(w.seed, B, N, V, w.logit_std, w.dtype == "bf16")
+            if w.planted and w.tree != "dynamic":
+                cand = synth.candidate_tokens(w.seed, B, self.shape.n_levels, max(w.caps or (2,)), V)
+                synth.plant_agreement(w.seed, lg, self.shape.parents, self.shape.level,
+                                      synth.node_tokens_from_table(self.shape, cand, synth.root_tokens(w)),
+                                      bf16=w.dtype == "bf16")
+            elif w.planted:
+                # plant on the tree the GPU builds from the seeded pool (deterministic)
+                self.stages[0][1]()
+                torch.cuda.synchronize()
+                synth.plant_agreement(w.seed, lg, self.par_out.cpu().numpy(), self.depth.cpu().numpy(),
+                                      self.tok.cpu().numpy(), bf16=True)
+            self.logits = cu(lg, tdt)
+            del lg
+        self._attn_stage()
+        if w.medusa:
+            self._lm_head_stage(cu)
+        self._accept_commit_stages()
+
+    # ---- stages ----------------------------------------------------------
+    def _medusa_stages(self, cu):
+        torch, sv, synth, w = self.torch, self.sv, self.synth, self.w
+        m = w.medusa
+        B, K, d, V, s = w.batch, m["heads"], m["hidden"], w.vocab, m["topk"]
+        h, w1, w2, wlm = synth.medusa_inputs(w)
+        bf = torch.bfloat16
+        self.h = cu(h, bf)
+        self.w1, self.w2, self.wlm = cu(w1, bf), cu(w2, bf), cu(wlm, bf)
+        del w1, w2, wlm
+        self.z = torch.empty((B, K, d), dtype=torch.float32, device=self.dev)
+        self.head_logits = torch.empty((B, K, V), dtype=torch.float32, device=self.dev)
+        self.cand = torch.empty((B, K, s), dtype=torch.int32, device=self.dev)
+        self.h2d.append((self.h.cpu().pin_memory(), self.h))
+        heads_bytes = 2 * K * d * d + 2 * K * V * d + 2 * B * d + 4 * B * K * (d + V)
+        self.stages.append(("medusa_heads", lambda: sv.spec_medusa_heads(self.h, self.w1, None, self.w2, self.z,
+                                                                        self.head_logits), 2, heads_bytes))
+        self.stages.append(("topk", lambda: sv.spec_topk(self.head_logits, s, self.cand), 1, 4 * B * K * V))
+        self.stages.append(("build_tree", lambda: sv.spec_build_tree(
+            self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos, self.anc,
+            self.fc, self.ns, self.status), 1, None))
+
+    def _static_or_dynamic_build(self, cu):
+        sv, synth, w = self.sv, self.synth, self.w
+        if w.tree == "dynamic":
+            par, tok, conf = self.pool
+            self.stages.append(("build_tree", lambda: sv.spec_build_tree_dynamic(
+                par, tok, conf, self.d_prefix, self.tok, self.par_out, self.depth, self.pos, self.anc, self.fc,
+                self.ns, None, None, self.status), 1, None))
+        else:
+            s = max(w.caps) if w.caps else 2
+            self.cand = cu(synth.candidate_tokens(w.seed, w.batch, self.shape.n_levels, s, w.vocab))
+            self.stages.append(("build_tree", lambda: sv.spec_build_tree(
+                self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos,
+                self.anc, self.fc, self.ns, self.status), 1, None))
+
+    def _attn_stage(self):
+        sv = self.sv
+        self.stages.append(("tree_attn", lambda: sv.tree_attn_verify(
+            self.q, self.kc, self.vc, self.kt, self.vt, self.d_prefix, self.anc, self.out, self.max_prefix,
+            workspace=self.ws, dev_status=self.status), self.attn_launches, self.attn_bytes))
+
+    def _lm_head_stage(self, cu):
+        torch, sv, synth, w = self.torch, self.sv, self.synth, self.w
+        B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
+        g = synth.stream(w.seed, "tree_hidden")
+        self.hid = cu(synth.gaussian(g, (B * N, d), 1.0, True), torch.bfloat16)
+        self.logits = torch.empty((B, N, V), dtype=torch.float32, device=self.dev)
+        self.logits_bytes_row = V * 4
+        self.h2d.append((self.hid.cpu().pin_memory(), self.hid))
+        self.stages.append(("lm_head", lambda: sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V)), 1,
+                            2 * V * d + 2 * B * N * d + 4 * B * N * V))
+
+    def _accept_commit_stages(self):
+        sv, w = self.sv, self.w
+        mode = {"greedy": sv.GREEDY, "typical": sv.TYPICAL, "reject": sv.REJECT}[w.accept]
+        parents = self.par_out if w.tree == "dynamic" else self.parents_b
+        self.step_counter = 0
+        self.stages.append(("accept", lambda: sv.spec_accept(
+            mode, self.logits, self.tok, parents, self.fc, self.ns, self.acc_len, self.acc_path, self.bonus,
+            temperature=w.temperature, eps=w.eps, delta=w.delta, seed=w.seed, step=0, dev_status=self.status),
+            1, None))
+        self.stages.append(("kv_commit", lambda: sv.kv_commit(
+            self.kc, self.vc, self.kt, self.vt, self.acc_len, self.acc_path, self.d_prefix, self.new_prefix,
+            self.status), 2, None))
+
+    # ---- running ---------------------------------------------------------
+    def launches_per_step(self):
+        return sum(s[2] for s in self.stages)
+
+    def run(self, events=None):
+        for i, (_, fn, _, _) in enumerate(self.stages):
+            if events is not None:
+                events[i].record()
+            fn()
+        if events is not None:
+            events[-1].record()
+
+    def dynamic_bytes(self):
+        """Algorithmic bytes of the stages that depend on the accepted path."""
+        L = self.acc_len.cpu().numpy().astype(np.int64)
+        esz = 2 if self.tdt == self.torch.bfloat16 else 4
+        rows = int((L + 1).sum())
+        out = {}
+        if self.w.accept == "typical":
+            out["accept"] = None
+        else:
+            out["accept"] = rows * self.logits_bytes_row
+        out["kv_commit"] = rows * self.w.hkv * self.w.head_dim * 2 * esz * 2
+        return out, float(L.mean())
+
+
+def attention_only(name: str, device, steps: int, warmup: int):
+    """tree_attn_verify alone at a workload's full shape (inputs drawn on the
+    device from a seeded torch generator; values do not affect the timing).
+    Per-launch CUDA-event times with an L2 flush between launches."""
+    import torch
+    from tree_speculative_decoding_attn_gb300 import specverify as sv
+    from tree_speculative_decoding_attn_gb300 import synth
+    w = synth.WORKLOADS[name]
+    B, N, Hq, Hkv, D = w.batch, w.n_nodes, w.hq, w.hkv, w.head_dim
+    prefix = synth.prefix_lengths(w)
+    S = int(prefix.max()) + 64
+    gen = torch.Generator(device=device).manual_seed(w.seed)
+    bf = torch.bfloat16
+    rnd = lambda *s: torch.randn(s, generator=gen, device=device, dtype=torch.float32).to(bf)
+    q, kc, vc, kt, vt = rnd(B, N, Hq, D), rnd(B, Hkv, S, D), rnd(B, Hkv, S, D), rnd(B, Hkv, N, D), rnd(B, Hkv, N, D)
+    shape = synth.random_tree(w.seed, N, w.caps if w.caps else (10, 4, 3, 2, 2))
+    i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device=device)
+    anc = torch.zeros((B, N), dtype=torch.int64, device=device)
+    d_prefix = torch.from_numpy(prefix).to(device)
+    sv.spec_build_tree(torch.from_numpy(shape.parents).to(device), torch.from_numpy(shape.rank).to(device), None,
+                       None, d_prefix, None, i32(B, N), i32(B, N), anc, i32(B, N), i32(B, N))
+    out = torch.empty_like(q)
+    wsb = sv.tree_attn_workspace_bytes(bf, B, N, Hq, Hkv, D, int(prefix.max()))
+    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()), workspace=ws)
+    for _ in range(warmup):
+        call()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); call(); e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(times)
+    nbytes = Hkv * D * 2 * 2 * (int(prefix.sum()) + B * N) + 2 * B * N * Hq * D * 2
+    flops = 4 * N * (Hq // Hkv) * D * Hkv * (int(prefix.sum()) + B * N)
+    del q, kc, vc, kt, vt, flush
+    return {"us": t * 1e6, "gbps": nbytes / t / 1e9, "tflops": flops / t / 1e12, "bytes": nbytes,
+            "launches": 2 if wsb else 1}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline leg)
+# ----------------------------------------------------------------------------
+def oracle_step_seconds(name: str, budget_s: float = 4.0):
+    """Time one verify step of the CPU oracle on a bounded sample of the
+    workload, extrapolated to the whole step by the sampled fraction of each
+    stage.  Returns (seconds per step, sample description)."""
+    from oracle import accept as ACC
+    from oracle import attention as A
+    from oracle import commit as COM
+    from oracle import heads as H
+    from oracle import tree as T
+    from tree_speculative_decoding_attn_gb300 import synth
+    w = synth.WORKLOADS[name]
+    B, N, Hq, Hkv, D, V = w.batch, w.n_nodes, w.hq, w.hkv, w.head_dim, w.vocab
+    prefix = synth.prefix_lengths(w)
+    parts, desc = {}, []
+    clock = time.perf_counter
+    # tree
+    if w.tree == "dynamic":
+        dk = w.dynamic
+        par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
+        t0 = clock()
+        trees = [T.rerank_dynamic(par[b], tok[b], conf[b], N, int(prefix[b])) for b in range(B)]
+        parts["build_tree"] = clock() - t0
+        tree = {k: np.stack([t[k] for t in trees]) for k in ("tok", "parent", "first_child", "next_sibling", "mask")}
+        levels = int(tree["parent"].shape[1])
+    else:
+        shape = synth.tree_shape(w)
+        s = w.medusa["topk"] if w.medusa else (max(w.caps) if w.caps else 2)
+        cand = synth.candidate_tokens(w.seed, B, shape.n_levels, s, V)
+        if w.medusa:
+            m = w.medusa
+            h, w1, w2, wlm = synth.medusa_inputs(w)
+            rows = np.arange(0, V, max(1, V // 1024))
+            t0 = clock()
+            _, hl = H.medusa_heads(h, w1, None, w2[:, rows])
+            t_h = clock() - t0
+            frac = (m["heads"] * m["hidden"] ** 2 + m["heads"] * len(rows) * m["hidden"]) / \
+                   (m["heads"] * m["hidden"] ** 2 + m["heads"] * V * m["hidden"])
+            parts["medusa_heads"] = t_h / frac
+            desc.append(f"heads on {len(rows)} of {V} vocabulary rows")
+            full_logits = synth.gaussian(synth.stream(0, "x"), (B * m["heads"], V), 1.0, False)
+            t0 = clock()
+            H.topk(full_logits, s)
+            parts["topk"] = clock() - t0
+        t0 = clock()
+        tr = T.build_tree_static(shape.parents, shape.rank, cand, synth.root_tokens(w), prefix)
+        parts["build_tree"] = clock() - t0
+        tree = tr
+    # attention on a subset of heads
+    q, kc, vc, kt, vt = synth.attention_inputs(w, prefix)
+    heads = list(range(0, Hq, max(1, Hq // 4)))[:4]
+    seqs = list(range(min(B, 2)))
+    mask = tree["mask"]
+    t0 = clock()
+    for b in seqs:
+        A.tree_attention(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], kt[b:b + 1], vt[b:b + 1], prefix[b:b + 1],
+                         mask[b], heads=heads)
+    t_a = clock() - t0
+    frac = len(seqs) * len(heads) * (float(prefix[seqs].mean()) + N) / (B * Hq * (float(prefix.mean()) + N))
+    parts["tree_attn"] = t_a / frac
+    desc.append(f"attention on {len(seqs)} of {B} sequences x {len(heads)} of {Hq} heads")
+    # LM head (Medusa workload)
+    if w.medusa:
+        d = w.medusa["hidden"]
+        hid = synth.gaussian(synth.stream(w.seed, "tree_hidden"), (B * N, d), 1.0, True)
+        cols = np.arange(0, V, max(1, V // 1024))
+        t0 = clock()
+        logits_s = H.lm_head(hid, wlm[cols])
+        parts["lm_head"] = (clock() - t0) * V / len(cols)
+        desc.append(f"LM head on {len(cols)} of {V} vocabulary columns")
+        logits = np.zeros((B, N, V), np.float32)
+        logits[:, :, cols] = logits_s.reshape(B, N, -1)
+    else:
+        logits = synth.target_logits(w.seed, B, N, V, w.logit_std, w.dtype == "bf16")
+    # acceptance + commit (full)
+    t0 = clock()
+    cap = 8
+    if w.accept == "greedy":
+        acc = ACC.accept_greedy(logits, tree["tok"], tree["first_child"], tree["next_sibling"], cap)
+    elif w.accept == "typical":
+        acc = ACC.accept_typical(logits, tree["tok"], tree["parent"], tree["first_child"], tree["next_sibling"],
+                                 w.eps, w.delta, w.temperature, cap)
+    else:
+        acc = ACC.accept_reject(logits, tree["tok"], tree["first_child"], tree["next_sibling"], w.seed, 0,
+                                w.temperature, cap)
+    parts["accept"] = clock() - t0
+    t0 = clock()
+    COM.kv_commit(kc, vc, kt, vt, prefix, acc[0], acc[1])
+    parts["kv_commit"] = clock() - t0
+    return sum(parts.values()), "; ".join(desc) if desc else "full step", parts
+
+
+def _cpu_baseline_subprocess(name: str, reps: int = 2):
+    """Run the oracle timing in a fresh single-threaded process (spawned,
+    not forked from this CUDA process)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"r = [bench.oracle_step_seconds({name!r}) for _ in range({reps})]; "
+            f"print(json.dumps({{'s': min(x[0] for x in r), 'sample': r[0][1], "
+            f"'parts': r[0][2]}}))")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    if out.returncode != 0:
+        return None, out.stderr[-400:]
+    res = json.loads(out.stdout.strip().splitlines()[-1])
+    return res, None
+
+
+# ----------------------------------------------------------------------------
+# main
+# ----------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        import torch
+        rank = int(os.environ.get("RANK", "0"))
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist, rank, local, ws
+    return None, 0, 0, 1
+
+
+def run_reference(args):
+    dist, rank, local, ws = _dist() if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (None, 0, 0, 1)
+    if rank != 0:
+        return
+    from tree_speculative_decoding_attn_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    times = []
+    sample = None
+    for i in range(args.warmup + args.steps):
+        s, sample, _ = oracle_step_seconds(args.workload)
+        if i >= args.warmup:
+            times.append(s)
+    t = sum(times) / len(times)
+    val = 1.0 / t
+    line = {"impl": "reference", "metric": "tree-verify steps/s", "value": val, "unit": "steps/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": w.batch, "prefix": list(w.prefix), "n_nodes": w.n_nodes},
+            "cpu_baseline": {"value": val, "unit": "steps/s", "cores": 1, "kind": "oracle",
+                             "sample": sample + " (per step; extrapolated by sampled fraction)"},
+            "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=DEFAULT)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-attention", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    dist, rank, local, ws = _dist()
+    import torch
+    from tree_speculative_decoding_attn_gb300 import specverify as sv
+    sv.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    step = GpuStep(args.workload, dev)
+    hbm, tc_peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
+
+    # timed region: K steps, per-stage events on the launch stream
+    n_st = len(step.stages)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            step.run(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist:
+        dist.barrier()
+    step_s = [evs[k][0].elapsed_time(evs[k][-1]) * 1e-3 for k in range(args.steps)]
+    total = sum(step_s)
+    stage_s = {step.stages[i][0]: sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
+               * 1e-3 / args.steps for i in range(n_st)}
+    if dist:
+        t = torch.tensor([total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total = float(t.item())
+    steps_per_s = ws * args.steps / total
+    dyn, mean_acc = step.dynamic_bytes()
+
+    # roofline for the dominant stage
+    dom = max(stage_s, key=stage_s.get)
+    dom_bytes = next(s[3] for s in step.stages if s[0] == dom)
+    if dom_bytes is None:
+        dom_bytes = dyn.get(dom)
+    roof = None
+    if dom_bytes:
+        ach = dom_bytes / stage_s[dom] / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": None, "peak_kind": peak_kind, "bytes_per_launch": dom_bytes}
+
+    # end-to-end leg through the public API: per-step H2D of this pass's
+    # inputs from pinned memory, D2H of the accepted path
+    h2d_bytes = sum(h.numel() * h.element_size() for h, _ in step.h2d)
+    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
+    d2h_bytes = sum(t.numel() * t.element_size() for t in outs_host)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        for hsrc, ddst in step.h2d:
+            ddst.copy_(hsrc, non_blocking=True)
+        step.run()
+        for hdst, dsrc in zip(outs_host, step.d2h):
+            hdst.copy_(dsrc, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) * 1e-3
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": ws * args.steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d_bytes,
+           "d2h_bytes_per_step": d2h_bytes}
+
+    launches = step.launches_per_step()
+    attn_cfg = stage_s.get("tree_attn")
+    attention = {"workload": args.workload, "us": attn_cfg * 1e6, "gbps": step.attn_bytes / attn_cfg / 1e9,
+                 "frac_hbm": step.attn_bytes / attn_cfg / 1e9 / hbm}
+    extra = {}
+    if rank == 0 and not args.no_attention:
+        del step
+        torch.cuda.empty_cache()
+        for nm in ("llama8b_eagle2", "llama70b_serving", "long_context"):
+            r = attention_only(nm, dev, steps=20, warmup=3)
+            r["frac_hbm"] = r["gbps"] / hbm
+            r["frac_tensor"] = r["tflops"] / tc_peak
+            extra[nm] = r
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        res, err = _cpu_baseline_subprocess(args.workload)
+        if res:
+            cpu = {"value": 1.0 / res["s"], "unit": "steps/s", "cores": 1, "kind": "oracle",
+                   "sample": res["sample"] + " (one step, extrapolated by sampled fraction of each stage)"}
+        else:
+            cpu = {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
+
+    if rank == 0:
+        from tree_speculative_decoding_attn_gb300 import synth
+        w = synth.WORKLOADS[args.workload]
+        line = {"metric": "tree-verify steps/s", "value": steps_per_s, "unit": "steps/s", "n_gpus": ws,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic (seeded; random weights)",
+                "config": {"workload": args.workload, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
+                           "head_dim": w.head_dim, "prefix": list(w.prefix), "n_nodes": w.n_nodes,
+                           "vocab": w.vocab, "accept": w.accept, "parallelism": f"replicas x{ws}",
+                           "l2": "inputs exceed L2 (weights + KV streamed each step)"},
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches * args.steps,
+                "stages_us": {k: v * 1e6 for k, v in stage_s.items()},
+                "mean_accepted": mean_acc, "attention": attention, "attention_full_shapes": extra,
+                "clocks": clocks.summary(), "wall_s": t_wall}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

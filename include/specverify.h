@@ -1,0 +1,313 @@
+/*
+ * specverify.h -- C ABI of the tree-verification step of Medusa/EAGLE
+ * self-speculative decoding, for NVIDIA GB300 (sm_103a).
+ *
+ * The step, as the pages state it:
+ *   - Medusa residual heads propose candidates: head k computes
+ *     softmax(W2_k (SiLU(W1_k h) + h)) and offers its top s_k tokens
+ *     ("Medusa, explained", procedure step 1 and step 5; "Medusa and EAGLE:
+ *     self-speculative decoding heads, explained", section "Medusa: heads,
+ *     losses and trees").
+ *   - The candidates form a tree, flattened in node order with an
+ *     ancestor mask and depth-based position ids ("5.3 Medusa、EAGLE 与 MTP",
+ *     sections 3.1, 3.2 and 8).  EAGLE-2 picks the nodes by the product of
+ *     draft confidences along their path (same page, section 5.2).
+ *   - One target pass scores every node (tree attention over the shared
+ *     prefix KV plus each node's own ancestors).
+ *   - The longest target-agreeing path is accepted: greedy match, typical
+ *     acceptance, or min(1, p/q) rejection with residual resampling
+ *     ("Drafters: draft models, Medusa, EAGLE, MTP, DFlash, DSpark", section
+ *     "Why the answer does not change"; "Medusa, explained", section
+ *     "Typical acceptance").
+ *   - Only the accepted path's KV is committed to the cache; sibling
+ *     branches are discarded ("5.3 Medusa、EAGLE 与 MTP", section 3.2).
+ *
+ * General rules for every entry point
+ *   - Every pointer argument is a DEVICE pointer to caller-owned memory
+ *     unless stated otherwise.  The library allocates nothing, keeps no
+ *     state between calls, and never frees caller memory.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
+ *     means the legacy default stream).  Calls are capturable in CUDA
+ *     graphs and are thread-safe (they share nothing).
+ *   - The return value is a host-side status (SPEC_OK, or an SPEC_ERR_*
+ *     code when an argument is invalid or a launch failed).  On an
+ *     argument error nothing is launched.
+ *   - Errors that only the device can see (a malformed parents array, a
+ *     commit past the cache capacity, a bad accepted path) are written to
+ *     the optional `dev_status` word (int32, device memory; the first
+ *     error wins, via atomicCAS from 0).  The kernel then skips the
+ *     offending work item; it never traps.  Pass NULL to not report.
+ *   - Layouts are dense row-major with the last index contiguous.
+ *     Dtype codes: SPEC_F32 (float) and SPEC_BF16 (__nv_bfloat16).
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *spec_stream_t; /* same handle as cudaStream_t */
+
+/* host-side return codes */
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* null pointer, bad size, inconsistent shapes */
+  SPEC_ERR_UNSUPPORTED = 2, /* dtype / head_dim / node count not built    */
+  SPEC_ERR_CAPACITY = 3,    /* a host-known size exceeds a buffer         */
+  SPEC_ERR_CUDA = 4         /* a kernel launch reported an error          */
+};
+
+/* device status codes written to dev_status */
+enum {
+  SPEC_DEV_OK = 0,
+  SPEC_DEV_BAD_PARENTS = 1,  /* parents[0] != -1 or not 0 <= parents[i] < i */
+  SPEC_DEV_CAPACITY = 2,     /* prefix_len + rows > s_max (or > max_prefix) */
+  SPEC_DEV_BAD_PATH = 3,     /* accepted path entry out of [0, n_nodes)     */
+  SPEC_DEV_BAD_POOL = 4,     /* pool parent not earlier / confidence > 1    */
+  SPEC_DEV_BAD_TOKEN = 5,    /* token id outside [0, vocab)                 */
+  SPEC_DEV_TIMEOUT = 6       /* a bounded device-side wait gave up          */
+};
+
+/* dtype codes */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+/* acceptance modes */
+enum { SPEC_ACCEPT_GREEDY = 0, SPEC_ACCEPT_TYPICAL = 1, SPEC_ACCEPT_REJECT = 2 };
+
+/* Largest tree the ancestor bitmask supports (one uint64 word per node). */
+#define SPEC_MAX_NODES 64
+
+/* Text for a host or device status code (static string, never NULL). */
+const char *spec_status_string(int status);
+
+/* ABI version of this header (bumped on any signature change). */
+int spec_abi_version(void);
+
+/* --------------------------------------------------------------------
+ * spec_medusa_heads -- Medusa residual heads (candidate proposal).
+ * "Medusa, explained", procedure step 1: head k maps the last hidden
+ * state h to W2_k (SiLU(W1_k h) + h); "Medusa and EAGLE ... explained",
+ * section "Implementation sketch": W1 may carry a bias, W2 has none.
+ *
+ *   h      [batch, hidden]               bf16
+ *   w1     [n_heads, hidden, hidden]     bf16, nn.Linear layout [out, in]
+ *   b1     [n_heads, hidden]             bf16, or NULL for no bias
+ *   w2     [n_heads, vocab, hidden]      bf16
+ *   z      [batch, n_heads, hidden]      f32 out: h + SiLU(W1 h + b1)
+ *   logits [batch, n_heads, vocab]       f32 out: W2 z (softmax omitted:
+ *                                        it does not change the top-s)
+ * Accumulation is float32.  Requires hidden % 8 == 0, 1 <= batch <= 8.
+ * ------------------------------------------------------------------ */
+int spec_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2,
+                      int batch, int n_heads, int hidden, int vocab,
+                      float *z, float *logits, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_topk -- top-s candidates per row ("Medusa and EAGLE ...
+ * explained", section "Medusa: heads, losses and trees": head k
+ * contributes its top s_k tokens).
+ *
+ *   rows     [n_rows, row_stride] (f32 or bf16 per `dtype`); the first
+ *            row_len entries of each row are ranked
+ *   idx_out  [n_rows, s] int32: column indices, by value descending;
+ *            equal values -> lower index first
+ *   val_out  [n_rows, s] f32: the values (may be NULL)
+ * Requires 1 <= s <= 16 and s <= row_len.
+ * ------------------------------------------------------------------ */
+int spec_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
+              int32_t *idx_out, float *val_out, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_build_tree -- static (Medusa) tree for a batch.
+ * "5.3 Medusa、EAGLE 与 MTP", section 8: node 0 is the root, parents[i] < i;
+ * a node sees its ancestors and itself (section 3.1); position id =
+ * prefix length + depth, siblings share a position (section 3.2).
+ * "Medusa, explained", step 5-6: node at depth d >= 1 carries candidate
+ * rank[i] of head d.
+ *
+ *   parents    [n_nodes] int32 (shared by the batch); parents[0] = -1
+ *   rank       [n_nodes] int32: candidate rank of node i (rank[0] unused)
+ *   cand_tok   [batch, cand_levels, cand_s] int32: cand_tok[b, d-1, r] is
+ *              head d's rank-r candidate; may be NULL (then `tok` is not
+ *              written)
+ *   root_tok   [batch] int32: token the target already chose (node 0)
+ *   prefix_len [batch] int32: committed cache length of each sequence
+ * Outputs, all [batch, n_nodes]:
+ *   tok (int32, may be NULL), depth (int32), pos_ids (int32) = prefix_len
+ *   + depth, anc_mask (uint64: bit j of word i set iff node j is node i or
+ *   an ancestor of it), first_child / next_sibling (int32, -1 = none;
+ *   children in node order).
+ * n_nodes <= SPEC_MAX_NODES.  A malformed parents array or a depth beyond
+ * cand_levels sets SPEC_DEV_BAD_PARENTS.
+ * ------------------------------------------------------------------ */
+int spec_build_tree(const int32_t *parents, const int32_t *rank, const int32_t *cand_tok,
+                    int cand_levels, int cand_s, const int32_t *root_tok,
+                    const int32_t *prefix_len, int batch, int n_nodes,
+                    int32_t *tok, int32_t *depth, int32_t *pos_ids, uint64_t *anc_mask,
+                    int32_t *first_child, int32_t *next_sibling, int32_t *dev_status,
+                    spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_build_tree_dynamic -- EAGLE-2 style tree from a drafted pool.
+ * "5.3 Medusa、EAGLE 与 MTP", section 5.2: a node's value is the product of
+ * the draft confidences along its path; the highest-value nodes go to
+ * verification; confidence never enters acceptance (section 5.3).
+ *
+ *   pool_parent [batch, pool_size] int32: pool_parent[b,0] = -1 (root),
+ *               0 <= pool_parent[b,i] < i otherwise
+ *   pool_tok    [batch, pool_size] int32
+ *   pool_conf   [batch, pool_size] f32 in [0, 1] (entry 0 ignored)
+ * val[i] = val[parent] * conf[i] (one float32 multiply each, root-to-node
+ * order, root 1).  Kept: the root and the n_nodes-1 nodes of highest value
+ * (ties: smaller depth, then lower pool index).  Emitted breadth-first:
+ * by depth, then new parent index, then value descending, then pool index.
+ * Outputs [batch, n_nodes]: tok, parents_out, depth, pos_ids, anc_mask,
+ * first_child, next_sibling (as spec_build_tree), pool_index (int32, may
+ * be NULL), val (f32, may be NULL).  pool_size <= 4096.
+ * ------------------------------------------------------------------ */
+int spec_build_tree_dynamic(const int32_t *pool_parent, const int32_t *pool_tok,
+                            const float *pool_conf, int pool_size, const int32_t *prefix_len,
+                            int batch, int n_nodes, int32_t *tok, int32_t *parents_out,
+                            int32_t *depth, int32_t *pos_ids, uint64_t *anc_mask,
+                            int32_t *first_child, int32_t *next_sibling, int32_t *pool_index,
+                            float *val, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_tree_expand -- one confidence-product expansion round of the
+ * draft tree ("5.3 Medusa、EAGLE 与 MTP", section 5.2; "Medusa and EAGLE
+ * ... explained", section "EAGLE: autoregression over features").
+ *
+ *   draft_logits [batch, n_front, vocab] (f32 or bf16): draft distribution
+ *                of each frontier node (softmax of logits / temperature)
+ *   frontier     [batch, n_front] int32 pool indices (all valid)
+ *   pool_parent, pool_tok [batch, pool_cap] int32, pool_conf, pool_val
+ *                [batch, pool_cap] f32: the pool, appended to in place
+ *   pool_count   [batch] int32, in/out: entries in use
+ * Frontier node f gets its k most probable tokens (ties: lower id) as
+ * children at pool positions count + f*k + j, with conf = probability and
+ * val = val(f) * conf (float32).  next_frontier [batch, n_next] receives
+ * the n_next new children of highest value (ties: lower pool index),
+ * highest first.  pool_val[b, 0] (the root) must hold 1.  Requires
+ * 1 <= k <= 16, n_front * k <= 1024, and pool_count + n_front * k <=
+ * pool_cap (else SPEC_DEV_CAPACITY).
+ * ------------------------------------------------------------------ */
+int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front, int vocab,
+                     const int32_t *frontier, int k, float temperature, int32_t *pool_parent,
+                     int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
+                     int pool_cap, int32_t *next_frontier, int n_next, int32_t *dev_status,
+                     spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * tree_attn_verify -- attention of every tree node over the shared prefix
+ * KV and its own ancestors ("5.3 Medusa、EAGLE 与 MTP", sections 3.1 and 8;
+ * "Medusa, explained", step 6; "Medusa and EAGLE ... explained", section
+ * "Medusa: heads, losses and trees").
+ *
+ * For node i of sequence b and query head h (KV head h / (hq/hkv)):
+ *   out[b,i,h] = softmax_j(scale * q[b,i,h] . k_j) v_j over
+ *   j in { cache rows 0 .. prefix_len[b]-1 } U { tree rows t : bit t of
+ *   anc_mask[b,i] }.
+ *
+ *   q        [batch, n_nodes, hq, head_dim]       dtype
+ *   k_cache, v_cache [batch, hkv, s_max, head_dim] dtype (rows at and past
+ *            prefix_len are ignored)
+ *   k_tree, v_tree   [batch, hkv, n_nodes, head_dim] dtype: this pass's
+ *            K/V of the tree nodes (position ids already applied)
+ *   prefix_len [batch] int32 (device), each <= max_prefix (host bound)
+ *   anc_mask   [batch, n_nodes] uint64 (from spec_build_tree*)
+ *   out      [batch, n_nodes, hq, head_dim]       dtype
+ *   scale    softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   num_splits  KV splits per (sequence, KV head); 0 = automatic
+ *   workspace   device scratch of tree_attn_workspace_bytes() bytes
+ *               (may be NULL when that size is 0)
+ * dtype SPEC_F32 or SPEC_BF16; head_dim 64 or 128; n_nodes <= 64;
+ * hq % hkv == 0; (hq / hkv) * n_nodes <= 512.  Softmax and accumulation
+ * are float32.  A prefix_len above max_prefix sets SPEC_DEV_CAPACITY and
+ * that sequence's output is left unwritten.
+ * ------------------------------------------------------------------ */
+size_t tree_attn_workspace_bytes(int dtype, int batch, int n_nodes, int hq, int hkv,
+                                 int head_dim, int max_prefix, int num_splits);
+int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache,
+                     const void *k_tree, const void *v_tree, const int32_t *prefix_len,
+                     const uint64_t *anc_mask, void *out, int dtype, int batch, int n_nodes,
+                     int hq, int hkv, int head_dim, int s_max, int max_prefix, float scale,
+                     int num_splits, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_lm_head -- target logits of every tree node ("Medusa, explained",
+ * step 6: one forward pass scores every node).
+ *   hid    [rows, hidden] bf16
+ *   w      [vocab, hidden] bf16 (LM head weight)
+ *   logits [rows, vocab]   f32 out = hid . w^T (float32 accumulation)
+ * Requires hidden % 64 == 0.
+ * ------------------------------------------------------------------ */
+int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
+                 spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_accept -- accept the longest target-agreeing path.
+ *
+ *   logits  [batch, n_nodes, vocab] (f32 or bf16): target logits at each
+ *           node (distribution of the token after it)
+ *   tok, parents, first_child, next_sibling [batch, n_nodes] int32
+ * Modes (p_v = softmax(logits[b,v] / temperature)):
+ *   SPEC_ACCEPT_GREEDY  child c of v is accepted iff tok[c] == argmax
+ *       logits[b,v] (ties: lowest id); walk from the root, stop when no
+ *       child agrees; bonus = that argmax ("Drafters: ...", section "Why
+ *       the answer does not change"; "Medusa, explained", step 7).
+ *   SPEC_ACCEPT_TYPICAL node c is valid iff p_parent(tok[c]) >
+ *       min(eps, delta * exp(-H(p_parent))), natural-log entropy; the
+ *       accepted path ends at the deepest node whose whole path is valid
+ *       (ties: lowest node index); bonus = greedy token there ("Medusa,
+ *       explained", section "Typical acceptance").
+ *   SPEC_ACCEPT_REJECT  at node v with residual r (= p_v on arrival),
+ *       children in node order: accept c iff u < r(tok[c]) (min(1, p/q)
+ *       with the point-mass proposal of a deterministic draft); otherwise
+ *       r <- r with tok[c] removed, renormalised.  If no child is
+ *       accepted the bonus is a sample of r ("Drafters: ...", section "Why
+ *       the answer does not change").  Uniforms: Philox4x32-10 with key
+ *       `seed`; accept draw counter (c, 0, b, step), sampling counter
+ *       (x, 256 + v, b, step); u = (word0 >> 8) * 2^-24.  Sampling is the
+ *       exponential race argmax_x (logits/T + Gumbel(u'_x)) over the
+ *       tokens not removed, u' = ((word0 >> 9) + 0.5) * 2^-23.
+ *       Requires temperature > 0.
+ * Outputs: acc_len [batch] (accepted nodes, root excluded), acc_path
+ * [batch, path_cap] (node ids root first, -1 after), bonus [batch].
+ * path_cap must exceed the tree depth.  Decisions use float32.
+ * ------------------------------------------------------------------ */
+int spec_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
+                const int32_t *tok, const int32_t *parents, const int32_t *first_child,
+                const int32_t *next_sibling, float temperature, float eps, float delta,
+                uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
+                int32_t *bonus, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * kv_commit -- append the accepted path's K/V rows to the cache and
+ * discard the rest ("5.3 Medusa、EAGLE 与 MTP", section 3.2).
+ *
+ * For every layer l, sequence b, KV head h and j = 0 .. acc_len[b]:
+ *   k_cache[l,b,h,prefix_len[b]+j,:] = k_tree[l,b,h,acc_path[b,j],:]
+ *   (same for v), then prefix_len_out[b] = prefix_len[b] + acc_len[b] + 1.
+ *   k_cache, v_cache  [n_layers, batch, hkv, s_max, head_dim]
+ *   k_tree,  v_tree   [n_layers, batch, hkv, n_nodes, head_dim]
+ *   elem_bytes        2 (bf16) or 4 (f32); head_dim * elem_bytes % 16 == 0
+ *   prefix_len_out    may equal prefix_len (updated in place after the
+ *                     copies, by a second kernel on the same stream)
+ * A row past s_max or a path entry outside [0, n_nodes) sets a device
+ * status and that sequence is neither copied nor advanced.
+ * ------------------------------------------------------------------ */
+int kv_commit(void *k_cache, void *v_cache, const void *k_tree, const void *v_tree,
+              int elem_bytes, int n_layers, int batch, int hkv, int s_max, int n_nodes,
+              int head_dim, const int32_t *acc_len, const int32_t *acc_path, int path_cap,
+              const int32_t *prefix_len, int32_t *prefix_len_out, int32_t *dev_status,
+              spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

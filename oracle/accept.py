@@ -103,9 +103,9 @@ def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, 
     """Node c (non-root) is valid iff p_parent(tok_c) > thr_parent; the
     accepted path is the root path of the deepest node whose whole path is
     valid (ties: lowest node index); bonus = argmax at that node.
-    Returns (acc_len, acc_path, bonus, near_ties)."""
+    Returns (acc_len, acc_path, bonus, near_ties[B])."""
     B, N, _ = logits.shape
-    paths, bonus, near = [], [], 0
+    paths, bonus, near = [], [], np.zeros(B, np.int64)
     for b in range(B):
         ok = np.zeros(N, bool)
         ok[0] = True
@@ -121,7 +121,7 @@ def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, 
                 depth[c] = depth[v] + 1
                 pc = p[int(tok[b, c])]
                 if abs(float(pc) - float(thr)) <= NEAR_TYPICAL * float(thr):
-                    near += 1
+                    near[b] += 1
                 ok[c] = bool(pc > thr)
         reach = [i for i in range(N) if ok[i]]
         best = max(reach, key=lambda i: (depth[i], -i))
@@ -140,9 +140,9 @@ def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, 
 def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_cap,
                   dtype=np.float32):
     """Rejection walk with point-mass sibling proposals and residual
-    resampling.  Returns (acc_len, acc_path, bonus, near_ties)."""
+    resampling.  Returns (acc_len, acc_path, bonus, near_ties[B])."""
     B, N, V = logits.shape
-    paths, bonus, near = [], [], 0
+    paths, bonus, near = [], [], np.zeros(B, np.int64)
     for b in range(B):
         v, path = 0, [0]
         while True:
@@ -157,7 +157,7 @@ def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_ca
                 r = dtype(0) if x in excluded else e[x] / (S - removed)
                 u = rng.uniform_accept(seed, b, step, c)
                 if abs(float(u) - float(r)) <= NEAR_REJECT * max(float(r), 1e-30):
-                    near += 1
+                    near[b] += 1
                 if u < r:
                     chosen = c
                     break
@@ -172,7 +172,7 @@ def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_ca
                 x = int(np.argmax(key))
                 top2 = np.partition(key, -2)[-2:]
                 if abs(float(top2[1] - top2[0])) <= NEAR_REJECT * max(1.0, abs(float(top2[1]))):
-                    near += 1
+                    near[b] += 1
                 bonus.append(x)
                 break
             v = chosen

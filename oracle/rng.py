@@ -16,7 +16,8 @@ published generator separately) draws the identical numbers:
   counter (x, 256 + v, b, t), same key, word 0.
 
 A 32-bit word w maps to u = (w >> 8) * 2^-24 in [0, 1) (exact in float32);
-for the race the open-interval form u' = ((w >> 8) + 0.5) * 2^-24 is used.
+for the race the open-interval form u' = ((w >> 9) + 0.5) * 2^-23 is used
+(exact in float32, never 0 or 1).
 """
 from __future__ import annotations
 
@@ -57,4 +58,4 @@ def uniform_accept(seed: int, b: int, step: int, child):
 def uniform_race(seed: int, b: int, step: int, node: int, tokens):
     """u' in (0,1) for the sampling race over ``tokens`` at stop node ``node``."""
     w = philox4x32_10((tokens, 256 + node, b, step), _key(seed))[0]
-    return ((w >> np.uint32(8)).astype(np.float64) + 0.5) * 2.0 ** -24
+    return ((w >> np.uint32(9)).astype(np.float64) + 0.5) * 2.0 ** -23

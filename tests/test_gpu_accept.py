@@ -1,0 +1,211 @@
+"""GPU parity: acceptance (greedy / typical / rejection), commit and the expansion round.
+
+Integer outputs are compared exactly.  The typical and rejection rules
+decide integers from float32 arithmetic; both sides take those decisions
+in float32, and a difference is allowed only for a sequence where the
+oracle flagged a near tie (decision margin below 1e-5 relative for the
+rejection draws and the sampling race, 1e-4 for the typical threshold).
+"""
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, host, i32, zeros_i32
+from oracle import accept as ACC
+from oracle import commit as COM
+from oracle import expand as X
+from oracle import tree as T
+from tree_speculative_decoding_attn_gb300 import specverify as sv
+from tree_speculative_decoding_attn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _tree_batch(shape, B, V, seed):
+    """Seeded candidates; the oracle builds its tree arrays, the GPU builds
+    its own (each side from the same synthetic inputs)."""
+    cand = synth.candidate_tokens(seed, B, shape.n_levels, int(shape.rank.max()) + 1, V)
+    root = synth.stream(seed, "root").integers(V, size=B).astype(np.int32)
+    t = T.build_tree_static(shape.parents, shape.rank, cand, root, np.zeros(B, np.int32))
+    N = shape.n
+    g = dict(tok=zeros_i32(B, N), depth=zeros_i32(B, N), pos=zeros_i32(B, N), first_child=zeros_i32(B, N),
+             next_sibling=zeros_i32(B, N), anc=torch.zeros((B, N), dtype=torch.int64, device="cuda"))
+    sv.spec_build_tree(i32(shape.parents), i32(shape.rank), i32(cand), i32(root), zeros_i32(B), g["tok"],
+                       g["depth"], g["pos"], g["anc"], g["first_child"], g["next_sibling"])
+    g["parent"] = i32(np.broadcast_to(shape.parents, (B, N)))
+    t["gpu"] = g
+    t["node_tok"] = synth.node_tokens_from_table(shape, cand, root)
+    return t
+
+
+def _accept(mode, logits, t, path_cap, **kw):
+    B, N, V = logits.shape
+    tdt = torch.bfloat16 if kw.pop("bf16", False) else torch.float32
+    acc_len, acc_path, bonus = zeros_i32(B), zeros_i32(B, path_cap), zeros_i32(B)
+    st = zeros_i32(1)
+    g = t["gpu"]
+    sv.spec_accept(mode, dev(logits, tdt), g["tok"], g["parent"], g["first_child"], g["next_sibling"],
+                   acc_len, acc_path, bonus, dev_status=st, **kw)
+    torch.cuda.synchronize()
+    return host(acc_len), host(acc_path), host(bonus), int(host(st)[0])
+
+
+def _logits(shape, t, B, V, seed, bf16, planted=True):
+    lg = synth.target_logits(seed, B, shape.n, V, 2.0, bf16)
+    if planted:
+        synth.plant_agreement(seed, lg, shape.parents, shape.level, t["node_tok"], bf16=bf16)
+    return lg
+
+
+SHAPES = [synth.p4_example(), synth.random_tree(1003, 32, (4, 3, 2)), synth.random_tree(1004, 64, (8, 4, 3, 2, 2)),
+          synth.chain(7), synth.chain(1)]
+
+
+@pytest.mark.parametrize("si", range(len(SHAPES)))
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("V", [1000, 32003])
+def test_greedy_bit_exact(si, bf16, V):
+    shape = SHAPES[si]
+    B = 6
+    t = _tree_batch(shape, B, V, si)
+    lg = _logits(shape, t, B, V, si + V, bf16)
+    lg[0, 0, :] = 0.0                     # all-equal row: argmax must be token 0
+    cap = shape.n_levels + 1
+    got = _accept(sv.GREEDY, lg, t, cap, bf16=bf16)
+    ref = ACC.accept_greedy(lg, t["tok"], t["first_child"], t["next_sibling"], cap)
+    assert got[3] == 0
+    for g_, r_ in zip(got[:3], ref):
+        np.testing.assert_array_equal(g_, r_)
+
+
+def _compare_with_near_ties(got, ref, near_per_seq):
+    for b in range(len(ref[0])):
+        same = got[0][b] == ref[0][b] and (got[1][b] == ref[1][b]).all() and got[2][b] == ref[2][b]
+        assert same or near_per_seq[b] > 0, f"sequence {b} differs without a near tie"
+
+
+@pytest.mark.parametrize("si", [0, 1, 2])
+@pytest.mark.parametrize("eps,delta", [(0.3, 0.09), (0.09, 0.3), (0.0, 0.0), (0.5, 10.0)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_typical_matches_oracle(si, eps, delta, bf16):
+    shape = SHAPES[si]
+    B, V = 6, 5000
+    t = _tree_batch(shape, B, V, 10 + si)
+    lg = _logits(shape, t, B, V, 20 + si, bf16)
+    cap = shape.n_levels + 1
+    got = _accept(sv.TYPICAL, lg, t, cap, bf16=bf16, eps=eps, delta=delta, temperature=1.0)
+    assert got[3] == 0
+    ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], eps, delta, 1.0, cap)
+    _compare_with_near_ties(got[:3], ref[:3], ref[3])
+
+
+@pytest.mark.parametrize("si", [0, 1, 2, 3])
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_reject_matches_oracle(si, bf16, temperature):
+    shape = SHAPES[si]
+    B, V = 5, 3000
+    t = _tree_batch(shape, B, V, 30 + si)
+    lg = _logits(shape, t, B, V, 40 + si, bf16)
+    cap = shape.n_levels + 1
+    for step in range(3):
+        got = _accept(sv.REJECT, lg, t, cap, bf16=bf16, temperature=temperature, seed=0x1234ABCD5678, step=step)
+        assert got[3] == 0
+        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 0x1234ABCD5678, step,
+                                temperature, cap)
+        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+
+
+FULL_ACCEPT = [("llama70b_serving", sv.GREEDY), ("long_context", sv.TYPICAL), ("llama8b_eagle2", sv.REJECT)]
+
+
+@pytest.mark.parametrize("name,mode", FULL_ACCEPT)
+def test_accept_full_size(name, mode):
+    """The workload's batch, tree and 128256-token vocabulary, bf16 logits
+    with planted agreement."""
+    w = synth.WORKLOADS[name]
+    shape = synth.random_tree(w.seed, w.n_nodes, w.caps if w.caps else (10, 4, 3, 2, 2))
+    t = _tree_batch(shape, w.batch, w.vocab, w.seed)
+    lg = _logits(shape, t, w.batch, w.vocab, w.seed, True)
+    cap = shape.n_levels + 1
+    kw = dict(bf16=True, temperature=1.0, eps=w.eps, delta=w.delta, seed=w.seed, step=7)
+    got = _accept(mode, lg, t, cap, **kw)
+    assert got[3] == 0
+    if mode == sv.GREEDY:
+        ref = ACC.accept_greedy(lg, t["tok"], t["first_child"], t["next_sibling"], cap)
+        for g_, r_ in zip(got[:3], ref):
+            np.testing.assert_array_equal(g_, r_)
+    elif mode == sv.TYPICAL:
+        ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], w.eps, w.delta,
+                                 1.0, cap)
+        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+    else:
+        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], w.seed, 7, 1.0, cap)
+        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+    assert got[0].mean() > 0.5            # planted agreement gives non-trivial paths
+
+
+# ---------------------------------------------------------------- commit
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("layers", [1, 3])
+def test_commit_bitwise_with_canaries(dtype, layers):
+    g = np.random.default_rng(4)
+    B, Hkv, S, N, D = 4, 2, 40, 6, 128
+    kc = g.standard_normal((layers, B, Hkv, S, D)).astype(np.float32)
+    vc = g.standard_normal((layers, B, Hkv, S, D)).astype(np.float32)
+    kt = g.standard_normal((layers, B, Hkv, N, D)).astype(np.float32)
+    vt = g.standard_normal((layers, B, Hkv, N, D)).astype(np.float32)
+    if dtype == torch.bfloat16:
+        kc, vc, kt, vt = (synth.round_bf16(x) for x in (kc, vc, kt, vt))
+    prefix = np.array([3, 10, 0, 36], np.int32)
+    acc_len = np.array([2, 0, 5, 5], np.int32)           # 36 + 6 rows > S = 40: reported, skipped
+    acc_path = np.array([[0, 2, 4, -1, -1, -1], [0, -1, -1, -1, -1, -1], [0, 1, 2, 3, 4, 5],
+                         [0, 1, 2, 3, 4, 5]], np.int32)
+    dkc, dvc = dev(kc, dtype), dev(vc, dtype)
+    plen = i32(prefix)
+    st = zeros_i32(1)
+    shp = lambda x: x if layers > 1 else x[0]
+    sv.kv_commit(shp(dkc), shp(dvc), shp(dev(kt, dtype)), shp(dev(vt, dtype)), i32(acc_len), i32(acc_path), plen,
+                 plen, st)                                  # prefix updated in place
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == sv.DEV_CAPACITY
+    ok = np.array([1, 1, 1, 0], bool)
+    rk, rv, rlen = COM.kv_commit(kc, vc, kt, vt, prefix, np.where(ok, acc_len, -1), acc_path)
+    rk[:, ~ok], rv[:, ~ok] = kc[:, ~ok], vc[:, ~ok]
+    rlen = np.where(ok, rlen, prefix)
+    np.testing.assert_array_equal(host(dkc).view(np.uint32), rk.view(np.uint32))
+    np.testing.assert_array_equal(host(dvc).view(np.uint32), rv.view(np.uint32))
+    np.testing.assert_array_equal(host(plen), rlen)
+
+
+# ---------------------------------------------------------------- expansion
+
+
+def test_expand_round_matches_oracle():
+    g = np.random.default_rng(8)
+    B, F, V, k, cap = 3, 4, 5000, 10, 64
+    logits = synth.round_bf16(g.standard_normal((B, F, V)).astype(np.float32) * 3)
+    par = np.full((B, cap), -1, np.int32); tok = np.zeros((B, cap), np.int32)
+    conf = np.zeros((B, cap), np.float32); val = np.zeros((B, cap), np.float32)
+    for b in range(B):
+        val[b, 0] = conf[b, 0] = 1.0
+        for j in range(1, 5):
+            par[b, j] = 0; tok[b, j] = j; conf[b, j] = val[b, j] = np.float32(0.2 * j)
+    front = np.array([[1, 2, 3, 4], [4, 3, 2, 1], [2, 1, 4, 3]], np.int32)
+    count = np.full(B, 5, np.int32)
+    dp, dt, dc, dv, dn = i32(par), i32(tok), dev(conf), dev(val), i32(count)
+    nxt = zeros_i32(B, 6)
+    st = zeros_i32(1)
+    sv.spec_tree_expand(dev(logits, torch.bfloat16), i32(front), k, 1.0, dp, dt, dc, dv, dn, nxt, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    rp, rt, rc, rv, rcnt, rnxt, near = X.expand_round(logits, front, par, tok, conf, val, count, k, 1.0, 6)
+    np.testing.assert_array_equal(host(dp), rp)
+    np.testing.assert_array_equal(host(dt), rt)
+    np.testing.assert_array_equal(host(dn), rcnt)
+    np.testing.assert_allclose(host(dc), rc, rtol=2e-6, atol=1e-9)
+    np.testing.assert_allclose(host(dv), rv, rtol=4e-6, atol=1e-9)
+    if near == 0:
+        np.testing.assert_array_equal(host(nxt), rnxt)

@@ -1,0 +1,102 @@
+"""GPU parity: tree attention against the oracle's explicit per-node attention.
+
+Tolerances: bf16 inputs, float32 softmax/accumulation on the GPU, float64 in
+the oracle: |gpu - ref| <= 2e-2 + 1e-2 |ref| (bf16 output rounding is 2^-9
+relative, far inside); float32 inputs: 1e-4 + 1e-4 |ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, host, i32, within, zeros_i32
+from oracle import attention as A
+from oracle import tree as T
+from tree_speculative_decoding_attn_gb300 import specverify as sv
+from tree_speculative_decoding_attn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": (2e-2, 1e-2), "f32": (1e-4, 1e-4)}
+
+
+def _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=0, max_prefix=None):
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    B, N = q.shape[0], q.shape[1]
+    anc = np.broadcast_to(T.mask_words(T.depth_and_mask(shape.parents)[1]), (B, N)).copy()
+    max_prefix = int(prefix.max()) if max_prefix is None else max_prefix
+    ws_bytes = sv.tree_attn_workspace_bytes(tdt, B, N, w.hq, w.hkv, w.head_dim, max_prefix, num_splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    out = torch.full(q.shape, float("nan"), dtype=tdt, device="cuda")
+    st = zeros_i32(1)
+    sv.tree_attn_verify(dev(q, tdt), dev(kc, tdt), dev(vc, tdt), dev(kt, tdt), dev(vt, tdt), i32(prefix),
+                        dev(anc.view(np.int64)), out, max_prefix, num_splits=num_splits, workspace=ws,
+                        dev_status=st)
+    torch.cuda.synchronize()
+    return host(out), int(host(st)[0]), anc
+
+
+def _small(dtype, B, hq, hkv, D, prefix, shape, q_scale=1.0, seed=1):
+    w = synth.Workload("t", seed, batch=B, hq=hq, hkv=hkv, head_dim=D, dtype=dtype, prefix=(0, 0),
+                       n_nodes=shape.n, n_levels=shape.n_levels, vocab=10, accept="greedy", tree="random")
+    prefix = np.asarray(prefix, np.int32)
+    q, kc, vc, kt, vt = synth.attention_inputs(w, prefix, q_scale=q_scale, s_max=int(prefix.max()) + 70)
+    return w, prefix, q, kc, vc, kt, vt
+
+
+CASES = [
+    # (dtype, B, hq, hkv, D, prefix per sequence, tree)
+    ("f32", 1, 4, 4, 64, [128], synth.p4_example()),                       # the tiny exact workload
+    ("bf16", 3, 16, 4, 128, [100, 37, 300], synth.random_tree(2, 24, (4, 3, 2))),
+    ("bf16", 2, 8, 8, 64, [513, 1], synth.random_tree(3, 40, (6, 3, 2, 2))),
+    ("f32", 2, 16, 2, 128, [257, 64], synth.random_tree(4, 32, (4, 3, 2))),  # 256 query rows / KV head
+    ("bf16", 2, 16, 2, 128, [0, 5], synth.random_tree(5, 64, (8, 4, 3, 2, 2))),  # 512 rows, empty prefix
+    ("bf16", 1, 4, 1, 128, [700], synth.chain(1)),                           # plain decode attention
+    ("bf16", 2, 32, 8, 128, [1000, 4097], synth.chain(6)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("splits", [1, 3, 0])
+@pytest.mark.parametrize("q_scale", [1.0, 4.0])
+def test_tree_attention_small(case, splits, q_scale):
+    dtype, B, hq, hkv, D, prefix, shape = CASES[case]
+    w, prefix, q, kc, vc, kt, vt = _small(dtype, B, hq, hkv, D, prefix, shape, q_scale, seed=case)
+    got, status, anc = _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=splits)
+    assert status == 0
+    ref = A.tree_attention(q, kc, vc, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
+    ok, excess = within(got, ref, *TOL[dtype])
+    assert ok, f"max excess over tolerance {excess}"
+
+
+def test_prefix_beyond_bound_is_reported():
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 2, 8, 2, 128, [50, 60], synth.p4_example())
+    got, status, _ = _run(w, synth.p4_example(), prefix, q, kc, vc, kt, vt, max_prefix=55)
+    assert status == sv.DEV_CAPACITY
+    ref = A.tree_attention(q[:1], kc[:1], vc[:1], kt[:1], vt[:1], prefix[:1], T.depth_and_mask(synth.P4_PARENTS)[1])
+    assert within(got[:1], ref, *TOL["bf16"])[0]          # the in-bound sequence is still computed
+
+
+FULL = ["vicuna7b_medusa", "llama8b_eagle2", "llama70b_serving", "long_context"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_tree_attention_full_size_sampled(name):
+    """The workload's full shapes in the default launch configuration;
+    48 sampled (sequence, node, head) outputs against the oracle, plus
+    properties of every output (finite, bounded by the value range)."""
+    w = synth.WORKLOADS[name]
+    shape = synth.random_tree(w.seed, w.n_nodes, w.caps if w.caps else (10, 4, 3, 2, 2))
+    prefix = synth.prefix_lengths(w)
+    q, kc, vc, kt, vt = synth.attention_inputs(w, prefix, q_scale=2.0)
+    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt)
+    assert status == 0
+    assert np.isfinite(got).all()
+    assert np.abs(got).max() <= max(np.abs(vc).max(), np.abs(vt).max()) * 1.01
+    g = np.random.default_rng(0)
+    mask = T.depth_and_mask(shape.parents)[1]
+    for _ in range(48):
+        b, i, h = int(g.integers(w.batch)), int(g.integers(w.n_nodes)), int(g.integers(w.hq))
+        ref = A.tree_attention(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], kt[b:b + 1], vt[b:b + 1], prefix[b:b + 1],
+                               mask, nodes=[i], heads=[h])[0, i, h]
+        ok, excess = within(got[b, i, h], ref, *TOL["bf16"])
+        assert ok, (b, i, h, excess)

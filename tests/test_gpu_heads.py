@@ -1,0 +1,119 @@
+"""GPU parity: Medusa heads, LM head and top-s selection."""
+import numpy as np
+import pytest
+import torch
+
+from _util import dev, host, within
+from oracle import heads as H
+from tree_speculative_decoding_attn_gb300 import specverify as sv
+from tree_speculative_decoding_attn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = (2e-2, 1e-2)   # bf16 weights/inputs, float32 accumulation vs float64
+
+
+def _heads(h, w1, b1, w2):
+    B, d = h.shape
+    K, V = w2.shape[:2]
+    z = torch.empty((B, K, d), dtype=torch.float32, device="cuda")
+    logits = torch.empty((B, K, V), dtype=torch.float32, device="cuda")
+    bf = torch.bfloat16
+    sv.spec_medusa_heads(dev(h, bf), dev(w1, bf), None if b1 is None else dev(b1, bf), dev(w2, bf), z, logits)
+    torch.cuda.synchronize()
+    return host(z), host(logits)
+
+
+@pytest.mark.parametrize("B,K,d,V,bias", [(1, 4, 256, 1000, False), (3, 2, 512, 777, True), (8, 1, 64, 50, True)])
+def test_medusa_heads_small(B, K, d, V, bias):
+    g = synth.stream(B * 100 + d, "h")
+    h = synth.gaussian(g, (B, d), 1.0, True)
+    w1 = synth.gaussian(g, (K, d, d), 0.05, True)
+    b1 = synth.gaussian(g, (K, d), 0.1, True) if bias else None
+    w2 = synth.gaussian(g, (K, V, d), 0.05, True)
+    z, logits = _heads(h, w1, b1, w2)
+    rz, rl = H.medusa_heads(h, w1, b1, w2)
+    assert within(z, rz, 1e-4, 1e-4)[0]          # float32 sums of d bf16 products
+    assert within(logits, rl, *TOL)[0]
+
+
+def test_medusa_heads_zero_w1_reproduce_lm_head_topk():
+    """W1 = 0 and W2 = copies of the LM head: every head's top-10 equals the
+    LM head's (the heads' initialisation on the pages)."""
+    g = synth.stream(3, "z")
+    d, V = 256, 2000
+    h = synth.gaussian(g, (2, d), 1.0, True)
+    wlm = synth.gaussian(g, (V, d), 0.05, True)
+    K = 3
+    z, logits = _heads(h, np.zeros((K, d, d), np.float32), None, np.broadcast_to(wlm, (K, V, d)).copy())
+    np.testing.assert_array_equal(z, np.broadcast_to(h[:, None, :], z.shape))
+    lm = torch.empty((2, V), dtype=torch.float32, device="cuda")
+    sv.spec_lm_head(dev(h, torch.bfloat16), dev(wlm, torch.bfloat16), lm)
+    for k in range(K):
+        np.testing.assert_array_equal(logits[:, k], logits[:, 0])
+    idx = torch.empty((2, 10), dtype=torch.int32, device="cuda")
+    sv.spec_topk(dev(logits[:, 0]), 10, idx)
+    idx2 = torch.empty((2, 10), dtype=torch.int32, device="cuda")
+    sv.spec_topk(lm, 10, idx2)
+    torch.cuda.synchronize()
+    assert (host(idx) == host(idx2)).all()
+
+
+def test_medusa_heads_full_size_sampled_rows():
+    """Hidden 4096, 4 heads, vocabulary 32000 (1.05 GB of head weights):
+    z in full, 512 sampled vocabulary rows of every head."""
+    w = synth.WORKLOADS["vicuna7b_medusa"]
+    h, w1, w2, _ = synth.medusa_inputs(w)
+    z, logits = _heads(h, w1, None, w2)
+    rows = np.sort(np.random.default_rng(0).choice(w.vocab, 512, replace=False))
+    rz, rl = H.medusa_heads(h, w1, None, w2[:, rows])
+    assert within(z, rz, 1e-3, 1e-3)[0]
+    assert within(logits[:, :, rows], rl, *TOL)[0]
+
+
+@pytest.mark.parametrize("R,d,V", [(5, 128, 300), (64, 4096, 32000), (130, 256, 1001)])
+def test_lm_head(R, d, V):
+    g = synth.stream(R + d + V, "lm")
+    hid = synth.gaussian(g, (R, d), 1.0, True)
+    wlm = synth.gaussian(g, (V, d), 0.02, True)
+    out = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    sv.spec_lm_head(dev(hid, torch.bfloat16), dev(wlm, torch.bfloat16), out)
+    torch.cuda.synchronize()
+    got = host(out)
+    cols = np.arange(V) if V <= 2000 else np.sort(np.random.default_rng(1).choice(V, 1000, replace=False))
+    ref = H.lm_head(hid, wlm[cols])
+    assert within(got[:, cols], ref, *TOL)[0]
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("V,s", [(1000, 10), (32000, 10), (128256, 16), (17, 1), (33, 16)])
+def test_topk_bit_exact(dtype, V, s):
+    g = synth.stream(V + s, "topk")
+    rows = np.round(synth.gaussian(g, (6, V), 2.0, False) * 4) / 4   # plenty of exact ties
+    rows = synth.round_bf16(rows) if dtype == torch.bfloat16 else rows.astype(np.float32)
+    idx = torch.empty((6, s), dtype=torch.int32, device="cuda")
+    val = torch.empty((6, s), dtype=torch.float32, device="cuda")
+    sv.spec_topk(dev(rows, dtype), s, idx, val)
+    torch.cuda.synchronize()
+    ridx, rval = H.topk(rows, s)
+    np.testing.assert_array_equal(host(idx), ridx)
+    np.testing.assert_array_equal(host(val), rval)
+
+
+def test_heads_then_topk_chain_matches_up_to_near_ties():
+    """GPU heads -> GPU top-10 against oracle heads -> oracle top-10: equal,
+    except where two candidates' oracle logits lie within the tolerance."""
+    w = synth.WORKLOADS["vicuna7b_medusa"]
+    h, w1, w2, _ = synth.medusa_inputs(w, hidden=512, vocab=4000)
+    _, logits = _heads(h, w1, None, w2)
+    idx = torch.empty((4, 10), dtype=torch.int32, device="cuda")
+    sv.spec_topk(dev(logits.reshape(4, -1)), 10, idx)
+    torch.cuda.synchronize()
+    _, rl = H.medusa_heads(h, w1, None, w2)
+    ridx, _ = H.topk(rl.reshape(4, -1), 10)
+    got = host(idx)
+    for r in range(4):
+        for j in range(10):
+            if got[r, j] != ridx[r, j]:
+                a, b = rl.reshape(4, -1)[r, got[r, j]], rl.reshape(4, -1)[r, ridx[r, j]]
+                assert abs(a - b) <= TOL[0] + TOL[1] * abs(b)

@@ -1,0 +1,62 @@
+// Internal launchers (host functions) implemented by the kernel files and
+// called by the C-ABI layer in spec_api.cu.  Arguments are validated there.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *cand_tok,
+                    int cand_levels, int cand_s, const int32_t *root_tok, const int32_t *prefix_len,
+                    int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
+                    int32_t *first_child, int32_t *next_sibling, int32_t *status, cudaStream_t stream);
+
+int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const float *pool_conf,
+                     int M, const int32_t *prefix_len, int batch, int n, int32_t *tok,
+                     int32_t *parents_out, int32_t *depth, int32_t *pos, uint64_t *anc,
+                     int32_t *first_child, int32_t *next_sibling, int32_t *pool_index, float *val,
+                     int32_t *status, cudaStream_t stream);
+
+// Tree attention.  `plan` picks the kernel family and split count; the
+// workspace size follows from it.
+struct SvAttnShape {
+  int dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix;
+};
+struct SvAttnPlan {
+  int use_tc;        // 1 = tcgen05 kernel, 0 = CUDA-core kernel
+  int splits;        // KV splits per (sequence, KV head)
+  int chunk;         // prefix keys per split (multiple of the key tile)
+  size_t ws_bytes;   // partials (0 when splits == 1)
+};
+SvAttnPlan sv_attn_plan(const SvAttnShape &s, int num_splits);
+int sv_attn_simt(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const void *kc,
+                 const void *vc, const void *kt, const void *vt, const int32_t *prefix_len,
+                 const uint64_t *anc, void *out, float scale, void *ws, int32_t *status,
+                 cudaStream_t stream);
+int sv_attn_tc(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const void *kc,
+               const void *vc, const void *kt, const void *vt, const int32_t *prefix_len,
+               const uint64_t *anc, void *out, float scale, void *ws, int32_t *status,
+               cudaStream_t stream);
+int sv_attn_combine(const SvAttnShape &s, const SvAttnPlan &p, const void *ws, void *out,
+                    const int32_t *prefix_len, cudaStream_t stream);
+
+int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
+                    int n_heads, int hidden, int vocab, float *z, float *logits,
+                    cudaStream_t stream);
+int sv_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
+               cudaStream_t stream);
+int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
+            int32_t *idx, float *val, cudaStream_t stream);
+int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,
+                   const int32_t *frontier, int k, float temperature, int32_t *pool_parent,
+                   int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
+                   int pool_cap, int32_t *next_frontier, int n_next, int32_t *status,
+                   cudaStream_t stream);
+int sv_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
+              const int32_t *tok, const int32_t *parents, const int32_t *first_child,
+              const int32_t *next_sibling, float temperature, float eps, float delta,
+              uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
+              int32_t *bonus, int32_t *status, cudaStream_t stream);
+int sv_kv_commit(void *kc, void *vc, const void *kt, const void *vt, int elem_bytes, int n_layers,
+                 int batch, int hkv, int s_max, int n_nodes, int head_dim, const int32_t *acc_len,
+                 const int32_t *acc_path, int path_cap, const int32_t *prefix_len,
+                 int32_t *prefix_len_out, int32_t *status, cudaStream_t stream);

@@ -1,0 +1,233 @@
+// Top-s candidate selection and one confidence-product expansion round.
+//
+// "Medusa and EAGLE ... explained", section "Medusa: heads, losses and
+// trees": head k contributes its top s_k tokens to the tree.
+// "5.3 Medusa、EAGLE 与 MTP", section 5.2: a node's value is the product of
+// draft confidences on its path; expansion grows the highest-value nodes.
+//
+// Selection order everywhere: larger value first, equal values by lower
+// index -- one 64-bit key per element (value bits made order-preserving in
+// the high word, the complemented index in the low word), so every
+// comparison is a single integer max.
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxS = 16;  // largest s / k (per-thread sorted list length)
+
+template <typename T, typename F>
+__device__ __forceinline__ void for_row(const T *row, int V, F &&f) {
+  constexpr int kVec = 16 / sizeof(T);
+  if ((V % kVec) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    for (int vi = threadIdx.x; vi < V / kVec; vi += kThreads) {
+      const uint4 u = sv::ldg_stream(row + (int64_t)vi * kVec);
+      float v[kVec];
+      if constexpr (sizeof(T) == 2) {
+        sv::bf16x8_to_f32(u, v);
+      } else {
+        v[0] = __uint_as_float(u.x);
+        v[1] = __uint_as_float(u.y);
+        v[2] = __uint_as_float(u.z);
+        v[3] = __uint_as_float(u.w);
+      }
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) f(vi * kVec + j, v[j]);
+    }
+  } else {
+    for (int x = threadIdx.x; x < V; x += kThreads) f(x, sv::to_f32(row[x]));
+  }
+}
+
+// Keep the S largest keys seen by this thread, sorted descending.
+template <int S>
+__device__ __forceinline__ void insert_key(unsigned long long (&best)[S], unsigned long long k) {
+  if (k <= best[S - 1]) return;
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const unsigned long long hi = best[j] > k ? best[j] : k;
+    k = best[j] > k ? k : best[j];
+    best[j] = hi;
+  }
+}
+
+// Merge the per-thread sorted lists held in shared memory: s rounds, each
+// takes the largest list head across the CTA and advances that list.
+template <int S>
+__device__ void merge_top(const unsigned long long (&best)[S], unsigned long long *lists, int s,
+                          unsigned long long *out) {
+  __shared__ unsigned long long red[kWarps];
+#pragma unroll
+  for (int j = 0; j < S; ++j) lists[threadIdx.x * S + j] = best[j];
+  int head = 0;
+  __syncthreads();
+  for (int r = 0; r < s; ++r) {
+    const unsigned long long mine = head < S ? lists[threadIdx.x * S + head] : 0ull;
+    unsigned long long w = sv::warp_max_u64(mine);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = w;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      unsigned long long v = threadIdx.x < kWarps ? red[threadIdx.x] : 0ull;
+      v = sv::warp_max_u64(v);
+      if (threadIdx.x == 0) out[r] = v;
+    }
+    __syncthreads();
+    if (mine == out[r] && mine != 0ull) ++head;  // keys are unique: one winner
+    __syncthreads();
+  }
+}
+
+template <typename T, int S>
+__global__ void __launch_bounds__(kThreads)
+    topk_kernel(const T *__restrict__ rows, int row_len, int64_t row_stride, int s,
+                int32_t *__restrict__ idx, float *__restrict__ val) {
+  __shared__ unsigned long long lists[kThreads * S];
+  __shared__ unsigned long long top[32];
+  unsigned long long best[S];
+#pragma unroll
+  for (int j = 0; j < S; ++j) best[j] = 0ull;
+  const T *row = rows + (int64_t)blockIdx.x * row_stride;
+  for_row(row, row_len, [&](int x, float v) { insert_key<S>(best, sv::rank_key(v, (uint32_t)x)); });
+  merge_top<S>(best, lists, s, top);
+  if (threadIdx.x < s) {
+    idx[(int64_t)blockIdx.x * s + threadIdx.x] = (int32_t)sv::key_index(top[threadIdx.x]);
+    if (val) val[(int64_t)blockIdx.x * s + threadIdx.x] = sv::key_value(top[threadIdx.x]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Expansion round, part 1: one CTA per (sequence, frontier node): top-k
+// tokens of the draft row, their softmax probabilities (float32), children
+// appended to the pool.
+// ---------------------------------------------------------------------------
+template <typename T, int S>
+__global__ void __launch_bounds__(kThreads)
+    expand_rows_kernel(const T *__restrict__ logits, int n_front, int V, const int32_t *frontier,
+                       int k, float temp, int32_t *pool_parent, int32_t *pool_tok, float *pool_conf,
+                       float *pool_val, const int32_t *pool_count, int pool_cap, int32_t *status) {
+  __shared__ unsigned long long lists[kThreads * S];
+  __shared__ unsigned long long top[32];
+  __shared__ float red[kWarps];
+  __shared__ float s_bcast;
+  const int b = blockIdx.x / n_front, f = blockIdx.x % n_front;
+  const int base = pool_count[b];
+  if (base + n_front * k > pool_cap) {
+    if (threadIdx.x == 0) sv::report(status, SPEC_DEV_CAPACITY);
+    return;
+  }
+  const int src = frontier[(int64_t)b * n_front + f];
+  if (src < 0 || src >= base) {
+    if (threadIdx.x == 0) sv::report(status, SPEC_DEV_BAD_POOL);
+    return;
+  }
+  const T *row = logits + ((int64_t)b * n_front + f) * V;
+  unsigned long long best[S];
+#pragma unroll
+  for (int j = 0; j < S; ++j) best[j] = 0ull;
+  float m = -INFINITY;
+  for_row(row, V, [&](int x, float v) {
+    insert_key<S>(best, sv::rank_key(v, (uint32_t)x));
+    m = fmaxf(m, v / temp);
+  });
+  m = sv::warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = red[0];
+    for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, red[w]);
+    s_bcast = mm;
+  }
+  __syncthreads();
+  m = s_bcast;
+  float S_ = 0.f;
+  for_row(row, V, [&](int, float v) { S_ += expf(v / temp - m); });
+  S_ = sv::warp_sum(S_);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = S_;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float ss = 0.f;
+    for (int w = 0; w < kWarps; ++w) ss += red[w];
+    s_bcast = ss;
+  }
+  merge_top<S>(best, lists, k, top);  // contains __syncthreads
+  S_ = s_bcast;
+  if (threadIdx.x < k) {
+    const int x = (int)sv::key_index(top[threadIdx.x]);
+    const float p = expf(sv::to_f32(row[x]) / temp - m) / S_;
+    const int64_t slot = (int64_t)b * pool_cap + base + f * k + threadIdx.x;
+    pool_parent[slot] = src;
+    pool_tok[slot] = x;
+    pool_conf[slot] = p;
+    pool_val[slot] = __fmul_rn(pool_val[(int64_t)b * pool_cap + src], p);
+  }
+}
+
+// Part 2: one CTA per sequence ranks the n_front * k new children by
+// (value desc, pool index asc), writes the next frontier, bumps the count.
+__global__ void __launch_bounds__(1024)
+    expand_select_kernel(int n_new, const float *__restrict__ pool_val, int32_t *pool_count,
+                         int pool_cap, int32_t *next_frontier, int n_next) {
+  __shared__ unsigned long long keys[1024];
+  const int b = blockIdx.x;
+  const int base = pool_count[b];
+  if (base + n_new > pool_cap) return;  // reported by part 1
+  const int t = threadIdx.x;
+  if (t < n_new) {
+    const float v = pool_val[(int64_t)b * pool_cap + base + t];
+    keys[t] = ((unsigned long long)(0xFFFFFFFFu - (__float_as_uint(v) & 0x7FFFFFFFu)) << 32) |  // v >= 0
+              (unsigned)(base + t);
+  }
+  __syncthreads();
+  if (t < n_new) {
+    int r = 0;
+    for (int j = 0; j < n_new; ++j) r += keys[j] < keys[t];
+    if (r < n_next) next_frontier[(int64_t)b * n_next + r] = base + t;
+  }
+  for (int r = n_new + t; r < n_next; r += blockDim.x) next_frontier[(int64_t)b * n_next + r] = -1;
+  __syncthreads();
+  if (t == 0) pool_count[b] = base + n_new;
+}
+
+template <typename T, int S>
+int launch_topk(const void *rows, int n_rows, int row_len, int row_stride, int s, int32_t *idx,
+                float *val, cudaStream_t stream) {
+  topk_kernel<T, S><<<n_rows, kThreads, 0, stream>>>((const T *)rows, row_len, row_stride, s, idx, val);
+  return sv_launch_status();
+}
+
+}  // namespace
+
+int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
+            int32_t *idx, float *val, cudaStream_t stream) {
+  if (s > kMaxS) return SPEC_ERR_UNSUPPORTED;
+  if (dtype == SPEC_BF16)
+    return launch_topk<__nv_bfloat16, kMaxS>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
+  return launch_topk<float, kMaxS>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
+}
+
+int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,
+                   const int32_t *frontier, int k, float temperature, int32_t *pool_parent,
+                   int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
+                   int pool_cap, int32_t *next_frontier, int n_next, int32_t *status,
+                   cudaStream_t stream) {
+  const int grid = batch * n_front;
+  if (k > kMaxS) return SPEC_ERR_UNSUPPORTED;
+  if (dtype == SPEC_BF16)
+    expand_rows_kernel<__nv_bfloat16, kMaxS><<<grid, kThreads, 0, stream>>>(
+        (const __nv_bfloat16 *)logits, n_front, vocab, frontier, k, temperature, pool_parent,
+        pool_tok, pool_conf, pool_val, pool_count, pool_cap, status);
+  else
+    expand_rows_kernel<float, kMaxS><<<grid, kThreads, 0, stream>>>(
+        (const float *)logits, n_front, vocab, frontier, k, temperature, pool_parent, pool_tok,
+        pool_conf, pool_val, pool_count, pool_cap, status);
+  int rc = sv_launch_status();
+  if (rc != SPEC_OK) return rc;
+  expand_select_kernel<<<batch, 1024, 0, stream>>>(n_front * k, pool_val, pool_count, pool_cap,
+                                                   next_frontier, n_next);
+  return sv_launch_status();
+}

@@ -1,0 +1,251 @@
+// Tree bookkeeping of the verify pass: depth, ancestor bitmask, depth
+// position ids, child links; static (Medusa) token placement and the
+// confidence-product rerank (EAGLE-2).
+//
+// "5.3 Medusa、EAGLE 与 MTP" (infra-guide): section 3.1 (a node sees the
+// prefix and its ancestors only), 3.2 (position id = depth; siblings share
+// one), 5.2 (path value = product of draft confidences; the best nodes go to
+// verification), 8 (parents array with parent < node, ancestor walk).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxNodes = SPEC_MAX_NODES;
+
+// Emits depth/pos/mask/child links for one sequence's parents array held in
+// shared memory.  One thread per node; the walk is bounded because the
+// caller validated parent < node.
+__device__ void emit_tree_arrays(const int *par, int N, int i, int prefix, int64_t row,
+                                 int32_t *depth, int32_t *pos, uint64_t *anc, int32_t *first_child,
+                                 int32_t *next_sibling, int *depth_out) {
+  uint64_t m = 0;
+  int d = -1;
+  for (int c = i; c != -1; c = par[c]) {
+    m |= 1ull << c;
+    ++d;
+  }
+  int fc = -1, ns = -1;
+  for (int c = i + 1; c < N; ++c)
+    if (par[c] == i) {
+      fc = c;
+      break;
+    }
+  if (i > 0)
+    for (int c = i + 1; c < N; ++c)
+      if (par[c] == par[i]) {
+        ns = c;
+        break;
+      }
+  depth[row + i] = d;
+  pos[row + i] = prefix + d;
+  anc[row + i] = m;
+  first_child[row + i] = fc;
+  next_sibling[row + i] = ns;
+  *depth_out = d;
+}
+
+__global__ void __launch_bounds__(kMaxNodes)
+    build_static_kernel(const int32_t *__restrict__ parents, const int32_t *__restrict__ rank,
+                        const int32_t *__restrict__ cand_tok, int cand_levels, int cand_s,
+                        const int32_t *__restrict__ root_tok, const int32_t *__restrict__ prefix_len,
+                        int N, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
+                        int32_t *first_child, int32_t *next_sibling, int32_t *status) {
+  __shared__ int par[kMaxNodes];
+  __shared__ int bad;
+  const int b = blockIdx.x, i = threadIdx.x;
+  if (i == 0) bad = 0;
+  __syncthreads();
+  if (i < N) {
+    const int p = parents[i];
+    par[i] = p;
+    if (i == 0 ? p != -1 : (p < 0 || p >= i)) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (i == 0) sv::report(status, SPEC_DEV_BAD_PARENTS);
+    return;
+  }
+  if (i >= N) return;
+  const int64_t row = (int64_t)b * N;
+  int d;
+  emit_tree_arrays(par, N, i, prefix_len[b], row, depth, pos, anc, first_child, next_sibling, &d);
+  if (tok) {
+    int t = -1;
+    if (i == 0) {
+      t = root_tok[b];
+    } else {
+      const int r = rank[i];
+      if (d - 1 < cand_levels && r >= 0 && r < cand_s)
+        t = cand_tok[((int64_t)b * cand_levels + (d - 1)) * cand_s + r];
+      else
+        sv::report(status, SPEC_DEV_BAD_PARENTS);
+    }
+    tok[row + i] = t;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Confidence-product rerank.  One CTA per sequence.
+//   1. val[i] = val[parent] * conf[i] in root-to-node order (float32).
+//   2. rank of every pool node under (val desc, depth asc, index asc) by
+//      counting; the n lowest ranks are kept (the root has rank 0).
+//   3. breadth-first renumbering, level by level: (new parent, val desc,
+//      index asc).
+// ---------------------------------------------------------------------------
+constexpr int kDynThreads = 1024;
+constexpr int kMaxPool = 4096;
+constexpr int kMaxPoolDepth = 64;
+
+__global__ void __launch_bounds__(kDynThreads)
+    build_dynamic_kernel(const int32_t *__restrict__ pool_parent, const int32_t *__restrict__ pool_tok,
+                         const float *__restrict__ pool_conf, int M, const int32_t *__restrict__ prefix_len,
+                         int N, int32_t *tok, int32_t *parents_out, int32_t *depth, int32_t *pos,
+                         uint64_t *anc, int32_t *first_child, int32_t *next_sibling, int32_t *pool_index,
+                         float *val_out, int32_t *status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  unsigned long long *key = reinterpret_cast<unsigned long long *>(smem);  // [M]
+  int *ppar = reinterpret_cast<int *>(key + M);                          // [M]
+  float *val = reinterpret_cast<float *>(ppar + M);                      // [M]
+  __shared__ int kept[kMaxNodes];       // pool index of kept slot r (sorted by key)
+  __shared__ int kept_new[kMaxNodes];   // new (breadth-first) index of kept slot r
+  __shared__ int new_par[kMaxNodes];    // parents by new index
+  __shared__ int bad;
+
+  const int b = blockIdx.x, t = threadIdx.x;
+  const int64_t prow = (int64_t)b * M;
+  if (t == 0) bad = 0;
+  __syncthreads();
+  for (int i = t; i < M; i += kDynThreads) {
+    const int p = pool_parent[prow + i];
+    const float c = pool_conf[prow + i];
+    ppar[i] = p;
+    if (i == 0 ? p != -1 : (p < 0 || p >= i || !(c >= 0.f && c <= 1.f))) atomicOr(&bad, 1);
+  }
+  __syncthreads();
+  if (bad) {
+    if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
+    return;
+  }
+  // 1. path values and depths
+  for (int i = t; i < M; i += kDynThreads) {
+    int chain[kMaxPoolDepth];
+    int d = 0;
+    int c = i;
+    while (c > 0 && d < kMaxPoolDepth) {
+      chain[d++] = c;
+      c = ppar[c];
+    }
+    if (c != 0) {
+      atomicOr(&bad, 1);
+      d = 0;
+    }
+    float v = 1.0f;
+    for (int j = d - 1; j >= 0; --j) v = __fmul_rn(v, pool_conf[prow + chain[j]]);
+    val[i] = v;
+    // v >= 0, so clearing the sign bit only maps -0 to +0
+    key[i] = ((unsigned long long)(0xFFFFFFFFu - (__float_as_uint(v) & 0x7FFFFFFFu)) << 32) |
+             ((unsigned long long)d << 16) | (unsigned long long)i;
+  }
+  __syncthreads();
+  if (bad) {
+    if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
+    return;
+  }
+  // 2. keep the N smallest keys
+  for (int i = t; i < M; i += kDynThreads) {
+    const unsigned long long k = key[i];
+    int r = 0;
+    for (int j = 0; j < M; ++j) r += key[j] < k;
+    if (r < N) kept[r] = i;
+  }
+  __syncthreads();
+  // parent closure check and breadth-first renumbering (N <= 64 threads)
+  int my_pool = -1, my_depth = 0, my_pslot = -1;
+  if (t < N) {
+    my_pool = kept[t];
+    my_depth = (int)((key[my_pool] >> 16) & 0xFFFF);
+    if (t > 0) {
+      const int pp = ppar[my_pool];
+      for (int r = 0; r < N; ++r)
+        if (kept[r] == pp) my_pslot = r;
+      if (my_pslot < 0) atomicOr(&bad, 1);
+    }
+  }
+  __syncthreads();
+  if (bad) {
+    if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
+    return;
+  }
+  int base = 0;
+  for (int d = 0; d < kMaxPoolDepth; ++d) {
+    int here = 0;  // kept nodes at depth d (uniform across threads)
+    for (int r = 0; r < N; ++r) here += ((int)((key[kept[r]] >> 16) & 0xFFFF) == d);
+    if (here == 0) break;
+    if (t < N && my_depth == d) {
+      const int mp = (t == 0) ? -1 : kept_new[my_pslot];
+      int before = 0;
+      for (int r = 0; r < N; ++r) {
+        if (r == t) continue;
+        const int u = kept[r];
+        if ((int)((key[u] >> 16) & 0xFFFF) != d) continue;
+        int upar = -1;  // new index of u's parent (assigned on an earlier level)
+        if (r != 0) {
+          const int pp = ppar[u];
+          for (int q = 0; q < N; ++q)
+            if (kept[q] == pp) upar = kept_new[q];
+        }
+        if (upar < mp || (upar == mp && key[u] < key[my_pool])) ++before;
+      }
+      kept_new[t] = base + before;
+      new_par[base + before] = mp;
+    }
+    base += here;
+    __syncthreads();
+  }
+  // 3. outputs by new index
+  if (t < N) {
+    const int ni = kept_new[t];
+    const int64_t row = (int64_t)b * N;
+    tok[row + ni] = pool_tok[prow + my_pool];
+    parents_out[row + ni] = new_par[ni];
+    if (pool_index) pool_index[row + ni] = my_pool;
+    if (val_out) val_out[row + ni] = val[my_pool];
+  }
+  __syncthreads();
+  if (t < N) {
+    int d;
+    emit_tree_arrays(new_par, N, t, prefix_len[b], (int64_t)b * N, depth, pos, anc, first_child,
+                     next_sibling, &d);
+  }
+}
+
+}  // namespace
+
+int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *cand_tok,
+                    int cand_levels, int cand_s, const int32_t *root_tok, const int32_t *prefix_len,
+                    int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
+                    int32_t *first_child, int32_t *next_sibling, int32_t *status,
+                    cudaStream_t stream) {
+  build_static_kernel<<<batch, kMaxNodes, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s,
+                                                       root_tok, prefix_len, n, tok, depth, pos, anc,
+                                                       first_child, next_sibling, status);
+  return sv_launch_status();
+}
+
+int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const float *pool_conf,
+                     int M, const int32_t *prefix_len, int batch, int n, int32_t *tok,
+                     int32_t *parents_out, int32_t *depth, int32_t *pos, uint64_t *anc,
+                     int32_t *first_child, int32_t *next_sibling, int32_t *pool_index, float *val,
+                     int32_t *status, cudaStream_t stream) {
+  if (M > kMaxPool) return SPEC_ERR_UNSUPPORTED;
+  const size_t smem = (size_t)M * (8 + 4 + 4);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(build_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  build_dynamic_kernel<<<batch, kDynThreads, smem, stream>>>(
+      pool_parent, pool_tok, pool_conf, M, prefix_len, n, tok, parents_out, depth, pos, anc,
+      first_child, next_sibling, pool_index, val, status);
+  return sv_launch_status();
+}
