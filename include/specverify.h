@@ -239,6 +239,32 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache,
                      int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
+ * tree_attn_verify_noalloc -- tree_attn_verify without a caller workspace.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot allocate device memory: a plugin inside a host runtime that
+ * owns all device memory and hands it only its input and output buffers,
+ * or a serving loop that bans cudaMalloc/cudaFree after start-up because
+ * they synchronise the device.
+ *
+ * Arguments and results are those of tree_attn_verify, minus the workspace:
+ * the split-KV partials go to a library-owned device array of
+ * SPEC_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library keeps
+ * until the process exits.  Allocates nothing.  Returns SPEC_ERR_CAPACITY
+ * (nothing launched) when tree_attn_workspace_bytes() for these arguments
+ * exceeds SPEC_NOALLOC_SCRATCH_BYTES.  The first call on each device looks
+ * up the array's device address; make that first call before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU
+ * (unordered streams) race on it.  Nothing in it needs to start at zero.
+ * ------------------------------------------------------------------ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB */
+int tree_attn_verify_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                             const void *k_tree, const void *v_tree, const int32_t *prefix_len,
+                             const uint64_t *anc_mask, void *out, int dtype, int batch,
+                             int n_nodes, int hq, int hkv, int head_dim, int s_max, int max_prefix,
+                             float scale, int num_splits, int32_t *dev_status,
+                             spec_stream_t stream);
+
+/* --------------------------------------------------------------------
  * spec_lm_head -- target logits of every tree node ("Medusa, explained",
  * step 6: one forward pass scores every node).
  *   hid    [rows, hidden] bf16

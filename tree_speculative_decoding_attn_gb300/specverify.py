@@ -38,6 +38,8 @@ _SIGS = {
     "tree_attn_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "tree_attn_verify": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                           _vp, _sz, _vp, _vp], _i),
+    "tree_attn_verify_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                                  _i, _vp, _vp], _i),
     "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp], _i),
     "spec_accept": ([_i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp, _vp,
                      _vp, _vp], _i),
@@ -184,6 +186,27 @@ def tree_attn_verify(q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, 
         _p(q), _p(k_cache), _p(v_cache), _p(k_tree), _p(v_tree), _p(prefix_len), _p(anc_mask), _p(out),
         _DT[q.dtype], B, N, Hq, Hkv, D, S, int(max_prefix), float(scale), int(num_splits), _p(workspace),
         ws_bytes, _p(dev_status), _stream()))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def tree_attn_verify_noalloc(q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out, max_prefix,
+                             scale=0.0, num_splits=0, dev_status=None):
+    """tree_attn_verify for callers that cannot allocate: the split-KV
+    partials live in the library's own fixed device array (32 MiB, shared by
+    every call; calls that overlap on the GPU race on it)."""
+    B, N, Hq, D = q.shape
+    Hkv, S = k_cache.shape[1], k_cache.shape[2]
+    _want(q, torch.float32, torch.bfloat16)
+    for t in (k_cache, v_cache, k_tree, v_tree, out):
+        if t.dtype != q.dtype:
+            raise TypeError("q, caches, tree K/V and out must share one dtype")
+    _want(anc_mask, torch.int64); _want(prefix_len, torch.int32)
+    _check("tree_attn_verify_noalloc", load().tree_attn_verify_noalloc(
+        _p(q), _p(k_cache), _p(v_cache), _p(k_tree), _p(v_tree), _p(prefix_len), _p(anc_mask), _p(out),
+        _DT[q.dtype], B, N, Hq, Hkv, D, S, int(max_prefix), float(scale), int(num_splits), _p(dev_status),
+        _stream()))
 
 
 def spec_lm_head(hid, w, logits):
