@@ -52,6 +52,9 @@ CASES = [
     ("bf16", 2, 16, 2, 128, [0, 5], synth.random_tree(5, 64, (8, 4, 3, 2, 2))),  # 512 rows, empty prefix
     ("bf16", 1, 4, 1, 128, [700], synth.chain(1)),                           # plain decode attention
     ("bf16", 2, 32, 8, 128, [1000, 4097], synth.chain(6)),
+    ("bf16", 2, 64, 8, 128, [4096, 1111], synth.random_tree(7, 32, (4, 3, 2))),      # 256 rows per KV head
+    ("bf16", 1, 32, 32, 128, [2048], synth.random_tree(8, 64, (10, 10, 10, 10))),    # MHA, 64 rows
+    ("bf16", 3, 32, 8, 128, [513, 8192, 129], synth.random_tree(9, 60, (10, 4, 3, 2, 2))),
 ]
 
 
@@ -66,6 +69,37 @@ def test_tree_attention_small(case, splits, q_scale):
     ref = A.tree_attention(q, kc, vc, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
     ok, excess = within(got, ref, *TOL[dtype])
     assert ok, f"max excess over tolerance {excess}"
+
+
+def test_growing_scores_force_rescaling():
+    """Keys whose norm grows along the prefix make each tile's row max
+    exceed the running one, so the running output is rescaled many times."""
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 2, 16, 4, 128, [1500, 700], synth.random_tree(3, 16, (4, 3)),
+                                          q_scale=2.0, seed=21)
+    grow = (1.0 + np.arange(kc.shape[2]) / 96.0).astype(np.float32)
+    kc = synth.round_bf16(kc * grow[None, None, :, None])
+    shape = synth.random_tree(3, 16, (4, 3))
+    for splits in (1, 2):
+        got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=splits)
+        assert status == 0
+        ref = A.tree_attention(q, kc, vc, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
+        ok, excess = within(got, ref, *TOL["bf16"])
+        assert ok, f"max excess over tolerance {excess}"
+
+
+def test_non_finite_stale_cache_rows_are_ignored():
+    """Cache rows past the prefix hold NaN/Inf (never-written memory): the
+    output must not see them."""
+    shape = synth.random_tree(4, 24, (4, 3, 2))
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 2, 32, 8, 128, [300, 77], shape, seed=22)
+    for b, p in enumerate(prefix):
+        kc[b, :, p:] = np.nan
+        vc[b, :, p:] = np.inf
+    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt)
+    assert status == 0 and np.isfinite(got).all()
+    kc2, vc2 = np.nan_to_num(kc, nan=0.0, posinf=0.0), np.nan_to_num(vc, nan=0.0, posinf=0.0)
+    ref = A.tree_attention(q, kc2, vc2, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
+    assert within(got, ref, *TOL["bf16"])[0]
 
 
 def test_prefix_beyond_bound_is_reported():

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int dd = 0; dd < DL; ++dd) o[lane + 32 * dd] = sv::from_f32<T>(acc[k][dd] * inv);
     } else {
       const int64_t slot = (((int64_t)b * Hkv + kvh) * splits + split) * R + r;
-      float *wa = ws + slot * (D + 2);
+      float *wa = ws + slot * sv_partial_stride(D);
 #pragma unroll
       for (int dd = 0; dd < DL; ++dd) wa[lane + 32 * dd] = acc[k][dd];
       if (lane == 0) {
@@ -185,8 +185,8 @@ __global__ void __launch_bounds__(128)
   const int b = bh / Hkv, kvh = bh % Hkv;
   const int P = prefix_len[b];
   if (P < 0 || P > max_prefix || P > s_max) return;  // reported by the main kernel
-  const float *w0 = ws + ((int64_t)bh * splits * R + r) * (D + 2);
-  const int64_t sstride = (int64_t)R * (D + 2);
+  const float *w0 = ws + ((int64_t)bh * splits * R + r) * sv_partial_stride(D);
+  const int64_t sstride = (int64_t)R * sv_partial_stride(D);
   float M = -INFINITY;
   for (int s = 0; s < splits; ++s) M = fmaxf(M, w0[s * sstride + D]);
   float L = 0.f, acc[DL];
@@ -247,7 +247,7 @@ SvAttnPlan sv_attn_simt_plan(const SvAttnShape &s, int num_splits) {
   chunk = (chunk + kKeyTile - 1) / kKeyTile * kKeyTile;
   p.splits = splits;
   p.chunk = chunk;
-  p.ws_bytes = splits > 1 ? (size_t)s.batch * s.hkv * splits * R * (s.head_dim + 2) * sizeof(float) : 0;
+  p.ws_bytes = splits > 1 ? (size_t)s.batch * s.hkv * splits * R * sv_partial_stride(s.head_dim) * sizeof(float) : 0;
   return p;
 }
 

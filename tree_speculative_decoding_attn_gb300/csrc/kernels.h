@@ -17,7 +17,10 @@ int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const 
                      int32_t *status, cudaStream_t stream);
 
 // Tree attention.  `plan` picks the kernel family and split count; the
-// workspace size follows from it.
+// workspace size follows from it.  Split-KV partials: one row per (sequence,
+// KV head, split, query row) of head_dim unnormalised accumulators, then the
+// running max (log2 units) and the running sum, padded to a 16-byte multiple.
+inline constexpr int sv_partial_stride(int head_dim) { return head_dim + 4; }
 struct SvAttnShape {
   int dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix;
 };
