@@ -480,6 +480,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -491,6 +492,10 @@ def main():
     sv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.batch:
+        import dataclasses
+        from tree_speculative_decoding_attn_gb300 import synth
+        synth.WORKLOADS[args.workload] = dataclasses.replace(synth.WORKLOADS[args.workload], batch=args.batch)
     step = GpuStep(args.workload, dev)
     hbm, tc_peak, peak_kind = _peaks()
     stream = torch.cuda.current_stream()

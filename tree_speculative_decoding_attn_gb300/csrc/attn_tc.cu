@@ -20,9 +20,11 @@
 //               softmax runs
 //   warps 2-9   two softmax warpgroups, one per query tile; thread = row:
 //               S from TMEM, scale and mask (prefix range; ancestor bits on
-//               the tree tile), online max, P = 2^(s - m) written back as
-//               bf16 into the S columns, lazy rescale of O (only when the
-//               row max grows by more than 2^8)
+//               the tree tile), P = 2^(s - m) written back as bf16 into the
+//               S columns, one read of S per tile: the running max only
+//               moves when a 64-column group exceeds it by more than 2^64
+//               (then the sum, O and the tile's earlier P are rescaled in
+//               place), which keeps every value in float32 / bf16 range.
 //
 // TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
 // Every mbarrier wait is bounded; on a timeout the CTA reports
@@ -46,7 +48,7 @@ constexpr int kThreads = 320;
 constexpr uint32_t kTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 tile
 constexpr uint32_t kHalf = kTile / 2;      // 128 rows x 64 dims (one swizzle column)
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr float kRescale = 8.0f;       // log2 growth of the row max that forces a rescale
+constexpr float kGrow = 64.0f;         // log2 headroom above the running max before it is raised
 constexpr int kSms = 152;
 
 struct Bars {
@@ -288,60 +290,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const bool tree = with_tree && j == n_tiles - 1;
         const int nvalid = tree ? N : min(kBN, k1 - (k0 + j * kBN));
-        // scaled, masked score of column `col` from a raw TMEM word
-        auto score = [&](uint32_t w, int col) {
-          const bool vis = col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));  // tree: col < N <= 64
-          return vis ? __uint_as_float(w) * scale_log2 : -INFINITY;
+        const bool masked = tree || nvalid < kBN;  // full prefix tiles need no mask
+        // column `col` visible to this row (tree: col < N <= 64)
+        auto visible = [&](int col) {
+          return col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));
         };
-        // pass 1 over S: row max
-        float mt = -INFINITY;
+        const float NEG_INF = -INFINITY;
+        const uint32_t s_addr = tmem + lane_off + s_col(t);
+        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+        // Two groups of 64 S columns; each is read into registers, then P =
+        // 2^(s * scale - m) goes as bf16 pairs into 32 P columns (P columns
+        // of group g only cover S columns already read).  The running max m
+        // moves only when a group's max exceeds it by more than 2^kGrow (the
+        // first visible scores, or inputs of extraordinary range): the row
+        // sum, O and the group already written are then rescaled in place.
+        // Otherwise every P stays within [0, 2^kGrow], far inside float32 and
+        // bf16 range, and the normalisation by the row sum is unchanged.
 #pragma unroll
-        for (int c = 0; c < 4; c += 2) {
-          uint32_t sa[32], sb[32];
-          tmem_ld32(tmem + lane_off + s_col(t) + c * 32, sa);
-          tmem_ld32(tmem + lane_off + s_col(t) + c * 32 + 32, sb);
+        for (int g = 0; g < 2; ++g) {
+          uint32_t sv2[2][32];
+          tmem_ld32(s_addr + g * 64, sv2[0]);
+          tmem_ld32(s_addr + g * 64 + 32, sv2[1]);
           tmem_wait_ld();
+          float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mt = fmaxf(mt, fmaxf(score(sa[i], c * 32 + i), score(sb[i], c * 32 + 32 + i)));
-        }
-        const float m_new = fmaxf(m_used, mt);
-        float alpha = 1.f;
-        if (m_new > m_used + kRescale) {
-          alpha = ex2(m_used - m_new);  // 0 when nothing was accumulated yet
-          m_used = m_new;
-          l *= alpha;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_t holds every PV issued before this S (the S commit covered
-          // them); scale it in place
+          for (int h = 0; h < 2; ++h) {
+            if (masked) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + o_col(t) + c * 32, o);
-            tmem_wait_ld();
+              for (int i = 0; i < 32; ++i)
+                if (!visible(g * 64 + h * 32 + i)) sv2[h][i] = __float_as_uint(NEG_INF);
+            }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tmem + lane_off + o_col(t) + c * 32, o);
+            for (int i = 0; i < 16; ++i)
+              mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv2[h][2 * i]), __uint_as_float(sv2[h][2 * i + 1]));
+          }
+          const float m_g = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+          const bool need = m_g > m_used + kGrow;  // true for the first visible scores
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2(m_used - m_g) : 1.f;  // 0 when m was -inf
+            if (need) {
+              m_used = m_g;
+              l *= alpha;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) acc2[k] = make_float2(acc2[k].x * alpha, acc2[k].y * alpha);
+            }
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+              if (j > 0) {  // the S commit this tile waited on covered every earlier PV
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                  uint32_t o[16];
+                  tmem_ld16(tmem + lane_off + o_col(t) + c * 16, o);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                  tmem_st16(tmem + lane_off + o_col(t) + c * 16, o);
+                }
+              }
+              if (g == 1) {  // group 0 of this tile was written with the old max
+                tmem_wait_st();
+#pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                  uint32_t pw[16];
+                  tmem_ld16(s_addr + c * 16, pw);
+                  tmem_wait_ld();
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) {
+                    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&pw[i]);
+                    pw[i] = pack_bf16(__low2float(v) * alpha, __high2float(v) * alpha);
+                  }
+                  tmem_st16(s_addr + c * 16, pw);
+                }
+              }
+            }
+          }
+          const bool live = m_used != NEG_INF;
+          const float2 sc2 = make_float2(scale_log2, scale_log2);
+          const float2 nm2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fma2(make_float2(__uint_as_float(sv2[h][2 * i]), __uint_as_float(sv2[h][2 * i + 1])),
+                                    sc2, nm2);
+              const float2 pp = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
+              acc2[i & 3] = add2(acc2[i & 3], pp);
+              pk[i] = pack_bf16(pp.x, pp.y);
+            }
+            tmem_st16(s_addr + g * 32 + h * 16, pk);
           }
         }
-        const bool live = m_used != -INFINITY;
-        float lsum = 0.f;
-        // pass 2 over S: P = 2^(s - m) as bf16 pairs into the first 64 S columns
-        // (all S words of a chunk are read before its P words are written)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sc[32], pk[16];
-          tmem_ld32(tmem + lane_off + s_col(t) + c * 32, sc);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = live ? ex2(score(sc[2 * i], c * 32 + 2 * i) - m_used) : 0.f;
-            const float p1 = live ? ex2(score(sc[2 * i + 1], c * 32 + 2 * i + 1) - m_used) : 0.f;
-            lsum += p0 + p1;
-            pk[i] = pack_bf16(p0, p1);
-          }
-          tmem_st16(tmem + lane_off + s_col(t) + c * 16, pk);
-        }
+        const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
+        const float lsum = st2.x + st2.y;
         l += lsum;
         tmem_wait_st();
         tc_fence_before();
