@@ -304,7 +304,9 @@ def attention_only(name: str, device, steps: int, warmup: int):
     wsb = sv.tree_attn_workspace_bytes(bf, B, N, Hq, Hkv, D, int(prefix.max()))
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
-    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()), workspace=ws)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()), workspace=ws,
+                                       dev_status=status)
     for _ in range(warmup):
         call()
     times = []
@@ -314,6 +316,8 @@ def attention_only(name: str, device, steps: int, warmup: int):
         e0.record(); call(); e1.record()
         e1.synchronize()
         times.append(e0.elapsed_time(e1) * 1e-3)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {sv.spec_status_string(int(status.item()))} ({int(status.item())})")
     t = statistics.median(times)
     nbytes = Hkv * D * 2 * 2 * (int(prefix.sum()) + B * N) + 2 * B * N * Hq * D * 2
     flops = 4 * N * (Hq // Hkv) * D * Hkv * (int(prefix.sum()) + B * N)

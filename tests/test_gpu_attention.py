@@ -19,7 +19,10 @@ pytestmark = pytest.mark.gpu
 TOL = {"bf16": (2e-2, 1e-2), "f32": (1e-4, 1e-4)}
 
 
-def _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=0, max_prefix=None):
+def _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=0, max_prefix=None, repeats=1):
+    """Runs tree_attn_verify ``repeats`` times (an L2 flush before each
+    repeat after the first, so cold-cache timing is exercised too); returns
+    the output and the device status of the last run."""
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     B, N = q.shape[0], q.shape[1]
     anc = np.broadcast_to(T.mask_words(T.depth_and_mask(shape.parents)[1]), (B, N)).copy()
@@ -27,11 +30,16 @@ def _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=0, max_prefix=None):
     ws_bytes = sv.tree_attn_workspace_bytes(tdt, B, N, w.hq, w.hkv, w.head_dim, max_prefix, num_splits)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda") if ws_bytes else None
     out = torch.full(q.shape, float("nan"), dtype=tdt, device="cuda")
-    st = zeros_i32(1)
-    sv.tree_attn_verify(dev(q, tdt), dev(kc, tdt), dev(vc, tdt), dev(kt, tdt), dev(vt, tdt), i32(prefix),
-                        dev(anc.view(np.int64)), out, max_prefix, num_splits=num_splits, workspace=ws,
-                        dev_status=st)
-    torch.cuda.synchronize()
+    args = (dev(q, tdt), dev(kc, tdt), dev(vc, tdt), dev(kt, tdt), dev(vt, tdt), i32(prefix),
+            dev(anc.view(np.int64)), out, max_prefix)
+    flush = torch.empty(64 << 20, dtype=torch.float32, device="cuda") if repeats > 1 else None
+    for k in range(repeats):
+        if k:
+            flush.fill_(float(k))
+        st = zeros_i32(1)
+        sv.tree_attn_verify(*args, num_splits=num_splits, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(host(st)[0]) == 0 or k == repeats - 1, f"run {k}: status {int(host(st)[0])}"
     return host(out), int(host(st)[0]), anc
 
 
@@ -122,7 +130,7 @@ def test_tree_attention_full_size_sampled(name):
     shape = synth.random_tree(w.seed, w.n_nodes, w.caps if w.caps else (10, 4, 3, 2, 2))
     prefix = synth.prefix_lengths(w)
     q, kc, vc, kt, vt = synth.attention_inputs(w, prefix, q_scale=2.0)
-    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt)
+    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt, repeats=3)
     assert status == 0
     assert np.isfinite(got).all()
     assert np.abs(got).max() <= max(np.abs(vc).max(), np.abs(vt).max()) * 1.01

@@ -5,28 +5,30 @@
 // attends to the shared prefix and to its ancestors-or-self; "Medusa,
 // explained", step 6: all nodes are scored in one pass.
 //
-// One CTA per (256 query rows, KV split, sequence x KV head).  Query row r
-// of a (sequence, KV head) is node r / G, head kvh*G + r % G, so the G heads
-// of a GQA group and all tree nodes share every K/V tile: the tile is read
-// from HBM once and feeds up to two 128-row query tiles.
+// Query row r of a (sequence, KV head) is node r / G, head kvh*G + r % G, so
+// the G heads of a GQA group and all tree nodes share every K/V tile.  One
+// CTA owns one 128-row query tile.  With more than 128 rows per KV head the
+// query tiles of a (sequence, KV head) run as a two-CTA cluster: each CTA
+// TMA-loads one 64-dim half of every K and V tile and multicasts it to both,
+// so each tile leaves HBM / L2 once and fills both CTAs' shared memory.
 //
 //   warp 0      TMA producer: Q once, then K and V tiles (128 keys x 128
-//               dims, 128-byte swizzle) through a two-stage ring each
+//               dims, 128-byte swizzle) through three-stage rings
 //   warp 1      TMEM allocation and the MMA issuer (one lane):
-//                 S_t = Q_t K^T        (A, B from shared memory)
-//                 O_t += P_t V         (A = P from TMEM, B = V, MN-major)
-//               issued in the order S0 S1 | PV0 S0' PV1 S1' | ... so the
-//               tensor core works on one query tile while the other's
-//               softmax runs
-//   warps 2-9   two softmax warpgroups, one per query tile; thread = row:
-//               S from TMEM, scale and mask (prefix range; ancestor bits on
-//               the tree tile), P = 2^(s - m) written back as bf16 into the
-//               S columns, one read of S per tile: the running max only
-//               moves when a 64-column group exceeds it by more than 2^64
-//               (then the sum, O and the tile's earlier P are rescaled in
-//               place), which keeps every value in float32 / bf16 range.
+//                 S(j) = Q K(j)^T     into TMEM buffer j % 2 (A, B in smem)
+//                 O   += P(j) V(j)    (A = P in TMEM, B = V, MN-major)
+//               S(j+2) is issued right after PV(j), so S for the next tile
+//               is ready while the softmax of the current one runs
+//   warps 2-9   softmax: two warps per TMEM lane quarter, one per half of the
+//               tile's columns; thread = (row, column half).  S from TMEM,
+//               scale and mask (prefix range; ancestor bits on the tree
+//               tile), row max shared by the pair through shared memory,
+//               P = 2^(s - m) written back as bf16 over the S columns.  The running max m
+//               moves only when a tile exceeds it by more than 2^64 (then the
+//               sum and O are rescaled in place); otherwise every P stays
+//               inside [0, 2^64], far within float32 / bf16 range.
 //
-// TMEM: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512) columns.
+// TMEM columns: S0 [0,128)  S1 [128,256)  O [256,384).
 // Every mbarrier wait is bounded; on a timeout the CTA reports
 // SPEC_DEV_TIMEOUT, waits (bounded) for its own loads and MMAs, frees TMEM
 // and returns.
@@ -42,27 +44,24 @@ using namespace sv::ptx;
 
 constexpr int kBN = 128;               // keys per K/V tile
 constexpr int kD = 128;                // head_dim
-constexpr int kStages = 2;             // K and V ring depth
-constexpr int kQT = 2;                 // 128-row query tiles per CTA
+constexpr int kStages = 3;             // K and V ring depth
 constexpr int kThreads = 320;
 constexpr uint32_t kTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 tile
 constexpr uint32_t kHalf = kTile / 2;      // 128 rows x 64 dims (one swizzle column)
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kGrow = 64.0f;         // log2 headroom above the running max before it is raised
 constexpr int kSms = 152;
+constexpr uint32_t kColO = 256;
 
 struct Bars {
   uint64_t q;
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s[kQT], p[kQT];
-  uint64_t done, drain;
+  uint64_t sfull[2], ofull[2], pfull[2], done, drain;
   uint32_t tmem;
   volatile int abort;
+  float xmax[2][128];  // per-row partial maxima (then sums) of the two softmax column halves
 };
-constexpr uint32_t kSmemBytes = (kQT + 2 * kStages) * kTile + sizeof(Bars) + 1024;
-
-__device__ __forceinline__ uint32_t s_col(int t) { return (uint32_t)t * 128u; }
-__device__ __forceinline__ uint32_t o_col(int t) { return 256u + (uint32_t)t * 128u; }
+constexpr uint32_t kSmemBytes = (1 + 2 * kStages) * kTile + sizeof(Bars) + 1024;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // V is MN-major (dims contiguous)
@@ -83,6 +82,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                    const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
@@ -93,17 +93,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = smem;
-  uint8_t *sK = sQ + kQT * kTile;
+  uint8_t *sK = sQ + kTile;
   uint8_t *sV = sK + kStages * kTile;
   Bars *bars = reinterpret_cast<Bars *>(sV + kStages * kTile);
 
   const int G = Hq / Hkv, R = N * G;
-  const int qg = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
+  const int qt = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
   const int b = bh / Hkv, kvh = bh % Hkv;
-  const int row0 = qg * (kQT * 128);
-  const int nq = min(kQT, (R - row0 + 127) / 128);
+  const int row0 = qt * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+  constexpr uint16_t kPair = (uint16_t)((1u << CL) - 1u);
 
+  // Both CTAs of a cluster share (sequence, split), so they take these
+  // early exits together, before any cluster-wide synchronisation.
   const int P = prefix_len[b];
   if (P < 0 || P > max_prefix || P > s_max) {
     if (threadIdx.x == 0) sv::report(status, SPEC_DEV_CAPACITY);
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool with_tree = split == splits - 1;
   const int n_tiles = n_pref + (with_tree ? 1 : 0);
   if (n_tiles == 0) {  // empty split: neutral partials (only when splits > 1)
-    for (int e = threadIdx.x; e < nq * 128; e += kThreads) {
+    for (int e = threadIdx.x; e < 128; e += kThreads) {
       const int rg = row0 + e;
       if (rg >= R) continue;
       float *w = ws + (((int64_t)bh * splits + split) * R + rg) * sv_partial_stride(kD);
@@ -131,12 +134,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->kfull[s], 1);
       mbar_init(&bars->vfull[s], 1);
-      mbar_init(&bars->kempty[s], 1);
-      mbar_init(&bars->vempty[s], 1);
+      mbar_init(&bars->kempty[s], CL);  // one MMA commit from each CTA of the cluster
+      mbar_init(&bars->vempty[s], CL);
     }
-    for (int t = 0; t < kQT; ++t) {
-      mbar_init(&bars->s[t], 1);
-      mbar_init(&bars->p[t], 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->sfull[i], 1);
+      mbar_init(&bars->ofull[i], 1);
+      // one P barrier per S buffer: the softmax may finish tiles j and j+1
+      // before the MMA warp observes tile j, but never tile j+2 (it needs
+      // S(j+2), issued after PV(j)), so neither barrier can run two phases
+      // ahead of its waiter
+      mbar_init(&bars->pfull[i], 256);
     }
     mbar_init(&bars->done, 1);
     mbar_init(&bars->drain, 1);
@@ -146,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(&bars->tmem, 512);
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // partner barriers initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
 
@@ -155,76 +164,87 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kc);
       tma_prefetch_desc(&tm_vc);
-      mbar_expect_tx(&bars->q, nq * kTile);
-      for (int t = 0; t < nq; ++t) {
-        const int node0 = b * N + (row0 + t * 128) / G;
-        tma_load_4d(sQ + t * kTile, &tm_q, 0, 0, kvh, node0, &bars->q);
-        tma_load_4d(sQ + t * kTile + kHalf, &tm_q, 64, 0, kvh, node0, &bars->q);
-      }
+      mbar_expect_tx(&bars->q, kTile);
+      const int node0 = b * N + row0 / G;
+      tma_load_4d(sQ, &tm_q, 0, 0, kvh, node0, &bars->q);
+      tma_load_4d(sQ + kHalf, &tm_q, 64, 0, kvh, node0, &bars->q);
       int nk = 0, nv = 0;  // tiles whose K / V loads were issued
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+      // tile j: the CUtensorMaps and row of its K and V
+      auto tile_src = [&](int j, const CUtensorMap *&mk, const CUtensorMap *&mv, int &row) {
         const bool tree = with_tree && j == n_tiles - 1;
-        const CUtensorMap *mk = tree ? &tm_kt : &tm_kc;
-        const CUtensorMap *mv = tree ? &tm_vt : &tm_vc;
-        const int row = tree ? bh * N : bh * s_max + k0 + j * kBN;
+        mk = tree ? &tm_kt : &tm_kc;
+        mv = tree ? &tm_vt : &tm_vc;
+        row = tree ? bh * N : bh * s_max + k0 + j * kBN;
+      };
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = (j / kStages) & 1;
+        const CUtensorMap *mk, *mv;
+        int row;
+        tile_src(j, mk, mv, row);
         if (!mbar_wait(&bars->kempty[s], ph ^ 1, kWaitLimit) || bars->abort) {
           give_up(bars, status);
           break;
         }
         mbar_expect_tx(&bars->kfull[s], kTile);
-        tma_load_2d(sK + s * kTile, mk, 0, row, &bars->kfull[s]);
-        tma_load_2d(sK + s * kTile + kHalf, mk, 64, row, &bars->kfull[s]);
+        if (CL > 1) {
+          tma_load_2d_mc(sK + s * kTile + rank * kHalf, mk, 64 * rank, row, &bars->kfull[s], kPair);
+        } else {
+          tma_load_2d(sK + s * kTile, mk, 0, row, &bars->kfull[s]);
+          tma_load_2d(sK + s * kTile + kHalf, mk, 64, row, &bars->kfull[s]);
+        }
         ++nk;
         if (!mbar_wait(&bars->vempty[s], ph ^ 1, kWaitLimit) || bars->abort) {
           give_up(bars, status);
           break;
         }
         mbar_expect_tx(&bars->vfull[s], kTile);
-        tma_load_2d(sV + s * kTile, mv, 0, row, &bars->vfull[s]);
-        tma_load_2d(sV + s * kTile + kHalf, mv, 64, row, &bars->vfull[s]);
+        if (CL > 1) {
+          tma_load_2d_mc(sV + s * kTile + rank * kHalf, mv, 64 * rank, row, &bars->vfull[s], kPair);
+        } else {
+          tma_load_2d(sV + s * kTile, mv, 0, row, &bars->vfull[s]);
+          tma_load_2d(sV + s * kTile + kHalf, mv, 64, row, &bars->vfull[s]);
+        }
         ++nv;
       }
-      if (bars->abort) {  // let this CTA's own copies land before it exits
+      if (bars->abort) {  // let the copies into this CTA land before it exits
         mbar_wait(&bars->q, 0, kWaitLimit);
-        for (int j = nk > 2 ? nk - 2 : 0; j < nk; ++j) mbar_wait(&bars->kfull[j & 1], (j >> 1) & 1, kWaitLimit);
-        for (int j = nv > 2 ? nv - 2 : 0; j < nv; ++j) mbar_wait(&bars->vfull[j & 1], (j >> 1) & 1, kWaitLimit);
+        for (int j = nk > kStages ? nk - kStages : 0; j < nk; ++j)
+          mbar_wait(&bars->kfull[j % kStages], (j / kStages) & 1, kWaitLimit);
+        for (int j = nv > kStages ? nv - kStages : 0; j < nv; ++j)
+          mbar_wait(&bars->vfull[j % kStages], (j / kStages) & 1, kWaitLimit);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
-    auto issue_s = [&](int t, int j) {
-      const uint32_t kb = ka + (uint32_t)(j & 1) * kTile, qb = qa + (uint32_t)t * kTile;
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
-        mma_ss(tmem + s_col(t), smem_desc_sw128(qb + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-               kIdescQK, kk > 0);
-      }
-      mma_commit(&bars->s[t]);
+    auto release = [&](uint64_t *bar) {
+      if (CL > 1) mma_commit_mc(bar, kPair);
+      else mma_commit(bar);
     };
-    auto issue_pv = [&](int t, int j) {
-      const uint32_t vb = va + (uint32_t)(j & 1) * kTile;
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_ts(tmem + o_col(t), tmem + s_col(t) + (uint32_t)kk * 8u,
-               smem_desc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024), kIdescPV, (j > 0 || kk > 0));
-    };
-    bool ok = warp_wait(&bars->q, 0) && warp_wait(&bars->kfull[0], 0);
-    if (ok) {
+    // S(j) = Q K(j)^T into S buffer j % 2
+    auto issue_s = [&](int j) -> bool {
+      const int s = j % kStages;
+      if (!warp_wait(&bars->kfull[s], (j / kStages) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
-        for (int t = 0; t < nq; ++t) issue_s(t, 0);
-        mma_commit(&bars->kempty[0]);
+        const uint32_t kb = ka + (uint32_t)s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kHalf + (uint32_t)(kk & 3) * 32u;
+          mma_ss(tmem + (uint32_t)(j & 1) * 128u, smem_desc_sw128(qa + off, 16, 1024),
+                 smem_desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0);
+        }
+        mma_commit(&bars->sfull[j & 1]);
+        release(&bars->kempty[s]);
       }
       __syncwarp();
-    }
+      return true;
+    };
+    bool ok = warp_wait(&bars->q, 0) && issue_s(0) && (n_tiles < 2 || issue_s(1));
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!(ok = warp_wait(&bars->vfull[s], ph))) break;
+      const int s = j % kStages;
+      if (!(ok = warp_wait(&bars->vfull[s], (j / kStages) & 1))) break;
       // the last prefix tile of a split may run past the split's keys: zero
       // those V rows so that stale cache rows (possibly not finite) never
       // meet the zero probabilities of masked keys
@@ -240,26 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
       }
-      if (!(ok = warp_wait(&bars->p[0], j & 1))) break;
+      if (!(ok = warp_wait(&bars->pfull[j & 1], (j >> 1) & 1))) break;
       tc_fence_after();
-      if (lane == 0) issue_pv(0, j);
-      const bool more = j + 1 < n_tiles;
-      if (more) {
-        if (!(ok = warp_wait(&bars->kfull[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
-        tc_fence_after();
-        if (lane == 0) issue_s(0, j + 1);
-      }
-      if (nq > 1) {
-        if (!(ok = warp_wait(&bars->p[1], j & 1))) break;
-        tc_fence_after();
-        if (lane == 0) issue_pv(1, j);
-      }
-      if (lane == 0) mma_commit(&bars->vempty[s]);
-      if (more && lane == 0) {
-        if (nq > 1) issue_s(1, j + 1);
-        mma_commit(&bars->kempty[(j + 1) & 1]);
+      if (lane == 0) {
+        const uint32_t vb = va + (uint32_t)s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + kColO, tmem + (uint32_t)(j & 1) * 128u + (uint32_t)kk * 8u,
+                 smem_desc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024), kIdescPV, (j > 0 || kk > 0));
+        mma_commit(&bars->ofull[j & 1]);
+        release(&bars->vempty[s]);
       }
       __syncwarp();
+      if (j + 2 < n_tiles && !(ok = issue_s(j + 2))) break;
     }
     if (ok) {
       if (lane == 0) mma_commit(&bars->done);
@@ -271,176 +284,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    // Warps 2-9: warp w reads TMEM lane quarter w % 4 (32 rows) and column
+    // half h = (w - 2) / 4 of each tile; the two warps of a quarter exchange
+    // their partial row maxima through shared memory (named barrier 1 + q).
+    const int quarter = warp & 3;
+    const int h = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int rg = row0 + t * 128 + r;
+    const uint32_t pair_bar = 1u + (uint32_t)quarter;
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    const int rg = row0 + r;
     const bool row_ok = rg < R;
     const int node = rg / G;
     const uint64_t amask = row_ok ? anc[(int64_t)b * N + node] : 0ull;
-    if (t < nq) {
-      float m_used = -INFINITY, l = 0.f;
-      bool ok = true;
-      for (int j = 0; j < n_tiles; ++j) {
-        if (!warp_wait(&bars->s[t], j & 1) || __any_sync(0xffffffffu, bars->abort != 0)) {
-          ok = false;
-          break;
-        }
+    const float NEG_INF = -INFINITY;
+    float m_used = NEG_INF, l = 0.f;  // l: this warp's half of the row sum
+    bool ok = true;
+    // A failed wait (timeout) or an abort turns the rest of the loop into a
+    // no-op that still passes every pair barrier, so the two warps of a pair
+    // always execute the same barriers.
+    for (int j = 0; j < n_tiles; ++j) {
+      if (ok && (!warp_wait(&bars->sfull[j & 1], (j >> 1) & 1) || __any_sync(0xffffffffu, bars->abort != 0)))
+        ok = false;
+      const uint32_t s_addr = tmem + lane_off + (uint32_t)(j & 1) * 128u;
+      uint32_t sv[2][32];
+      if (ok) {
         tc_fence_after();
-        const bool tree = with_tree && j == n_tiles - 1;
-        const int nvalid = tree ? N : min(kBN, k1 - (k0 + j * kBN));
-        const bool masked = tree || nvalid < kBN;  // full prefix tiles need no mask
-        // column `col` visible to this row (tree: col < N <= 64)
-        auto visible = [&](int col) {
-          return col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));
-        };
-        const float NEG_INF = -INFINITY;
-        const uint32_t s_addr = tmem + lane_off + s_col(t);
-        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
-        // Two groups of 64 S columns; each is read into registers, then P =
-        // 2^(s * scale - m) goes as bf16 pairs into 32 P columns (P columns
-        // of group g only cover S columns already read).  The running max m
-        // moves only when a group's max exceeds it by more than 2^kGrow (the
-        // first visible scores, or inputs of extraordinary range): the row
-        // sum, O and the group already written are then rescaled in place.
-        // Otherwise every P stays within [0, 2^kGrow], far inside float32 and
-        // bf16 range, and the normalisation by the row sum is unchanged.
+        tmem_ld32(s_addr + h * 64, sv[0]);
+        tmem_ld32(s_addr + h * 64 + 32, sv[1]);
+        tmem_wait_ld();
+      } else {
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint32_t sv2[2][32];
-          tmem_ld32(s_addr + g * 64, sv2[0]);
-          tmem_ld32(s_addr + g * 64 + 32, sv2[1]);
+        for (int i = 0; i < 32; ++i) sv[0][i] = sv[1][i] = __float_as_uint(NEG_INF);
+      }
+      const bool tree = with_tree && j == n_tiles - 1;
+      const int nvalid = tree ? N : min(kBN, k1 - (k0 + j * kBN));
+      if (tree || nvalid < kBN) {  // full prefix tiles need no mask
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int col = h * 64 + i;
+          const bool vis = col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));  // tree: col < N <= 64
+          if (!vis) sv[i >> 5][i & 31] = __float_as_uint(NEG_INF);
+        }
+      }
+      float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                          __uint_as_float(sv[i >> 4][(2 * i + 1) & 31]));
+      // both warps have read their S columns once they pass this barrier, so
+      // P may then overwrite the first 64 S columns
+      bars->xmax[h][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      pair_sync();
+      const float m_t = fmaxf(bars->xmax[0][r], bars->xmax[1][r]) * scale_log2;
+      pair_sync();  // both maxima read before the next tile overwrites them
+      const bool need = m_t > m_used + kGrow;  // true for the first visible scores
+      if (ok && __any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(m_used - m_t) : 1.f;  // 0 when m was -inf
+        if (need) {
+          m_used = m_t;
+          l *= alpha;
+        }
+        // O holds PV(j-1) once that MMA completes: wait for it, then scale
+        // this warp's half of the O columns
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
+            (ok = warp_wait(&bars->ofull[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[16];
+            const uint32_t oa = tmem + lane_off + kColO + h * 64 + c * 16;
+            tmem_ld16(oa, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(oa, o);
+          }
+        }
+      }
+      if (!ok) continue;
+      const bool live = m_used != NEG_INF;
+      const float2 sc2 = make_float2(scale_log2, scale_log2);
+      const float2 nm2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
+      float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 x =
+              fma2(make_float2(__uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1])), sc2, nm2);
+          const float2 pp = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
+          acc2[i & 3] = add2(acc2[i & 3], pp);
+          pk[i] = pack_bf16(pp.x, pp.y);
+        }
+        tmem_st16(s_addr + h * 32 + c * 16, pk);  // P for S columns [64h + 32c, +32)
+      }
+      const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
+      l += st2.x + st2.y;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->pfull[j & 1]);
+    }
+    // full row sum: both halves (same running max on both warps)
+    bars->xmax[h][r] = l;
+    pair_sync();
+    const float l_row = bars->xmax[0][r] + bars->xmax[1][r];
+    if (ok && !warp_wait(&bars->done, 0)) ok = false;
+    if (ok && !__any_sync(0xffffffffu, bars->abort != 0)) {
+      tc_fence_after();
+      const int g = rg % G;
+      if (splits == 1) {
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        __nv_bfloat16 *o = out + (((int64_t)b * N + node) * Hq + kvh * G + g) * kD + h * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_off + kColO + h * 64 + c * 32, ov);
           tmem_wait_ld();
-          float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (masked) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (!visible(g * 64 + h * 32 + i)) sv2[h][i] = __float_as_uint(NEG_INF);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv2[h][2 * i]), __uint_as_float(sv2[h][2 * i + 1]));
-          }
-          const float m_g = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
-          const bool need = m_g > m_used + kGrow;  // true for the first visible scores
-          if (__any_sync(0xffffffffu, need)) {
-            const float alpha = need ? ex2(m_used - m_g) : 1.f;  // 0 when m was -inf
-            if (need) {
-              m_used = m_g;
-              l *= alpha;
-#pragma unroll
-              for (int k = 0; k < 4; ++k) acc2[k] = make_float2(acc2[k].x * alpha, acc2[k].y * alpha);
-            }
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {
-              if (j > 0) {  // the S commit this tile waited on covered every earlier PV
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                  uint32_t o[16];
-                  tmem_ld16(tmem + lane_off + o_col(t) + c * 16, o);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                  tmem_st16(tmem + lane_off + o_col(t) + c * 16, o);
-                }
-              }
-              if (g == 1) {  // group 0 of this tile was written with the old max
-                tmem_wait_st();
-#pragma unroll 1
-                for (int c = 0; c < 2; ++c) {
-                  uint32_t pw[16];
-                  tmem_ld16(s_addr + c * 16, pw);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int i = 0; i < 16; ++i) {
-                    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&pw[i]);
-                    pw[i] = pack_bf16(__low2float(v) * alpha, __high2float(v) * alpha);
-                  }
-                  tmem_st16(s_addr + c * 16, pw);
-                }
-              }
-            }
-          }
-          const bool live = m_used != NEG_INF;
-          const float2 sc2 = make_float2(scale_log2, scale_log2);
-          const float2 nm2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float2 x = fma2(make_float2(__uint_as_float(sv2[h][2 * i]), __uint_as_float(sv2[h][2 * i + 1])),
-                                    sc2, nm2);
-              const float2 pp = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
-              acc2[i & 3] = add2(acc2[i & 3], pp);
-              pk[i] = pack_bf16(pp.x, pp.y);
-            }
-            tmem_st16(s_addr + g * 32 + h * 16, pk);
-          }
-        }
-        const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
-        const float lsum = st2.x + st2.y;
-        l += lsum;
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars->p[t]);
-      }
-      if (ok && !warp_wait(&bars->done, 0)) ok = false;
-      if (ok && !__any_sync(0xffffffffu, bars->abort != 0)) {
-        tc_fence_after();
-        const int g = rg % G;
-        if (splits == 1) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          __nv_bfloat16 *o = out + (((int64_t)b * N + node) * Hq + kvh * G + g) * kD;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tmem + lane_off + o_col(t) + c * 32, ov);
-            tmem_wait_ld();
-            if (row_ok) {
-              uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                uint4 v;
-                v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-                v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-                v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-                v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-                dst[q4] = v;
-              }
-            }
-          }
-        } else {
-          float *w = ws + (((int64_t)bh * splits + split) * R + rg) * sv_partial_stride(kD);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tmem + lane_off + o_col(t) + c * 32, ov);
-            tmem_wait_ld();
-            if (row_ok) {
-              float4 *dst = reinterpret_cast<float4 *>(w + c * 32);
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                dst[q4] = make_float4(__uint_as_float(ov[4 * q4]), __uint_as_float(ov[4 * q4 + 1]),
-                                      __uint_as_float(ov[4 * q4 + 2]), __uint_as_float(ov[4 * q4 + 3]));
-            }
-          }
           if (row_ok) {
-            w[kD] = m_used;
-            w[kD + 1] = l;
+            uint4 *dst = reinterpret_cast<uint4 *>(o + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint4 v;
+              v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+              v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+              v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+              v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+              dst[q4] = v;
+            }
           }
         }
-      } else if (!ok) {
-        give_up(bars, status);
+      } else {
+        float *w = ws + (((int64_t)bh * splits + split) * R + rg) * sv_partial_stride(kD);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tmem + lane_off + kColO + h * 64 + c * 32, ov);
+          tmem_wait_ld();
+          if (row_ok) {
+            float4 *dst = reinterpret_cast<float4 *>(w + h * 64 + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(ov[4 * q4]), __uint_as_float(ov[4 * q4 + 1]),
+                                    __uint_as_float(ov[4 * q4 + 2]), __uint_as_float(ov[4 * q4 + 3]));
+          }
+        }
+        if (row_ok && h == 0) {
+          w[kD] = m_used;
+          w[kD + 1] = l_row;
+        }
       }
+    } else if (!ok) {
+      give_up(bars, status);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  // the partner's multicast copies into this CTA and its commits to this
+  // CTA's barriers are complete once it has passed its own __syncthreads
+  if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -480,6 +484,38 @@ int make_map(CUtensorMap *m, const void *base, cuuint32_t rank, const cuuint64_t
   return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+template <int CL>
+int launch_tc(dim3 grid, cudaStream_t stream, const CUtensorMap &mq, const CUtensorMap &mkc, const CUtensorMap &mvc,
+              const CUtensorMap &mkt, const CUtensorMap &mvt, const int32_t *prefix_len, const uint64_t *anc,
+              void *out, void *ws, const SvAttnShape &s, const SvAttnPlan &p, float scale, int32_t *status) {
+  if (cudaFuncSetAttribute(attn_tc_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, attn_tc_kernel<CL>, mq, mkc, mvc, mkt, mvt, prefix_len, anc, (__nv_bfloat16 *)out, (float *)ws,
+      s.n_nodes, s.hq, s.hkv, s.s_max, s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+// Query tiles per (sequence, KV head): pairs run as two-CTA clusters.
+inline int tc_cluster(int R) { return R > 128 ? 2 : 1; }
+inline int tc_qtiles(int R) {
+  const int t = (R + 127) / 128;
+  return tc_cluster(R) == 2 ? (t + 1) / 2 * 2 : t;
+}
+
 }  // namespace
 
 SvAttnPlan sv_attn_tc_plan(const SvAttnShape &s, int num_splits, bool *ok) {
@@ -489,10 +525,27 @@ SvAttnPlan sv_attn_tc_plan(const SvAttnShape &s, int num_splits, bool *ok) {
   const int G = s.hq / s.hkv;
   if (G > 128 || (128 % G) != 0) return p;
   const int R = s.n_nodes * G;
-  const int qgroups = (R + kQT * 128 - 1) / (kQT * 128);
-  const int base = qgroups * s.batch * s.hkv;
+  const int base = tc_qtiles(R) * s.batch * s.hkv;  // CTAs per split
   const int max_useful = s.max_prefix > 0 ? (s.max_prefix + kBN - 1) / kBN : 1;
-  int splits = num_splits > 0 ? num_splits : (2 * kSms + base - 1) / base;
+  int splits = num_splits;
+  if (splits <= 0) {
+    // Cost in bytes moved at full bandwidth: waves (one CTA per SM) times
+    // the tiles a CTA streams (its prefix chunk, the tree tile, and two
+    // tiles' worth of fixed set-up), plus writing and re-reading the split
+    // partials and a combine launch.
+    const double tile = (double)kBN * kD * 2 * 2;
+    double best = 0.0;
+    for (int c = 1; c <= 64 && c <= max_useful; ++c) {
+      const double waves = (double)((base * c + kSms - 1) / kSms);
+      const double tiles = (double)((max_useful + c - 1) / c) + 3.0;
+      double cost = waves * tiles * tile * kSms;
+      if (c > 1) cost += 2.0 * s.batch * s.hkv * c * R * sv_partial_stride(kD) * 4.0 + 20e6;
+      if (c == 1 || cost < best) {
+        best = cost;
+        splits = c;
+      }
+    }
+  }
   if (splits > max_useful) splits = max_useful;
   if (splits > 64) splits = 64;
   if (splits < 1) splits = 1;
@@ -534,13 +587,9 @@ int sv_attn_tc(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const v
     if (make_map(&mkt, kt, 2, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
     if (make_map(&mvt, vt, 2, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-      cudaSuccess)
-    return SPEC_ERR_CUDA;
   const int R = s.n_nodes * G;
-  dim3 grid((R + kQT * 128 - 1) / (kQT * 128), p.splits, s.batch * s.hkv);
-  attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      mq, mkc, mvc, mkt, mvt, prefix_len, anc, (__nv_bfloat16 *)out, (float *)ws, s.n_nodes, s.hq, s.hkv, s.s_max,
-      s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status);
-  return sv_launch_status();
+  const dim3 grid(tc_qtiles(R), p.splits, s.batch * s.hkv);
+  return tc_cluster(R) == 2
+             ? launch_tc<2>(grid, stream, mq, mkc, mvc, mkt, mvt, prefix_len, anc, out, ws, s, p, scale, status)
+             : launch_tc<1>(grid, stream, mq, mkc, mvc, mkt, mvt, prefix_len, anc, out, ws, s, p, scale, status);
 }
