@@ -270,10 +270,11 @@ int tree_attn_verify_noalloc(const void *q, const void *k_cache, const void *v_c
  *   hid    [rows, hidden] bf16
  *   w      [vocab, hidden] bf16 (LM head weight)
  *   logits [rows, vocab]   f32 out = hid . w^T (float32 accumulation)
- * Requires hidden % 64 == 0.
+ * Requires hidden % 64 == 0.  Runs on the tensor cores; a device-side
+ * timeout (never expected) sets SPEC_DEV_TIMEOUT in dev_status (optional).
  * ------------------------------------------------------------------ */
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-                 spec_stream_t stream);
+                 int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
  * spec_accept -- accept the longest target-agreeing path.

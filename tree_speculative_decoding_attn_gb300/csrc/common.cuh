@@ -13,6 +13,10 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+__device__ __forceinline__ uint32_t ptx_smem(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 

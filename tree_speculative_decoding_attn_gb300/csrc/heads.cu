@@ -1,10 +1,8 @@
-// Medusa residual heads and the LM head.
+// Medusa residual heads.
 //
 // "Medusa, explained", procedure step 1: head k computes
 // W2_k (SiLU(W1_k h) + h); "Medusa and EAGLE ... explained", section
 // "Implementation sketch": the first linear layer may carry a bias.
-// "Medusa, explained", step 6: one pass of the target scores every node
-// (the LM head over the tree's hidden states).
 //
 // At the heads' batch (one hidden state per sequence) both projections are
 // matrix-vector products that stream their weights once: 2 flops per 2-byte
@@ -125,60 +123,6 @@ int launch_gemv(int batch, const __nv_bfloat16 *W, const TX *x, int64_t xhs, int
   return sv_launch_status();
 }
 
-// ---------------------------------------------------------------------------
-// LM head on CUDA cores: logits[r, v] = sum_i hid[r, i] W[v, i].
-// 64 x 64 output tile per CTA, 4 x 4 per thread, K staged 32 at a time.
-// ---------------------------------------------------------------------------
-constexpr int kTM = 64, kTN = 64, kTK = 32;
-
-__global__ void __launch_bounds__(256)
-    lm_head_simt_kernel(const __nv_bfloat16 *__restrict__ A, const __nv_bfloat16 *__restrict__ W,
-                        int M, int N, int K, float *__restrict__ C) {
-  __shared__ float sA[kTK][kTM + 4];
-  __shared__ float sB[kTK][kTN + 4];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-  const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += kTK) {
-    // 64 rows x 32 k of A and W: 256 threads x 8 elements each
-    {
-      const int r = threadIdx.x / 4, c = (threadIdx.x % 4) * 8;
-      float f[8];
-      if (m0 + r < M) sv::bf16x8_to_f32(*reinterpret_cast<const uint4 *>(A + (int64_t)(m0 + r) * K + k0 + c), f);
-      else for (int j = 0; j < 8; ++j) f[j] = 0.f;
-      for (int j = 0; j < 8; ++j) sA[c + j][r] = f[j];
-      if (n0 + r < N) sv::bf16x8_to_f32(sv::ldg_stream(W + (int64_t)(n0 + r) * K + k0 + c), f);
-      else for (int j = 0; j < 8; ++j) f[j] = 0.f;
-      for (int j = 0; j < 8; ++j) sB[c + j][r] = f[j];
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kTK; ++kk) {
-      float a[4], bw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        a[i] = sA[kk][ty * 4 + i];
-        bw[i] = sB[kk][tx * 4 + i];
-      }
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bw[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = m0 + ty * 4 + i;
-    if (r >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = n0 + tx * 4 + j;
-      if (c < N) C[(int64_t)r * N + c] = acc[i][j];
-    }
-  }
-}
-
 }  // namespace
 
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
@@ -194,13 +138,4 @@ int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w
   return launch_gemv<float, kPlain>(batch, (const __nv_bfloat16 *)w2, z, hidden,
                                     (int64_t)n_heads * hidden, n_heads * vocab, vocab, hidden,
                                     logits, (int64_t)n_heads * vocab, nullptr, nullptr, 0, stream);
-}
-
-int sv_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-               cudaStream_t stream) {
-  dim3 grid((vocab + kTN - 1) / kTN, (rows + kTM - 1) / kTM);
-  lm_head_simt_kernel<<<grid, 256, 0, stream>>>((const __nv_bfloat16 *)hid,
-                                                (const __nv_bfloat16 *)w, rows, vocab, hidden,
-                                                logits);
-  return sv_launch_status();
 }

@@ -45,8 +45,8 @@ int sv_attn_combine(const SvAttnShape &s, const SvAttnPlan &p, const void *ws, v
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
                     int n_heads, int hidden, int vocab, float *z, float *logits,
                     cudaStream_t stream);
-int sv_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-               cudaStream_t stream);
+int sv_lm_head_tc(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
+                  int32_t *status, cudaStream_t stream);
 int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
             int32_t *idx, float *val, cudaStream_t stream);
 int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,

@@ -152,11 +152,11 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache, co
 }
 
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-                 spec_stream_t stream) {
+                 int32_t *dev_status, spec_stream_t stream) {
   if (!hid || !w || !logits) return SPEC_ERR_INVALID_ARG;
   if (rows < 1 || vocab < 1 || hidden < 64 || hidden % 64) return SPEC_ERR_INVALID_ARG;
   if (!aligned16(hid) || !aligned16(w)) return SPEC_ERR_INVALID_ARG;
-  return sv_lm_head(hid, w, rows, hidden, vocab, logits, cs(stream));
+  return sv_lm_head_tc(hid, w, rows, hidden, vocab, logits, dev_status, cs(stream));
 }
 
 int spec_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,

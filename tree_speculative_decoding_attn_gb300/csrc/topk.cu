@@ -81,22 +81,58 @@ __device__ void merge_top(const unsigned long long (&best)[S], unsigned long lon
   }
 }
 
+// Top-s of one row by a cluster of kCluster CTAs: CTA c ranks the c-th slice
+// of the row, then CTA 0 gathers the kCluster candidate lists through
+// distributed shared memory and keeps the s best (keys are unique, so a
+// key's rank is the number of larger keys).
+constexpr int kCluster = 8;
+
+__device__ __forceinline__ uint64_t ld_cluster_u64(const void *local, uint32_t cta) {
+  uint32_t remote;
+  uint64_t v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(sv::ptx_smem(local)), "r"(cta));
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 template <typename T, int S>
 __global__ void __launch_bounds__(kThreads)
-    topk_kernel(const T *__restrict__ rows, int row_len, int64_t row_stride, int s,
-                int32_t *__restrict__ idx, float *__restrict__ val) {
+    topk_cluster_kernel(const T *__restrict__ rows, int row_len, int64_t row_stride, int s,
+                        int32_t *__restrict__ idx, float *__restrict__ val) {
   __shared__ unsigned long long lists[kThreads * S];
   __shared__ unsigned long long top[32];
+  __shared__ unsigned long long all[kCluster * S];
+  const uint32_t cta = blockIdx.x;  // rank within the cluster (cluster spans x)
+  const int slice = ((row_len + kCluster - 1) / kCluster + 7) / 8 * 8;
+  const int lo = min(row_len, (int)cta * slice), hi = min(row_len, lo + slice);
   unsigned long long best[S];
 #pragma unroll
   for (int j = 0; j < S; ++j) best[j] = 0ull;
-  const T *row = rows + (int64_t)blockIdx.x * row_stride;
-  for_row(row, row_len, [&](int x, float v) { insert_key<S>(best, sv::rank_key(v, (uint32_t)x)); });
-  merge_top<S>(best, lists, s, top);
-  if (threadIdx.x < s) {
-    idx[(int64_t)blockIdx.x * s + threadIdx.x] = (int32_t)sv::key_index(top[threadIdx.x]);
-    if (val) val[(int64_t)blockIdx.x * s + threadIdx.x] = sv::key_value(top[threadIdx.x]);
+  const T *row = rows + (int64_t)blockIdx.y * row_stride;
+  if ((lo % (16 / (int)sizeof(T))) == 0) {
+    for_row(row + lo, hi - lo, [&](int x, float v) { insert_key<S>(best, sv::rank_key(v, (uint32_t)(lo + x))); });
+  } else {
+    for (int x = lo + threadIdx.x; x < hi; x += kThreads) insert_key<S>(best, sv::rank_key(sv::to_f32(row[x]), (uint32_t)x));
   }
+  merge_top<S>(best, lists, s, top);  // top[0..s) of this slice (0 = empty)
+  cluster_barrier();
+  if (cta == 0) {
+    for (int e = threadIdx.x; e < kCluster * s; e += kThreads) all[e] = ld_cluster_u64(&top[e % s], e / s);
+    __syncthreads();
+    for (int e = threadIdx.x; e < kCluster * s; e += kThreads) {
+      const unsigned long long k = all[e];
+      int rank = 0;
+      for (int f = 0; f < kCluster * s; ++f) rank += all[f] > k;
+      if (k != 0ull && rank < s) {
+        idx[(int64_t)blockIdx.y * s + rank] = (int32_t)sv::key_index(k);
+        if (val) val[(int64_t)blockIdx.y * s + rank] = sv::key_value(k);
+      }
+    }
+  }
+  cluster_barrier();  // remote reads done before any CTA of the cluster exits
 }
 
 // ---------------------------------------------------------------------------
@@ -194,10 +230,23 @@ __global__ void __launch_bounds__(1024)
 }
 
 template <typename T, int S>
-int launch_topk(const void *rows, int n_rows, int row_len, int row_stride, int s, int32_t *idx,
-                float *val, cudaStream_t stream) {
-  topk_kernel<T, S><<<n_rows, kThreads, 0, stream>>>((const T *)rows, row_len, row_stride, s, idx, val);
-  return sv_launch_status();
+int launch_topk(const void *rows, int n_rows, int row_len, int row_stride, int s, int32_t *idx, float *val,
+                cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster, n_rows);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_cluster_kernel<T, S>, (const T *)rows, row_len, (int64_t)row_stride, s,
+                            idx, val) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
 }
 
 }  // namespace

@@ -40,7 +40,7 @@ _SIGS = {
                           _vp, _sz, _vp, _vp], _i),
     "tree_attn_verify_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                   _i, _vp, _vp], _i),
-    "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp], _i),
+    "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
     "spec_accept": ([_i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp, _vp,
                      _vp, _vp], _i),
     "kv_commit": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
@@ -209,11 +209,11 @@ def tree_attn_verify_noalloc(q, k_cache, v_cache, k_tree, v_tree, prefix_len, an
         _stream()))
 
 
-def spec_lm_head(hid, w, logits):
+def spec_lm_head(hid, w, logits, dev_status=None):
     R, d = hid.shape
     V = w.shape[0]
     _want(hid, torch.bfloat16); _want(w, torch.bfloat16); _want(logits, torch.float32)
-    _check("spec_lm_head", load().spec_lm_head(_p(hid), _p(w), R, d, V, _p(logits), _stream()))
+    _check("spec_lm_head", load().spec_lm_head(_p(hid), _p(w), R, d, V, _p(logits), _p(dev_status), _stream()))
 
 
 def spec_accept(mode, logits, tok, parents, first_child, next_sibling, acc_len, acc_path, bonus,
