@@ -27,6 +27,12 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+if "reference" in sys.argv and "--impl" in sys.argv:
+    # the CPU oracle runs on one core; pin the numeric libraries before
+    # numpy loads them so the reported core count is the one used
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
 import numpy as np  # noqa: E402
 
 DEFAULT = "vicuna7b_medusa"
@@ -329,95 +335,108 @@ def attention_only(name: str, device, steps: int, warmup: int):
 # ----------------------------------------------------------------------------
 # CPU oracle (reference arm and cpu_baseline leg)
 # ----------------------------------------------------------------------------
-def oracle_step_seconds(name: str, budget_s: float = 4.0):
-    """Time one verify step of the CPU oracle on a bounded sample of the
-    workload, extrapolated to the whole step by the sampled fraction of each
-    stage.  Returns (seconds per step, sample description)."""
-    from oracle import accept as ACC
-    from oracle import attention as A
-    from oracle import commit as COM
-    from oracle import heads as H
-    from oracle import tree as T
-    from tree_speculative_decoding_attn_gb300 import synth
-    w = synth.WORKLOADS[name]
-    B, N, Hq, Hkv, D, V = w.batch, w.n_nodes, w.hq, w.hkv, w.head_dim, w.vocab
-    prefix = synth.prefix_lengths(w)
-    parts, desc = {}, []
-    clock = time.perf_counter
-    # tree
-    if w.tree == "dynamic":
-        dk = w.dynamic
-        par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
-        t0 = clock()
-        trees = [T.rerank_dynamic(par[b], tok[b], conf[b], N, int(prefix[b])) for b in range(B)]
-        parts["build_tree"] = clock() - t0
-        tree = {k: np.stack([t[k] for t in trees]) for k in ("tok", "parent", "first_child", "next_sibling", "mask")}
-        levels = int(tree["parent"].shape[1])
-    else:
-        shape = synth.tree_shape(w)
-        s = w.medusa["topk"] if w.medusa else (max(w.caps) if w.caps else 2)
-        cand = synth.candidate_tokens(w.seed, B, shape.n_levels, s, V)
+class OracleStep:
+    """One verify step of the CPU oracle on a bounded sample of a workload.
+
+    Inputs are drawn once (untimed); ``step()`` times each stage on its
+    sample and extrapolates it to the whole batch by the sampled fraction
+    (vocabulary rows/columns for the head and LM-head products, sequences x
+    query heads for attention, sequences for acceptance and commit)."""
+
+    def __init__(self, name: str):
+        from oracle import tree as T
+        from tree_speculative_decoding_attn_gb300 import synth
+        self.w = w = synth.WORKLOADS[name]
+        B, N, Hq, V = w.batch, w.n_nodes, w.hq, w.vocab
+        self.prefix = synth.prefix_lengths(w)
+        self.seqs = list(range(min(B, 2)))
+        self.heads = list(range(0, Hq, max(1, Hq // 4)))[:4]
+        desc = []
+        if w.tree == "dynamic":
+            dk = w.dynamic
+            self.pool = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
+        else:
+            self.shape = synth.tree_shape(w)
+            self.s = w.medusa["topk"] if w.medusa else (max(w.caps) if w.caps else 2)
+            self.cand = synth.candidate_tokens(w.seed, B, self.shape.n_levels, self.s, V)
+            self.root = synth.root_tokens(w)
         if w.medusa:
             m = w.medusa
             h, w1, w2, wlm = synth.medusa_inputs(w)
-            rows = np.arange(0, V, max(1, V // 1024))
+            self.rows = np.arange(0, V, max(1, V // 1024))
+            self.h, self.w1, self.w2s, self.wlms = h, w1, np.ascontiguousarray(w2[:, self.rows]), \
+                np.ascontiguousarray(wlm[self.rows])
+            del w2, wlm
+            self.head_logits = synth.gaussian(synth.stream(0, "x"), (B * m["heads"], V), 1.0, False)
+            self.hid = synth.gaussian(synth.stream(w.seed, "tree_hidden"), (B * N, m["hidden"]), 1.0, True)
+            desc.append(f"heads and LM head on {len(self.rows)} of {V} vocabulary rows")
+        sub = [int(self.prefix[b]) for b in self.seqs]
+        self.att = synth.attention_inputs(w, np.array(sub, np.int32), batch=len(self.seqs))
+        self.sub_prefix = np.array(sub, np.int32)
+        self.logits = synth.target_logits(w.seed, len(self.seqs), N, V, w.logit_std, w.dtype == "bf16")
+        desc.append(f"attention on {len(self.seqs)} of {B} sequences x {len(self.heads)} of {Hq} heads")
+        desc.append(f"acceptance and commit on {len(self.seqs)} of {B} sequences")
+        self.sample = "; ".join(desc)
+
+    def step(self):
+        """Returns (extrapolated seconds for one step, per-stage seconds)."""
+        from oracle import accept as ACC
+        from oracle import attention as A
+        from oracle import commit as COM
+        from oracle import heads as H
+        from oracle import tree as T
+        w = self.w
+        B, N, Hq, V = w.batch, w.n_nodes, w.hq, w.vocab
+        clock = time.perf_counter
+        parts = {}
+        if w.tree == "dynamic":
+            par, tok, conf = self.pool
             t0 = clock()
-            _, hl = H.medusa_heads(h, w1, None, w2[:, rows])
-            t_h = clock() - t0
-            frac = (m["heads"] * m["hidden"] ** 2 + m["heads"] * len(rows) * m["hidden"]) / \
-                   (m["heads"] * m["hidden"] ** 2 + m["heads"] * V * m["hidden"])
-            parts["medusa_heads"] = t_h / frac
-            desc.append(f"heads on {len(rows)} of {V} vocabulary rows")
-            full_logits = synth.gaussian(synth.stream(0, "x"), (B * m["heads"], V), 1.0, False)
+            trees = [T.rerank_dynamic(par[b], tok[b], conf[b], N, int(self.prefix[b])) for b in range(B)]
+            parts["build_tree"] = clock() - t0
+            tree = {k: np.stack([t[k] for t in trees]) for k in ("tok", "parent", "first_child", "next_sibling", "mask")}
+        else:
+            if w.medusa:
+                m = w.medusa
+                t0 = clock()
+                H.medusa_heads(self.h, self.w1, None, self.w2s)
+                t_h = clock() - t0
+                frac = (m["hidden"] ** 2 + len(self.rows) * m["hidden"]) / (m["hidden"] ** 2 + V * m["hidden"])
+                parts["medusa_heads"] = t_h / frac
+                t0 = clock()
+                H.topk(self.head_logits, self.s)
+                parts["topk"] = clock() - t0
             t0 = clock()
-            H.topk(full_logits, s)
-            parts["topk"] = clock() - t0
+            tree = T.build_tree_static(self.shape.parents, self.shape.rank, self.cand, self.root, self.prefix)
+            parts["build_tree"] = clock() - t0
+        q, kc, vc, kt, vt = self.att
         t0 = clock()
-        tr = T.build_tree_static(shape.parents, shape.rank, cand, synth.root_tokens(w), prefix)
-        parts["build_tree"] = clock() - t0
-        tree = tr
-    # attention on a subset of heads
-    q, kc, vc, kt, vt = synth.attention_inputs(w, prefix)
-    heads = list(range(0, Hq, max(1, Hq // 4)))[:4]
-    seqs = list(range(min(B, 2)))
-    mask = tree["mask"]
-    t0 = clock()
-    for b in seqs:
-        A.tree_attention(q[b:b + 1], kc[b:b + 1], vc[b:b + 1], kt[b:b + 1], vt[b:b + 1], prefix[b:b + 1],
-                         mask[b], heads=heads)
-    t_a = clock() - t0
-    frac = len(seqs) * len(heads) * (float(prefix[seqs].mean()) + N) / (B * Hq * (float(prefix.mean()) + N))
-    parts["tree_attn"] = t_a / frac
-    desc.append(f"attention on {len(seqs)} of {B} sequences x {len(heads)} of {Hq} heads")
-    # LM head (Medusa workload)
-    if w.medusa:
-        d = w.medusa["hidden"]
-        hid = synth.gaussian(synth.stream(w.seed, "tree_hidden"), (B * N, d), 1.0, True)
-        cols = np.arange(0, V, max(1, V // 1024))
+        for i, b in enumerate(self.seqs):
+            A.tree_attention(q[i:i + 1], kc[i:i + 1], vc[i:i + 1], kt[i:i + 1], vt[i:i + 1],
+                             self.sub_prefix[i:i + 1], tree["mask"][b], heads=self.heads)
+        frac = len(self.seqs) * len(self.heads) * (float(self.sub_prefix.mean()) + N) / \
+            (B * Hq * (float(self.prefix.mean()) + N))
+        parts["tree_attn"] = (clock() - t0) / frac
+        if w.medusa:
+            t0 = clock()
+            H.lm_head(self.hid, self.wlms)
+            parts["lm_head"] = (clock() - t0) * V / len(self.rows)
+        sel = {k: tree[k][self.seqs] for k in ("tok", "parent", "first_child", "next_sibling")}
         t0 = clock()
-        logits_s = H.lm_head(hid, wlm[cols])
-        parts["lm_head"] = (clock() - t0) * V / len(cols)
-        desc.append(f"LM head on {len(cols)} of {V} vocabulary columns")
-        logits = np.zeros((B, N, V), np.float32)
-        logits[:, :, cols] = logits_s.reshape(B, N, -1)
-    else:
-        logits = synth.target_logits(w.seed, B, N, V, w.logit_std, w.dtype == "bf16")
-    # acceptance + commit (full)
-    t0 = clock()
-    cap = 8
-    if w.accept == "greedy":
-        acc = ACC.accept_greedy(logits, tree["tok"], tree["first_child"], tree["next_sibling"], cap)
-    elif w.accept == "typical":
-        acc = ACC.accept_typical(logits, tree["tok"], tree["parent"], tree["first_child"], tree["next_sibling"],
-                                 w.eps, w.delta, w.temperature, cap)
-    else:
-        acc = ACC.accept_reject(logits, tree["tok"], tree["first_child"], tree["next_sibling"], w.seed, 0,
-                                w.temperature, cap)
-    parts["accept"] = clock() - t0
-    t0 = clock()
-    COM.kv_commit(kc, vc, kt, vt, prefix, acc[0], acc[1])
-    parts["kv_commit"] = clock() - t0
-    return sum(parts.values()), "; ".join(desc) if desc else "full step", parts
+        cap = 8
+        if w.accept == "greedy":
+            acc = ACC.accept_greedy(self.logits, sel["tok"], sel["first_child"], sel["next_sibling"], cap)
+        elif w.accept == "typical":
+            acc = ACC.accept_typical(self.logits, sel["tok"], sel["parent"], sel["first_child"], sel["next_sibling"],
+                                     w.eps, w.delta, w.temperature, cap)
+        else:
+            acc = ACC.accept_reject(self.logits, sel["tok"], sel["first_child"], sel["next_sibling"], w.seed, 0,
+                                    w.temperature, cap)
+        parts["accept"] = (clock() - t0) * B / len(self.seqs)
+        t0 = clock()
+        COM.kv_commit(kc, vc, kt, vt, self.sub_prefix, acc[0], acc[1])
+        parts["kv_commit"] = (clock() - t0) * B / len(self.seqs)
+        return sum(parts.values()), parts
 
 
 def _cpu_baseline_subprocess(name: str, reps: int = 2):
@@ -425,9 +444,8 @@ def _cpu_baseline_subprocess(name: str, reps: int = 2):
     not forked from this CUDA process)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
-            f"r = [bench.oracle_step_seconds({name!r}) for _ in range({reps})]; "
-            f"print(json.dumps({{'s': min(x[0] for x in r), 'sample': r[0][1], "
-            f"'parts': r[0][2]}}))")
+            f"o = bench.OracleStep({name!r}); r = [o.step() for _ in range({reps})]; "
+            f"print(json.dumps({{'s': min(x[0] for x in r), 'sample': o.sample, 'parts': r[0][1]}}))")
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if out.returncode != 0:
         return None, out.stderr[-400:]
@@ -451,18 +469,41 @@ def _dist():
     return None, 0, 0, 1
 
 
+def job_max(value: float, dist, device) -> float:
+    """Largest per-rank value (seconds) over all ranks; the local value when
+    there is a single process."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(steps_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: every rank's steps over the slowest rank's time."""
+    return world * steps_per_rank / max_seconds
+
+
 def run_reference(args):
-    dist, rank, local, ws = _dist() if int(os.environ.get("WORLD_SIZE", "1")) > 1 else (None, 0, 0, 1)
-    if rank != 0:
+    # rank 0 alone times the oracle; other ranks of a torchrun launch exit
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     from tree_speculative_decoding_attn_gb300 import synth
     w = synth.WORKLOADS[args.workload]
     times = []
-    sample = None
-    for i in range(args.warmup + args.steps):
-        s, sample, _ = oracle_step_seconds(args.workload)
-        if i >= args.warmup:
-            times.append(s)
+    o = OracleStep(args.workload)
+    for _ in range(min(args.warmup, 1)):  # the oracle has nothing to warm beyond one pass
+        o.step()
+    # every step is the same deterministic sample, so the timed oracle steps
+    # stop at a bounded budget of CPU time (the line says how many ran)
+    budget_s, spent = 150.0, 0.0
+    while len(times) < args.steps and (not times or spent < budget_s):
+        t0 = time.perf_counter()
+        s, _ = o.step()
+        spent += time.perf_counter() - t0
+        times.append(s)
+    sample = f"{o.sample}; {len(times)} of {args.steps} steps timed (identical deterministic steps)"
     t = sum(times) / len(times)
     val = 1.0 / t
     line = {"impl": "reference", "metric": "tree-verify steps/s", "value": val, "unit": "steps/s",
@@ -478,7 +519,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT)
@@ -510,29 +551,45 @@ def main():
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
 
-    # timed region: K steps, per-stage events on the launch stream
+    # timed region: K steps, per-stage events on the launch stream.  The K
+    # steps are captured once into a CUDA graph (events as external record
+    # nodes) and replayed as one launch, so host launch latency between the
+    # library's kernels is not part of the measurement; without graph event
+    # support the steps run eagerly.
     n_st = len(step.stages)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
+    try:
+        mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        evs = [[mk_ev() for _ in range(n_st + 1)] for _ in range(args.steps)]
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for k in range(args.steps):
+                step.run(evs[k])
+        mode = "cuda_graph"
+    except (TypeError, RuntimeError):
+        torch.cuda.synchronize()
+        graph = None
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
+        mode = "eager"
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
-        for k in range(args.steps):
-            step.run(evs[k])
+        if graph is not None:
+            graph.replay()
+        else:
+            for k in range(args.steps):
+                step.run(evs[k])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     if dist:
         dist.barrier()
-    step_s = [evs[k][0].elapsed_time(evs[k][-1]) * 1e-3 for k in range(args.steps)]
-    total = sum(step_s)
+    assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
+    total = evs[0][0].elapsed_time(evs[-1][-1]) * 1e-3
     stage_s = {step.stages[i][0]: sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                * 1e-3 / args.steps for i in range(n_st)}
-    if dist:
-        t = torch.tensor([total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total = float(t.item())
-    steps_per_s = ws * args.steps / total
+    total = job_max(total, dist, dev)
+    steps_per_s = job_rate(args.steps, ws, total)
     dyn, mean_acc = step.dynamic_bytes()
 
     # roofline for the dominant stage
@@ -563,11 +620,8 @@ def main():
     e1.record()
     torch.cuda.synchronize()
     e2e_s = e0.elapsed_time(e1) * 1e-3
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": ws * args.steps / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d_bytes,
+    e2e_s = job_max(e2e_s, dist, dev)
+    e2e = {"value": job_rate(args.steps, ws, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d_bytes,
            "d2h_bytes_per_step": d2h_bytes}
 
     launches = step.launches_per_step()
@@ -604,6 +658,7 @@ def main():
                 "config": {"workload": args.workload, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
                            "head_dim": w.head_dim, "prefix": list(w.prefix), "n_nodes": w.n_nodes,
                            "vocab": w.vocab, "accept": w.accept, "parallelism": f"replicas x{ws}",
+                           "launch": mode,
                            "l2": "inputs exceed L2 (weights + KV streamed each step)"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches * args.steps,
