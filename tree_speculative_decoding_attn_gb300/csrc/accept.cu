@@ -9,10 +9,13 @@
 // (min(1, p/q); on rejection sample the target minus the drafter), with
 // the point-mass proposal of a deterministic tree sibling.
 //
-// One CTA per sequence walks the tree from the root; each visited node's
-// vocabulary row is reduced by the whole CTA with 16-byte loads, so only
-// the rows on the walk are read (plus, for typical acceptance, the rows of
-// every node reachable through valid children).
+// One cluster of kCluster CTAs per sequence walks the tree from the root.
+// Each visited node's vocabulary row is reduced in slices: CTA c reduces the
+// c-th slice with 16-byte loads, the kCluster partial results are exchanged
+// through distributed shared memory and combined in CTA order, so every CTA
+// of the cluster holds the same totals and takes the same decisions without
+// a broadcast.  Only the rows on the walk are read (plus, for typical
+// acceptance, the rows of every node reachable through valid children).
 #include <math.h>
 
 #include "common.cuh"
@@ -23,36 +26,51 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNodes = SPEC_MAX_NODES;
+constexpr int kCluster = 8;
 
 struct Red {
   float f[kWarps];
   unsigned long long u[kWarps];
   float bf;
   unsigned long long bu;
+  // cluster exchange slots, double-buffered by reduction parity: a slot is
+  // rewritten two reductions later, after every CTA has passed the barrier
+  // that follows its last read of it
+  float xf[2][2];
+  unsigned long long xu[2];
+  float cf[2];
+  unsigned long long cu;
 };
 
-__device__ float block_max(float v, Red &r) {
-  v = sv::warp_max(v);
-  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float w = threadIdx.x < kWarps ? r.f[threadIdx.x] : -INFINITY;
-    w = sv::warp_max(w);
-    if (threadIdx.x == 0) r.bf = w;
-  }
-  __syncthreads();
-  const float out = r.bf;
-  __syncthreads();
-  return out;
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t remote(const void *local, uint32_t cta) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(sv::ptx_smem(local)), "r"(cta));
+  return r;
+}
+__device__ __forceinline__ float ld_remote_f32(const void *local, uint32_t cta) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote(local, cta)) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long ld_remote_u64(const void *local, uint32_t cta) {
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote(local, cta)) : "memory");
+  return v;
 }
 
-__device__ float block_sum(float v, Red &r) {
-  v = sv::warp_sum(v);
+template <typename Op>
+__device__ float block_reduce(float v, float ident, Red &r, Op op) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
   if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float w = threadIdx.x < kWarps ? r.f[threadIdx.x] : 0.f;
-    w = sv::warp_sum(w);
+    float w = threadIdx.x < kWarps ? r.f[threadIdx.x] : ident;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) w = op(w, __shfl_xor_sync(0xffffffffu, w, o));
     if (threadIdx.x == 0) r.bf = w;
   }
   __syncthreads();
@@ -76,14 +94,81 @@ __device__ unsigned long long block_max_u64(unsigned long long v, Red &r) {
   return out;
 }
 
-// Visit every element of a logits row: f(x, value).  16-byte loads when the
-// row is aligned and its length a multiple of the vector width.
+// Cluster-wide reductions: every CTA gets the identical result (partials
+// combined in CTA order).  All threads of all CTAs must call them together.
+struct ClusterOps {
+  Red &r;
+  int parity;
+
+  __device__ float max(float v) {
+    v = block_reduce(v, -INFINITY, r, [](float a, float b) { return fmaxf(a, b); });
+    if (threadIdx.x == 0) r.xf[parity][0] = v;
+    cluster_barrier();
+    if (threadIdx.x == 0) {
+      float m = -INFINITY;
+      for (uint32_t c = 0; c < kCluster; ++c) m = fmaxf(m, ld_remote_f32(&r.xf[parity][0], c));
+      r.cf[0] = m;
+    }
+    __syncthreads();
+    const float out = r.cf[0];
+    __syncthreads();
+    parity ^= 1;
+    return out;
+  }
+  // two sums at once
+  __device__ void sum2(float &a, float &b) {
+    a = block_reduce(a, 0.f, r, [](float x, float y) { return x + y; });
+    b = block_reduce(b, 0.f, r, [](float x, float y) { return x + y; });
+    if (threadIdx.x == 0) {
+      r.xf[parity][0] = a;
+      r.xf[parity][1] = b;
+    }
+    cluster_barrier();
+    if (threadIdx.x == 0) {
+      float sa = 0.f, sb = 0.f;
+      for (uint32_t c = 0; c < kCluster; ++c) {
+        sa += ld_remote_f32(&r.xf[parity][0], c);
+        sb += ld_remote_f32(&r.xf[parity][1], c);
+      }
+      r.cf[0] = sa;
+      r.cf[1] = sb;
+    }
+    __syncthreads();
+    a = r.cf[0];
+    b = r.cf[1];
+    __syncthreads();
+    parity ^= 1;
+  }
+  __device__ unsigned long long max_u64(unsigned long long v) {
+    v = block_max_u64(v, r);
+    if (threadIdx.x == 0) r.xu[parity] = v;
+    cluster_barrier();
+    if (threadIdx.x == 0) {
+      unsigned long long m = 0ull;
+      for (uint32_t c = 0; c < kCluster; ++c) {
+        const unsigned long long w = ld_remote_u64(&r.xu[parity], c);
+        m = w > m ? w : m;
+      }
+      r.cu = m;
+    }
+    __syncthreads();
+    const unsigned long long out = r.cu;
+    __syncthreads();
+    parity ^= 1;
+    return out;
+  }
+};
+
+// Visit every element of this CTA's slice [lo, hi) of a logits row:
+// f(x, value) with x the column.  16-byte loads when the slice start is
+// aligned and its length a multiple of the vector width.
 template <typename T, typename F>
-__device__ __forceinline__ void for_row(const T *row, int V, F &&f) {
+__device__ __forceinline__ void for_slice(const T *row, int lo, int hi, F &&f) {
   constexpr int kVec = 16 / sizeof(T);
-  if ((V % kVec) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-    for (int vi = threadIdx.x; vi < V / kVec; vi += kThreads) {
-      const uint4 u = *reinterpret_cast<const uint4 *>(row + (int64_t)vi * kVec);
+  if (((hi - lo) % kVec) == 0 && (reinterpret_cast<uintptr_t>(row + lo) & 15) == 0) {
+    const int nv = (hi - lo) / kVec;
+    for (int vi = threadIdx.x; vi < nv; vi += kThreads) {
+      const uint4 u = *reinterpret_cast<const uint4 *>(row + lo + (int64_t)vi * kVec);
       float v[kVec];
       if constexpr (sizeof(T) == 2) {
         sv::bf16x8_to_f32(u, v);
@@ -94,29 +179,11 @@ __device__ __forceinline__ void for_row(const T *row, int V, F &&f) {
         v[3] = __uint_as_float(u.w);
       }
 #pragma unroll
-      for (int j = 0; j < kVec; ++j) f(vi * kVec + j, v[j]);
+      for (int j = 0; j < kVec; ++j) f(lo + vi * kVec + j, v[j]);
     }
   } else {
-    for (int x = threadIdx.x; x < V; x += kThreads) f(x, sv::to_f32(row[x]));
+    for (int x = lo + threadIdx.x; x < hi; x += kThreads) f(x, sv::to_f32(row[x]));
   }
-}
-
-template <typename T>
-__device__ int row_argmax(const T *row, int V, Red &r) {
-  unsigned long long best = 0ull;
-  for_row(row, V, [&](int x, float v) {
-    const unsigned long long k = sv::rank_key(v, (uint32_t)x);
-    best = k > best ? k : best;
-  });
-  return (int)sv::key_index(block_max_u64(best, r));
-}
-
-// max of z = logits / T over the row
-template <typename T>
-__device__ float row_max_z(const T *row, int V, float T_, Red &r) {
-  float m = -INFINITY;
-  for_row(row, V, [&](int, float v) { m = fmaxf(m, v / T_); });
-  return block_max(m, r);
 }
 
 template <typename T>
@@ -134,7 +201,12 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int s_exc[kMaxNodes];
   __shared__ int s_nexc;
 
-  const int b = blockIdx.x;
+  const uint32_t cta = blockIdx.x;  // rank in the cluster (cluster spans x)
+  const int b = blockIdx.y;
+  const int slice = ((V + kCluster - 1) / kCluster + 7) / 8 * 8;
+  const int lo = min(V, (int)cta * slice), hi = min(V, lo + slice);
+  ClusterOps cl{red, 0};
+
   const int64_t row0 = (int64_t)b * N;
   for (int i = threadIdx.x; i < N; i += kThreads) {
     s_fc[i] = first_child[row0 + i];
@@ -151,10 +223,24 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t st = (uint32_t)step;
   const T *base = logits + row0 * V;
 
+  auto row_argmax = [&](const T *row) -> int {
+    unsigned long long best = 0ull;
+    for_slice(row, lo, hi, [&](int x, float v) {
+      const unsigned long long k = sv::rank_key(v, (uint32_t)x);
+      best = k > best ? k : best;
+    });
+    return (int)sv::key_index(cl.max_u64(best));
+  };
+  auto row_max_z = [&](const T *row) -> float {
+    float m = -INFINITY;
+    for_slice(row, lo, hi, [&](int, float v) { m = fmaxf(m, v / temp); });
+    return cl.max(m);
+  };
+
   if (mode == SPEC_ACCEPT_GREEDY) {
     int v = 0;
     for (int guard = 0; guard < kMaxNodes; ++guard) {
-      const int a = row_argmax(base + (int64_t)v * V, V, red);
+      const int a = row_argmax(base + (int64_t)v * V);
       if (threadIdx.x == 0) {
         int nxt = -1;
         for (int c = s_fc[v]; c >= 0 && c < N; c = s_ns[c])
@@ -182,18 +268,17 @@ __global__ void __launch_bounds__(kThreads)
     }
     __syncthreads();
     for (int v = 0; v < N; ++v) {
-      if (!s_ok[v] || s_fc[v] < 0) continue;  // uniform: shared flags
+      if (!s_ok[v] || s_fc[v] < 0) continue;  // uniform: shared flags, identical in every CTA
       const T *row = base + (int64_t)v * V;
-      const float m = row_max_z(row, V, temp, red);
+      const float m = row_max_z(row);
       float S = 0.f, Q = 0.f;
-      for_row(row, V, [&](int, float x) {
+      for_slice(row, lo, hi, [&](int, float x) {
         const float z = x / temp - m;
         const float e = expf(z);
         S += e;
         Q = fmaf(e, z, Q);
       });
-      S = block_sum(S, red);
-      Q = block_sum(Q, red);
+      cl.sum2(S, Q);
       if (threadIdx.x == 0) {
         const float H = logf(S) - Q / S;
         const float thr = fminf(eps, delta * expf(-H));
@@ -213,8 +298,7 @@ __global__ void __launch_bounds__(kThreads)
       int best = 0;
       for (int i = 1; i < N; ++i)
         if (s_ok[i] && s_depth[i] > s_depth[best]) best = i;
-      // root-first path of `best`
-      int d = s_depth[best];
+      int d = s_depth[best];  // root-first path of `best`
       s_len = d + 1;
       for (int u = best; d >= 0; --d) {
         s_path[d] = u;
@@ -223,16 +307,16 @@ __global__ void __launch_bounds__(kThreads)
       s_next = best;
     }
     __syncthreads();
-    const int a = row_argmax(base + (int64_t)s_next * V, V, red);
+    const int a = row_argmax(base + (int64_t)s_next * V);
     if (threadIdx.x == 0) s_bonus = a;
   } else {  // SPEC_ACCEPT_REJECT
     int v = 0;
     for (int guard = 0; guard < kMaxNodes; ++guard) {
       const T *row = base + (int64_t)v * V;
-      const float m = row_max_z(row, V, temp, red);
-      float S = 0.f;
-      for_row(row, V, [&](int, float x) { S += expf(x / temp - m); });
-      S = block_sum(S, red);
+      const float m = row_max_z(row);
+      float S = 0.f, unused = 0.f;
+      for_slice(row, lo, hi, [&](int, float x) { S += expf(x / temp - m); });
+      cl.sum2(S, unused);
       if (threadIdx.x == 0) {
         int nxt = -1;
         float removed = 0.f;
@@ -272,7 +356,7 @@ __global__ void __launch_bounds__(kThreads)
       // residual sample: exponential race in log form over non-removed tokens
       const int nexc = s_nexc;
       unsigned long long best = 0ull;
-      for_row(row, V, [&](int x, float val) {
+      for_slice(row, lo, hi, [&](int x, float val) {
         for (int e = 0; e < nexc; ++e)
           if (s_exc[e] == x) return;
         const sv::u32x4 w =
@@ -283,14 +367,14 @@ __global__ void __launch_bounds__(kThreads)
         const unsigned long long k = sv::rank_key(key, (uint32_t)x);
         best = k > best ? k : best;
       });
-      best = block_max_u64(best, red);
+      best = cl.max_u64(best);
       if (threadIdx.x == 0) s_bonus = (int)sv::key_index(best);
       __syncthreads();
       break;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (cta == 0 && threadIdx.x == 0) {
     int len = s_len;
     if (len > path_cap) {
       sv::report(status, SPEC_DEV_CAPACITY);
@@ -300,6 +384,30 @@ __global__ void __launch_bounds__(kThreads)
     for (int j = 0; j < path_cap; ++j) acc_path[(int64_t)b * path_cap + j] = j < len ? s_path[j] : -1;
     bonus_out[b] = s_bonus;
   }
+  cluster_barrier();  // partners' reads of this CTA's exchange slots are done
+}
+
+template <typename T>
+int launch_accept(int mode, const void *logits, int batch, int n_nodes, int vocab, const int32_t *tok,
+                  const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
+                  float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
+                  int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster, batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_kernel<T>, mode, (const T *)logits, n_nodes, vocab, tok, parents,
+                            first_child, next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
+                            acc_path, bonus, status) == cudaSuccess
+             ? SPEC_OK
+             : SPEC_ERR_CUDA;
 }
 
 }  // namespace
@@ -310,13 +418,10 @@ int sv_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, i
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
               int32_t *bonus, int32_t *status, cudaStream_t stream) {
   if (dtype == SPEC_BF16)
-    accept_kernel<__nv_bfloat16><<<batch, kThreads, 0, stream>>>(
-        mode, (const __nv_bfloat16 *)logits, n_nodes, vocab, tok, parents, first_child,
-        next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus,
-        status);
-  else
-    accept_kernel<float><<<batch, kThreads, 0, stream>>>(
-        mode, (const float *)logits, n_nodes, vocab, tok, parents, first_child, next_sibling,
-        temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus, status);
-  return sv_launch_status();
+    return launch_accept<__nv_bfloat16>(mode, logits, batch, n_nodes, vocab, tok, parents, first_child,
+                                        next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
+                                        acc_path, bonus, status, stream);
+  return launch_accept<float>(mode, logits, batch, n_nodes, vocab, tok, parents, first_child, next_sibling,
+                              temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus, status,
+                              stream);
 }

@@ -160,7 +160,10 @@ __global__ void __launch_bounds__(kDynThreads)
     if (r < N) kept[r] = i;
   }
   __syncthreads();
-  // parent closure check and breadth-first renumbering (N <= 64 threads)
+  // parent closure check and breadth-first renumbering (N <= 64 threads):
+  // each kept slot's parent slot and depth are looked up once, then every
+  // level is numbered by counting the predecessors of each node on it
+  __shared__ int kept_pslot[kMaxNodes], kept_depth[kMaxNodes];
   int my_pool = -1, my_depth = 0, my_pslot = -1;
   if (t < N) {
     my_pool = kept[t];
@@ -171,6 +174,8 @@ __global__ void __launch_bounds__(kDynThreads)
         if (kept[r] == pp) my_pslot = r;
       if (my_pslot < 0) atomicOr(&bad, 1);
     }
+    kept_pslot[t] = my_pslot;
+    kept_depth[t] = my_depth;
   }
   __syncthreads();
   if (bad) {
@@ -180,22 +185,15 @@ __global__ void __launch_bounds__(kDynThreads)
   int base = 0;
   for (int d = 0; d < kMaxPoolDepth; ++d) {
     int here = 0;  // kept nodes at depth d (uniform across threads)
-    for (int r = 0; r < N; ++r) here += ((int)((key[kept[r]] >> 16) & 0xFFFF) == d);
+    for (int r = 0; r < N; ++r) here += kept_depth[r] == d;
     if (here == 0) break;
     if (t < N && my_depth == d) {
       const int mp = (t == 0) ? -1 : kept_new[my_pslot];
       int before = 0;
       for (int r = 0; r < N; ++r) {
-        if (r == t) continue;
-        const int u = kept[r];
-        if ((int)((key[u] >> 16) & 0xFFFF) != d) continue;
-        int upar = -1;  // new index of u's parent (assigned on an earlier level)
-        if (r != 0) {
-          const int pp = ppar[u];
-          for (int q = 0; q < N; ++q)
-            if (kept[q] == pp) upar = kept_new[q];
-        }
-        if (upar < mp || (upar == mp && key[u] < key[my_pool])) ++before;
+        if (r == t || kept_depth[r] != d) continue;
+        const int upar = r == 0 ? -1 : kept_new[kept_pslot[r]];  // assigned on an earlier level
+        if (upar < mp || (upar == mp && key[kept[r]] < key[my_pool])) ++before;
       }
       kept_new[t] = base + before;
       new_par[base + before] = mp;
