@@ -170,7 +170,9 @@ class GpuStep:
         self.q, self.kc, self.vc, self.kt, self.vt = (cu(x, tdt) for x in (q, kc, vc, kt, vt))
         del q, kc, vc, kt, vt
         self.out = torch.empty((B, N, Hq, D), dtype=tdt, device=dev)
-        wsb = sv.tree_attn_workspace_bytes(tdt, B, N, Hq, Hkv, D, self.max_prefix)
+        # split count from the host-known prefix lengths (matters for ragged batches)
+        self.splits = sv.tree_attn_plan_splits(tdt, B, N, Hq, Hkv, D, self.prefix)
+        wsb = sv.tree_attn_workspace_bytes(tdt, B, N, Hq, Hkv, D, self.max_prefix, self.splits)
         self.ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         self.attn_launches = 2 if wsb > 0 else 1
         esz = 2 if tdt == bf else 4
@@ -251,7 +253,7 @@ class GpuStep:
         sv = self.sv
         self.stages.append(("tree_attn", lambda: sv.tree_attn_verify(
             self.q, self.kc, self.vc, self.kt, self.vt, self.d_prefix, self.anc, self.out, self.max_prefix,
-            workspace=self.ws, dev_status=self.status), self.attn_launches, self.attn_bytes))
+            num_splits=self.splits, workspace=self.ws, dev_status=self.status), self.attn_launches, self.attn_bytes))
 
     def _lm_head_stage(self, cu):
         torch, sv, synth, w = self.torch, self.sv, self.synth, self.w
@@ -325,12 +327,13 @@ def attention_only(name: str, device, steps: int, warmup: int):
     sv.spec_build_tree(torch.from_numpy(shape.parents).to(device), torch.from_numpy(shape.rank).to(device), None,
                        None, d_prefix, None, i32(B, N), i32(B, N), anc, i32(B, N), i32(B, N))
     out = torch.empty_like(q)
-    wsb = sv.tree_attn_workspace_bytes(bf, B, N, Hq, Hkv, D, int(prefix.max()))
+    splits = sv.tree_attn_plan_splits(bf, B, N, Hq, Hkv, D, prefix)
+    wsb = sv.tree_attn_workspace_bytes(bf, B, N, Hq, Hkv, D, int(prefix.max()), splits)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()), workspace=ws,
-                                       dev_status=status)
+    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()),
+                                       num_splits=splits, workspace=ws, dev_status=status)
     for _ in range(warmup):
         call()
     times = []
@@ -347,7 +350,7 @@ def attention_only(name: str, device, steps: int, warmup: int):
     flops = 4 * N * (Hq // Hkv) * D * Hkv * (int(prefix.sum()) + B * N)
     del q, kc, vc, kt, vt, flush
     return {"us": t * 1e6, "gbps": nbytes / t / 1e9, "tflops": flops / t / 1e12, "bytes": nbytes,
-            "launches": 2 if wsb else 1}
+            "launches": 2 if wsb else 1, "splits": splits}
 
 
 # ----------------------------------------------------------------------------

@@ -231,6 +231,15 @@ int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front
  * ------------------------------------------------------------------ */
 size_t tree_attn_workspace_bytes(int dtype, int batch, int n_nodes, int hq, int hkv,
                                  int head_dim, int max_prefix, int num_splits);
+/* tree_attn_plan_splits -- KV split count for a batch whose prefix lengths
+ * the host knows (HOST pointer, [batch] int32).  num_splits = 0 in
+ * tree_attn_verify plans for every sequence at max_prefix; with ragged
+ * prefixes this planner (a simulation of the kernel's work distribution
+ * over the SMs) usually finds a better count.  Pass the result as
+ * num_splits to tree_attn_workspace_bytes and tree_attn_verify.  Returns
+ * >= 1, or 0 on invalid arguments. */
+int tree_attn_plan_splits(int dtype, int batch, int n_nodes, int hq, int hkv, int head_dim,
+                          const int32_t *host_prefix_len);
 int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache,
                      const void *k_tree, const void *v_tree, const int32_t *prefix_len,
                      const uint64_t *anc_mask, void *out, int dtype, int batch, int n_nodes,

@@ -41,3 +41,19 @@ def test_status_strings_without_gpu(built_lib):
     assert sv.spec_status_string(0) == "ok"
     assert "invalid" in sv.spec_status_string(1)
     assert sv.spec_abi_version() == 1
+
+
+def test_split_planner_is_host_only_and_sane(built_lib):
+    """tree_attn_plan_splits runs on the host: a uniform batch of long
+    prefixes that already fills the SMs keeps one split; a ragged batch of
+    few sequences is split; bad arguments return an error."""
+    import torch
+    from tree_speculative_decoding_attn_gb300 import specverify as sv
+    bf = torch.bfloat16
+    assert sv.tree_attn_plan_splits(bf, 64, 32, 64, 8, 128, [4096] * 64) == 1
+    ragged = [512, 8192, 1024, 3000, 700, 6000, 2048, 4000]
+    assert sv.tree_attn_plan_splits(bf, 8, 60, 32, 8, 128, ragged) > 1
+    assert 1 <= sv.tree_attn_plan_splits(bf, 4, 64, 32, 8, 128, [32768] * 4) <= 64
+    assert 1 <= sv.tree_attn_plan_splits(torch.float32, 1, 5, 4, 4, 64, [128]) <= 64
+    with pytest.raises(sv.SpecError):
+        sv.tree_attn_plan_splits(bf, 2, 65, 8, 8, 128, [10, 10])     # more than 64 tree nodes

@@ -12,8 +12,9 @@
 // TMA-loads one 64-dim half of every K and V tile and multicasts it to both,
 // so each tile leaves HBM / L2 once and fills both CTAs' shared memory.
 //
-//   warp 0      TMA producer: Q once, then K and V tiles (128 keys x 128
-//               dims, 128-byte swizzle) through three-stage rings
+//   warp 0      TMA producers, lane 0: Q once, then K; lane 1: V.  Tiles of
+//               128 keys x 128 dims, 128-byte swizzle, through two rings
+//               that refill independently
 //   warp 1      TMEM allocation and the MMA issuer (one lane):
 //                 S(j) = Q K(j)^T     into TMEM buffer j % 2 (A, B in smem)
 //                 O   += P(j) V(j)    (A = P in TMEM, B = V, MN-major)
@@ -44,7 +45,8 @@ using namespace sv::ptx;
 
 constexpr int kBN = 128;               // keys per K/V tile
 constexpr int kD = 128;                // head_dim
-constexpr int kStages = 3;             // K and V ring depth
+constexpr int kKStages = 3;            // K ring depth
+constexpr int kVStages = 3;            // V ring depth
 constexpr int kThreads = 320;
 constexpr uint32_t kTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 tile
 constexpr uint32_t kHalf = kTile / 2;      // 128 rows x 64 dims (one swizzle column)
@@ -55,13 +57,13 @@ constexpr uint32_t kColO = 256;
 
 struct Bars {
   uint64_t q;
-  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
+  uint64_t kfull[kKStages], kempty[kKStages], vfull[kVStages], vempty[kVStages];
   uint64_t sfull[2], ofull[2], pfull[2], done, drain;
   uint32_t tmem;
   volatile int abort;
   float xmax[2][128];  // per-row partial maxima (then sums) of the two softmax column halves
 };
-constexpr uint32_t kSmemBytes = (1 + 2 * kStages) * kTile + sizeof(Bars) + 1024;
+constexpr uint32_t kSmemBytes = (1 + kKStages + kVStages) * kTile + sizeof(Bars) + 1024;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // V is MN-major (dims contiguous)
@@ -94,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + kTile;
-  uint8_t *sV = sK + kStages * kTile;
-  Bars *bars = reinterpret_cast<Bars *>(sV + kStages * kTile);
+  uint8_t *sV = sK + kKStages * kTile;
+  Bars *bars = reinterpret_cast<Bars *>(sV + kVStages * kTile);
 
   const int G = Hq / Hkv, R = N * G;
   const int qt = blockIdx.x, split = blockIdx.y, bh = blockIdx.z;
@@ -131,10 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->q, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->kfull[s], 1);
-      mbar_init(&bars->vfull[s], 1);
       mbar_init(&bars->kempty[s], CL);  // one MMA commit from each CTA of the cluster
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&bars->vfull[s], 1);
       mbar_init(&bars->vempty[s], CL);
     }
     for (int i = 0; i < 2; ++i) {
@@ -159,7 +163,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ producers
+    // lane 0 streams Q then K, lane 1 streams V: the two rings refill
+    // independently (K is released by S, V only after the softmax and PV)
+    auto tile_row = [&](int j, bool &tree) {
+      tree = with_tree && j == n_tiles - 1;
+      return tree ? bh * N : bh * s_max + k0 + j * kBN;
+    };
+    auto stream_ring = [&](bool is_v) {
+      const int n_st = is_v ? kVStages : kKStages;
+      uint64_t *full = is_v ? bars->vfull : bars->kfull;
+      uint64_t *empty = is_v ? bars->vempty : bars->kempty;
+      uint8_t *ring = is_v ? sV : sK;
+      int issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % n_st;
+        bool tree;
+        const int row = tile_row(j, tree);
+        const CUtensorMap *m = is_v ? (tree ? &tm_vt : &tm_vc) : (tree ? &tm_kt : &tm_kc);
+        if (!mbar_wait(&empty[s], ((j / n_st) & 1) ^ 1, kWaitLimit) || bars->abort) {
+          give_up(bars, status);
+          break;
+        }
+        mbar_expect_tx(&full[s], kTile);
+        if (CL > 1) {
+          tma_load_2d_mc(ring + s * kTile + rank * kHalf, m, 64 * rank, row, &full[s], kPair);
+        } else {
+          tma_load_2d(ring + s * kTile, m, 0, row, &full[s]);
+          tma_load_2d(ring + s * kTile + kHalf, m, 64, row, &full[s]);
+        }
+        ++issued;
+      }
+      if (bars->abort)  // let the copies into this CTA land before it exits
+        for (int j = issued > n_st ? issued - n_st : 0; j < issued; ++j)
+          mbar_wait(&full[j % n_st], (j / n_st) & 1, kWaitLimit);
+    };
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_kc);
@@ -168,53 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int node0 = b * N + row0 / G;
       tma_load_4d(sQ, &tm_q, 0, 0, kvh, node0, &bars->q);
       tma_load_4d(sQ + kHalf, &tm_q, 64, 0, kvh, node0, &bars->q);
-      int nk = 0, nv = 0;  // tiles whose K / V loads were issued
-      // tile j: the CUtensorMaps and row of its K and V
-      auto tile_src = [&](int j, const CUtensorMap *&mk, const CUtensorMap *&mv, int &row) {
-        const bool tree = with_tree && j == n_tiles - 1;
-        mk = tree ? &tm_kt : &tm_kc;
-        mv = tree ? &tm_vt : &tm_vc;
-        row = tree ? bh * N : bh * s_max + k0 + j * kBN;
-      };
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        const CUtensorMap *mk, *mv;
-        int row;
-        tile_src(j, mk, mv, row);
-        if (!mbar_wait(&bars->kempty[s], ph ^ 1, kWaitLimit) || bars->abort) {
-          give_up(bars, status);
-          break;
-        }
-        mbar_expect_tx(&bars->kfull[s], kTile);
-        if (CL > 1) {
-          tma_load_2d_mc(sK + s * kTile + rank * kHalf, mk, 64 * rank, row, &bars->kfull[s], kPair);
-        } else {
-          tma_load_2d(sK + s * kTile, mk, 0, row, &bars->kfull[s]);
-          tma_load_2d(sK + s * kTile + kHalf, mk, 64, row, &bars->kfull[s]);
-        }
-        ++nk;
-        if (!mbar_wait(&bars->vempty[s], ph ^ 1, kWaitLimit) || bars->abort) {
-          give_up(bars, status);
-          break;
-        }
-        mbar_expect_tx(&bars->vfull[s], kTile);
-        if (CL > 1) {
-          tma_load_2d_mc(sV + s * kTile + rank * kHalf, mv, 64 * rank, row, &bars->vfull[s], kPair);
-        } else {
-          tma_load_2d(sV + s * kTile, mv, 0, row, &bars->vfull[s]);
-          tma_load_2d(sV + s * kTile + kHalf, mv, 64, row, &bars->vfull[s]);
-        }
-        ++nv;
-      }
-      if (bars->abort) {  // let the copies into this CTA land before it exits
-        mbar_wait(&bars->q, 0, kWaitLimit);
-        for (int j = nk > kStages ? nk - kStages : 0; j < nk; ++j)
-          mbar_wait(&bars->kfull[j % kStages], (j / kStages) & 1, kWaitLimit);
-        for (int j = nv > kStages ? nv - kStages : 0; j < nv; ++j)
-          mbar_wait(&bars->vfull[j % kStages], (j / kStages) & 1, kWaitLimit);
-      }
+      stream_ring(false);
+      if (bars->abort) mbar_wait(&bars->q, 0, kWaitLimit);
+    } else if (lane == 1) {
+      stream_ring(true);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
@@ -224,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // S(j) = Q K(j)^T into S buffer j % 2
     auto issue_s = [&](int j) -> bool {
-      const int s = j % kStages;
-      if (!warp_wait(&bars->kfull[s], (j / kStages) & 1)) return false;
+      const int s = j % kKStages;
+      if (!warp_wait(&bars->kfull[s], (j / kKStages) & 1)) return false;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t kb = ka + (uint32_t)s * kTile;
@@ -243,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = warp_wait(&bars->q, 0) && issue_s(0) && (n_tiles < 2 || issue_s(1));
     for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kStages;
-      if (!(ok = warp_wait(&bars->vfull[s], (j / kStages) & 1))) break;
+      const int s = j % kVStages;
+      if (!(ok = warp_wait(&bars->vfull[s], (j / kVStages) & 1))) break;
       // the last prefix tile of a split may run past the split's keys: zero
       // those V rows so that stale cache rows (possibly not finite) never
       // meet the zero probabilities of masked keys
@@ -516,36 +513,80 @@ inline int tc_qtiles(int R) {
   return tc_cluster(R) == 2 ? (t + 1) / 2 * 2 : t;
 }
 
+// Modelled time of one split count, in units of one K/V tile streamed by
+// one cluster slot: clusters are dispatched in launch order (query-tile
+// pair fastest, then split, then sequence x KV head) onto the free slots;
+// each streams its prefix chunk, the tree tile on the last split, and about
+// one tile's worth of set-up.  Split partials cost their write and re-read
+// plus a combine launch.  `prefix` holds each sequence's prefix length, or
+// is null for "every sequence at max_prefix".
+double tc_split_cost(const SvAttnShape &s, const int32_t *prefix, int splits) {
+  const int G = s.hq / s.hkv, R = s.n_nodes * G;
+  const int cl = tc_cluster(R);
+  const int pairs = tc_qtiles(R) / cl;
+  const int slots = kSms / cl;
+  int chunk = (s.max_prefix + splits - 1) / splits;
+  chunk = (chunk + kBN - 1) / kBN * kBN;
+  // min-heap of slot finish times (small arrays: slots <= 152)
+  double finish[kSms];
+  for (int i = 0; i < slots; ++i) finish[i] = 0.0;
+  for (int bh = 0; bh < s.batch * s.hkv; ++bh) {
+    const int P = prefix ? prefix[bh / s.hkv] : s.max_prefix;
+    for (int sp = 0; sp < splits; ++sp) {
+      const int k0 = sp * chunk, k1 = P < k0 + chunk ? P : k0 + chunk;
+      const int tiles = k1 > k0 ? (k1 - k0 + kBN - 1) / kBN : 0;
+      const double work = tiles + (sp == splits - 1 ? 2.0 : (tiles ? 1.0 : 0.1));
+      for (int pr = 0; pr < pairs; ++pr) {
+        int best = 0;
+        for (int i = 1; i < slots; ++i)
+          if (finish[i] < finish[best]) best = i;
+        finish[best] += work;
+      }
+    }
+  }
+  double makespan = 0.0;
+  for (int i = 0; i < slots; ++i) makespan = finish[i] > makespan ? finish[i] : makespan;
+  if (splits > 1) {
+    const double tile_bytes = (double)kBN * kD * 2 * 2 * slots;  // bytes moved per unit of time
+    const double partial = 2.0 * s.batch * s.hkv * splits * R * sv_partial_stride(kD) * 4.0;
+    makespan += partial / tile_bytes + 4.0;
+  }
+  return makespan;
+}
+
+int tc_best_splits(const SvAttnShape &s, const int32_t *prefix) {
+  const int max_useful = s.max_prefix > 0 ? (s.max_prefix + kBN - 1) / kBN : 1;
+  int best = 1;
+  double best_cost = tc_split_cost(s, prefix, 1);
+  for (int c = 2; c <= 64 && c <= max_useful; ++c) {
+    const double cost = tc_split_cost(s, prefix, c);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+    }
+  }
+  return best;
+}
+
 }  // namespace
+
+bool sv_attn_tc_supported(const SvAttnShape &s) {
+  if (s.dtype != SPEC_BF16 || s.head_dim != kD) return false;
+  const int G = s.hq / s.hkv;
+  return G <= 128 && (128 % G) == 0;
+}
+
+int sv_attn_tc_ragged_splits(const SvAttnShape &s, const int32_t *host_prefix) {
+  return tc_best_splits(s, host_prefix);
+}
 
 SvAttnPlan sv_attn_tc_plan(const SvAttnShape &s, int num_splits, bool *ok) {
   *ok = false;
   SvAttnPlan p{};
-  if (s.dtype != SPEC_BF16 || s.head_dim != kD) return p;
-  const int G = s.hq / s.hkv;
-  if (G > 128 || (128 % G) != 0) return p;
-  const int R = s.n_nodes * G;
-  const int base = tc_qtiles(R) * s.batch * s.hkv;  // CTAs per split
+  if (!sv_attn_tc_supported(s)) return p;
+  const int R = s.n_nodes * (s.hq / s.hkv);
   const int max_useful = s.max_prefix > 0 ? (s.max_prefix + kBN - 1) / kBN : 1;
-  int splits = num_splits;
-  if (splits <= 0) {
-    // Cost in bytes moved at full bandwidth: waves (one CTA per SM) times
-    // the tiles a CTA streams (its prefix chunk, the tree tile, and two
-    // tiles' worth of fixed set-up), plus writing and re-reading the split
-    // partials and a combine launch.
-    const double tile = (double)kBN * kD * 2 * 2;
-    double best = 0.0;
-    for (int c = 1; c <= 64 && c <= max_useful; ++c) {
-      const double waves = (double)((base * c + kSms - 1) / kSms);
-      const double tiles = (double)((max_useful + c - 1) / c) + 3.0;
-      double cost = waves * tiles * tile * kSms;
-      if (c > 1) cost += 2.0 * s.batch * s.hkv * c * R * sv_partial_stride(kD) * 4.0 + 20e6;
-      if (c == 1 || cost < best) {
-        best = cost;
-        splits = c;
-      }
-    }
-  }
+  int splits = num_splits > 0 ? num_splits : tc_best_splits(s, nullptr);
   if (splits > max_useful) splits = max_useful;
   if (splits > 64) splits = 64;
   if (splits < 1) splits = 1;

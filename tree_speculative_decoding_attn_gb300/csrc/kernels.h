@@ -31,6 +31,8 @@ struct SvAttnPlan {
   size_t ws_bytes;   // partials (0 when splits == 1)
 };
 SvAttnPlan sv_attn_plan(const SvAttnShape &s, int num_splits);
+bool sv_attn_tc_supported(const SvAttnShape &s);
+int sv_attn_tc_ragged_splits(const SvAttnShape &s, const int32_t *host_prefix);
 int sv_attn_simt(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const void *kc,
                  const void *vc, const void *kt, const void *vt, const int32_t *prefix_len,
                  const uint64_t *anc, void *out, float scale, void *ws, int32_t *status,

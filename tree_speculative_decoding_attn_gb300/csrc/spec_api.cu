@@ -126,6 +126,20 @@ size_t tree_attn_workspace_bytes(int dtype, int batch, int n_nodes, int hq, int 
   return sv_attn_plan(s, num_splits).ws_bytes;
 }
 
+int tree_attn_plan_splits(int dtype, int batch, int n_nodes, int hq, int hkv, int head_dim,
+                          const int32_t *host_prefix_len) {
+  if (!host_prefix_len) return 0;
+  int max_prefix = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (host_prefix_len[b] < 0) return 0;
+    max_prefix = host_prefix_len[b] > max_prefix ? host_prefix_len[b] : max_prefix;
+  }
+  if (attn_check(dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, max_prefix) != SPEC_OK) return 0;
+  const SvAttnShape s{dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, max_prefix};
+  if (sv_attn_tc_supported(s)) return sv_attn_tc_ragged_splits(s, host_prefix_len);
+  return sv_attn_plan(s, 0).splits;
+}
+
 int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache, const void *k_tree,
                      const void *v_tree, const int32_t *prefix_len, const uint64_t *anc_mask,
                      void *out, int dtype, int batch, int n_nodes, int hq, int hkv, int head_dim,

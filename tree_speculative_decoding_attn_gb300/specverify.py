@@ -36,6 +36,7 @@ _SIGS = {
                                  _vp, _vp, _vp], _i),
     "spec_tree_expand": ([_vp, _i, _i, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp], _i),
     "tree_attn_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
+    "tree_attn_plan_splits": ([_i, _i, _i, _i, _i, _i, _vp], _i),
     "tree_attn_verify": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                           _vp, _sz, _vp, _vp], _i),
     "tree_attn_verify_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
@@ -170,6 +171,19 @@ def spec_tree_expand(draft_logits, frontier, k, temperature, pool_parent, pool_t
 def tree_attn_workspace_bytes(dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, num_splits=0):
     code = _DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     return int(load().tree_attn_workspace_bytes(code, batch, n_nodes, hq, hkv, head_dim, max_prefix, num_splits))
+
+
+def tree_attn_plan_splits(dtype, batch, n_nodes, hq, hkv, head_dim, host_prefix_len):
+    """Split count for a batch whose prefix lengths the host knows (a
+    sequence of ints); pass it as num_splits."""
+    import numpy as np
+    code = _DT[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    arr = np.ascontiguousarray(np.asarray(host_prefix_len, dtype=np.int32))
+    n = int(load().tree_attn_plan_splits(code, batch, n_nodes, hq, hkv, head_dim,
+                                         arr.ctypes.data_as(C.c_void_p)))
+    if n <= 0:
+        raise SpecError("tree_attn_plan_splits", ERR_INVALID_ARG)
+    return n
 
 
 def tree_attn_verify(q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out, max_prefix,
