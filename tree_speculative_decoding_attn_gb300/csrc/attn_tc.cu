@@ -23,13 +23,15 @@
 //   warps 2-9   softmax: two warps per TMEM lane quarter, one per half of the
 //               tile's columns; thread = (row, column half).  S from TMEM,
 //               scale and mask (prefix range; ancestor bits on the tree
-//               tile), row max shared by the pair through shared memory,
-//               P = 2^(s - m) written back as bf16 over the S columns.  The running max m
-//               moves only when a tile exceeds it by more than 2^64 (then the
-//               sum and O are rescaled in place); otherwise every P stays
-//               inside [0, 2^64], far within float32 / bf16 range.
+//               tile), P = 2^(s - m) written as bf16 to a P buffer.  The first
+//               tile of a row takes the exact max (shared by the pair through
+//               shared memory); later tiles exponentiate against the running
+//               max m in one pass and are redone exactly only if their row sum
+//               leaves [0, 2^64] (a score far above m, rescaling the sum and O
+//               in place), so every P stays far within float32 / bf16 range.
 //
-// TMEM columns: S0 [0,128)  S1 [128,256)  O [256,384).
+// TMEM columns: S0 [0,128)  S1 [128,256)  O [256,384)  P0 [384,448)
+// P1 [448,512).
 // Every mbarrier wait is bounded; on a timeout the CTA reports
 // SPEC_DEV_TIMEOUT, waits (bounded) for its own loads and MMAs, frees TMEM
 // and returns.
@@ -51,9 +53,10 @@ constexpr int kThreads = 320;
 constexpr uint32_t kTile = 128 * 128 * 2;  // bytes of one 128 x 128 bf16 tile
 constexpr uint32_t kHalf = kTile / 2;      // 128 rows x 64 dims (one swizzle column)
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr float kGrow = 64.0f;         // log2 headroom above the running max before it is raised
+constexpr float kMaxTileSum = 18446744073709551616.0f;  // 2^64: bound on a tile's row sum against the running max
 constexpr int kSms = 152;
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;        // two P buffers of 64 columns (128 bf16 per row)
 
 struct Bars {
   uint64_t q;
@@ -62,8 +65,10 @@ struct Bars {
   uint32_t tmem;
   volatile int abort;
   float xmax[2][128];  // per-row partial maxima (then sums) of the two softmax column halves
+  unsigned char xflag[2][2][128];  // per-row "tile needs the exact max" flags, by tile parity
 };
 constexpr uint32_t kSmemBytes = (1 + kKStages + kVStages) * kTile + sizeof(Bars) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, 0, 1);  // V is MN-major (dims contiguous)
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t vb = va + (uint32_t)s * kTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + kColO, tmem + (uint32_t)(j & 1) * 128u + (uint32_t)kk * 8u,
+          mma_ts(tmem + kColO, tmem + kColP + (uint32_t)(j & 1) * 64u + (uint32_t)kk * 8u,
                  smem_desc_sw128(vb + (uint32_t)kk * 2048u, kHalf, 1024), kIdescPV, (j > 0 || kk > 0));
         mma_commit(&bars->ofull[j & 1]);
         release(&bars->vempty[s]);
@@ -324,61 +329,89 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!vis) sv[i >> 5][i & 31] = __float_as_uint(NEG_INF);
         }
       }
-      float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+      // P goes to its own TMEM buffer (P(j+2) reuses it once S(j+2),
+      // issued after PV(j), has completed), so it may be written as soon as
+      // it is computed
+      const uint32_t p_addr = tmem + lane_off + kColP + (uint32_t)(j & 1) * 64u + (uint32_t)h * 32u;
+      // P = 2^(s * scale - m) of this warp's 64 columns; returns their sum
+      auto exp_write = [&](float m) -> float {
+        if (!ok) return 0.f;
+        const bool live = m != NEG_INF;
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(live ? -m : 0.f, live ? -m : 0.f);
+        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv[i >> 4][(2 * i) & 31]),
-                          __uint_as_float(sv[i >> 4][(2 * i + 1) & 31]));
-      // both warps have read their S columns once they pass this barrier, so
-      // P may then overwrite the first 64 S columns
-      bars->xmax[h][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      pair_sync();
-      const float m_t = fmaxf(bars->xmax[0][r], bars->xmax[1][r]) * scale_log2;
-      pair_sync();  // both maxima read before the next tile overwrites them
-      const bool need = m_t > m_used + kGrow;  // true for the first visible scores
-      if (ok && __any_sync(0xffffffffu, need)) {
-        const float alpha = need ? ex2(m_used - m_t) : 1.f;  // 0 when m was -inf
-        if (need) {
-          m_used = m_t;
-          l *= alpha;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x =
+                fma2(make_float2(__uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1])), sc2, nm2);
+            const float2 pp = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
+            acc2[i & 3] = add2(acc2[i & 3], pp);
+            pk[i] = pack_bf16(pp.x, pp.y);
+          }
+          tmem_st16(p_addr + c * 16, pk);
         }
-        // O holds PV(j-1) once that MMA completes: wait for it, then scale
-        // this warp's half of the O columns
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
-            (ok = warp_wait(&bars->ofull[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[16];
-            const uint32_t oa = tmem + lane_off + kColO + h * 64 + c * 16;
-            tmem_ld16(oa, o);
-            tmem_wait_ld();
+        const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
+        return st2.x + st2.y;
+      };
+      // Exact step: the tile's row max over both column halves; a larger max
+      // rescales the running sum and (from the second tile on) O, then P.
+      auto exact = [&]() -> float {
+        float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st16(oa, o);
+        for (int i = 0; i < 32; ++i)
+          mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                            __uint_as_float(sv[i >> 4][(2 * i + 1) & 31]));
+        bars->xmax[h][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        pair_sync();
+        const float m_t = fmaxf(bars->xmax[0][r], bars->xmax[1][r]) * scale_log2;
+        pair_sync();  // both maxima read before they are overwritten
+        const bool need = m_t > m_used;
+        if (ok && __any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(m_used - m_t) : 1.f;  // 0 when m was -inf
+          if (need) {
+            m_used = m_t;
+            l *= alpha;
+          }
+          // O holds PV(j-1) once that MMA completes: wait for it, then scale
+          // this warp's half of the O columns
+          if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f) &&
+              (ok = warp_wait(&bars->ofull[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[16];
+              const uint32_t oa = tmem + lane_off + kColO + h * 64 + c * 16;
+              tmem_ld16(oa, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(oa, o);
+            }
           }
         }
+        return exp_write(m_used);
+      };
+      // Both warps of a pair hold the same running max, so these decisions
+      // are the same in both and the pair barriers stay matched.
+      float tsum;
+      if (__any_sync(0xffffffffu, m_used == NEG_INF)) {
+        tsum = exact();  // first visible scores of the row
+      } else {
+        // later tiles: against the running max in one pass; a row whose
+        // tile sum leaves [0, 2^kGrow] (a score far above the running max,
+        // or an overflow) is redone exactly by both warps of the pair
+        tsum = exp_write(m_used);
+        bars->xflag[j & 1][h][r] = !(tsum <= kMaxTileSum);
+        pair_sync();
+        const bool redo = bars->xflag[j & 1][0][r] | bars->xflag[j & 1][1][r];
+        if (__any_sync(0xffffffffu, redo)) tsum = exact();
       }
       if (!ok) continue;
-      const bool live = m_used != NEG_INF;
-      const float2 sc2 = make_float2(scale_log2, scale_log2);
-      const float2 nm2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
-      float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x =
-              fma2(make_float2(__uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1])), sc2, nm2);
-          const float2 pp = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
-          acc2[i & 3] = add2(acc2[i & 3], pp);
-          pk[i] = pack_bf16(pp.x, pp.y);
-        }
-        tmem_st16(s_addr + h * 32 + c * 16, pk);  // P for S columns [64h + 32c, +32)
-      }
-      const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
-      l += st2.x + st2.y;
+      l += tsum;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bars->pfull[j & 1]);
