@@ -332,8 +332,8 @@ int spec_accept(int mode, const void *logits, int dtype, int batch, int n_nodes,
  *   k_cache, v_cache  [n_layers, batch, hkv, s_max, head_dim]
  *   k_tree,  v_tree   [n_layers, batch, hkv, n_nodes, head_dim]
  *   elem_bytes        2 (bf16) or 4 (f32); head_dim * elem_bytes % 16 == 0
- *   prefix_len_out    may equal prefix_len (updated in place after the
- *                     copies, by a second kernel on the same stream)
+ *   prefix_len_out    may equal prefix_len (each sequence's entry is
+ *                     updated in place after its copies); may be NULL
  * A row past s_max or a path entry outside [0, n_nodes) sets a device
  * status and that sequence is neither copied nor advanced.
  * ------------------------------------------------------------------ */

@@ -8,7 +8,7 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 
 __device__ __forceinline__ bool commit_ok(int P, int L, int s_max, int path_cap, int N,
                                           const int32_t *path, int *code) {
@@ -24,54 +24,48 @@ __device__ __forceinline__ bool commit_ok(int P, int L, int s_max, int path_cap,
   return true;
 }
 
-// grid: (layer * batch * hkv); each CTA copies rows 0..L of one
-// (layer, sequence, KV head) for K and V with 16-byte vectors.
+// One CTA per sequence: copies rows 0..L of every (layer, KV head) for K and
+// V with 16-byte vectors, then advances that sequence's prefix length.  No
+// other CTA reads or writes the sequence's entry, so the update may be in
+// place (prefix_len_out == prefix_len) without a second launch.
 __global__ void __launch_bounds__(kThreads)
-    commit_copy_kernel(uint4 *kc, uint4 *vc, const uint4 *__restrict__ kt,
-                       const uint4 *__restrict__ vt, int batch, int hkv, int s_max, int N,
-                       int vec_per_row, const int32_t *__restrict__ acc_len,
-                       const int32_t *__restrict__ acc_path, int path_cap,
-                       const int32_t *__restrict__ prefix_len, int32_t *status) {
+    commit_kernel(uint4 *kc, uint4 *vc, const uint4 *__restrict__ kt, const uint4 *__restrict__ vt, int n_layers,
+                  int batch, int hkv, int s_max, int N, int vec_per_row, const int32_t *__restrict__ acc_len,
+                  const int32_t *__restrict__ acc_path, int path_cap, const int32_t *prefix_len,
+                  int32_t *prefix_len_out, int32_t *status) {
   __shared__ int s_path[SPEC_MAX_NODES + 1];
-  __shared__ int s_ok;
-  const int lbh = blockIdx.x;
-  const int h = lbh % hkv, b = (lbh / hkv) % batch;
-  const int64_t layer = lbh / (hkv * batch);
-  const int P = prefix_len[b], L = acc_len[b];
+  __shared__ int s_ok, s_P, s_L;
+  const int b = blockIdx.x;
   if (threadIdx.x == 0) {
+    const int P = prefix_len[b], L = acc_len[b];
     int code = 0;
     const int32_t *path = acc_path + (int64_t)b * path_cap;
     s_ok = commit_ok(P, L, s_max, path_cap, N, path, &code);
     if (!s_ok) sv::report(status, code);
     else
       for (int j = 0; j <= L; ++j) s_path[j] = path[j];
+    s_P = P;
+    s_L = L;
   }
   __syncthreads();
-  if (!s_ok) return;
-  const int64_t lb = (layer * batch + b) * hkv + h;
-  const int64_t cache_row0 = (lb * s_max + P) * vec_per_row;
-  const int64_t tree_row0 = lb * N * vec_per_row;
-  const int total = (L + 1) * vec_per_row;
-  for (int e = threadIdx.x; e < 2 * total; e += kThreads) {
-    const bool is_v = e >= total;
-    const int f = is_v ? e - total : e;
-    const int j = f / vec_per_row, c = f % vec_per_row;
-    const int64_t src = tree_row0 + (int64_t)s_path[j] * vec_per_row + c;
-    const int64_t dst = cache_row0 + (int64_t)j * vec_per_row + c;
-    if (is_v) vc[dst] = vt[src];
-    else kc[dst] = kt[src];
+  const int P = s_P, L = s_L;
+  if (s_ok) {
+    const int per_head = (L + 1) * vec_per_row;  // vectors of one (layer, head) for K or V
+    const int64_t total = (int64_t)n_layers * hkv * per_head;
+    for (int64_t e = threadIdx.x; e < 2 * total; e += kThreads) {
+      const bool is_v = e >= total;
+      const int64_t f = is_v ? e - total : e;
+      const int64_t lh = f / per_head;  // layer * hkv + head
+      const int rem = (int)(f % per_head);
+      const int j = rem / vec_per_row, c = rem % vec_per_row;
+      const int64_t lb = ((lh / hkv) * batch + b) * hkv + lh % hkv;
+      const int64_t src = (lb * N + s_path[j]) * vec_per_row + c;
+      const int64_t dst = (lb * s_max + P + j) * vec_per_row + c;
+      if (is_v) vc[dst] = vt[src];
+      else kc[dst] = kt[src];
+    }
   }
-}
-
-__global__ void commit_len_kernel(int batch, int s_max, int N, const int32_t *__restrict__ acc_len,
-                                  const int32_t *__restrict__ acc_path, int path_cap,
-                                  const int32_t *prefix_len, int32_t *prefix_len_out) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= batch) return;
-  const int P = prefix_len[b], L = acc_len[b];
-  int code = 0;
-  const bool ok = commit_ok(P, L, s_max, path_cap, N, acc_path + (int64_t)b * path_cap, &code);
-  prefix_len_out[b] = ok ? P + L + 1 : P;
+  if (prefix_len_out && threadIdx.x == 0) prefix_len_out[b] = s_ok ? P + L + 1 : P;
 }
 
 }  // namespace
@@ -81,12 +75,8 @@ int sv_kv_commit(void *kc, void *vc, const void *kt, const void *vt, int elem_by
                  const int32_t *acc_path, int path_cap, const int32_t *prefix_len,
                  int32_t *prefix_len_out, int32_t *status, cudaStream_t stream) {
   const int vec_per_row = head_dim * elem_bytes / 16;
-  commit_copy_kernel<<<n_layers * batch * hkv, kThreads, 0, stream>>>(
-      (uint4 *)kc, (uint4 *)vc, (const uint4 *)kt, (const uint4 *)vt, batch, hkv, s_max, n_nodes,
-      vec_per_row, acc_len, acc_path, path_cap, prefix_len, status);
-  int rc = sv_launch_status();
-  if (rc != SPEC_OK || prefix_len_out == nullptr) return rc;
-  commit_len_kernel<<<(batch + 127) / 128, 128, 0, stream>>>(batch, s_max, n_nodes, acc_len, acc_path,
-                                                             path_cap, prefix_len, prefix_len_out);
+  commit_kernel<<<batch, kThreads, 0, stream>>>((uint4 *)kc, (uint4 *)vc, (const uint4 *)kt, (const uint4 *)vt,
+                                                n_layers, batch, hkv, s_max, n_nodes, vec_per_row, acc_len,
+                                                acc_path, path_cap, prefix_len, prefix_len_out, status);
   return sv_launch_status();
 }
