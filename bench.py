@@ -339,6 +339,9 @@ def attention_only(name: str, device, steps: int, warmup: int):
     times = []
     for _ in range(steps):
         flush.fill_(1.0)
+        # the GPU idles here while the host queues the events and launches,
+        # so the timed interval holds device work only
+        torch.cuda._sleep(2_000_000)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(); call(); e1.record()
         e1.synchronize()

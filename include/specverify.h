@@ -69,7 +69,8 @@ enum {
   SPEC_DEV_BAD_PATH = 3,     /* accepted path entry out of [0, n_nodes)     */
   SPEC_DEV_BAD_POOL = 4,     /* pool parent not earlier / confidence > 1    */
   SPEC_DEV_BAD_TOKEN = 5,    /* token id outside [0, vocab)                 */
-  SPEC_DEV_TIMEOUT = 6       /* a bounded device-side wait gave up          */
+  SPEC_DEV_TIMEOUT = 6,      /* a bounded device-side wait gave up          */
+  SPEC_DEV_INTERNAL = 7      /* a kernel's own layout precondition failed   */
 };
 
 /* dtype codes */

@@ -44,16 +44,18 @@ def test_status_strings_without_gpu(built_lib):
 
 
 def test_split_planner_is_host_only_and_sane(built_lib):
-    """tree_attn_plan_splits runs on the host: a uniform batch of long
-    prefixes that already fills the SMs keeps one split; a ragged batch of
-    few sequences is split; bad arguments return an error."""
+    """tree_attn_plan_splits runs on the host.  Shapes with more than 128
+    query rows per KV head go to the SM-pair kernel, which balances its own
+    work (one "split"); for the single-CTA kernel a few long ragged
+    sequences are split; bad arguments return an error."""
     import torch
     from tree_speculative_decoding_attn_gb300 import specverify as sv
     bf = torch.bfloat16
-    assert sv.tree_attn_plan_splits(bf, 64, 32, 64, 8, 128, [4096] * 64) == 1
     ragged = [512, 8192, 1024, 3000, 700, 6000, 2048, 4000]
-    assert sv.tree_attn_plan_splits(bf, 8, 60, 32, 8, 128, ragged) > 1
-    assert 1 <= sv.tree_attn_plan_splits(bf, 4, 64, 32, 8, 128, [32768] * 4) <= 64
+    assert sv.tree_attn_plan_splits(bf, 64, 32, 64, 8, 128, [4096] * 64) == 1
+    assert sv.tree_attn_plan_splits(bf, 8, 60, 32, 8, 128, ragged) == 1
+    assert sv.tree_attn_plan_splits(bf, 4, 64, 32, 8, 128, [32768] * 4) == 1
+    assert sv.tree_attn_plan_splits(bf, 2, 64, 32, 32, 128, [8192, 600]) > 1       # MHA: 64 rows per KV head
     assert 1 <= sv.tree_attn_plan_splits(torch.float32, 1, 5, 4, 4, 64, [128]) <= 64
     with pytest.raises(sv.SpecError):
         sv.tree_attn_plan_splits(bf, 2, 65, 8, 8, 128, [10, 10])     # more than 64 tree nodes

@@ -1,0 +1,947 @@
+// Tree attention for GQA groups with more than 128 query rows per KV head
+// (bf16 in, float32 softmax and accumulation, head_dim 128), on pairs of
+// SMs: tcgen05.mma.cta_group::2 with M = 256, a persistent grid, and a
+// stream-K split of the work.
+//
+// "5.3 Medusa、EAGLE 与 MTP" (infra-guide), sections 3.1 and 8: every node
+// attends to the shared prefix and to its ancestors-or-self; "Medusa,
+// explained", step 6: all nodes are scored in one pass.
+//
+// Rows.  Query row r of a (sequence, KV head) is node r / G, query head
+// kvh*G + r % G, so the G heads of a GQA group and all tree nodes share
+// every K/V tile.  A row group is (sequence, KV head, pair of 128-row query
+// tiles): CTA k of a cluster owns rows [256 p + 128 k, +128) of pair p.
+//
+// Work.  The units of a row group are its tree tile (unit 0) and its prefix
+// tiles of 128 keys (units 1..).  All units of all row groups, in order
+// (sequence, KV head, pair, unit), form one sequence of U units; cluster c
+// of C takes units [floor(cU/C), floor((c+1)U/C)).  A row group that lies
+// wholly inside one cluster's range is normalised and written out; the row
+// groups cut by a range end leave float32 partials (unnormalised O, running
+// max in log2 units, row sum) in workspace slot (c, first/last), merged by
+// attn_tc2_combine_kernel.  Every cluster streams the same number of tiles
+// whatever the prefix lengths.
+//
+// Pair MMA.  The even CTA issues every MMA for both.  M = 256: each CTA
+// holds its own 128 query rows (Q in shared memory; S, P and O in its own
+// TMEM) and half of every K/V tile: CTA k stages keys [64k, 64k+64) of K and
+// head dims [64k, 64k+64) of V, 16 KB each, so five-deep K and V rings and
+// two Q buffers fit in one SM's shared memory.
+//
+//   warp 0   Q and K loads; warp 10: V loads (TMA, 128-byte swizzle; one
+//            warp each, so neither ring waits on the other's releases).
+//            The even CTA's Q/K loads signal its full barriers directly; the
+//            odd CTA's signal local barriers
+//   warp 1   pair TMEM allocation; in the even CTA it issues
+//              S(g) = Q K(g)^T   into TMEM columns [128 (g%3), +128)
+//            once PV(g-3), which read that buffer's P, has completed; in the
+//            odd CTA it forwards the arrival of its Q/K halves to the even CTA
+//   warp 11  in the even CTA, issues
+//              O   += P(g) V(g)  (P written over S(g)'s columns as bf16)
+//            Two issuing threads: one thread's tcgen05.mma / commit stream
+//            (about 60 cycles per instruction) would otherwise bound the tile
+//            rate
+//   warps 2-9  softmax and epilogue: two warps per TMEM lane quarter, one
+//            per 64-key half.  The first tile of a row group takes the exact
+//            row max (shared by the pair of warps through shared memory);
+//            later tiles exponentiate against the running max in one pass
+//            and are redone exactly only if their row sum leaves [0, 2^64].
+//            V: before PV(g) the even CTA's PV issuer waits for its own V
+//            half to land and zeroes the V rows past the last key of a
+//            partial tile (stale cache rows need not be finite); the odd
+//            CTA's warp 11 does the same for its half and then arrives on the
+//            even CTA's P barrier of the tile.
+//
+// Every mbarrier wait is bounded; on a timeout the CTA reports
+// SPEC_DEV_TIMEOUT, lets its own copies and the pair's MMAs finish, frees
+// TMEM and returns.
+#include <math.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace {
+
+using namespace sv::ptx;
+
+constexpr int kBN = 128;                     // keys per tile
+constexpr int kD = 128;                      // head_dim
+constexpr int kKS = 5;                       // K ring stages
+constexpr int kVS = 5;                       // V ring stages
+constexpr int kQB = 2;                       // Q buffers
+constexpr int kPrefetch = 0;                 // L2 prefetch distance in tiles (0: none)
+constexpr int kThreads = 384;
+constexpr int kPairRows = 256;
+constexpr uint32_t kQBytes = 128 * kD * 2;   // 128 rows x 128 dims
+constexpr uint32_t kQHalf = kQBytes / 2;     // one 64-dim swizzle column
+constexpr uint32_t kKBytes = 64 * kD * 2;    // 64 keys x 128 dims
+constexpr uint32_t kKHalf = kKBytes / 2;
+constexpr uint32_t kVBytes = kBN * 64 * 2;   // 128 keys x 64 dims
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kSB = 3;                       // S/P buffers in TMEM (128 columns each)
+constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 in all)
+constexpr float kMaxTileSum = 18446744073709551616.0f;  // 2^64
+constexpr uint16_t kBoth = 3;                // CTA mask of the pair
+constexpr int kPartial = sv_partial_stride(kD);
+
+struct Bars {
+  uint64_t kland[kKS], kempty[kKS], kfull[kKS];
+  uint64_t vland[kVS], vempty[kVS];
+  uint64_t qland[kQB], qempty[kQB], qfull[kQB];
+  uint64_t sfull[kSB], pfull[kSB], ofull[kSB], drain;
+  uint32_t tmem;
+  volatile int abort;
+  int start_b, start_gi, start_t, n_tiles;     // this cluster's first unit and unit count
+  float xmax[2][128];                          // per-row partial maxima of the two key halves
+  float xsum[2][128];                          // per-row partial sums at a row group's end
+  unsigned char xflag[2][2][128];              // "tile needs the exact max", by tile parity
+};
+constexpr uint32_t kTileBytes = kQB * kQBytes + kKS * kKBytes + kVS * kVBytes;
+constexpr uint32_t kSmemBytes = kTileBytes + sizeof(Bars);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA exceeds 227 KB");
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(256, 128, 0, 0);   // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(256, 128, 0, 1);  // V MN-major (dims contiguous)
+
+// ---------------------------------------------------------------------------
+// Work schedule, shared by the main and combine kernels
+// ---------------------------------------------------------------------------
+struct Sched {
+  const int32_t *prefix_len;
+  int batch, hkv, pairs, n_nodes, s_max, max_prefix, n_clusters;
+  __device__ int gpb() const { return hkv * pairs; }  // row groups per sequence
+};
+
+// Effective prefix of sequence b: its length, or 0 when out of bounds (the
+// sequence is reported and its output left unwritten).
+__device__ __forceinline__ int seq_prefix(const Sched &s, int b, bool *valid) {
+  const int P = s.prefix_len[b];
+  const bool ok = P >= 0 && P <= s.max_prefix && P <= s.s_max;
+  *valid = ok;
+  return ok ? P : 0;
+}
+__device__ __forceinline__ int seq_tiles(int P) { return 1 + (P + kBN - 1) / kBN; }
+
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Units of the row groups of sequences [0, b_end) (full warp).
+__device__ long long warp_units_before(const Sched &s, int b_end) {
+  const int lane = threadIdx.x & 31;
+  long long acc = 0;
+  for (int b0 = 0; b0 < b_end; b0 += 32) {
+    long long v = 0;
+    if (b0 + lane < b_end) {
+      bool ok;
+      v = seq_tiles(seq_prefix(s, b0 + lane, &ok));
+    }
+    acc += warp_sum_ll(v);
+  }
+  return acc * s.gpb();
+}
+
+// Sequence, row group and tile of unit u < U (full warp).
+__device__ void warp_locate(const Sched &s, long long u, int *b_out, int *gi_out, int *t_out) {
+  const int lane = threadIdx.x & 31;
+  long long base = 0;
+  for (int b0 = 0; b0 < s.batch; b0 += 32) {
+    const int b = b0 + lane;
+    int n = 0;
+    if (b < s.batch) {
+      bool ok;
+      n = seq_tiles(seq_prefix(s, b, &ok));
+    }
+    const long long v = (long long)n * s.gpb();
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, b < s.batch && base + incl > u);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const long long before = base + __shfl_sync(0xffffffffu, incl - v, l);
+      const int nl = __shfl_sync(0xffffffffu, n, l);
+      const long long local = u - before;
+      *b_out = b0 + l;
+      *gi_out = (int)(local / nl);
+      *t_out = (int)(local % nl);
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  *b_out = s.batch;
+  *gi_out = 0;
+  *t_out = 0;
+}
+
+__device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
+// Cluster whose range holds unit u (the largest c with range_start(c) <= u).
+__device__ __forceinline__ int cluster_of(long long u, long long U, long long C) {
+  return (int)(((u + 1) * C - 1) / U);
+}
+
+// Walks the tiles of a cluster's range in order.  The next sequence's
+// prefix length is loaded one sequence ahead: a global load waited for at a
+// sequence boundary would stall the walk for a full memory latency.
+struct Cur {
+  int b, gi, t;   // sequence, row group within it, tile within the row group
+  int n, P;       // tiles of the row group, effective prefix
+  bool ok;        // prefix within bounds
+  int raw_next;   // prefix_len[b + 1] (0 past the batch)
+};
+__device__ __forceinline__ int load_prefix(const Sched &s, int b) { return b < s.batch ? s.prefix_len[b] : 0; }
+__device__ __forceinline__ void cur_apply(Cur &c, const Sched &s, int raw) {
+  c.ok = raw >= 0 && raw <= s.max_prefix && raw <= s.s_max;
+  c.P = c.ok ? raw : 0;
+  c.n = seq_tiles(c.P);
+}
+__device__ __forceinline__ Cur cur_begin(const Bars *bars, const Sched &s) {
+  Cur c;
+  c.b = bars->start_b;
+  c.gi = bars->start_gi;
+  c.t = bars->start_t;
+  cur_apply(c, s, load_prefix(s, c.b));
+  c.raw_next = load_prefix(s, c.b + 1);
+  return c;
+}
+__device__ __forceinline__ void cur_next(Cur &c, const Sched &s) {
+  if (++c.t == c.n) {
+    c.t = 0;
+    if (++c.gi == s.gpb()) {
+      c.gi = 0;
+      ++c.b;
+      cur_apply(c, s, c.raw_next);
+      c.raw_next = load_prefix(s, c.b + 1);
+    }
+  }
+}
+// Valid keys of a prefix tile (t >= 1).
+__device__ __forceinline__ int tile_keys(const Cur &c) { return min(kBN, c.P - (c.t - 1) * kBN); }
+
+__device__ __forceinline__ void give_up(Bars *bars, int32_t *status) {
+  bars->abort = 1;
+  sv::report(status, SPEC_DEV_TIMEOUT);
+}
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_wait_cluster(bar, parity, kWaitLimit));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Waits for this CTA's V half of tile g to land and zeroes its rows past the
+// last key of a partial tile, up to the next multiple of 16 (the last PV
+// k-step reads them with zero probabilities; stale cache rows need not be
+// finite).  Full warp; false on timeout.
+__device__ __forceinline__ bool v_ready(Bars *bars, uint8_t *sV, int g, int nkeys) {
+  const int st = g % kVS;
+  if (!warp_wait(&bars->vland[st], (g / kVS) & 1)) return false;
+  if (nkeys < kBN) {
+    uint4 *v = reinterpret_cast<uint4 *>(sV + st * kVBytes);
+    const int end = min(kBN, (nkeys + 15) & ~15) * 8;
+    for (int e = nkeys * 8 + (int)(threadIdx.x & 31); e < end; e += 32) v[e] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  return true;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                    const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
+                    const __grid_constant__ CUtensorMap tm_vt, const Sched s, const uint64_t *__restrict__ anc,
+                    __nv_bfloat16 *__restrict__ out, float *__restrict__ ws, int Hq, float scale_log2,
+                    int32_t *status) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t *sQ = smem;
+  uint8_t *sK = sQ + kQB * kQBytes;
+  uint8_t *sV = sK + kKS * kKBytes;
+  Bars *bars = reinterpret_cast<Bars *>(sV + kVS * kVBytes);
+
+  const int N = s.n_nodes, G = Hq / s.hkv, R = N * G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int cluster = blockIdx.x >> 1;
+
+  // The 128-byte swizzle needs 1024-byte aligned tiles; both CTAs of a
+  // cluster see the same layout, so they leave together.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) sv::report(status, SPEC_DEV_INTERNAL);
+    return;
+  }
+  if (warp == 0) {
+    // with C = min(clusters, U) every range below C holds at least one unit
+    const long long U = warp_units_before(s, s.batch);
+    const long long C = min((long long)s.n_clusters, U);
+    const long long u0 = cluster < C ? range_start(cluster, U, C) : 0;
+    const long long u1 = cluster < C ? range_start(cluster + 1, U, C) : 0;
+    int b = s.batch, gi = 0, t = 0;
+    if (u1 > u0) warp_locate(s, u0, &b, &gi, &t);
+    if (lane == 0) {
+      bars->start_b = b;
+      bars->start_gi = gi;
+      bars->start_t = t;
+      bars->n_tiles = (int)(u1 - u0);
+    }
+  }
+  __syncthreads();
+  const int T = bars->n_tiles;
+  if (T == 0) return;  // same range for both CTAs of the cluster
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kKS; ++i) {
+      mbar_init(&bars->kland[i], 1);
+      mbar_init(&bars->kempty[i], 1);
+      mbar_init(&bars->kfull[i], 2);
+    }
+    for (int i = 0; i < kVS; ++i) {
+      mbar_init(&bars->vland[i], 1);
+      mbar_init(&bars->vempty[i], 1);
+    }
+    for (int i = 0; i < kQB; ++i) {
+      mbar_init(&bars->qland[i], 1);
+      mbar_init(&bars->qempty[i], 1);
+      mbar_init(&bars->qfull[i], 2);
+    }
+    for (int i = 0; i < kSB; ++i) {
+      mbar_init(&bars->sfull[i], 1);
+      mbar_init(&bars->ofull[i], 1);
+      // one arrival per softmax warp of both CTAs and one for the odd CTA's
+      // V half; the softmax may finish tiles g .. g+kSB-1 before the PV
+      // issuer observes tile g, never g+kSB (it needs S(g+kSB), issued
+      // after PV(g) completed)
+      mbar_init(&bars->pfull[i], 17);
+    }
+    mbar_init(&bars->drain, 2);  // one commit from each MMA-issuing warp
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 1) tmem_alloc_pair(&bars->tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the partner's barriers exist before any remote arrival or commit
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem;
+  const int pairs = s.pairs;
+
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ loads
+    if (lane == 0) {
+      const bool is_v = warp == 10;
+      Cur c = cur_begin(bars, s);
+      int seg = 0, issued = 0, q_issued = 0;
+      if (!is_v) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_kc);
+        tma_prefetch_desc(&tm_kt);
+      } else {
+        tma_prefetch_desc(&tm_vc);
+        tma_prefetch_desc(&tm_vt);
+      }
+      Cur cpf = c;  // kPrefetch tiles ahead of c
+      for (int i = 0; i < kPrefetch && i < T; ++i) cur_next(cpf, s);
+      for (int g = 0; g < T; ++g) {
+        const bool first = g == 0 || c.t == 0;
+        if (first && g > 0) ++seg;
+        const int kvh = c.gi / pairs, pair = c.gi % pairs;
+        const int bh = c.b * s.hkv + kvh;
+        if (kPrefetch > 0 && g + kPrefetch < T) {
+          // warm L2 with this CTA's half of tile g + kPrefetch
+          const int pbh = cpf.b * s.hkv + cpf.gi / pairs;
+          const bool ptree = cpf.t == 0;
+          const int prow = ptree ? pbh * N : pbh * s.s_max + (cpf.t - 1) * kBN;
+          if (is_v) {
+            tma_prefetch_2d(ptree ? &tm_vt : &tm_vc, 64 * (int)rank, prow);
+          } else {
+            tma_prefetch_2d(ptree ? &tm_kt : &tm_kc, 0, prow + 64 * (int)rank);
+            tma_prefetch_2d(ptree ? &tm_kt : &tm_kc, 64, prow + 64 * (int)rank);
+          }
+          cur_next(cpf, s);
+        }
+        if (!is_v && first) {
+          const int qb = seg % kQB;
+          if (!mbar_wait_cluster(&bars->qempty[qb], ((seg / kQB) & 1) ^ 1, kWaitLimit) || bars->abort) {
+            give_up(bars, status);
+            break;
+          }
+          uint64_t *qbar = rank == 0 ? &bars->qfull[qb] : &bars->qland[qb];
+          mbar_expect_tx(qbar, kQBytes);
+          const int node0 = c.b * N + (pair * kPairRows + (int)rank * 128) / G;
+          tma_load_4d(sQ + qb * kQBytes, &tm_q, 0, 0, kvh, node0, qbar);
+          tma_load_4d(sQ + qb * kQBytes + kQHalf, &tm_q, 64, 0, kvh, node0, qbar);
+          ++q_issued;
+        }
+        const int st = g % (is_v ? kVS : kKS);
+        const int use = g / (is_v ? kVS : kKS);
+        uint64_t *empty = is_v ? &bars->vempty[st] : &bars->kempty[st];
+        uint64_t *land = is_v ? &bars->vland[st] : (rank == 0 ? &bars->kfull[st] : &bars->kland[st]);
+        if (!mbar_wait_cluster(empty, (use & 1) ^ 1, kWaitLimit) || bars->abort) {
+          give_up(bars, status);
+          break;
+        }
+        const bool tree = c.t == 0;
+        const int row0 = tree ? bh * N : bh * s.s_max + (c.t - 1) * kBN;
+        if (is_v) {
+          mbar_expect_tx(land, kVBytes);
+          tma_load_2d(sV + st * kVBytes, tree ? &tm_vt : &tm_vc, 64 * (int)rank, row0, land);
+        } else {
+          mbar_expect_tx(land, kKBytes);
+          const CUtensorMap *m = tree ? &tm_kt : &tm_kc;
+          tma_load_2d(sK + st * kKBytes, m, 0, row0 + 64 * (int)rank, land);
+          tma_load_2d(sK + st * kKBytes + kKHalf, m, 64, row0 + 64 * (int)rank, land);
+        }
+        ++issued;
+        cur_next(c, s);
+      }
+      if (bars->abort) {  // let the copies into this CTA land before it exits (bounded)
+        // (a full barrier of the even CTA completes only with the odd CTA's
+        // half as well; its own copies are then done too)
+        const int ns = is_v ? kVS : kKS;
+        for (int j = issued > ns ? issued - ns : 0; j < issued; ++j)
+          mbar_wait_cluster(is_v ? &bars->vland[j % ns] : (rank == 0 ? &bars->kfull[j % ns] : &bars->kland[j % ns]),
+                            (j / ns) & 1, kWaitLimit);
+        if (!is_v)
+          for (int j = q_issued > kQB ? q_issued - kQB : 0; j < q_issued; ++j)
+            mbar_wait_cluster(rank == 0 ? &bars->qfull[j % kQB] : &bars->qland[j % kQB], (j / kQB) & 1, kWaitLimit);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (rank == 0) {
+      const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK);
+      Cur cs = cur_begin(bars, s);
+      int seg_s = 0;
+      // S(g) = Q K(g)^T into S buffer g % kSB; called for g = 0, 1, 2, ...
+      // in order.  Descriptors are a base plus constant offsets (the start
+      // address field is the low 14 bits, in 16-byte units).
+      auto issue_s = [&](int g) -> bool {
+        const bool first = g == 0 || cs.t == 0;
+        if (first && g > 0) ++seg_s;
+        const int qb = seg_s % kQB, st = g % kKS;
+        if (first && !warp_wait(&bars->qfull[qb], (seg_s / kQB) & 1)) return false;
+        if (!warp_wait(&bars->kfull[st], (g / kKS) & 1)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t qd = smem_desc_sw128(qa + (uint32_t)qb * kQBytes, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(ka + (uint32_t)st * kKBytes, 16, 1024);
+          const uint32_t d = tmem + (uint32_t)(g % kSB) * 128u;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss_pair(d, qd + (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                        kd + (uint64_t)(((kk >> 2) * kKHalf + (kk & 3) * 32) >> 4), kIdescS, kk > 0);
+          mma_commit_pair_mc(&bars->sfull[g % kSB], kBoth);
+          mma_commit_pair_mc(&bars->kempty[st], kBoth);
+          if (g == T - 1 || cs.t == cs.n - 1) mma_commit_pair_mc(&bars->qempty[qb], kBoth);
+        }
+        __syncwarp();
+        cur_next(cs, s);
+        return true;
+      };
+      bool ok = true;
+      for (int g = 0; ok && g < T; ++g) {
+        // S(g) overwrites the buffer whose P PV(g - kSB) read
+        if (g >= kSB && !(ok = warp_wait(&bars->ofull[g % kSB], ((g - kSB) / kSB) & 1))) break;
+        ok = issue_s(g);
+      }
+      if (!ok) give_up(bars, status);
+      if (lane == 0) mma_commit_pair_mc(&bars->drain, kBoth);  // after every MMA issued above
+      __syncwarp();
+    } else {
+      // odd CTA: its Q and K halves have landed -> arrive on the even CTA's
+      // full barriers
+      Cur c = cur_begin(bars, s);
+      int seg = 0;
+      for (int g = 0; g < T; ++g) {
+        const bool first = g == 0 || c.t == 0;
+        if (first && g > 0) ++seg;
+        if (first) {
+          const int qb = seg % kQB;
+          if (!warp_wait(&bars->qland[qb], (seg / kQB) & 1) || bars->abort) {
+            give_up(bars, status);
+            break;
+          }
+          if (lane == 0) mbar_arrive_cluster(mapa_cluster(&bars->qfull[qb], 0));
+        }
+        const int st = g % kKS;
+        if (!warp_wait(&bars->kland[st], (g / kKS) & 1) || bars->abort) {
+          give_up(bars, status);
+          break;
+        }
+        if (lane == 0) mbar_arrive_cluster(mapa_cluster(&bars->kfull[st], 0));
+        cur_next(c, s);
+      }
+      __syncwarp();
+    }
+    // both CTAs: every pair MMA (and its commits into this CTA) done
+    mbar_wait_cluster(&bars->drain, 0, kWaitLimit);
+    __syncwarp();
+  } else if (warp == 11) {
+    // ------------------------------------------------------------ PV issuer
+    if (rank == 0) {
+      const uint32_t va = smem_u32(sV);
+      Cur cp = cur_begin(bars, s);
+      bool ok = true;
+      for (int g = 0; ok && g < T; ++g) {
+        // O += P(g) V(g) once P of both CTAs is ready (which also covers both
+        // V halves of tile g)
+        const int nkeys = cp.t == 0 ? N : tile_keys(cp);
+        if (!(ok = warp_wait(&bars->pfull[g % kSB], (g / kSB) & 1) && v_ready(bars, sV, g, nkeys))) break;
+        tc_fence_after();
+        const bool first = g == 0 || cp.t == 0;
+        const int st = g % kVS;
+        const int ksteps = (nkeys + 15) >> 4;
+        if (lane == 0) {
+          const uint64_t vd = smem_desc_sw128(va + (uint32_t)st * kVBytes, kVBytes, 1024);
+          const uint32_t pbase = tmem + (uint32_t)(g % kSB) * 128u;
+          const uint32_t acc0 = first ? 0u : 1u;
+          // P of keys [16kk, +16): the first key half's softmax warps wrote
+          // columns [0, 32) of the buffer, the second half's [64, 96)
+          if (ksteps == kBN / 16) {
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts_pair(tmem + kColO, pbase + (kk < 4 ? (uint32_t)kk * 8u : 64u + (uint32_t)(kk - 4) * 8u),
+                          vd + (uint64_t)((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+          } else {
+            for (int kk = 0; kk < ksteps; ++kk)
+              mma_ts_pair(tmem + kColO, pbase + (kk < 4 ? (uint32_t)kk * 8u : 64u + (uint32_t)(kk - 4) * 8u),
+                          vd + (uint64_t)((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+          }
+          mma_commit_pair_mc(&bars->vempty[st], kBoth);
+          mma_commit_pair_mc(&bars->ofull[g % kSB], kBoth);
+        }
+        __syncwarp();
+        cur_next(cp, s);
+      }
+      if (!ok) give_up(bars, status);
+      if (lane == 0) mma_commit_pair_mc(&bars->drain, kBoth);  // after every MMA issued above
+      __syncwarp();
+    } else {
+      // odd CTA: its V half of each tile is ready -> arrive on the even
+      // CTA's P barrier of that tile.  V runs ahead of the softmax, so this
+      // arrival first waits for S(g) to complete: S(g) was issued after
+      // PV(g-kSB) completed, i.e. after the barrier's phase for tile g-kSB,
+      // so the arrival cannot fall into that earlier phase.
+      const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
+      Cur c = cur_begin(bars, s);
+      for (int g = 0; g < T; ++g) {
+        if (!warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1) || !v_ready(bars, sV, g, c.t == 0 ? N : tile_keys(c)) ||
+            bars->abort) {
+          give_up(bars, status);
+          break;
+        }
+        if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
+        cur_next(c, s);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int quarter = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t pair_bar = 1u + (uint32_t)quarter;
+    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
+    const float NEG_INF = -INFINITY;
+    Cur c = cur_begin(bars, s);
+    int seg = 0;
+    bool from_start = c.t == 0;
+    float m_used = NEG_INF, l = 0.f;  // l: this warp's half of the row sum
+    // ancestor bits of this thread's row in a row group (padding rows: all
+    // tree keys), loaded one row group ahead so the tree tile never waits
+    auto row_of = [&](int gi) { return (gi % pairs) * kPairRows + (int)rank * 128 + r; };
+    auto load_mask = [&](int b, int gi) -> uint64_t {
+      const int rr = row_of(gi);
+      return rr < R ? anc[(int64_t)b * N + rr / G] : ~0ull;
+    };
+    uint64_t amask = c.t == 0 ? load_mask(c.b, c.gi) : 0ull, amask_next = 0ull;
+    int rg = row_of(c.gi);
+    bool ok = true;
+    // A failed wait (timeout) or an abort turns the rest into a no-op that
+    // still passes every pair barrier, so the two warps of a pair always
+    // execute the same barriers.
+    for (int g = 0; g < T; ++g) {
+      const bool first = g == 0 || c.t == 0;
+      if (first) {
+        if (g > 0) {
+          ++seg;
+          from_start = true;
+          amask = amask_next;
+        }
+        m_used = NEG_INF;
+        l = 0.f;
+        rg = row_of(c.gi);
+      }
+      if (c.t == c.n - 1 && g + 1 < T) {  // the next tile starts the next row group
+        const bool same_b = c.gi + 1 < s.gpb();
+        amask_next = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0);
+      }
+      if (ok && (!warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1) || __any_sync(0xffffffffu, bars->abort != 0)))
+        ok = false;
+      const uint32_t s_addr = tmem + lane_off + (uint32_t)(g % kSB) * 128u;
+      uint32_t sv[2][32];
+      if (ok) {
+        tc_fence_after();
+        tmem_ld32(s_addr + h * 64, sv[0]);
+        tmem_ld32(s_addr + h * 64 + 32, sv[1]);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[0][i] = sv[1][i] = __float_as_uint(0.f);
+      }
+      const bool tree = c.t == 0;
+      const int nvalid = tree ? N : tile_keys(c);
+      if (tree || nvalid < kBN) {  // full prefix tiles need no mask
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const int col = h * 64 + i;
+          const bool vis = col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));  // tree: col < N <= 64
+          if (!vis) sv[i >> 5][i & 31] = __float_as_uint(NEG_INF);
+        }
+      }
+      // P of this warp's 64 keys, as bf16 pairs over the first 32 of its own
+      // 64 S columns
+      const uint32_t p_addr = s_addr + (uint32_t)h * 64u;
+      // P = 2^(s * scale - m) of this warp's 64 columns; returns their sum.
+      // Every row has a visible key in every tile (itself on the tree tile),
+      // so m is finite once a row group's first tile is done.
+      auto exp_write = [&](float m) -> float {
+        if (!ok) return 0.f;
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 nm2 = make_float2(-m, -m);
+        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 x =
+                fma2(make_float2(__uint_as_float(sv[cc][2 * i]), __uint_as_float(sv[cc][2 * i + 1])), sc2, nm2);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            acc2[i & 3] = add2(acc2[i & 3], pp);
+            pk[i] = pack_bf16(pp.x, pp.y);
+          }
+          tmem_st16(p_addr + cc * 16, pk);
+        }
+        const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
+        return st2.x + st2.y;
+      };
+      // Exact step: the tile's row max over both key halves; a larger max
+      // rescales the running sum and (after a row group's first tile) O.
+      auto exact = [&]() -> float {
+        float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv[i >> 4][(2 * i) & 31]),
+                            __uint_as_float(sv[i >> 4][(2 * i + 1) & 31]));
+        bars->xmax[h][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        pair_sync();
+        const float m_t = fmaxf(bars->xmax[0][r], bars->xmax[1][r]) * scale_log2;
+        pair_sync();  // both maxima read before they are overwritten
+        const bool need = m_t > m_used;
+        if (ok && __any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2(m_used - m_t) : 1.f;  // 0 when m was -inf
+          if (need) {
+            m_used = m_t;
+            l *= alpha;
+          }
+          // O holds PV(g-1) once that MMA completes: wait for it, then scale
+          // this warp's half of the O columns
+          if (!first && __any_sync(0xffffffffu, alpha != 1.f) &&
+              (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t o[16];
+              const uint32_t oa = tmem + lane_off + kColO + h * 64 + cc * 16;
+              tmem_ld16(oa, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st16(oa, o);
+            }
+          }
+        }
+        return exp_write(m_used);
+      };
+      // Both warps of a pair hold the same running max, so these decisions
+      // are the same in both and the pair barriers stay matched.
+      float tsum;
+      if (first) {
+        tsum = exact();
+      } else {
+        tsum = exp_write(m_used);
+        bars->xflag[g & 1][h][r] = !(tsum <= kMaxTileSum);
+        pair_sync();
+        const bool redo = bars->xflag[g & 1][0][r] | bars->xflag[g & 1][1][r];
+        if (__any_sync(0xffffffffu, redo)) tsum = exact();
+      }
+      if (ok) {
+        l += tsum;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
+      }
+      if (g == T - 1 || c.t == c.n - 1) {
+        // ---------------------------------------------------- epilogue
+        if (ok && !warp_wait(&bars->ofull[g % kSB], (g / kSB) & 1)) ok = false;
+        // the row sum's two halves through shared memory (the second barrier:
+        // both halves read before either warp can write the next row group's)
+        bars->xsum[h][r] = l;
+        pair_sync();
+        const float l_row = bars->xsum[0][r] + bars->xsum[1][r];
+        pair_sync();
+        const bool complete = from_start && c.t == c.n - 1;
+        const bool row_ok = rg < R;
+        const int kvh = c.gi / pairs;
+        if (ok && !__any_sync(0xffffffffu, bars->abort != 0)) {
+          tc_fence_after();
+          if (complete) {
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            __nv_bfloat16 *o = out + (((int64_t)c.b * N + rg / G) * Hq + kvh * G + rg % G) * kD + h * 64;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t ov[32];
+              tmem_ld32(tmem + lane_off + kColO + h * 64 + cc * 32, ov);
+              tmem_wait_ld();
+              if (row_ok && c.ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + cc * 32);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                  uint4 v;
+                  v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
+                  v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
+                  v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
+                  v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
+                  dst[q4] = v;
+                }
+              }
+            }
+          } else {
+            const int slot = cluster * 2 + (seg == 0 ? 0 : 1);
+            float *w = ws + ((int64_t)slot * kPairRows + (int)rank * 128 + r) * kPartial;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+              uint32_t ov[32];
+              tmem_ld32(tmem + lane_off + kColO + h * 64 + cc * 32, ov);
+              tmem_wait_ld();
+              if (row_ok) {
+                float4 *dst = reinterpret_cast<float4 *>(w + h * 64 + cc * 32);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4)
+                  dst[q4] = make_float4(__uint_as_float(ov[4 * q4]), __uint_as_float(ov[4 * q4 + 1]),
+                                        __uint_as_float(ov[4 * q4 + 2]), __uint_as_float(ov[4 * q4 + 3]));
+              }
+            }
+            if (row_ok && h == 0) {
+              w[kD] = m_used;
+              w[kD + 1] = l_row;
+            }
+          }
+        } else if (!ok) {
+          give_up(bars, status);
+        }
+      }
+      cur_next(c, s);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  // remote arrivals and multicast commits into either CTA are complete once
+  // both have passed their own __syncthreads
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+// Merges the partials of row groups cut by a cluster range end.  Block =
+// (row group, quarter of its 256 rows); warp = row; lane = 4 head dims.
+__global__ void __launch_bounds__(256) attn_tc2_combine_kernel(const float *__restrict__ ws,
+                                                               __nv_bfloat16 *__restrict__ out, const Sched s,
+                                                               int Hq) {
+  __shared__ int sh[4];  // c_lo, c_hi, first unit of the row group, usable
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gidx = blockIdx.x, b = gidx / s.gpb(), gi = gidx % s.gpb();
+  if (warp == 0) {
+    const long long U = warp_units_before(s, s.batch);
+    const long long C = min((long long)s.n_clusters, U);
+    const long long before = warp_units_before(s, b);
+    bool ok;
+    const int n = seq_tiles(seq_prefix(s, b, &ok));
+    const long long ug = before + (long long)gi * n;
+    if (lane == 0) {
+      sh[0] = cluster_of(ug, U, C);
+      sh[1] = cluster_of(ug + n - 1, U, C);
+      sh[2] = (int)(range_start(sh[0], U, C) == ug);  // the row group is c_lo's first segment
+      sh[3] = ok;
+    }
+  }
+  __syncthreads();
+  const int c_lo = sh[0], c_hi = sh[1];
+  if (c_lo == c_hi || !sh[3]) return;  // written by the main kernel, or reported there
+  const int G = Hq / s.hkv, R = s.n_nodes * G;
+  const int kvh = gi / s.pairs, pair = gi % s.pairs;
+  for (int rr = blockIdx.y * 64 + warp; rr < blockIdx.y * 64 + 64; rr += 8) {
+    const int rg = pair * kPairRows + rr;
+    if (rg >= R) break;
+    auto slot_row = [&](int c) -> const float * {
+      const int slot = c * 2 + ((c == c_lo && !sh[2]) ? 1 : 0);
+      return ws + ((int64_t)slot * kPairRows + rr) * kPartial;
+    };
+    float M = -INFINITY;
+    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, slot_row(c)[kD]);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c_lo; c <= c_hi; ++c) {
+      const float *w = slot_row(c);
+      const float f = exp2f(w[kD] - M);
+      L = fmaf(f, w[kD + 1], L);
+      const float4 o = reinterpret_cast<const float4 *>(w)[lane];
+      acc.x = fmaf(f, o.x, acc.x);
+      acc.y = fmaf(f, o.y, acc.y);
+      acc.z = fmaf(f, o.z, acc.z);
+      acc.w = fmaf(f, o.w, acc.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16 *o = out + (((int64_t)b * s.n_nodes + rg / G) * Hq + kvh * G + rg % G) * kD + lane * 4;
+    uint2 v;
+    v.x = pack_bf16(acc.x * inv, acc.y * inv);
+    v.y = pack_bf16(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(o) = v;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::atomic<EncodeTiledFn> fn{nullptr};
+  EncodeTiledFn f = fn.load();
+  if (!f) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      f = reinterpret_cast<EncodeTiledFn>(p);
+      fn.store(f);
+    }
+  }
+  return f;
+}
+
+int make_map(CUtensorMap *m, const void *base, cuuint32_t rank, const cuuint64_t *dims, const cuuint64_t *strides,
+             const cuuint32_t *box) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return SPEC_ERR_CUDA;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_clusters[kMaxDevices];
+
+// Clusters of the persistent grid: as many as fit on the current device at
+// once (one CTA per SM); looked up once per device.
+int tc2_clusters() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = g_clusters[dev].load();
+  if (n > 0) return n;
+  if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc2_kernel, &cfg) != cudaSuccess || clusters < 1) return 0;
+  g_clusters[dev].store(clusters);
+  return clusters;
+}
+
+}  // namespace
+
+bool sv_attn_tc2_supported(const SvAttnShape &s) {
+  if (s.dtype != SPEC_BF16 || s.head_dim != kD || s.hkv < 1) return false;
+  const int G = s.hq / s.hkv;
+  return G <= 128 && (128 % G) == 0 && s.n_nodes * G > 128;
+}
+
+size_t sv_attn_tc2_ws_bytes() {
+  const int c = tc2_clusters();
+  return c > 0 ? (size_t)c * 2 * kPairRows * kPartial * sizeof(float) : 0;
+}
+
+int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void *vc, const void *kt, const void *vt,
+                const int32_t *prefix_len, const uint64_t *anc, void *out, float scale, void *ws, size_t ws_bytes,
+                int32_t *status, cudaStream_t stream) {
+  const int C = tc2_clusters();
+  if (C < 1) return SPEC_ERR_CUDA;
+  if (!ws || ws_bytes < sv_attn_tc2_ws_bytes()) return SPEC_ERR_CAPACITY;
+  const int G = s.hq / s.hkv, R = s.n_nodes * G;
+  CUtensorMap mq, mkc, mvc, mkt, mvt;
+  {
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)s.hkv, (cuuint64_t)s.batch * s.n_nodes};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)s.hq * kD * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G)};
+    if (make_map(&mq, q, 4, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
+  }
+  {
+    // (at least one row so the map is valid when no prefix tile is ever loaded)
+    const cuuint64_t rows = (cuuint64_t)s.batch * s.hkv * s.s_max;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, rows > 0 ? rows : 1};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t kbox[2] = {64, 64}, vbox[2] = {64, (cuuint32_t)kBN};
+    if (make_map(&mkc, kc, 2, dims, strides, kbox) != SPEC_OK) return SPEC_ERR_CUDA;
+    if (make_map(&mvc, vc, 2, dims, strides, vbox) != SPEC_OK) return SPEC_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)s.batch * s.hkv * s.n_nodes};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t kbox[2] = {64, 64}, vbox[2] = {64, (cuuint32_t)kBN};
+    if (make_map(&mkt, kt, 2, dims, strides, kbox) != SPEC_OK) return SPEC_ERR_CUDA;
+    if (make_map(&mvt, vt, 2, dims, strides, vbox) != SPEC_OK) return SPEC_ERR_CUDA;
+  }
+  Sched sc;
+  sc.prefix_len = prefix_len;
+  sc.batch = s.batch;
+  sc.hkv = s.hkv;
+  sc.pairs = (R + kPairRows - 1) / kPairRows;
+  sc.n_nodes = s.n_nodes;
+  sc.s_max = s.s_max;
+  sc.max_prefix = s.max_prefix;
+  sc.n_clusters = C;
+  if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  attn_tc2_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, sc, anc, (__nv_bfloat16 *)out,
+                                                          (float *)ws, s.hq, scale * 1.4426950408889634f, status);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  const dim3 cgrid(s.batch * s.hkv * sc.pairs, kPairRows / 64);
+  attn_tc2_combine_kernel<<<cgrid, 256, 0, stream>>>((const float *)ws, (__nv_bfloat16 *)out, sc, s.hq);
+  return sv_launch_status();
+}

@@ -25,7 +25,7 @@ struct SvAttnShape {
   int dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix;
 };
 struct SvAttnPlan {
-  int use_tc;        // 1 = tcgen05 kernel, 0 = CUDA-core kernel
+  int use_tc;        // 2 = pair (cta_group::2) kernel, 1 = tcgen05 kernel, 0 = CUDA-core kernel
   int splits;        // KV splits per (sequence, KV head)
   int chunk;         // prefix keys per split (multiple of the key tile)
   size_t ws_bytes;   // partials (0 when splits == 1)
@@ -41,6 +41,14 @@ int sv_attn_tc(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const v
                const void *vc, const void *kt, const void *vt, const int32_t *prefix_len,
                const uint64_t *anc, void *out, float scale, void *ws, int32_t *status,
                cudaStream_t stream);
+// Pair kernel (bf16, head_dim 128, more than 128 query rows per KV head):
+// persistent, stream-K; launches its own combine.  Workspace: a fixed
+// number of partial slots per cluster of the grid.
+bool sv_attn_tc2_supported(const SvAttnShape &s);
+size_t sv_attn_tc2_ws_bytes();
+int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void *vc, const void *kt,
+                const void *vt, const int32_t *prefix_len, const uint64_t *anc, void *out,
+                float scale, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
 int sv_attn_combine(const SvAttnShape &s, const SvAttnPlan &p, const void *ws, void *out,
                     const int32_t *prefix_len, cudaStream_t stream);
 

@@ -18,6 +18,13 @@ SvAttnPlan sv_attn_simt_plan(const SvAttnShape &s, int num_splits);
 SvAttnPlan sv_attn_tc_plan(const SvAttnShape &s, int num_splits, bool *ok);
 
 SvAttnPlan sv_attn_plan(const SvAttnShape &s, int num_splits) {
+  if (sv_attn_tc2_supported(s)) {
+    SvAttnPlan p{};
+    p.use_tc = 2;
+    p.splits = 1;  // the pair kernel balances its own work
+    p.ws_bytes = sv_attn_tc2_ws_bytes();
+    return p;
+  }
   bool ok = false;
   SvAttnPlan p = sv_attn_tc_plan(s, num_splits, &ok);
   if (ok) return p;
@@ -136,6 +143,7 @@ int tree_attn_plan_splits(int dtype, int batch, int n_nodes, int hq, int hkv, in
   }
   if (attn_check(dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, max_prefix) != SPEC_OK) return 0;
   const SvAttnShape s{dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, max_prefix};
+  if (sv_attn_tc2_supported(s)) return 1;
   if (sv_attn_tc_supported(s)) return sv_attn_tc_ragged_splits(s, host_prefix_len);
   return sv_attn_plan(s, 0).splits;
 }
@@ -157,6 +165,11 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache, co
   if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned16(workspace)))
     return SPEC_ERR_CAPACITY;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)head_dim);
+  if (p.use_tc == 2) {
+    if (p.ws_bytes == 0) return SPEC_ERR_CUDA;
+    return sv_attn_tc2(s, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out, scale,
+                       workspace, workspace_bytes, dev_status, cs(stream));
+  }
   rc = p.use_tc ? sv_attn_tc(s, p, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out,
                              scale, workspace, dev_status, cs(stream))
                 : sv_attn_simt(s, p, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask,

@@ -18,7 +18,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA = range(5)
-DEV_OK, DEV_BAD_PARENTS, DEV_CAPACITY, DEV_BAD_PATH, DEV_BAD_POOL, DEV_BAD_TOKEN, DEV_TIMEOUT = range(7)
+DEV_OK, DEV_BAD_PARENTS, DEV_CAPACITY, DEV_BAD_PATH, DEV_BAD_POOL, DEV_BAD_TOKEN, DEV_TIMEOUT, DEV_INTERNAL = range(8)
 F32, BF16 = 0, 1
 GREEDY, TYPICAL, REJECT = 0, 1, 2
 MAX_NODES = 64
