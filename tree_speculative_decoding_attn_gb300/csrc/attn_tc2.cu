@@ -37,15 +37,16 @@
 //            once PV(g-3), which read that buffer's P, has completed; in the
 //            odd CTA it forwards the arrival of its Q/K halves to the even CTA
 //   warp 11  in the even CTA, issues
-//              O   += P(g) V(g)  (P written over S(g)'s columns as bf16)
+//              O   += P(g) V(g)  (P over S(g)'s first 64 columns, bf16 pairs)
 //            Two issuing threads: one thread's tcgen05.mma / commit stream
 //            (about 60 cycles per instruction) would otherwise bound the tile
 //            rate
-//   warps 2-9  softmax and epilogue: two warps per TMEM lane quarter, one
-//            per 64-key half.  The first tile of a row group takes the exact
-//            row max (shared by the pair of warps through shared memory);
-//            later tiles exponentiate against the running max in one pass
-//            and are redone exactly only if their row sum leaves [0, 2^64].
+//   warps 2-9  softmax and epilogue: each owns 16 TMEM lanes (rows) and
+//            reads all 128 keys of a tile with the 16-lane load shape, so a
+//            row lives in 4 threads of one warp and its exact tile max is two
+//            shuffles away; the running max moves only when a tile exceeds
+//            it by 2^8 (then the sum and O are rescaled).  P = 2^(s - m) is
+//            written as bf16 pairs over the tile's first 64 S columns.
 //            V: before PV(g) the even CTA's PV issuer waits for its own V
 //            half to land and zeroes the V rows past the last key of a
 //            partial tile (stale cache rows need not be finite); the odd
@@ -83,7 +84,7 @@ constexpr uint32_t kVBytes = kBN * 64 * 2;   // 128 keys x 64 dims
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kSB = 3;                       // S/P buffers in TMEM (128 columns each)
 constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 in all)
-constexpr float kMaxTileSum = 18446744073709551616.0f;  // 2^64
+constexpr float kTau = 8.f;                  // running max moves only when a tile exceeds it by 2^8
 constexpr uint16_t kBoth = 3;                // CTA mask of the pair
 constexpr int kPartial = sv_partial_stride(kD);
 
@@ -95,9 +96,7 @@ struct Bars {
   uint32_t tmem;
   volatile int abort;
   int start_b, start_gi, start_t, n_tiles;     // this cluster's first unit and unit count
-  float xmax[2][128];                          // per-row partial maxima of the two key halves
-  float xsum[2][128];                          // per-row partial sums at a row group's end
-  unsigned char xflag[2][2][128];              // "tile needs the exact max", by tile parity
+  float xm[128], xl[128];                      // per-row running max and sum at a row group's end
 };
 constexpr uint32_t kTileBytes = kQB * kQBytes + kKS * kKBytes + kVS * kVBytes;
 constexpr uint32_t kSmemBytes = kTileBytes + sizeof(Bars);
@@ -502,19 +501,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int ksteps = (nkeys + 15) >> 4;
         if (lane == 0) {
           const uint64_t vd = smem_desc_sw128(va + (uint32_t)st * kVBytes, kVBytes, 1024);
-          const uint32_t pbase = tmem + (uint32_t)(g % kSB) * 128u;
+          const uint32_t pbase = tmem + (uint32_t)(g % kSB) * 128u;  // P of keys [16kk, +16) at + 8kk
           const uint32_t acc0 = first ? 0u : 1u;
-          // P of keys [16kk, +16): the first key half's softmax warps wrote
-          // columns [0, 32) of the buffer, the second half's [64, 96)
           if (ksteps == kBN / 16) {
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts_pair(tmem + kColO, pbase + (kk < 4 ? (uint32_t)kk * 8u : 64u + (uint32_t)(kk - 4) * 8u),
-                          vd + (uint64_t)((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+              mma_ts_pair(tmem + kColO, pbase + (uint32_t)kk * 8u, vd + (uint64_t)((kk * 2048) >> 4), kIdescPV,
+                          kk > 0 ? 1u : acc0);
           } else {
             for (int kk = 0; kk < ksteps; ++kk)
-              mma_ts_pair(tmem + kColO, pbase + (kk < 4 ? (uint32_t)kk * 8u : 64u + (uint32_t)(kk - 4) * 8u),
-                          vd + (uint64_t)((kk * 2048) >> 4), kIdescPV, kk > 0 ? 1u : acc0);
+              mma_ts_pair(tmem + kColO, pbase + (uint32_t)kk * 8u, vd + (uint64_t)((kk * 2048) >> 4), kIdescPV,
+                          kk > 0 ? 1u : acc0);
           }
           mma_commit_pair_mc(&bars->vempty[st], kBoth);
           mma_commit_pair_mc(&bars->ofull[g % kSB], kBoth);
@@ -545,10 +542,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
+    // Warp w owns TMEM lanes [32 (w%4) + 16 u, +16), u = (w - 2) / 4: thread
+    // t holds rows lb + t/4 and lb + t/4 + 8 (lb = that lane base), 32 key
+    // columns of each row (pairs 2 (t%4), +1 of every 8-key group), so a
+    // row's max and sum are reduced over the 4 threads t%4 with shuffles.
     const int quarter = warp & 3;
-    const int h = (warp - 2) >> 2;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int u = (warp - 2) >> 2;
+    const int lb = quarter * 32 + u * 16;  // lane base of this warp
+    const int tq = lane & 3;
+    const int ra = lb + (lane >> 2), rb = ra + 8;  // this thread's rows (TMEM lanes)
+    const uint32_t lane_off = (uint32_t)lb << 16;
     const uint32_t pair_bar = 1u + (uint32_t)quarter;
     auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
     const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
@@ -556,16 +559,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Cur c = cur_begin(bars, s);
     int seg = 0;
     bool from_start = c.t == 0;
-    float m_used = NEG_INF, l = 0.f;  // l: this warp's half of the row sum
-    // ancestor bits of this thread's row in a row group (padding rows: all
-    // tree keys), loaded one row group ahead so the tree tile never waits
-    auto row_of = [&](int gi) { return (gi % pairs) * kPairRows + (int)rank * 128 + r; };
-    auto load_mask = [&](int b, int gi) -> uint64_t {
-      const int rr = row_of(gi);
+    float ma = NEG_INF, mb = NEG_INF;  // running max of rows ra, rb (log2 units)
+    float la = 0.f, lb_sum = 0.f;      // this thread's part of their sums
+    // ancestor bits of a row in a row group (padding rows: all tree keys),
+    // loaded one row group ahead so the tree tile never waits
+    auto grow = [&](int gi, int lane_row) { return (gi % pairs) * kPairRows + (int)rank * 128 + lane_row; };
+    auto load_mask = [&](int b, int gi, int lane_row) -> uint64_t {
+      const int rr = grow(gi, lane_row);
       return rr < R ? anc[(int64_t)b * N + rr / G] : ~0ull;
     };
-    uint64_t amask = c.t == 0 ? load_mask(c.b, c.gi) : 0ull, amask_next = 0ull;
-    int rg = row_of(c.gi);
+    uint64_t amask_a = c.t == 0 ? load_mask(c.b, c.gi, ra) : 0ull, amask_b = c.t == 0 ? load_mask(c.b, c.gi, rb) : 0ull;
+    uint64_t next_a = 0ull, next_b = 0ull;
     bool ok = true;
     // A failed wait (timeout) or an abort turns the rest into a no-op that
     // still passes every pair barrier, so the two warps of a pair always
@@ -576,119 +580,113 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (g > 0) {
           ++seg;
           from_start = true;
-          amask = amask_next;
+          amask_a = next_a;
+          amask_b = next_b;
         }
-        m_used = NEG_INF;
-        l = 0.f;
-        rg = row_of(c.gi);
+        ma = mb = NEG_INF;
+        la = lb_sum = 0.f;
       }
       if (c.t == c.n - 1 && g + 1 < T) {  // the next tile starts the next row group
         const bool same_b = c.gi + 1 < s.gpb();
-        amask_next = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0);
+        next_a = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, ra);
+        next_b = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, rb);
       }
-      if (ok && (!warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1) || __any_sync(0xffffffffu, bars->abort != 0)))
-        ok = false;
+      if (ok && !warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1)) ok = false;
       const uint32_t s_addr = tmem + lane_off + (uint32_t)(g % kSB) * 128u;
-      uint32_t sv[2][32];
+      // sv[4j + e]: row ra, key 8j + 2 tq + e;  sv[4j + 2 + e]: row rb
+      uint32_t sv[64];
       if (ok) {
         tc_fence_after();
-        tmem_ld32(s_addr + h * 64, sv[0]);
-        tmem_ld32(s_addr + h * 64 + 32, sv[1]);
+        tmem_ld_16x256b_x16(s_addr, sv);
         tmem_wait_ld();
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[0][i] = sv[1][i] = __float_as_uint(0.f);
+        for (int i = 0; i < 64; ++i) sv[i] = __float_as_uint(0.f);
       }
       const bool tree = c.t == 0;
       const int nvalid = tree ? N : tile_keys(c);
       if (tree || nvalid < kBN) {  // full prefix tiles need no mask
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const int col = h * 64 + i;
-          const bool vis = col < nvalid && (!tree || ((amask >> (col & 63)) & 1ull));  // tree: col < N <= 64
-          if (!vis) sv[i >> 5][i & 31] = __float_as_uint(NEG_INF);
-        }
+        for (int j = 0; j < 16; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 8 * j + 2 * tq + e;
+            const bool in = col < nvalid;
+            if (!(in && (!tree || ((amask_a >> (col & 63)) & 1ull)))) sv[4 * j + e] = __float_as_uint(NEG_INF);
+            if (!(in && (!tree || ((amask_b >> (col & 63)) & 1ull)))) sv[4 * j + 2 + e] = __float_as_uint(NEG_INF);
+          }
       }
-      // P of this warp's 64 keys, as bf16 pairs over the first 32 of its own
-      // 64 S columns
-      const uint32_t p_addr = s_addr + (uint32_t)h * 64u;
-      // P = 2^(s * scale - m) of this warp's 64 columns; returns their sum.
-      // Every row has a visible key in every tile (itself on the tree tile),
-      // so m is finite once a row group's first tile is done.
-      auto exp_write = [&](float m) -> float {
-        if (!ok) return 0.f;
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 nm2 = make_float2(-m, -m);
-        float2 acc2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                          make_float2(0.f, 0.f)};
+      // exact row max of the tile; every row sees a key in every tile
+      // (itself on the tree tile), so it is finite
+      float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x =
-                fma2(make_float2(__uint_as_float(sv[cc][2 * i]), __uint_as_float(sv[cc][2 * i + 1])), sc2, nm2);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            acc2[i & 3] = add2(acc2[i & 3], pp);
-            pk[i] = pack_bf16(pp.x, pp.y);
-          }
-          tmem_st16(p_addr + cc * 16, pk);
+      for (int j = 0; j < 16; ++j) {
+        xa[j & 1] = fmax3(xa[j & 1], __uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]));
+        xb[j & 1] = fmax3(xb[j & 1], __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
+      }
+      float ta = fmaxf(xa[0], xa[1]), tb = fmaxf(xb[0], xb[1]);
+      ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
+      tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
+      ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2)) * scale_log2;
+      tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2)) * scale_log2;
+      // The running max moves only when a tile exceeds it by more than
+      // kTau: P = 2^(s - m) stays below 2^kTau, and the sum and O are
+      // rescaled (O once PV(g-1) has completed) only then.
+      const bool need_a = ta > ma + kTau, need_b = tb > mb + kTau;
+      if (ok && __any_sync(0xffffffffu, need_a || need_b)) {
+        const float alpha_a = need_a ? ex2(ma - ta) : 1.f;  // 0 when m was -inf
+        const float alpha_b = need_b ? ex2(mb - tb) : 1.f;
+        if (need_a) {
+          ma = ta;
+          la *= alpha_a;
         }
-        const float2 st2 = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
-        return st2.x + st2.y;
-      };
-      // Exact step: the tile's row max over both key halves; a larger max
-      // rescales the running sum and (after a row group's first tile) O.
-      auto exact = [&]() -> float {
-        float mx[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          mx[i & 3] = fmax3(mx[i & 3], __uint_as_float(sv[i >> 4][(2 * i) & 31]),
-                            __uint_as_float(sv[i >> 4][(2 * i + 1) & 31]));
-        bars->xmax[h][r] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        pair_sync();
-        const float m_t = fmaxf(bars->xmax[0][r], bars->xmax[1][r]) * scale_log2;
-        pair_sync();  // both maxima read before they are overwritten
-        const bool need = m_t > m_used;
-        if (ok && __any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(m_used - m_t) : 1.f;  // 0 when m was -inf
-          if (need) {
-            m_used = m_t;
-            l *= alpha;
-          }
-          // O holds PV(g-1) once that MMA completes: wait for it, then scale
-          // this warp's half of the O columns
-          if (!first && __any_sync(0xffffffffu, alpha != 1.f) &&
-              (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
-            tc_fence_after();
+        if (need_b) {
+          mb = tb;
+          lb_sum *= alpha_b;
+        }
+        if (!first && __any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f) &&
+            (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
+          tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-              uint32_t o[16];
-              const uint32_t oa = tmem + lane_off + kColO + h * 64 + cc * 16;
-              tmem_ld16(oa, o);
-              tmem_wait_ld();
+          for (int cc = 0; cc < 4; ++cc) {  // O columns [32 cc, +32) of this warp's 16 rows
+            uint32_t o[16];
+            const uint32_t oa = tmem + lane_off + kColO + (uint32_t)cc * 32u;
+            tmem_ld_16x256b_x4(oa, o);
+            tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st16(oa, o);
+            for (int j = 0; j < 4; ++j) {
+              o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
+              o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
+              o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
+              o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
             }
+            tmem_st_16x256b_x4(oa, o);
           }
         }
-        return exp_write(m_used);
-      };
-      // Both warps of a pair hold the same running max, so these decisions
-      // are the same in both and the pair barriers stay matched.
-      float tsum;
-      if (first) {
-        tsum = exact();
-      } else {
-        tsum = exp_write(m_used);
-        bars->xflag[g & 1][h][r] = !(tsum <= kMaxTileSum);
-        pair_sync();
-        const bool redo = bars->xflag[g & 1][0][r] | bars->xflag[g & 1][1][r];
-        if (__any_sync(0xffffffffu, redo)) tsum = exact();
       }
       if (ok) {
-        l += tsum;
+        // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
+        // column 4j + tq, written over the tile's first 64 S columns of this
+        // warp's lanes (all of them were read above)
+        const float2 sc2 = make_float2(scale_log2, scale_log2);
+        const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
+        float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
+          const float2 xb2 =
+              fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
+          const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
+          const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
+          sa2 = add2(sa2, pa);
+          sb2 = add2(sb2, pb);
+          pk[2 * j] = pack_bf16(pa.x, pa.y);
+          pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
+        }
+        tmem_st_16x128b_x16(s_addr, pk);
+        la += sa2.x + sa2.y;
+        lb_sum += sb2.x + sb2.y;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -696,25 +694,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (g == T - 1 || c.t == c.n - 1) {
         // ---------------------------------------------------- epilogue
+        // Rows' running max and full sum through shared memory, then one row
+        // per thread again (lanes of the quarter) for the O read-out: warp u
+        // takes O columns [64 u, +64).
         if (ok && !warp_wait(&bars->ofull[g % kSB], (g / kSB) & 1)) ok = false;
-        // the row sum's two halves through shared memory (the second barrier:
-        // both halves read before either warp can write the next row group's)
-        bars->xsum[h][r] = l;
+        float sa = la + __shfl_xor_sync(0xffffffffu, la, 1);
+        float sb = lb_sum + __shfl_xor_sync(0xffffffffu, lb_sum, 1);
+        sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+        if (tq == 0) {
+          bars->xm[ra] = ma;
+          bars->xl[ra] = sa;
+          bars->xm[rb] = mb;
+          bars->xl[rb] = sb;
+        }
         pair_sync();
-        const float l_row = bars->xsum[0][r] + bars->xsum[1][r];
-        pair_sync();
+        const int r = quarter * 32 + lane;  // the row this thread writes out
+        const float m_row = bars->xm[r], l_row = bars->xl[r];
+        pair_sync();  // read before either warp writes the next row group's
+        const int rg = grow(c.gi, r);
         const bool complete = from_start && c.t == c.n - 1;
         const bool row_ok = rg < R;
         const int kvh = c.gi / pairs;
+        const uint32_t q_off = (uint32_t)(quarter * 32) << 16;
         if (ok && !__any_sync(0xffffffffu, bars->abort != 0)) {
           tc_fence_after();
           if (complete) {
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            __nv_bfloat16 *o = out + (((int64_t)c.b * N + rg / G) * Hq + kvh * G + rg % G) * kD + h * 64;
+            __nv_bfloat16 *o = out + (((int64_t)c.b * N + rg / G) * Hq + kvh * G + rg % G) * kD + u * 64;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               uint32_t ov[32];
-              tmem_ld32(tmem + lane_off + kColO + h * 64 + cc * 32, ov);
+              tmem_ld32(tmem + q_off + kColO + u * 64 + cc * 32, ov);
               tmem_wait_ld();
               if (row_ok && c.ok) {
                 uint4 *dst = reinterpret_cast<uint4 *>(o + cc * 32);
@@ -735,18 +746,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               uint32_t ov[32];
-              tmem_ld32(tmem + lane_off + kColO + h * 64 + cc * 32, ov);
+              tmem_ld32(tmem + q_off + kColO + u * 64 + cc * 32, ov);
               tmem_wait_ld();
               if (row_ok) {
-                float4 *dst = reinterpret_cast<float4 *>(w + h * 64 + cc * 32);
+                float4 *dst = reinterpret_cast<float4 *>(w + u * 64 + cc * 32);
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4)
                   dst[q4] = make_float4(__uint_as_float(ov[4 * q4]), __uint_as_float(ov[4 * q4 + 1]),
                                         __uint_as_float(ov[4 * q4 + 2]), __uint_as_float(ov[4 * q4 + 3]));
               }
             }
-            if (row_ok && h == 0) {
-              w[kD] = m_used;
+            if (row_ok && u == 0) {
+              w[kD] = m_row;
               w[kD + 1] = l_row;
             }
           }
