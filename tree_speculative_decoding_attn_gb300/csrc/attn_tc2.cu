@@ -17,9 +17,9 @@
 // (sequence, KV head, pair, unit), form one sequence of U units; cluster c
 // of C takes units [floor(cU/C), floor((c+1)U/C)).  A row group that lies
 // wholly inside one cluster's range is normalised and written out; the row
-// groups cut by a range end leave float32 partials (unnormalised O, running
-// max in log2 units, row sum) in workspace slot (c, first/last), merged by
-// attn_tc2_combine_kernel.  Every cluster streams the same number of tiles
+// groups cut by a range end leave partials (unnormalised O in bf16, running
+// max in log2 units and row sum in float32) in workspace slot (c, first/
+// last), merged by attn_tc2_combine_kernel.  Every cluster streams the same number of tiles
 // whatever the prefix lengths.
 //
 // Pair MMA.  The even CTA issues every MMA for both.  M = 256: each CTA
@@ -59,6 +59,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -86,7 +87,9 @@ constexpr int kSB = 3;                       // S/P buffers in TMEM (128 columns
 constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 in all)
 constexpr float kTau = 8.f;                  // running max moves only when a tile exceeds it by 2^8
 constexpr uint16_t kBoth = 3;                // CTA mask of the pair
-constexpr int kPartial = sv_partial_stride(kD);
+// A partial row: 128 bf16 of unnormalised O (256 B), then the running max
+// (log2 units) and the sum as float32, padded to 272 B.
+constexpr int kPartialBytes = kD * 2 + 16;
 
 struct Bars {
   uint64_t kland[kKS], kempty[kKS], kfull[kKS];
@@ -181,6 +184,71 @@ __device__ void warp_locate(const Sched &s, long long u, int *b_out, int *gi_out
   *t_out = 0;
 }
 
+// Tiles per row group of the lane's sequences b = 32 i + lane (B <= 128),
+// loaded in one round; returns U, the units of all row groups (full warp).
+constexpr int kLookupSeqs = 128;
+__device__ long long warp_load_tiles(const Sched &s, int (&n)[4]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int b = 32 * i + lane;
+    bool ok;
+    n[i] = b < s.batch ? seq_tiles(seq_prefix(s, b, &ok)) : 0;
+  }
+  long long acc = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc += warp_sum_ll(n[i]);
+  return acc * s.gpb();
+}
+// warp_locate with the tile counts already in registers (B <= 128).
+__device__ void warp_locate_n(const Sched &s, const int (&n)[4], long long u, int *b_out, int *gi_out, int *t_out) {
+  const int lane = threadIdx.x & 31;
+  long long base = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long v = (long long)n[i] * s.gpb();
+    long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, 32 * i + lane < s.batch && base + incl > u);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      const long long before = base + __shfl_sync(0xffffffffu, incl - v, l);
+      const int nl = __shfl_sync(0xffffffffu, n[i], l);
+      const long long local = u - before;
+      *b_out = 32 * i + l;
+      *gi_out = (int)(local / nl);
+      *t_out = (int)(local % nl);
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  *b_out = s.batch;
+  *gi_out = 0;
+  *t_out = 0;
+}
+// Total units U, and the sequence / row group / tile of unit u(U) (full
+// warp; one round of loads when B <= 128).
+template <typename UnitOf>
+__device__ long long warp_find(const Sched &s, UnitOf unit_of, long long *u_out, int *b, int *gi, int *t) {
+  long long U, u;
+  if (s.batch <= kLookupSeqs) {
+    int n[4];
+    U = warp_load_tiles(s, n);
+    u = unit_of(U);
+    if (u >= 0) warp_locate_n(s, n, u, b, gi, t);
+  } else {
+    U = warp_units_before(s, s.batch);
+    u = unit_of(U);
+    if (u >= 0) warp_locate(s, u, b, gi, t);
+  }
+  *u_out = u;
+  return U;
+}
+
 __device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
 // Cluster whose range holds unit u (the largest c with range_start(c) <= u).
 __device__ __forceinline__ int cluster_of(long long u, long long U, long long C) {
@@ -258,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                     const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
                     const __grid_constant__ CUtensorMap tm_vt, const Sched s, const uint64_t *__restrict__ anc,
-                    __nv_bfloat16 *__restrict__ out, float *__restrict__ ws, int Hq, float scale_log2,
+                    __nv_bfloat16 *__restrict__ out, void *__restrict__ ws, int Hq, float scale_log2,
                     int32_t *status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sQ = smem;
@@ -279,17 +347,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (warp == 0) {
     // with C = min(clusters, U) every range below C holds at least one unit
-    const long long U = warp_units_before(s, s.batch);
-    const long long C = min((long long)s.n_clusters, U);
-    const long long u0 = cluster < C ? range_start(cluster, U, C) : 0;
-    const long long u1 = cluster < C ? range_start(cluster + 1, U, C) : 0;
     int b = s.batch, gi = 0, t = 0;
-    if (u1 > u0) warp_locate(s, u0, &b, &gi, &t);
+    long long u0;
+    const long long U = warp_find(
+        s, [&](long long U_) -> long long {
+          const long long C = min((long long)s.n_clusters, U_);
+          return cluster < C ? range_start(cluster, U_, C) : -1;
+        },
+        &u0, &b, &gi, &t);
+    const long long C = min((long long)s.n_clusters, U);
+    const long long u1 = cluster < C ? range_start(cluster + 1, U, C) : 0;
     if (lane == 0) {
       bars->start_b = b;
       bars->start_gi = gi;
       bars->start_t = t;
-      bars->n_tiles = (int)(u1 - u0);
+      bars->n_tiles = u0 >= 0 ? (int)(u1 - u0) : 0;
     }
   }
   __syncthreads();
@@ -605,93 +677,115 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const bool tree = c.t == 0;
       const int nvalid = tree ? N : tile_keys(c);
-      if (tree || nvalid < kBN) {  // full prefix tiles need no mask
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 8 * j + 2 * tq + e;
-            const bool in = col < nvalid;
-            if (!(in && (!tree || ((amask_a >> (col & 63)) & 1ull)))) sv[4 * j + e] = __float_as_uint(NEG_INF);
-            if (!(in && (!tree || ((amask_b >> (col & 63)) & 1ull)))) sv[4 * j + 2 + e] = __float_as_uint(NEG_INF);
+      // The tile body comes in two instances so that full prefix tiles, the
+      // steady state, carry no masking code: the masked one serves the tree
+      // tile and the last, partial prefix tile.
+      auto tile = [&](auto masked) {
+        if constexpr (decltype(masked)::value) {
+          // Visibility of this thread's keys 8j + 2 tq + e as bits 2j + e: the
+          // keys below nvalid are a prefix of these bits (they increase with
+          // the bit index); on the tree tile (N <= 64) also the ancestor bits.
+          const int m8 = nvalid - 2 * tq;
+          const int nb = m8 <= 0 ? 0 : min(32, 2 * (m8 >> 3) + min(2, m8 & 7));
+          const uint32_t in = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
+          uint32_t va = in, vb = in;
+          if (tree) {
+            auto mine = [&](uint64_t m) -> uint32_t {
+              uint64_t x = (m >> (2 * tq)) & 0x0303030303030303ull;
+              x = (x | (x >> 6)) & 0x000F000F000F000Full;
+              x = (x | (x >> 12)) & 0x000000FF000000FFull;
+              return (uint32_t)((x | (x >> 24)) & 0xFFFFull);
+            };
+            va &= mine(amask_a);
+            vb &= mine(amask_b);
           }
-      }
-      // exact row max of the tile; every row sees a key in every tile
-      // (itself on the tree tile), so it is finite
-      float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        xa[j & 1] = fmax3(xa[j & 1], __uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]));
-        xb[j & 1] = fmax3(xb[j & 1], __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
-      }
-      float ta = fmaxf(xa[0], xa[1]), tb = fmaxf(xb[0], xb[1]);
-      ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
-      tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
-      ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2)) * scale_log2;
-      tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2)) * scale_log2;
-      // The running max moves only when a tile exceeds it by more than
-      // kTau: P = 2^(s - m) stays below 2^kTau, and the sum and O are
-      // rescaled (O once PV(g-1) has completed) only then.
-      const bool need_a = ta > ma + kTau, need_b = tb > mb + kTau;
-      if (ok && __any_sync(0xffffffffu, need_a || need_b)) {
-        const float alpha_a = need_a ? ex2(ma - ta) : 1.f;  // 0 when m was -inf
-        const float alpha_b = need_b ? ex2(mb - tb) : 1.f;
-        if (need_a) {
-          ma = ta;
-          la *= alpha_a;
-        }
-        if (need_b) {
-          mb = tb;
-          lb_sum *= alpha_b;
-        }
-        if (!first && __any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f) &&
-            (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {  // O columns [32 cc, +32) of this warp's 16 rows
-            uint32_t o[16];
-            const uint32_t oa = tmem + lane_off + kColO + (uint32_t)cc * 32u;
-            tmem_ld_16x256b_x4(oa, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
-              o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
-              o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
-              o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
-            }
-            tmem_st_16x256b_x4(oa, o);
+          for (int i = 0; i < 32; ++i) {  // i = 2j + e: register 4j + e of row ra, 4j + 2 + e of row rb
+            if (!((va >> i) & 1u)) sv[4 * (i >> 1) + (i & 1)] = __float_as_uint(NEG_INF);
+            if (!((vb >> i) & 1u)) sv[4 * (i >> 1) + 2 + (i & 1)] = __float_as_uint(NEG_INF);
           }
         }
-      }
-      if (ok) {
-        // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
-        // column 4j + tq, written over the tile's first 64 S columns of this
-        // warp's lanes (all of them were read above)
-        const float2 sc2 = make_float2(scale_log2, scale_log2);
-        const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
-        float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
-        uint32_t pk[32];
-#pragma unroll
+        // exact row max of the tile; every row sees a key in every tile
+        // (itself on the tree tile), so it is finite
+        float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
+  #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
-          const float2 xb2 =
-              fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
-          const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
-          const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
-          sa2 = add2(sa2, pa);
-          sb2 = add2(sb2, pb);
-          pk[2 * j] = pack_bf16(pa.x, pa.y);
-          pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
+          xa[j & 1] = fmax3(xa[j & 1], __uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]));
+          xb[j & 1] = fmax3(xb[j & 1], __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
         }
-        tmem_st_16x128b_x16(s_addr, pk);
-        la += sa2.x + sa2.y;
-        lb_sum += sb2.x + sb2.y;
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
-      }
+        float ta = fmaxf(xa[0], xa[1]), tb = fmaxf(xb[0], xb[1]);
+        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
+        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
+        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2)) * scale_log2;
+        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2)) * scale_log2;
+        // The running max moves only when a tile exceeds it by more than
+        // kTau: P = 2^(s - m) stays below 2^kTau, and the sum and O are
+        // rescaled (O once PV(g-1) has completed) only then.
+        const bool need_a = ta > ma + kTau, need_b = tb > mb + kTau;
+        if (ok && __any_sync(0xffffffffu, need_a || need_b)) {
+          const float alpha_a = need_a ? ex2(ma - ta) : 1.f;  // 0 when m was -inf
+          const float alpha_b = need_b ? ex2(mb - tb) : 1.f;
+          if (need_a) {
+            ma = ta;
+            la *= alpha_a;
+          }
+          if (need_b) {
+            mb = tb;
+            lb_sum *= alpha_b;
+          }
+          if (!first && __any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f) &&
+              (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
+            tc_fence_after();
+  #pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {  // O columns [32 cc, +32) of this warp's 16 rows
+              uint32_t o[16];
+              const uint32_t oa = tmem + lane_off + kColO + (uint32_t)cc * 32u;
+              tmem_ld_16x256b_x4(oa, o);
+              tmem_wait_ld();
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
+                o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
+                o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
+                o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
+              }
+              tmem_st_16x256b_x4(oa, o);
+            }
+          }
+        }
+        if (ok) {
+          // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
+          // column 4j + tq, written over the tile's first 64 S columns of this
+          // warp's lanes (all of them were read above)
+          const float2 sc2 = make_float2(scale_log2, scale_log2);
+          const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
+          float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+          uint32_t pk[32];
+  #pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
+            const float2 xb2 =
+                fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
+            const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
+            const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
+            sa2 = add2(sa2, pa);
+            sb2 = add2(sb2, pb);
+            pk[2 * j] = pack_bf16(pa.x, pa.y);
+            pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
+          }
+          tmem_st_16x128b_x16(s_addr, pk);
+          la += sa2.x + sa2.y;
+          lb_sum += sb2.x + sb2.y;
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
+        }
+      };
+      if (tree || nvalid < kBN)
+        tile(std::true_type{});
+      else
+        tile(std::false_type{});
       if (g == T - 1 || c.t == c.n - 1) {
         // ---------------------------------------------------- epilogue
         // Rows' running max and full sum through shared memory, then one row
@@ -742,24 +836,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           } else {
             const int slot = cluster * 2 + (seg == 0 ? 0 : 1);
-            float *w = ws + ((int64_t)slot * kPairRows + (int)rank * 128 + r) * kPartial;
+            uint8_t *w = reinterpret_cast<uint8_t *>(ws) +
+                         ((int64_t)slot * kPairRows + (int)rank * 128 + r) * kPartialBytes;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
               uint32_t ov[32];
               tmem_ld32(tmem + q_off + kColO + u * 64 + cc * 32, ov);
               tmem_wait_ld();
               if (row_ok) {
-                float4 *dst = reinterpret_cast<float4 *>(w + u * 64 + cc * 32);
+                uint4 *dst = reinterpret_cast<uint4 *>(w + u * 128 + cc * 64);
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4)
-                  dst[q4] = make_float4(__uint_as_float(ov[4 * q4]), __uint_as_float(ov[4 * q4 + 1]),
-                                        __uint_as_float(ov[4 * q4 + 2]), __uint_as_float(ov[4 * q4 + 3]));
+                for (int q4 = 0; q4 < 4; ++q4)
+                  dst[q4] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q4 + 0]), __uint_as_float(ov[8 * q4 + 1])),
+                                       pack_bf16(__uint_as_float(ov[8 * q4 + 2]), __uint_as_float(ov[8 * q4 + 3])),
+                                       pack_bf16(__uint_as_float(ov[8 * q4 + 4]), __uint_as_float(ov[8 * q4 + 5])),
+                                       pack_bf16(__uint_as_float(ov[8 * q4 + 6]), __uint_as_float(ov[8 * q4 + 7])));
               }
             }
-            if (row_ok && u == 0) {
-              w[kD] = m_row;
-              w[kD + 1] = l_row;
-            }
+            if (row_ok && u == 0) *reinterpret_cast<float2 *>(w + kD * 2) = make_float2(m_row, l_row);
           }
         } else if (!ok) {
           give_up(bars, status);
@@ -780,54 +874,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merges the partials of row groups cut by a cluster range end.  Block =
-// (row group, quarter of its 256 rows); warp = row; lane = 4 head dims.
-__global__ void __launch_bounds__(256) attn_tc2_combine_kernel(const float *__restrict__ ws,
+// Merges the partials of the row groups cut by cluster range ends.  At most
+// C - 1 row groups are cut; a cut row group is merged by the blocks of the
+// first range boundary inside it.  Block = (boundary k, 16 of the 256 rows);
+// warp = 2 rows, lane = 4 head dims; all partials of a row are loaded at
+// once (lane i: the i-th contributor's max and sum).
+constexpr int kCombRows = 16;
+__global__ void __launch_bounds__(256) attn_tc2_combine_kernel(const void *__restrict__ ws,
                                                                __nv_bfloat16 *__restrict__ out, const Sched s,
                                                                int Hq) {
-  __shared__ int sh[4];  // c_lo, c_hi, first unit of the row group, usable
+  __shared__ int sh[7];  // usable, b, gi, c_lo, c_hi, c_lo's slot is its first
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gidx = blockIdx.x, b = gidx / s.gpb(), gi = gidx % s.gpb();
+  const int k = blockIdx.x + 1;  // boundary between clusters k-1 and k
   if (warp == 0) {
-    const long long U = warp_units_before(s, s.batch);
+    int b = s.batch, gi = 0, t = 0;
+    long long u;
+    const long long U = warp_find(
+        s, [&](long long U_) -> long long {
+          const long long C = min((long long)s.n_clusters, U_);
+          return k < C ? range_start(k, U_, C) : -1;
+        },
+        &u, &b, &gi, &t);
     const long long C = min((long long)s.n_clusters, U);
-    const long long before = warp_units_before(s, b);
-    bool ok;
-    const int n = seq_tiles(seq_prefix(s, b, &ok));
-    const long long ug = before + (long long)gi * n;
+    int usable = 0, c_lo = 0, c_hi = 0, first = 0;
+    if (u >= 0 && t != 0) {  // the boundary cuts row group (b, gi)
+      bool ok;
+      const int n = seq_tiles(seq_prefix(s, b, &ok));
+      const long long ug = u - t;
+      c_lo = cluster_of(ug, U, C);
+      usable = ok && c_lo == k - 1;  // k is the first boundary inside it
+      c_hi = cluster_of(ug + n - 1, U, C);
+      first = range_start(c_lo, U, C) == ug;
+    }
     if (lane == 0) {
-      sh[0] = cluster_of(ug, U, C);
-      sh[1] = cluster_of(ug + n - 1, U, C);
-      sh[2] = (int)(range_start(sh[0], U, C) == ug);  // the row group is c_lo's first segment
-      sh[3] = ok;
+      sh[0] = usable;
+      sh[1] = b;
+      sh[2] = gi;
+      sh[3] = c_lo;
+      sh[4] = c_hi;
+      sh[5] = first;
     }
   }
   __syncthreads();
-  const int c_lo = sh[0], c_hi = sh[1];
-  if (c_lo == c_hi || !sh[3]) return;  // written by the main kernel, or reported there
+  if (!sh[0]) return;
+  const int b = sh[1], gi = sh[2], c_lo = sh[3], c_hi = sh[4], first = sh[5];
+  const int nc = c_hi - c_lo + 1;
   const int G = Hq / s.hkv, R = s.n_nodes * G;
   const int kvh = gi / s.pairs, pair = gi % s.pairs;
-  for (int rr = blockIdx.y * 64 + warp; rr < blockIdx.y * 64 + 64; rr += 8) {
+  auto row_of = [&](int c, int rr) -> const uint8_t * {
+    const int slot = c * 2 + ((c == c_lo && !first) ? 1 : 0);
+    return reinterpret_cast<const uint8_t *>(ws) + ((int64_t)slot * kPairRows + rr) * kPartialBytes;
+  };
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int rr = blockIdx.y * kCombRows + warp * 2 + q;
     const int rg = pair * kPairRows + rr;
-    if (rg >= R) break;
-    auto slot_row = [&](int c) -> const float * {
-      const int slot = c * 2 + ((c == c_lo && !sh[2]) ? 1 : 0);
-      return ws + ((int64_t)slot * kPairRows + rr) * kPartial;
-    };
+    if (rg >= R) continue;
+    // the largest running max over the contributors
     float M = -INFINITY;
-    for (int c = c_lo; c <= c_hi; ++c) M = fmaxf(M, slot_row(c)[kD]);
+    for (int c0 = 0; c0 < nc; c0 += 32)
+      if (c0 + lane < nc) M = fmaxf(M, reinterpret_cast<const float *>(row_of(c_lo + c0 + lane, rr) + kD * 2)[0]);
+    M = sv::warp_max(M);
     float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const float *w = slot_row(c);
-      const float f = exp2f(w[kD] - M);
-      L = fmaf(f, w[kD + 1], L);
-      const float4 o = reinterpret_cast<const float4 *>(w)[lane];
-      acc.x = fmaf(f, o.x, acc.x);
-      acc.y = fmaf(f, o.y, acc.y);
-      acc.z = fmaf(f, o.z, acc.z);
-      acc.w = fmaf(f, o.w, acc.w);
+    for (int c0 = 0; c0 < nc; c0 += 32) {
+      float f = 0.f;
+      if (c0 + lane < nc) {
+        const float2 ml = *reinterpret_cast<const float2 *>(row_of(c_lo + c0 + lane, rr) + kD * 2);
+        f = exp2f(ml.x - M);
+        L = fmaf(f, ml.y, L);
+      }
+      const int m = min(32, nc - c0);
+      for (int i = 0; i < m; ++i) {
+        const float fi = __shfl_sync(0xffffffffu, f, i);
+        const uint2 o = reinterpret_cast<const uint2 *>(row_of(c_lo + c0 + i, rr))[lane];  // dims 4 lane .. +3
+        acc.x = fmaf(fi, __uint_as_float(o.x << 16), acc.x);
+        acc.y = fmaf(fi, __uint_as_float(o.x & 0xFFFF0000u), acc.y);
+        acc.z = fmaf(fi, __uint_as_float(o.y << 16), acc.z);
+        acc.w = fmaf(fi, __uint_as_float(o.y & 0xFFFF0000u), acc.w);
+      }
     }
+    L = sv::warp_sum(L);
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat16 *o = out + (((int64_t)b * s.n_nodes + rg / G) * Hq + kvh * G + rg % G) * kD + lane * 4;
     uint2 v;
@@ -904,7 +1031,7 @@ bool sv_attn_tc2_supported(const SvAttnShape &s) {
 
 size_t sv_attn_tc2_ws_bytes() {
   const int c = tc2_clusters();
-  return c > 0 ? (size_t)c * 2 * kPairRows * kPartial * sizeof(float) : 0;
+  return c > 0 ? (size_t)c * 2 * kPairRows * kPartialBytes : 0;
 }
 
 int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void *vc, const void *kt, const void *vt,
@@ -950,9 +1077,11 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
       cudaSuccess)
     return SPEC_ERR_CUDA;
   attn_tc2_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, sc, anc, (__nv_bfloat16 *)out,
-                                                          (float *)ws, s.hq, scale * 1.4426950408889634f, status);
+                                                          ws, s.hq, scale * 1.4426950408889634f, status);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-  const dim3 cgrid(s.batch * s.hkv * sc.pairs, kPairRows / 64);
-  attn_tc2_combine_kernel<<<cgrid, 256, 0, stream>>>((const float *)ws, (__nv_bfloat16 *)out, sc, s.hq);
+  if (C > 1) {
+    const dim3 cgrid(C - 1, kPairRows / kCombRows);
+    attn_tc2_combine_kernel<<<cgrid, 256, 0, stream>>>(ws, (__nv_bfloat16 *)out, sc, s.hq);
+  }
   return sv_launch_status();
 }
