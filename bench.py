@@ -550,6 +550,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-attention", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling cases)")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="time tree_attn_verify alone at the workload's shape (profiling runs)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -565,8 +567,13 @@ def main():
         import dataclasses
         from tree_speculative_decoding_attn_gb300 import synth
         synth.WORKLOADS[args.workload] = dataclasses.replace(synth.WORKLOADS[args.workload], batch=args.batch)
-    step = GpuStep(args.workload, dev)
     hbm, tc_peak, peak_kind = _peaks()
+    if args.attention_only:
+        r = attention_only(args.workload, dev, steps=args.steps, warmup=args.warmup)
+        r.update(workload=args.workload, frac_hbm=r["gbps"] / hbm, peak_kind=peak_kind)
+        print(json.dumps({"attention_only": r}), flush=True)
+        return
+    step = GpuStep(args.workload, dev)
     stream = torch.cuda.current_stream()
 
     # warm-up

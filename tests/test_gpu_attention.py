@@ -118,6 +118,29 @@ def test_prefix_beyond_bound_is_reported():
     assert within(got[:1], ref, *TOL["bf16"])[0]          # the in-bound sequence is still computed
 
 
+def test_one_row_group_across_every_cluster():
+    """One (sequence, KV head) of 256 query rows with a 20000-key prefix:
+    its single row group is cut into one part per cluster of the persistent
+    grid (more than 32), so the merge folds its contributors in rounds."""
+    shape = synth.random_tree(31, 32, (4, 3, 2))
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 1, 8, 1, 128, [20000], shape, seed=31)
+    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt, repeats=2)
+    assert status == 0
+    ref = A.tree_attention(q, kc, vc, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
+    assert within(got, ref, *TOL["bf16"])[0]
+
+
+def test_pair_shape_prefix_beyond_bound_is_reported():
+    """256 query rows per KV head (the SM-pair kernel): a sequence whose
+    prefix exceeds max_prefix is reported, the others are still computed."""
+    shape = synth.random_tree(32, 32, (4, 3, 2))
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 3, 16, 2, 128, [300, 900, 2000], shape, seed=32)
+    got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt, max_prefix=1000)
+    assert status == sv.DEV_CAPACITY
+    ref = A.tree_attention(q[:2], kc[:2], vc[:2], kt[:2], vt[:2], prefix[:2], T.depth_and_mask(shape.parents)[1])
+    assert within(got[:2], ref, *TOL["bf16"])[0]
+
+
 FULL = ["vicuna7b_medusa", "llama8b_eagle2", "llama70b_serving", "long_context"]
 
 

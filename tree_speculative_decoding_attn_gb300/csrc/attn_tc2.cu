@@ -14,13 +14,15 @@
 //
 // Work.  The units of a row group are its tree tile (unit 0) and its prefix
 // tiles of 128 keys (units 1..).  All units of all row groups, in order
-// (sequence, KV head, pair, unit), form one sequence of U units; cluster c
-// of C takes units [floor(cU/C), floor((c+1)U/C)).  A row group that lies
-// wholly inside one cluster's range is normalised and written out; the row
-// groups cut by a range end leave partials (unnormalised O in bf16, running
-// max in log2 units and row sum in float32) in workspace slot (c, first/
-// last), merged by attn_tc2_combine_kernel.  Every cluster streams the same number of tiles
-// whatever the prefix lengths.
+// (sequence, KV head, pair, unit), form one sequence of U units, split into
+// C contiguous ranges of equal weight: a prefix tile weighs 1 and a tree
+// tile 1 + kSegW, the row group's fixed cost (pipeline drain, epilogue,
+// mask), so ranges with more row-group starts hold fewer tiles.  A row
+// group that lies wholly inside one cluster's range is normalised and
+// written out; the parts of a row group cut by range ends leave partials
+// (unnormalised O in bf16, running max in log2 units and row sum in
+// float32) in workspace slots (2c + 1 for the part cut at cluster c's range
+// end, 2c for the one cut at its start), merged by attn_tc2_combine_kernel.
 //
 // Pair MMA.  The even CTA issues every MMA for both.  M = 256: each CTA
 // holds its own 128 query rows (Q in shared memory; S, P and O in its own
@@ -99,6 +101,7 @@ struct Bars {
   uint32_t tmem;
   volatile int abort;
   int start_b, start_gi, start_t, n_tiles;     // this cluster's first unit and unit count
+  int start_raw, start_raw_next;               // prefix_len[start_b], prefix_len[start_b + 1] (0 past the batch)
   float xm[128], xl[128];                      // per-row running max and sum at a row group's end
 };
 constexpr uint32_t kTileBytes = kQB * kQBytes + kKS * kKBytes + kVS * kVBytes;
@@ -109,7 +112,7 @@ constexpr uint32_t kIdescS = idesc_bf16_f32(256, 128, 0, 0);   // Q, K both K-ma
 constexpr uint32_t kIdescPV = idesc_bf16_f32(256, 128, 0, 1);  // V MN-major (dims contiguous)
 
 // ---------------------------------------------------------------------------
-// Work schedule, shared by the main and combine kernels
+// Work schedule
 // ---------------------------------------------------------------------------
 struct Sched {
   const int32_t *prefix_len;
@@ -117,142 +120,162 @@ struct Sched {
   __device__ int gpb() const { return hkv * pairs; }  // row groups per sequence
 };
 
-// Effective prefix of sequence b: its length, or 0 when out of bounds (the
-// sequence is reported and its output left unwritten).
-__device__ __forceinline__ int seq_prefix(const Sched &s, int b, bool *valid) {
-  const int P = s.prefix_len[b];
-  const bool ok = P >= 0 && P <= s.max_prefix && P <= s.s_max;
-  *valid = ok;
-  return ok ? P : 0;
+// A row group's fixed cost (the pipeline drain and epilogue at its end, the
+// tree mask) in tile equivalents, carried by its tree tile in the balanced
+// split: a row group of n tiles weighs n + kSegW, and its unit t starts at
+// weight unit_start_w(t) within it.
+constexpr int kSegW = 3;
+__device__ __forceinline__ int unit_start_w(int t) { return t == 0 ? 0 : kSegW + t; }
+
+// A prefix length out of bounds counts as 0 (the sequence is reported and
+// its output left unwritten).
+__device__ __forceinline__ bool prefix_ok(const Sched &s, int raw) {
+  return raw >= 0 && raw <= s.max_prefix && raw <= s.s_max;
 }
 __device__ __forceinline__ int seq_tiles(int P) { return 1 + (P + kBN - 1) / kBN; }
+__device__ __forceinline__ int tiles_of(const Sched &s, int raw) { return seq_tiles(prefix_ok(s, raw) ? raw : 0); }
 
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-
-// Units of the row groups of sequences [0, b_end) (full warp).
-__device__ long long warp_units_before(const Sched &s, int b_end) {
+__device__ __forceinline__ long long warp_incl_ll(long long v) {  // inclusive prefix sum over lanes
   const int lane = threadIdx.x & 31;
-  long long acc = 0;
-  for (int b0 = 0; b0 < b_end; b0 += 32) {
-    long long v = 0;
-    if (b0 + lane < b_end) {
-      bool ok;
-      v = seq_tiles(seq_prefix(s, b0 + lane, &ok));
-    }
-    acc += warp_sum_ll(v);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
   }
-  return acc * s.gpb();
+  return v;
 }
 
-// Sequence, row group and tile of unit u < U (full warp).
-__device__ void warp_locate(const Sched &s, long long u, int *b_out, int *gi_out, int *t_out) {
+// Prefix lengths of sequences 32 i + lane (i < 4) in a warp's registers,
+// loaded in one round; chunks of 32 sequences past the first 128 are loaded
+// where they are walked.
+constexpr int kTabSeqs = 128;
+struct SeqTab {
+  int raw[4];
+};
+__device__ __forceinline__ void tab_load(const Sched &s, SeqTab &tb) {
   const int lane = threadIdx.x & 31;
-  long long base = 0;
-  for (int b0 = 0; b0 < s.batch; b0 += 32) {
-    const int b = b0 + lane;
-    int n = 0;
-    if (b < s.batch) {
-      bool ok;
-      n = seq_tiles(seq_prefix(s, b, &ok));
-    }
-    const long long v = (long long)n * s.gpb();
-    long long incl = v;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, b < s.batch && base + incl > u);
+  for (int i = 0; i < 4; ++i) tb.raw[i] = 32 * i + lane < s.batch ? s.prefix_len[32 * i + lane] : 0;
+}
+// f(i, raw) for the chunks i of 32 sequences in order (raw: the lane's
+// sequence 32 i + lane, 0 past the batch) until f returns true (uniform).
+template <typename F>
+__device__ __forceinline__ void for_chunks(const Sched &s, const SeqTab &tb, F f) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (32 * i >= s.batch || f(i, tb.raw[i])) return;
+  }
+  for (int i = 4; 32 * i < s.batch; ++i)
+    if (f(i, 32 * i + lane < s.batch ? s.prefix_len[32 * i + lane] : 0)) return;
+}
+// prefix_len[b] for a warp-uniform b (0 past the batch).
+__device__ __forceinline__ int warp_raw(const Sched &s, const SeqTab &tb, int b) {
+  if (b >= s.batch) return 0;
+  if (b >= kTabSeqs) return s.prefix_len[b];
+  int v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int x = __shfl_sync(0xffffffffu, tb.raw[i], b & 31);
+    if ((b >> 5) == i) v = x;
+  }
+  return v;
+}
+// Total weight W and units U of all row groups.
+__device__ __forceinline__ void warp_totals(const Sched &s, const SeqTab &tb, long long *W, long long *U) {
+  const int lane = threadIdx.x & 31;
+  long long n = 0;
+  for_chunks(s, tb, [&](int i, int raw) {
+    n += 32 * i + lane < s.batch ? tiles_of(s, raw) : 0;
+    return false;
+  });
+  const long long nt = warp_sum_ll(n);
+  *U = nt * s.gpb();
+  *W = (nt + (long long)kSegW * s.batch) * s.gpb();
+}
+
+// A unit: sequence, row group, tile; its index among all units; the start
+// weight of its row group.
+struct Pos {
+  int b, gi, t;
+  long long u, wrg;
+};
+// The first unit whose start weight is >= x (past the last unit: b = batch,
+// u = U, wrg = W).
+__device__ Pos warp_seek(const Sched &s, const SeqTab &tb, long long x) {
+  const int lane = threadIdx.x & 31;
+  const int gpb = s.gpb();
+  long long W0 = 0, U0 = 0;
+  Pos p{s.batch, 0, 0, 0, 0};
+  bool found = false;
+  for_chunks(s, tb, [&](int i, int raw) -> bool {
+    const bool in = 32 * i + lane < s.batch;
+    const int n = in ? tiles_of(s, raw) : 0;
+    const long long w = in ? (long long)gpb * (n + kSegW) : 0, uu = (long long)gpb * n;
+    const long long wi = warp_incl_ll(w), ui = warp_incl_ll(uu);
+    const unsigned hit = __ballot_sync(0xffffffffu, in && W0 + wi > x);
     if (hit) {
       const int l = __ffs(hit) - 1;
-      const long long before = base + __shfl_sync(0xffffffffu, incl - v, l);
+      const long long wb = W0 + __shfl_sync(0xffffffffu, wi - w, l);
+      const long long ub = U0 + __shfl_sync(0xffffffffu, ui - uu, l);
       const int nl = __shfl_sync(0xffffffffu, n, l);
-      const long long local = u - before;
-      *b_out = b0 + l;
-      *gi_out = (int)(local / nl);
-      *t_out = (int)(local % nl);
-      return;
+      int gi = (int)((x - wb) / (nl + kSegW));
+      const int r = (int)(x - wb - (long long)gi * (nl + kSegW));
+      int t = r == 0 ? 0 : max(1, r - kSegW);
+      int b = 32 * i + l;
+      p.u = ub + (long long)gi * nl + t;
+      p.wrg = wb + (long long)gi * (nl + kSegW);
+      if (t >= nl) {  // past the row group's last tile: the next row group's tree tile
+        t = 0;
+        p.wrg += nl + kSegW;
+        if (++gi == gpb) {
+          gi = 0;
+          ++b;
+        }
+      }
+      p.b = b;
+      p.gi = gi;
+      p.t = t;
+      found = true;
+      return true;
     }
-    base += __shfl_sync(0xffffffffu, incl, 31);
+    W0 += __shfl_sync(0xffffffffu, wi, 31);
+    U0 += __shfl_sync(0xffffffffu, ui, 31);
+    return false;
+  });
+  if (!found) {
+    p.u = U0;
+    p.wrg = W0;
   }
-  *b_out = s.batch;
-  *gi_out = 0;
-  *t_out = 0;
+  return p;
 }
 
-// Tiles per row group of the lane's sequences b = 32 i + lane (B <= 128),
-// loaded in one round; returns U, the units of all row groups (full warp).
-constexpr int kLookupSeqs = 128;
-__device__ long long warp_load_tiles(const Sched &s, int (&n)[4]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int b = 32 * i + lane;
-    bool ok;
-    n[i] = b < s.batch ? seq_tiles(seq_prefix(s, b, &ok)) : 0;
-  }
-  long long acc = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) acc += warp_sum_ll(n[i]);
-  return acc * s.gpb();
+// Clusters in use: each range is at least as wide as the heaviest unit, so
+// every range holds a unit's start.
+__device__ __forceinline__ long long clusters_used(const Sched &s, long long W) {
+  return max(1ll, min((long long)s.n_clusters, W / (1 + kSegW)));
 }
-// warp_locate with the tile counts already in registers (B <= 128).
-__device__ void warp_locate_n(const Sched &s, const int (&n)[4], long long u, int *b_out, int *gi_out, int *t_out) {
-  const int lane = threadIdx.x & 31;
-  long long base = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const long long v = (long long)n[i] * s.gpb();
-    long long incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, 32 * i + lane < s.batch && base + incl > u);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      const long long before = base + __shfl_sync(0xffffffffu, incl - v, l);
-      const int nl = __shfl_sync(0xffffffffu, n[i], l);
-      const long long local = u - before;
-      *b_out = 32 * i + l;
-      *gi_out = (int)(local / nl);
-      *t_out = (int)(local % nl);
-      return;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  *b_out = s.batch;
-  *gi_out = 0;
-  *t_out = 0;
-}
-// Total units U, and the sequence / row group / tile of unit u(U) (full
-// warp; one round of loads when B <= 128).
-template <typename UnitOf>
-__device__ long long warp_find(const Sched &s, UnitOf unit_of, long long *u_out, int *b, int *gi, int *t) {
-  long long U, u;
-  if (s.batch <= kLookupSeqs) {
-    int n[4];
-    U = warp_load_tiles(s, n);
-    u = unit_of(U);
-    if (u >= 0) warp_locate_n(s, n, u, b, gi, t);
-  } else {
-    U = warp_units_before(s, s.batch);
-    u = unit_of(U);
-    if (u >= 0) warp_locate(s, u, b, gi, t);
-  }
-  *u_out = u;
-  return U;
+__device__ __forceinline__ long long range_start(long long c, long long W, long long C) { return c * W / C; }
+// Cluster whose range holds weight x (the largest c with range_start(c) <= x).
+__device__ __forceinline__ int cluster_of(long long x, long long W, long long C) {
+  return (int)(((x + 1) * C - 1) / W);
 }
 
-__device__ __forceinline__ long long range_start(long long c, long long U, long long C) { return c * U / C; }
-// Cluster whose range holds unit u (the largest c with range_start(c) <= u).
-__device__ __forceinline__ int cluster_of(long long u, long long U, long long C) {
-  return (int)(((u + 1) * C - 1) / U);
+// Range boundary k (the start of cluster k's range, k >= 1): whether it is
+// the first range start inside a row group cut by range ends, that row
+// group, and the last cluster holding a part of it (the first is k - 1).
+// Written by cluster k for every k of the grid, read by the merge kernel.
+struct CutDesc {
+  int usable, b, gi, c_hi;
+};
+__device__ __forceinline__ CutDesc *cut_descs(void *ws, int n_clusters) {
+  return reinterpret_cast<CutDesc *>(reinterpret_cast<uint8_t *>(ws) +
+                                     (size_t)n_clusters * 2 * kPairRows * kPartialBytes);
 }
 
 // Walks the tiles of a cluster's range in order.  The next sequence's
@@ -266,7 +289,7 @@ struct Cur {
 };
 __device__ __forceinline__ int load_prefix(const Sched &s, int b) { return b < s.batch ? s.prefix_len[b] : 0; }
 __device__ __forceinline__ void cur_apply(Cur &c, const Sched &s, int raw) {
-  c.ok = raw >= 0 && raw <= s.max_prefix && raw <= s.s_max;
+  c.ok = prefix_ok(s, raw);
   c.P = c.ok ? raw : 0;
   c.n = seq_tiles(c.P);
 }
@@ -275,8 +298,8 @@ __device__ __forceinline__ Cur cur_begin(const Bars *bars, const Sched &s) {
   c.b = bars->start_b;
   c.gi = bars->start_gi;
   c.t = bars->start_t;
-  cur_apply(c, s, load_prefix(s, c.b));
-  c.raw_next = load_prefix(s, c.b + 1);
+  cur_apply(c, s, bars->start_raw);
+  c.raw_next = bars->start_raw_next;
   return c;
 }
 __device__ __forceinline__ void cur_next(Cur &c, const Sched &s) {
@@ -345,63 +368,89 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) sv::report(status, SPEC_DEV_INTERNAL);
     return;
   }
-  if (warp == 0) {
-    // with C = min(clusters, U) every range below C holds at least one unit
-    int b = s.batch, gi = 0, t = 0;
-    long long u0;
-    const long long U = warp_find(
-        s, [&](long long U_) -> long long {
-          const long long C = min((long long)s.n_clusters, U_);
-          return cluster < C ? range_start(cluster, U_, C) : -1;
-        },
-        &u0, &b, &gi, &t);
-    const long long C = min((long long)s.n_clusters, U);
-    const long long u1 = cluster < C ? range_start(cluster + 1, U, C) : 0;
-    if (lane == 0) {
-      bars->start_b = b;
-      bars->start_gi = gi;
-      bars->start_t = t;
-      bars->n_tiles = u0 >= 0 ? (int)(u1 - u0) : 0;
-    }
-  }
-  __syncthreads();
-  const int T = bars->n_tiles;
-  if (T == 0) return;  // same range for both CTAs of the cluster
-
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kKS; ++i) {
-      mbar_init(&bars->kland[i], 1);
-      mbar_init(&bars->kempty[i], 1);
-      mbar_init(&bars->kfull[i], 2);
-    }
-    for (int i = 0; i < kVS; ++i) {
-      mbar_init(&bars->vland[i], 1);
-      mbar_init(&bars->vempty[i], 1);
-    }
-    for (int i = 0; i < kQB; ++i) {
-      mbar_init(&bars->qland[i], 1);
-      mbar_init(&bars->qempty[i], 1);
-      mbar_init(&bars->qfull[i], 2);
-    }
-    for (int i = 0; i < kSB; ++i) {
-      mbar_init(&bars->sfull[i], 1);
-      mbar_init(&bars->ofull[i], 1);
-      // one arrival per softmax warp of both CTAs and one for the odd CTA's
-      // V half; the softmax may finish tiles g .. g+kSB-1 before the PV
-      // issuer observes tile g, never g+kSB (it needs S(g+kSB), issued
-      // after PV(g) completed)
-      mbar_init(&bars->pfull[i], 17);
-    }
-    mbar_init(&bars->drain, 2);  // one commit from each MMA-issuing warp
-    bars->abort = 0;
-    mbar_fence_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_kt);
+    tma_prefetch_desc(&tm_vt);
   }
-  if (warp == 1) tmem_alloc_pair(&bars->tmem, 512);
+  // The range lookup (warp 0) overlaps the barrier and TMEM set-up (warp 1).
+  if (warp == 0) {
+    SeqTab tb;
+    tab_load(s, tb);
+    long long W, U;
+    warp_totals(s, tb, &W, &U);
+    const long long C = clusters_used(s, W);
+    Pos p0{s.batch, 0, 0, 0, 0};
+    int T = 0;
+    if (cluster < C) {
+      p0 = warp_seek(s, tb, range_start(cluster, W, C));
+      const long long u1 = cluster + 1 < C ? warp_seek(s, tb, range_start(cluster + 1, W, C)).u : U;
+      T = (int)(u1 - p0.u);
+    }
+    const int raw0 = warp_raw(s, tb, p0.b), raw1 = warp_raw(s, tb, p0.b + 1);
+    if (lane == 0) {
+      bars->start_b = p0.b;
+      bars->start_gi = p0.gi;
+      bars->start_t = p0.t;
+      bars->n_tiles = T;
+      bars->start_raw = raw0;
+      bars->start_raw_next = raw1;
+      if (rank == 0 && cluster >= 1) {
+        CutDesc d{0, 0, 0, 0};
+        if (cluster < C && p0.t != 0) {  // this range starts inside row group (b, gi)
+          d.usable = cluster_of(p0.wrg, W, C) == cluster - 1;
+          d.b = p0.b;
+          d.gi = p0.gi;
+          d.c_hi = cluster_of(p0.wrg + unit_start_w(tiles_of(s, raw0) - 1), W, C);
+        }
+        cut_descs(ws, s.n_clusters)[cluster] = d;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < kKS; ++i) {
+        mbar_init(&bars->kland[i], 1);
+        mbar_init(&bars->kempty[i], 1);
+        mbar_init(&bars->kfull[i], 2);
+      }
+      for (int i = 0; i < kVS; ++i) {
+        mbar_init(&bars->vland[i], 1);
+        mbar_init(&bars->vempty[i], 1);
+      }
+      for (int i = 0; i < kQB; ++i) {
+        mbar_init(&bars->qland[i], 1);
+        mbar_init(&bars->qempty[i], 1);
+        mbar_init(&bars->qfull[i], 2);
+      }
+      for (int i = 0; i < kSB; ++i) {
+        mbar_init(&bars->sfull[i], 1);
+        mbar_init(&bars->ofull[i], 1);
+        // one arrival per softmax warp of both CTAs and one for the odd CTA's
+        // V half; the softmax may finish tiles g .. g+kSB-1 before the PV
+        // issuer observes tile g, never g+kSB (it needs S(g+kSB), issued
+        // after PV(g) completed)
+        mbar_init(&bars->pfull[i], 17);
+      }
+      mbar_init(&bars->drain, 2);  // one commit from each MMA-issuing warp
+      bars->abort = 0;
+      mbar_fence_init();
+    }
+    __syncwarp();
+    tmem_alloc_pair(&bars->tmem, 512);
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the partner's barriers exist before any remote arrival or commit
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
+  const int T = bars->n_tiles;
+  if (T == 0) {  // same (empty) range for both CTAs of the cluster
+    if (warp == 1) tmem_dealloc_pair(tmem, 512);
+    return;
+  }
+  if (threadIdx.x == 0) grid_dep_launch();  // the merge grid may start locating its row groups
   const int pairs = s.pairs;
 
   if (warp == 0 || warp == 10) {
@@ -410,14 +459,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool is_v = warp == 10;
       Cur c = cur_begin(bars, s);
       int seg = 0, issued = 0, q_issued = 0;
-      if (!is_v) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_kc);
-        tma_prefetch_desc(&tm_kt);
-      } else {
-        tma_prefetch_desc(&tm_vc);
-        tma_prefetch_desc(&tm_vt);
-      }
       Cur cpf = c;  // kPrefetch tiles ahead of c
       for (int i = 0; i < kPrefetch && i < T; ++i) cur_next(cpf, s);
       for (int g = 0; g < T; ++g) {
@@ -629,7 +670,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
     const float NEG_INF = -INFINITY;
     Cur c = cur_begin(bars, s);
-    int seg = 0;
     bool from_start = c.t == 0;
     float ma = NEG_INF, mb = NEG_INF;  // running max of rows ra, rb (log2 units)
     float la = 0.f, lb_sum = 0.f;      // this thread's part of their sums
@@ -650,7 +690,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool first = g == 0 || c.t == 0;
       if (first) {
         if (g > 0) {
-          ++seg;
           from_start = true;
           amask_a = next_a;
           amask_b = next_b;
@@ -808,6 +847,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pair_sync();  // read before either warp writes the next row group's
         const int rg = grow(c.gi, r);
         const bool complete = from_start && c.t == c.n - 1;
+        // a prefix out of bounds: the sequence is reported, its rows left unwritten
+        if (!c.ok && warp == 2 && lane == 0 && c.gi == 0) sv::report(status, SPEC_DEV_CAPACITY);
         const bool row_ok = rg < R;
         const int kvh = c.gi / pairs;
         const uint32_t q_off = (uint32_t)(quarter * 32) << 16;
@@ -835,7 +876,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            const int slot = cluster * 2 + (seg == 0 ? 0 : 1);
+            // a part cut at the range end: slot 2c + 1; the one cut at its start: 2c
+            const int slot = cluster * 2 + (g == T - 1 && c.t != c.n - 1 ? 1 : 0);
             uint8_t *w = reinterpret_cast<uint8_t *>(ws) +
                          ((int64_t)slot * kPairRows + (int)rank * 128 + r) * kPartialBytes;
 #pragma unroll
@@ -874,94 +916,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merges the partials of the row groups cut by cluster range ends.  At most
-// C - 1 row groups are cut; a cut row group is merged by the blocks of the
-// first range boundary inside it.  Block = (boundary k, 16 of the 256 rows);
-// warp = 2 rows, lane = 4 head dims; all partials of a row are loaded at
-// once (lane i: the i-th contributor's max and sum).
-constexpr int kCombRows = 16;
-__global__ void __launch_bounds__(256) attn_tc2_combine_kernel(const void *__restrict__ ws,
-                                                               __nv_bfloat16 *__restrict__ out, const Sched s,
-                                                               int Hq) {
-  __shared__ int sh[7];  // usable, b, gi, c_lo, c_hi, c_lo's slot is its first
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k = blockIdx.x + 1;  // boundary between clusters k-1 and k
-  if (warp == 0) {
-    int b = s.batch, gi = 0, t = 0;
-    long long u;
-    const long long U = warp_find(
-        s, [&](long long U_) -> long long {
-          const long long C = min((long long)s.n_clusters, U_);
-          return k < C ? range_start(k, U_, C) : -1;
-        },
-        &u, &b, &gi, &t);
-    const long long C = min((long long)s.n_clusters, U);
-    int usable = 0, c_lo = 0, c_hi = 0, first = 0;
-    if (u >= 0 && t != 0) {  // the boundary cuts row group (b, gi)
-      bool ok;
-      const int n = seq_tiles(seq_prefix(s, b, &ok));
-      const long long ug = u - t;
-      c_lo = cluster_of(ug, U, C);
-      usable = ok && c_lo == k - 1;  // k is the first boundary inside it
-      c_hi = cluster_of(ug + n - 1, U, C);
-      first = range_start(c_lo, U, C) == ug;
-    }
-    if (lane == 0) {
-      sh[0] = usable;
-      sh[1] = b;
-      sh[2] = gi;
-      sh[3] = c_lo;
-      sh[4] = c_hi;
-      sh[5] = first;
-    }
-  }
-  __syncthreads();
-  if (!sh[0]) return;
-  const int b = sh[1], gi = sh[2], c_lo = sh[3], c_hi = sh[4], first = sh[5];
-  const int nc = c_hi - c_lo + 1;
+// Merges the partials of the row groups cut by cluster range ends: block
+// (k - 1, y) merges rows [32 y, +32) of the row group whose first range
+// start inside it is boundary k, if any (its descriptor, written by cluster
+// k).  Thread = (row, 16 head dims), 8 threads per row; each reads every
+// contributor's max and sum itself, so a row needs no exchange, and the
+// loads of up to kCombBatch contributors are in flight together.  Launched
+// as a programmatic dependent of the main kernel: its blocks become
+// resident as the main kernel's CTAs leave and wait for it to complete.
+constexpr int kCombRows = 32;
+constexpr int kCombBatch = 3;
+__global__ void __launch_bounds__(256, 4) attn_tc2_combine_kernel(void *__restrict__ ws, __nv_bfloat16 *__restrict__ out,
+                                                                  const Sched s, int Hq) {
+  const int k = blockIdx.x + 1;                 // boundary between clusters k-1 and k
+  const int rr = blockIdx.y * kCombRows + (threadIdx.x >> 3);  // row of the pair
+  const int d0 = (threadIdx.x & 7) * 16;        // first head dim
+  grid_dep_wait();  // the main kernel's partials and descriptors are written and visible
+  const CutDesc d = cut_descs(ws, s.n_clusters)[k];
+  if (!d.usable) return;
   const int G = Hq / s.hkv, R = s.n_nodes * G;
-  const int kvh = gi / s.pairs, pair = gi % s.pairs;
-  auto row_of = [&](int c, int rr) -> const uint8_t * {
-    const int slot = c * 2 + ((c == c_lo && !first) ? 1 : 0);
+  const int kvh = d.gi / s.pairs, pair = d.gi % s.pairs;
+  const int rg = pair * kPairRows + rr;
+  if (rg >= R) return;
+  const int c_lo = k - 1, nc = d.c_hi - c_lo + 1;
+  // cluster c's part: slot 2c + 1 when cut at its range end (all but the last)
+  auto row_of = [&](int c) -> const uint8_t * {
+    const int slot = 2 * c + (c < d.c_hi ? 1 : 0);
     return reinterpret_cast<const uint8_t *>(ws) + ((int64_t)slot * kPairRows + rr) * kPartialBytes;
   };
+  float M = -INFINITY, L = 0.f;
+  float acc[16];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int rr = blockIdx.y * kCombRows + warp * 2 + q;
-    const int rg = pair * kPairRows + rr;
-    if (rg >= R) continue;
-    // the largest running max over the contributors
-    float M = -INFINITY;
-    for (int c0 = 0; c0 < nc; c0 += 32)
-      if (c0 + lane < nc) M = fmaxf(M, reinterpret_cast<const float *>(row_of(c_lo + c0 + lane, rr) + kD * 2)[0]);
-    M = sv::warp_max(M);
-    float L = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < nc; c0 += 32) {
-      float f = 0.f;
-      if (c0 + lane < nc) {
-        const float2 ml = *reinterpret_cast<const float2 *>(row_of(c_lo + c0 + lane, rr) + kD * 2);
-        f = exp2f(ml.x - M);
-        L = fmaf(f, ml.y, L);
-      }
-      const int m = min(32, nc - c0);
-      for (int i = 0; i < m; ++i) {
-        const float fi = __shfl_sync(0xffffffffu, f, i);
-        const uint2 o = reinterpret_cast<const uint2 *>(row_of(c_lo + c0 + i, rr))[lane];  // dims 4 lane .. +3
-        acc.x = fmaf(fi, __uint_as_float(o.x << 16), acc.x);
-        acc.y = fmaf(fi, __uint_as_float(o.x & 0xFFFF0000u), acc.y);
-        acc.z = fmaf(fi, __uint_as_float(o.y << 16), acc.z);
-        acc.w = fmaf(fi, __uint_as_float(o.y & 0xFFFF0000u), acc.w);
+  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+  for (int c0 = 0; c0 < nc; c0 += kCombBatch) {
+    float2 ml[kCombBatch];
+    uint4 o[kCombBatch][2];
+#pragma unroll
+    for (int i = 0; i < kCombBatch; ++i) {
+      if (c0 + i < nc) {
+        const uint8_t *row = row_of(c_lo + c0 + i);
+        ml[i] = *reinterpret_cast<const float2 *>(row + kD * 2);
+        o[i][0] = *reinterpret_cast<const uint4 *>(row + d0 * 2);
+        o[i][1] = *reinterpret_cast<const uint4 *>(row + d0 * 2 + 16);
+      } else {
+        ml[i] = make_float2(-INFINITY, 0.f);
+        o[i][0] = o[i][1] = make_uint4(0, 0, 0, 0);
       }
     }
-    L = sv::warp_sum(L);
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat16 *o = out + (((int64_t)b * s.n_nodes + rg / G) * Hq + kvh * G + rg % G) * kD + lane * 4;
-    uint2 v;
-    v.x = pack_bf16(acc.x * inv, acc.y * inv);
-    v.y = pack_bf16(acc.z * inv, acc.w * inv);
-    *reinterpret_cast<uint2 *>(o) = v;
+    float Mb = M;
+#pragma unroll
+    for (int i = 0; i < kCombBatch; ++i) Mb = fmaxf(Mb, ml[i].x);
+    // every part has a finite max (each tile holds a visible key)
+    const float r = exp2f(M - Mb);  // 0 on the first batch
+    L *= r;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] *= r;
+#pragma unroll
+    for (int i = 0; i < kCombBatch; ++i) {
+      const float f = c0 + i < nc ? exp2f(ml[i].x - Mb) : 0.f;
+      L = fmaf(f, ml[i].y, L);
+      const uint32_t w[8] = {o[i][0].x, o[i][0].y, o[i][0].z, o[i][0].w, o[i][1].x, o[i][1].y, o[i][1].z, o[i][1].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc[2 * j] = fmaf(f, __uint_as_float(w[j] << 16), acc[2 * j]);
+        acc[2 * j + 1] = fmaf(f, __uint_as_float(w[j] & 0xFFFF0000u), acc[2 * j + 1]);
+      }
+    }
+    M = Mb;
   }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint4 v0, v1;
+  v0.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  v0.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  v0.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  v0.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  v1.x = pack_bf16(acc[8] * inv, acc[9] * inv);
+  v1.y = pack_bf16(acc[10] * inv, acc[11] * inv);
+  v1.z = pack_bf16(acc[12] * inv, acc[13] * inv);
+  v1.w = pack_bf16(acc[14] * inv, acc[15] * inv);
+  uint4 *dst = reinterpret_cast<uint4 *>(out + (((int64_t)d.b * s.n_nodes + rg / G) * Hq + kvh * G + rg % G) * kD + d0);
+  dst[0] = v0;
+  dst[1] = v1;
 }
 
 // ---------------------------------------------------------------------------
@@ -1031,7 +1066,7 @@ bool sv_attn_tc2_supported(const SvAttnShape &s) {
 
 size_t sv_attn_tc2_ws_bytes() {
   const int c = tc2_clusters();
-  return c > 0 ? (size_t)c * 2 * kPairRows * kPartialBytes : 0;
+  return c > 0 ? (size_t)c * (2 * kPairRows * kPartialBytes + sizeof(CutDesc)) : 0;
 }
 
 int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void *vc, const void *kt, const void *vt,
@@ -1080,8 +1115,21 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
                                                           ws, s.hq, scale * 1.4426950408889634f, status);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (C > 1) {
-    const dim3 cgrid(C - 1, kPairRows / kCombRows);
-    attn_tc2_combine_kernel<<<cgrid, 256, 0, stream>>>(ws, (__nv_bfloat16 *)out, sc, s.hq);
+    // programmatic dependent launch: the merge blocks locate their row groups
+    // while the main kernel runs (it triggers its dependents after setup)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C - 1, kPairRows / kCombRows);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, attn_tc2_combine_kernel, ws, (__nv_bfloat16 *)out, sc, s.hq) !=
+        cudaSuccess)
+      return SPEC_ERR_CUDA;
   }
   return sv_launch_status();
 }

@@ -90,6 +90,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Programmatic dependent launch: the grid launched after this one with the
+// programmatic-serialization attribute may start once every CTA of this
+// grid has executed launch_dependents (or exited); the dependent grid's
+// grid_dep_wait returns once this grid has completed and its writes are
+// visible.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Bring a 2D tile into L2 ahead of its shared-memory load (no destination,
 // no barrier).
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
