@@ -683,6 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint64_t amask_a = c.t == 0 ? load_mask(c.b, c.gi, ra) : 0ull, amask_b = c.t == 0 ? load_mask(c.b, c.gi, rb) : 0ull;
     uint64_t next_a = 0ull, next_b = 0ull;
     bool ok = true;
+    bool s_ready = false;  // S(g) seen complete during tile g - 1
     // A failed wait (timeout) or an abort turns the rest into a no-op that
     // still passes every pair barrier, so the two warps of a pair always
     // execute the same barriers.
@@ -702,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         next_a = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, ra);
         next_b = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, rb);
       }
-      if (ok && !warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1)) ok = false;
+      if (ok && !s_ready && !warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1)) ok = false;
       const uint32_t s_addr = tmem + lane_off + (uint32_t)(g % kSB) * 128u;
       // sv[4j + e]: row ra, key 8j + 2 tq + e;  sv[4j + 2 + e]: row rb
       uint32_t sv[64];
@@ -792,6 +793,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // S(g + 1) has nearly always completed by now; testing it here lets
+        // the barrier's latency overlap the exponentials
+        const bool next_done = ok && g + 1 < T && mbar_test(&bars->sfull[(g + 1) % kSB], ((g + 1) / kSB) & 1);
         if (ok) {
           // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
           // column 4j + tq, written over the tile's first 64 S columns of this
@@ -820,12 +824,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
         }
+        s_ready = __all_sync(0xffffffffu, next_done);
       };
-      if (tree || nvalid < kBN)
+      if (__builtin_expect(tree || nvalid < kBN, 0))
         tile(std::true_type{});
       else
         tile(std::false_type{});
-      if (g == T - 1 || c.t == c.n - 1) {
+      if (__builtin_expect(g == T - 1 || c.t == c.n - 1, 0)) {
         // ---------------------------------------------------- epilogue
         // Rows' running max and full sum through shared memory, then one row
         // per thread again (lanes of the quarter) for the O read-out: warp u
