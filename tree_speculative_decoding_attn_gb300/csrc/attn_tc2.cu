@@ -89,6 +89,7 @@ constexpr int kSB = 3;                       // S/P buffers in TMEM (128 columns
 constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 in all)
 constexpr float kTau = 8.f;                  // running max moves only when a tile exceeds it by 2^8
 constexpr uint16_t kBoth = 3;                // CTA mask of the pair
+constexpr int kStoreThread = 64;             // softmax thread that issues the output stores (warp 2, lane 0)
 // A partial row: 128 bf16 of unnormalised O (256 B), then the running max
 // (log2 units) and the sum as float32, padded to 272 B.
 constexpr int kPartialBytes = kD * 2 + 16;
@@ -102,7 +103,6 @@ struct Bars {
   volatile int abort;
   int start_b, start_gi, start_t, n_tiles;     // this cluster's first unit and unit count
   int start_raw, start_raw_next;               // prefix_len[start_b], prefix_len[start_b + 1] (0 past the batch)
-  float xm[128], xl[128];                      // per-row running max and sum at a row group's end
 };
 constexpr uint32_t kTileBytes = kQB * kQBytes + kKS * kKBytes + kVS * kVBytes;
 constexpr uint32_t kSmemBytes = kTileBytes + sizeof(Bars);
@@ -348,9 +348,9 @@ __device__ __forceinline__ bool v_ready(Bars *bars, uint8_t *sV, int g, int nkey
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                     const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
-                    const __grid_constant__ CUtensorMap tm_vt, const Sched s, const uint64_t *__restrict__ anc,
-                    __nv_bfloat16 *__restrict__ out, void *__restrict__ ws, int Hq, float scale_log2,
-                    int32_t *status) {
+                    const __grid_constant__ CUtensorMap tm_vt, const __grid_constant__ CUtensorMap tm_o,
+                    const Sched s, const uint64_t *__restrict__ anc, void *__restrict__ ws, int Hq,
+                    float scale_log2, int32_t *status) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + kQB * kQBytes;
@@ -374,6 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_vc);
     tma_prefetch_desc(&tm_kt);
     tma_prefetch_desc(&tm_vt);
+    tma_prefetch_desc(&tm_o);
   }
   // The range lookup (warp 0) overlaps the barrier and TMEM set-up (warp 1).
   if (warp == 0) {
@@ -421,7 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int i = 0; i < kQB; ++i) {
         mbar_init(&bars->qland[i], 1);
-        mbar_init(&bars->qempty[i], 1);
+        mbar_init(&bars->qempty[i], 2);  // the segment's last S MMA, and its output store
         mbar_init(&bars->qfull[i], 2);
       }
       for (int i = 0; i < kSB; ++i) {
@@ -665,11 +666,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int tq = lane & 3;
     const int ra = lb + (lane >> 2), rb = ra + 8;  // this thread's rows (TMEM lanes)
     const uint32_t lane_off = (uint32_t)lb << 16;
-    const uint32_t pair_bar = 1u + (uint32_t)quarter;
-    auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(pair_bar) : "memory"); };
+    // the 8 softmax warps of this CTA (named barrier 1)
+    auto softmax_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
     const float NEG_INF = -INFINITY;
     Cur c = cur_begin(bars, s);
+    int seg = 0;        // segment (row group part) of this range: Q buffer seg % kQB
+    int q_pending = 0;  // 1 + the Q buffer the last output store reads (store thread)
     bool from_start = c.t == 0;
     float ma = NEG_INF, mb = NEG_INF;  // running max of rows ra, rb (log2 units)
     float la = 0.f, lb_sum = 0.f;      // this thread's part of their sums
@@ -687,226 +690,267 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // A failed wait (timeout) or an abort turns the rest into a no-op that
     // still passes every pair barrier, so the two warps of a pair always
     // execute the same barriers.
-    for (int g = 0; g < T; ++g) {
-      const bool first = g == 0 || c.t == 0;
-      if (first) {
-        if (g > 0) {
-          from_start = true;
-          amask_a = next_a;
-          amask_b = next_b;
-        }
-        ma = mb = NEG_INF;
-        la = lb_sum = 0.f;
+    // Outer loop: the segments of the range (a row group, or the part of one
+    // the range holds); inner loop: their tiles.  The epilogue and the
+    // segment set-up stay out of the per-tile loop.
+    for (int g = 0; g < T;) {
+      if (g > 0) {  // a later segment starts at a row group's tree tile
+        ++seg;
+        from_start = true;
+        amask_a = next_a;
+        amask_b = next_b;
       }
-      if (c.t == c.n - 1 && g + 1 < T) {  // the next tile starts the next row group
+      ma = mb = NEG_INF;
+      la = lb_sum = 0.f;
+      if (g + (c.n - 1 - c.t) + 1 < T) {  // the next segment's ancestor bits, a segment ahead
         const bool same_b = c.gi + 1 < s.gpb();
         next_a = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, ra);
         next_b = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, rb);
       }
-      if (ok && !s_ready && !warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1)) ok = false;
-      const uint32_t s_addr = tmem + lane_off + (uint32_t)(g % kSB) * 128u;
-      // sv[4j + e]: row ra, key 8j + 2 tq + e;  sv[4j + 2 + e]: row rb
-      uint32_t sv[64];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld_16x256b_x16(s_addr, sv);
-        tmem_wait_ld();
-      } else {
+      bool first = true;
+      for (;;) {
+        if (ok && !s_ready && !warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1)) ok = false;
+        const uint32_t s_addr = tmem + lane_off + (uint32_t)(g % kSB) * 128u;
+        // sv[4j + e]: row ra, key 8j + 2 tq + e;  sv[4j + 2 + e]: row rb
+        uint32_t sv[64];
+        if (ok) {
+          tc_fence_after();
+          tmem_ld_16x256b_x16(s_addr, sv);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) sv[i] = __float_as_uint(0.f);
-      }
-      const bool tree = c.t == 0;
-      const int nvalid = tree ? N : tile_keys(c);
-      // The tile body comes in two instances so that full prefix tiles, the
-      // steady state, carry no masking code: the masked one serves the tree
-      // tile and the last, partial prefix tile.
-      auto tile = [&](auto masked) {
-        if constexpr (decltype(masked)::value) {
-          // Visibility of this thread's keys 8j + 2 tq + e as bits 2j + e: the
-          // keys below nvalid are a prefix of these bits (they increase with
-          // the bit index); on the tree tile (N <= 64) also the ancestor bits.
-          const int m8 = nvalid - 2 * tq;
-          const int nb = m8 <= 0 ? 0 : min(32, 2 * (m8 >> 3) + min(2, m8 & 7));
-          const uint32_t in = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
-          uint32_t va = in, vb = in;
-          if (tree) {
-            auto mine = [&](uint64_t m) -> uint32_t {
-              uint64_t x = (m >> (2 * tq)) & 0x0303030303030303ull;
-              x = (x | (x >> 6)) & 0x000F000F000F000Full;
-              x = (x | (x >> 12)) & 0x000000FF000000FFull;
-              return (uint32_t)((x | (x >> 24)) & 0xFFFFull);
-            };
-            va &= mine(amask_a);
-            vb &= mine(amask_b);
-          }
+          for (int i = 0; i < 64; ++i) sv[i] = __float_as_uint(0.f);
+        }
+        const bool tree = c.t == 0;
+        const int nvalid = tree ? N : tile_keys(c);
+        // The tile body comes in two instances so that full prefix tiles, the
+        // steady state, carry no masking code: the masked one serves the tree
+        // tile and the last, partial prefix tile.
+        auto tile = [&](auto masked) {
+          if constexpr (decltype(masked)::value) {
+            // Visibility of this thread's keys 8j + 2 tq + e as bits 2j + e: the
+            // keys below nvalid are a prefix of these bits (they increase with
+            // the bit index); on the tree tile (N <= 64) also the ancestor bits.
+            const int m8 = nvalid - 2 * tq;
+            const int nb = m8 <= 0 ? 0 : min(32, 2 * (m8 >> 3) + min(2, m8 & 7));
+            const uint32_t in = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
+            uint32_t va = in, vb = in;
+            if (tree) {
+              auto mine = [&](uint64_t m) -> uint32_t {
+                uint64_t x = (m >> (2 * tq)) & 0x0303030303030303ull;
+                x = (x | (x >> 6)) & 0x000F000F000F000Full;
+                x = (x | (x >> 12)) & 0x000000FF000000FFull;
+                return (uint32_t)((x | (x >> 24)) & 0xFFFFull);
+              };
+              va &= mine(amask_a);
+              vb &= mine(amask_b);
+            }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {  // i = 2j + e: register 4j + e of row ra, 4j + 2 + e of row rb
-            if (!((va >> i) & 1u)) sv[4 * (i >> 1) + (i & 1)] = __float_as_uint(NEG_INF);
-            if (!((vb >> i) & 1u)) sv[4 * (i >> 1) + 2 + (i & 1)] = __float_as_uint(NEG_INF);
-          }
-        }
-        // exact row max of the tile; every row sees a key in every tile
-        // (itself on the tree tile), so it is finite
-        float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
-  #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          xa[j & 1] = fmax3(xa[j & 1], __uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]));
-          xb[j & 1] = fmax3(xb[j & 1], __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
-        }
-        float ta = fmaxf(xa[0], xa[1]), tb = fmaxf(xb[0], xb[1]);
-        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
-        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
-        ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2)) * scale_log2;
-        tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2)) * scale_log2;
-        // The running max moves only when a tile exceeds it by more than
-        // kTau: P = 2^(s - m) stays below 2^kTau, and the sum and O are
-        // rescaled (O once PV(g-1) has completed) only then.
-        const bool need_a = ta > ma + kTau, need_b = tb > mb + kTau;
-        if (ok && __any_sync(0xffffffffu, need_a || need_b)) {
-          const float alpha_a = need_a ? ex2(ma - ta) : 1.f;  // 0 when m was -inf
-          const float alpha_b = need_b ? ex2(mb - tb) : 1.f;
-          if (need_a) {
-            ma = ta;
-            la *= alpha_a;
-          }
-          if (need_b) {
-            mb = tb;
-            lb_sum *= alpha_b;
-          }
-          if (!first && __any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f) &&
-              (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
-            tc_fence_after();
-  #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {  // O columns [32 cc, +32) of this warp's 16 rows
-              uint32_t o[16];
-              const uint32_t oa = tmem + lane_off + kColO + (uint32_t)cc * 32u;
-              tmem_ld_16x256b_x4(oa, o);
-              tmem_wait_ld();
-  #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
-                o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
-                o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
-                o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
-              }
-              tmem_st_16x256b_x4(oa, o);
+            for (int i = 0; i < 32; ++i) {  // i = 2j + e: register 4j + e of row ra, 4j + 2 + e of row rb
+              if (!((va >> i) & 1u)) sv[4 * (i >> 1) + (i & 1)] = __float_as_uint(NEG_INF);
+              if (!((vb >> i) & 1u)) sv[4 * (i >> 1) + 2 + (i & 1)] = __float_as_uint(NEG_INF);
             }
           }
-        }
-        // S(g + 1) has nearly always completed by now; testing it here lets
-        // the barrier's latency overlap the exponentials
-        const bool next_done = ok && g + 1 < T && mbar_test(&bars->sfull[(g + 1) % kSB], ((g + 1) / kSB) & 1);
-        if (ok) {
+          // S(g + 1) has nearly always completed by now; testing it here lets
+          // the barrier's latency overlap this tile's work
+          const bool next_done = ok && g + 1 < T && mbar_test(&bars->sfull[(g + 1) % kSB], ((g + 1) / kSB) & 1);
           // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
           // column 4j + tq, written over the tile's first 64 S columns of this
-          // warp's lanes (all of them were read above)
-          const float2 sc2 = make_float2(scale_log2, scale_log2);
-          const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
-          float2 sa2 = make_float2(0.f, 0.f), sb2 = make_float2(0.f, 0.f);
+          // warp's lanes (all of them were read above); the row sums; and this
+          // thread's largest exponent s * scale - m.
           uint32_t pk[32];
-  #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
-            const float2 xb2 =
-                fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
-            const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
-            const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
-            sa2 = add2(sa2, pa);
-            sb2 = add2(sb2, pb);
-            pk[2 * j] = pack_bf16(pa.x, pa.y);
-            pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
+          float2 sa2, sb2;
+          auto exps = [&]() -> float {
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
+            float mx0 = NEG_INF, mx1 = NEG_INF;
+            sa2 = sb2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
+              const float2 xb2 =
+                  fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
+              mx0 = fmax3(mx0, xa2.x, xa2.y);
+              mx1 = fmax3(mx1, xb2.x, xb2.y);
+              const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
+              const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
+              sa2 = add2(sa2, pa);
+              sb2 = add2(sb2, pb);
+              pk[2 * j] = pack_bf16(pa.x, pa.y);
+              pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
+            }
+            return fmaxf(mx0, mx1);
+          };
+          // Past a row group's first tile, P is computed in one pass with the
+          // running max as it stands: the exact tile max matters only when some
+          // score exceeds the running max by more than kTau, and then the tile is
+          // read again and redone on the exact path (the tree and ragged tiles
+          // and a segment's first tile take the exact path at once).
+          bool exact = decltype(masked)::value || first;
+          for (;;) {
+            if (exact) {
+              // exact row max of the tile; every row sees a key in every tile
+              // (itself on the tree tile), so it is finite
+              float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                xa[j & 1] = fmax3(xa[j & 1], __uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1]));
+                xb[j & 1] = fmax3(xb[j & 1], __uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3]));
+              }
+              float ta = fmaxf(xa[0], xa[1]), tb = fmaxf(xb[0], xb[1]);
+              ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 1));
+              tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 1));
+              ta = fmaxf(ta, __shfl_xor_sync(0xffffffffu, ta, 2)) * scale_log2;
+              tb = fmaxf(tb, __shfl_xor_sync(0xffffffffu, tb, 2)) * scale_log2;
+              // The running max moves only when a tile exceeds it by more than
+              // kTau: P = 2^(s - m) stays below 2^kTau, and the sum and O are
+              // rescaled (O once PV(g-1) has completed) only then.
+              const bool need_a = ta > ma + kTau, need_b = tb > mb + kTau;
+              if (ok && __any_sync(0xffffffffu, need_a || need_b)) {
+                const float alpha_a = need_a ? ex2(ma - ta) : 1.f;  // 0 when m was -inf
+                const float alpha_b = need_b ? ex2(mb - tb) : 1.f;
+                if (need_a) {
+                  ma = ta;
+                  la *= alpha_a;
+                }
+                if (need_b) {
+                  mb = tb;
+                  lb_sum *= alpha_b;
+                }
+                if (!first && __any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f) &&
+                    (ok = warp_wait(&bars->ofull[(g - 1) % kSB], ((g - 1) / kSB) & 1))) {
+                  tc_fence_after();
+#pragma unroll 1
+                  for (int cc = 0; cc < 4; ++cc) {  // O columns [32 cc, +32) of this warp's 16 rows
+                    uint32_t o[16];
+                    const uint32_t oa = tmem + lane_off + kColO + (uint32_t)cc * 32u;
+                    tmem_ld_16x256b_x4(oa, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
+                      o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
+                      o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
+                      o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
+                    }
+                    tmem_st_16x256b_x4(oa, o);
+                  }
+                }
+              }
+            }
+            if (!ok) break;
+            const float mx = exps();
+            if (exact || !__any_sync(0xffffffffu, mx > kTau)) break;
+            exact = true;
+            tmem_ld_16x256b_x16(s_addr, sv);
+            tmem_wait_ld();
           }
-          tmem_st_16x128b_x16(s_addr, pk);
-          la += sa2.x + sa2.y;
-          lb_sum += sb2.x + sb2.y;
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
+          if (ok) {
+            tmem_st_16x128b_x16(s_addr, pk);
+            la += sa2.x + sa2.y;
+            lb_sum += sb2.x + sb2.y;
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(pfull_even0 + (uint32_t)(g % kSB) * (uint32_t)sizeof(uint64_t));
+          }
+          s_ready = __all_sync(0xffffffffu, next_done);
+        };
+        if (__builtin_expect(tree || nvalid < kBN, 0))
+          tile(std::true_type{});
+        else
+          tile(std::false_type{});
+        if (q_pending && threadIdx.x == kStoreThread) {  // the previous output store has long read its buffer
+          bulk_wait_read();
+          mbar_arrive(&bars->qempty[q_pending - 1]);
+          q_pending = 0;
         }
-        s_ready = __all_sync(0xffffffffu, next_done);
-      };
-      if (__builtin_expect(tree || nvalid < kBN, 0))
-        tile(std::true_type{});
-      else
-        tile(std::false_type{});
-      if (__builtin_expect(g == T - 1 || c.t == c.n - 1, 0)) {
+        if (g == T - 1 || c.t == c.n - 1) break;
+        cur_next(c, s);
+        ++g;
+        first = false;
+      }
+      {
         // ---------------------------------------------------- epilogue
-        // Rows' running max and full sum through shared memory, then one row
-        // per thread again (lanes of the quarter) for the O read-out: warp u
-        // takes O columns [64 u, +64).
+        // O of this warp's 16 rows is read in the softmax layout (thread:
+        // rows ra, rb, key-column pairs 8j + 2 tq), where each row's running
+        // max and sum already sit in its 4 threads.  Complete rows are
+        // normalised and staged as bf16 in this segment's Q buffer (its last
+        // S MMA has completed) in the output box's 128-byte-swizzled layout,
+        // then written by one TMA store per 64-dim half; the producer reloads
+        // that buffer only once the store has read it.  The rows of a row
+        // group cut by a range end are written as partials.
         if (ok && !warp_wait(&bars->ofull[g % kSB], (g / kSB) & 1)) ok = false;
         float sa = la + __shfl_xor_sync(0xffffffffu, la, 1);
         float sb = lb_sum + __shfl_xor_sync(0xffffffffu, lb_sum, 1);
         sa += __shfl_xor_sync(0xffffffffu, sa, 2);
         sb += __shfl_xor_sync(0xffffffffu, sb, 2);
-        if (tq == 0) {
-          bars->xm[ra] = ma;
-          bars->xl[ra] = sa;
-          bars->xm[rb] = mb;
-          bars->xl[rb] = sb;
-        }
-        pair_sync();
-        const int r = quarter * 32 + lane;  // the row this thread writes out
-        const float m_row = bars->xm[r], l_row = bars->xl[r];
-        pair_sync();  // read before either warp writes the next row group's
-        const int rg = grow(c.gi, r);
         const bool complete = from_start && c.t == c.n - 1;
         // a prefix out of bounds: the sequence is reported, its rows left unwritten
         if (!c.ok && warp == 2 && lane == 0 && c.gi == 0) sv::report(status, SPEC_DEV_CAPACITY);
-        const bool row_ok = rg < R;
-        const int kvh = c.gi / pairs;
-        const uint32_t q_off = (uint32_t)(quarter * 32) << 16;
-        if (ok && !__any_sync(0xffffffffu, bars->abort != 0)) {
+        const int qb = seg % kQB;
+        uint8_t *stage = sQ + qb * kQBytes;
+        const bool live = ok && !__any_sync(0xffffffffu, bars->abort != 0);
+        uint32_t ov[64];  // ov[4j + e]: row ra, column 8j + 2 tq + e;  ov[4j + 2 + e]: row rb
+        if (live) {
           tc_fence_after();
-          if (complete) {
-            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-            __nv_bfloat16 *o = out + (((int64_t)c.b * N + rg / G) * Hq + kvh * G + rg % G) * kD + u * 64;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              uint32_t ov[32];
-              tmem_ld32(tmem + q_off + kColO + u * 64 + cc * 32, ov);
-              tmem_wait_ld();
-              if (row_ok && c.ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(o + cc * 32);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                  uint4 v;
-                  v.x = pack_bf16(__uint_as_float(ov[8 * q4 + 0]) * inv, __uint_as_float(ov[8 * q4 + 1]) * inv);
-                  v.y = pack_bf16(__uint_as_float(ov[8 * q4 + 2]) * inv, __uint_as_float(ov[8 * q4 + 3]) * inv);
-                  v.z = pack_bf16(__uint_as_float(ov[8 * q4 + 4]) * inv, __uint_as_float(ov[8 * q4 + 5]) * inv);
-                  v.w = pack_bf16(__uint_as_float(ov[8 * q4 + 6]) * inv, __uint_as_float(ov[8 * q4 + 7]) * inv);
-                  dst[q4] = v;
-                }
-              }
-            }
-          } else {
-            // a part cut at the range end: slot 2c + 1; the one cut at its start: 2c
-            const int slot = cluster * 2 + (g == T - 1 && c.t != c.n - 1 ? 1 : 0);
-            uint8_t *w = reinterpret_cast<uint8_t *>(ws) +
-                         ((int64_t)slot * kPairRows + (int)rank * 128 + r) * kPartialBytes;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-              uint32_t ov[32];
-              tmem_ld32(tmem + q_off + kColO + u * 64 + cc * 32, ov);
-              tmem_wait_ld();
-              if (row_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(w + u * 128 + cc * 64);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                  dst[q4] = make_uint4(pack_bf16(__uint_as_float(ov[8 * q4 + 0]), __uint_as_float(ov[8 * q4 + 1])),
-                                       pack_bf16(__uint_as_float(ov[8 * q4 + 2]), __uint_as_float(ov[8 * q4 + 3])),
-                                       pack_bf16(__uint_as_float(ov[8 * q4 + 4]), __uint_as_float(ov[8 * q4 + 5])),
-                                       pack_bf16(__uint_as_float(ov[8 * q4 + 6]), __uint_as_float(ov[8 * q4 + 7])));
-              }
-            }
-            if (row_ok && u == 0) *reinterpret_cast<float2 *>(w + kD * 2) = make_float2(m_row, l_row);
-          }
-        } else if (!ok) {
-          give_up(bars, status);
+          tmem_ld_16x256b_x16(tmem + lane_off + kColO, ov);
+          tmem_wait_ld();
         }
+        if (live && complete) {
+          const float ia = sa > 0.f ? 1.f / sa : 0.f, ib = sb > 0.f ? 1.f / sb : 0.f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {  // 16-byte chunk j & 7 of 64-dim half j >> 3 of rows ra, rb
+            uint8_t *half = stage + (j >> 3) * kQHalf + 4 * tq;
+            *reinterpret_cast<uint32_t *>(half + ra * 128 + (((j & 7) ^ (ra & 7)) << 4)) =
+                pack_bf16(__uint_as_float(ov[4 * j]) * ia, __uint_as_float(ov[4 * j + 1]) * ia);
+            *reinterpret_cast<uint32_t *>(half + rb * 128 + (((j & 7) ^ (rb & 7)) << 4)) =
+                pack_bf16(__uint_as_float(ov[4 * j + 2]) * ib, __uint_as_float(ov[4 * j + 3]) * ib);
+          }
+          fence_proxy_async_smem();  // visible to the TMA store
+        } else if (live) {
+          // a part cut at the range end: slot 2c + 1; the one cut at its start: 2c
+          const int slot = cluster * 2 + (g == T - 1 && c.t != c.n - 1 ? 1 : 0);
+          uint8_t *w = reinterpret_cast<uint8_t *>(ws) + ((int64_t)slot * kPairRows + (int)rank * 128) * kPartialBytes;
+          const bool oka = grow(c.gi, ra) < R, okb = grow(c.gi, rb) < R;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (oka)
+              *reinterpret_cast<uint32_t *>(w + ra * kPartialBytes + 16 * j + 4 * tq) =
+                  pack_bf16(__uint_as_float(ov[4 * j]), __uint_as_float(ov[4 * j + 1]));
+            if (okb)
+              *reinterpret_cast<uint32_t *>(w + rb * kPartialBytes + 16 * j + 4 * tq) =
+                  pack_bf16(__uint_as_float(ov[4 * j + 2]), __uint_as_float(ov[4 * j + 3]));
+          }
+          if (tq == 0) {
+            if (oka) *reinterpret_cast<float2 *>(w + ra * kPartialBytes + kD * 2) = make_float2(ma, sa);
+            if (okb) *reinterpret_cast<float2 *>(w + rb * kPartialBytes + kD * 2) = make_float2(mb, sb);
+          }
+        }
+        softmax_sync();  // every row of this CTA staged
+        if (threadIdx.x == kStoreThread) {
+          const int node0 = ((c.gi % pairs) * kPairRows + (int)rank * 128) / G;
+          if (live && complete && c.ok && node0 < N) {  // (a CTA past the last node has no rows to write)
+            const int kvh = c.gi / pairs;
+            tma_store_5d(&tm_o, stage, 0, 0, kvh, node0, c.b);
+            tma_store_5d(&tm_o, stage + kQHalf, 64, 0, kvh, node0, c.b);
+            bulk_commit();
+            q_pending = qb + 1;  // Q buffer released once the store has read it
+          } else {
+            mbar_arrive(&bars->qempty[qb]);
+          }
+        }
+        if (!ok) give_up(bars, status);
       }
       cur_next(c, s);
+      ++g;
+    }
+    if (threadIdx.x == kStoreThread) {
+      if (q_pending) {
+        bulk_wait_read();
+        mbar_arrive(&bars->qempty[q_pending - 1]);
+      }
+      bulk_wait_all();
     }
   }
 
@@ -1081,12 +1125,22 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
   if (C < 1) return SPEC_ERR_CUDA;
   if (!ws || ws_bytes < sv_attn_tc2_ws_bytes()) return SPEC_ERR_CAPACITY;
   const int G = s.hq / s.hkv, R = s.n_nodes * G;
-  CUtensorMap mq, mkc, mvc, mkt, mvt;
+  CUtensorMap mq, mkc, mvc, mkt, mvt, mo;
   {
     const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)s.hkv, (cuuint64_t)s.batch * s.n_nodes};
     const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)s.hq * kD * 2};
     const cuuint32_t box[4] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G)};
     if (make_map(&mq, q, 4, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
+  }
+  {
+    // output rows of a CTA: 128 / G nodes x the G heads of a KV head; nodes
+    // past the sequence's last are outside the map and not written
+    const cuuint64_t dims[5] = {(cuuint64_t)kD, (cuuint64_t)G, (cuuint64_t)s.hkv, (cuuint64_t)s.n_nodes,
+                                (cuuint64_t)s.batch};
+    const cuuint64_t strides[4] = {(cuuint64_t)kD * 2, (cuuint64_t)G * kD * 2, (cuuint64_t)s.hq * kD * 2,
+                                   (cuuint64_t)s.n_nodes * s.hq * kD * 2};
+    const cuuint32_t box[5] = {64, (cuuint32_t)G, 1, (cuuint32_t)(128 / G), 1};
+    if (make_map(&mo, out, 5, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
   }
   {
     // (at least one row so the map is valid when no prefix tile is ever loaded)
@@ -1116,7 +1170,7 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
   if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
-  attn_tc2_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, sc, anc, (__nv_bfloat16 *)out,
+  attn_tc2_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, mo, sc, anc,
                                                           ws, s.hq, scale * 1.4426950408889634f, status);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (C > 1) {
