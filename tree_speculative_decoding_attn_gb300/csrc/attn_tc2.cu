@@ -205,21 +205,22 @@ struct Pos {
   int b, gi, t;
   long long u, wrg;
 };
-// The first unit whose start weight is >= x (past the last unit: b = batch,
-// u = U, wrg = W).
-__device__ Pos warp_seek(const Sched &s, const SeqTab &tb, long long x) {
+// The first units whose start weights are >= x0 and >= x1 (past the last
+// unit: b = batch, u = U, wrg = W), in one walk over the sequences.
+__device__ void warp_seek2(const Sched &s, const SeqTab &tb, long long x0, long long x1, Pos *p0, Pos *p1) {
   const int lane = threadIdx.x & 31;
   const int gpb = s.gpb();
   long long W0 = 0, U0 = 0;
-  Pos p{s.batch, 0, 0, 0, 0};
-  bool found = false;
+  *p0 = *p1 = Pos{s.batch, 0, 0, 0, 0};
+  bool found0 = false, found1 = false;
   for_chunks(s, tb, [&](int i, int raw) -> bool {
     const bool in = 32 * i + lane < s.batch;
     const int n = in ? tiles_of(s, raw) : 0;
     const long long w = in ? (long long)gpb * (n + kSegW) : 0, uu = (long long)gpb * n;
     const long long wi = warp_incl_ll(w), ui = warp_incl_ll(uu);
-    const unsigned hit = __ballot_sync(0xffffffffu, in && W0 + wi > x);
-    if (hit) {
+    auto place = [&](long long x, Pos *p, bool *found) {
+      const unsigned hit = __ballot_sync(0xffffffffu, in && W0 + wi > x);
+      if (!hit) return;
       const int l = __ffs(hit) - 1;
       const long long wb = W0 + __shfl_sync(0xffffffffu, wi - w, l);
       const long long ub = U0 + __shfl_sync(0xffffffffu, ui - uu, l);
@@ -228,31 +229,35 @@ __device__ Pos warp_seek(const Sched &s, const SeqTab &tb, long long x) {
       const int r = (int)(x - wb - (long long)gi * (nl + kSegW));
       int t = r == 0 ? 0 : max(1, r - kSegW);
       int b = 32 * i + l;
-      p.u = ub + (long long)gi * nl + t;
-      p.wrg = wb + (long long)gi * (nl + kSegW);
+      p->u = ub + (long long)gi * nl + t;
+      p->wrg = wb + (long long)gi * (nl + kSegW);
       if (t >= nl) {  // past the row group's last tile: the next row group's tree tile
         t = 0;
-        p.wrg += nl + kSegW;
+        p->wrg += nl + kSegW;
         if (++gi == gpb) {
           gi = 0;
           ++b;
         }
       }
-      p.b = b;
-      p.gi = gi;
-      p.t = t;
-      found = true;
-      return true;
-    }
+      p->b = b;
+      p->gi = gi;
+      p->t = t;
+      *found = true;
+    };
+    if (!found0) place(x0, p0, &found0);
+    if (!found1) place(x1, p1, &found1);
     W0 += __shfl_sync(0xffffffffu, wi, 31);
     U0 += __shfl_sync(0xffffffffu, ui, 31);
-    return false;
+    return found0 && found1;
   });
-  if (!found) {
-    p.u = U0;
-    p.wrg = W0;
+  if (!found0) {
+    p0->u = U0;
+    p0->wrg = W0;
   }
-  return p;
+  if (!found1) {
+    p1->u = U0;
+    p1->wrg = W0;
+  }
 }
 
 // Clusters in use: each range is at least as wide as the heaviest unit, so
@@ -383,12 +388,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     long long W, U;
     warp_totals(s, tb, &W, &U);
     const long long C = clusters_used(s, W);
-    Pos p0{s.batch, 0, 0, 0, 0};
+    Pos p0{s.batch, 0, 0, 0, 0}, p1;
     int T = 0;
     if (cluster < C) {
-      p0 = warp_seek(s, tb, range_start(cluster, W, C));
-      const long long u1 = cluster + 1 < C ? warp_seek(s, tb, range_start(cluster + 1, W, C)).u : U;
-      T = (int)(u1 - p0.u);
+      warp_seek2(s, tb, range_start(cluster, W, C), range_start(cluster + 1, W, C), &p0, &p1);
+      T = (int)(p1.u - p0.u);  // (range_start(C) = W: no unit starts there, p1.u = U)
     }
     const int raw0 = warp_raw(s, tb, p0.b), raw1 = warp_raw(s, tb, p0.b + 1);
     if (lane == 0) {
@@ -451,7 +455,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc_pair(tmem, 512);
     return;
   }
-  if (threadIdx.x == 0) grid_dep_launch();  // the merge grid may start locating its row groups
+  // the merge grid may be scheduled (from a softmax thread: the producers'
+  // first copies come first)
+  if (threadIdx.x == 96) grid_dep_launch();
   const int pairs = s.pairs;
 
   if (warp == 0 || warp == 10) {
@@ -482,7 +488,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!is_v && first) {
           const int qb = seg % kQB;
-          if (!mbar_wait_cluster(&bars->qempty[qb], ((seg / kQB) & 1) ^ 1, kWaitLimit) || bars->abort) {
+          // (a buffer's first use needs no wait: a completed-phase poll still costs a few hundred cycles)
+          if ((seg >= kQB && !mbar_wait_cluster(&bars->qempty[qb], ((seg / kQB) & 1) ^ 1, kWaitLimit)) || bars->abort) {
             give_up(bars, status);
             break;
           }
@@ -497,7 +504,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int use = g / (is_v ? kVS : kKS);
         uint64_t *empty = is_v ? &bars->vempty[st] : &bars->kempty[st];
         uint64_t *land = is_v ? &bars->vland[st] : (rank == 0 ? &bars->kfull[st] : &bars->kland[st]);
-        if (!mbar_wait_cluster(empty, (use & 1) ^ 1, kWaitLimit) || bars->abort) {
+        if ((use > 0 && !mbar_wait_cluster(empty, (use & 1) ^ 1, kWaitLimit)) || bars->abort) {
           give_up(bars, status);
           break;
         }
