@@ -63,6 +63,13 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   }
   return v;
 }
+// The same by two single-instruction 32-bit warp reductions: the largest
+// high word, then the largest low word among the lanes holding it.
+__device__ __forceinline__ unsigned long long warp_max_u64_redux(unsigned long long v) {
+  const unsigned hi = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32));
+  const unsigned lo = __reduce_max_sync(0xffffffffu, (unsigned)(v >> 32) == hi ? (unsigned)v : 0u);
+  return ((unsigned long long)hi << 32) | lo;
+}
 
 // Total order key for "larger value first, then lower index first":
 // maximising the key selects the larger value, and among equal values the

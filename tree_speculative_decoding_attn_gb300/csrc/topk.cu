@@ -55,30 +55,34 @@ __device__ __forceinline__ void insert_key(unsigned long long (&best)[S], unsign
   }
 }
 
-// Merge the per-thread sorted lists held in shared memory: s rounds, each
-// takes the largest list head across the CTA and advances that list.
+// Top-s of the CTA from the per-thread sorted lists (keys are unique; 0 =
+// empty).  Each warp takes its own top-s by s warp-wide maxima of the list
+// heads, the winning lane popping its head (no block barrier per round);
+// then the kWarps * s warp winners are ranked by counting the larger ones.
+// out[0..s) in shared memory, descending; contains __syncthreads.
 template <int S>
-__device__ void merge_top(const unsigned long long (&best)[S], unsigned long long *lists, int s,
-                          unsigned long long *out) {
-  __shared__ unsigned long long red[kWarps];
-#pragma unroll
-  for (int j = 0; j < S; ++j) lists[threadIdx.x * S + j] = best[j];
-  int head = 0;
-  __syncthreads();
+__device__ void merge_top(unsigned long long (&best)[S], int s, unsigned long long *out) {
+  __shared__ unsigned long long cand[kWarps][S];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int r = 0; r < s; ++r) {
-    const unsigned long long mine = head < S ? lists[threadIdx.x * S + head] : 0ull;
-    unsigned long long w = sv::warp_max_u64(mine);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = w;
-    __syncthreads();
-    if (threadIdx.x < 32) {
-      unsigned long long v = threadIdx.x < kWarps ? red[threadIdx.x] : 0ull;
-      v = sv::warp_max_u64(v);
-      if (threadIdx.x == 0) out[r] = v;
+    const unsigned long long w = sv::warp_max_u64_redux(best[0]);
+    if (lane == 0) cand[warp][r] = w;
+    if (w != 0ull && best[0] == w) {
+#pragma unroll
+      for (int j = 0; j < S - 1; ++j) best[j] = best[j + 1];
+      best[S - 1] = 0ull;
     }
-    __syncthreads();
-    if (mine == out[r] && mine != 0ull) ++head;  // keys are unique: one winner
-    __syncthreads();
   }
+  if (threadIdx.x < s) out[threadIdx.x] = 0ull;
+  __syncthreads();
+  if (threadIdx.x < kWarps * s) {
+    const unsigned long long k = cand[threadIdx.x / s][threadIdx.x % s];
+    int rank = 0;
+    for (int w = 0; w < kWarps; ++w)
+      for (int r = 0; r < s; ++r) rank += cand[w][r] > k;
+    if (k != 0ull && rank < s) out[rank] = k;
+  }
+  __syncthreads();
 }
 
 // Top-s of one row by a cluster of kCluster CTAs: CTA c ranks the c-th slice
@@ -102,7 +106,6 @@ template <typename T, int S>
 __global__ void __launch_bounds__(kThreads)
     topk_cluster_kernel(const T *__restrict__ rows, int row_len, int64_t row_stride, int s,
                         int32_t *__restrict__ idx, float *__restrict__ val) {
-  __shared__ unsigned long long lists[kThreads * S];
   __shared__ unsigned long long top[32];
   __shared__ unsigned long long all[kCluster * S];
   const uint32_t cta = blockIdx.x;  // rank within the cluster (cluster spans x)
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kThreads)
   } else {
     for (int x = lo + threadIdx.x; x < hi; x += kThreads) insert_key<S>(best, sv::rank_key(sv::to_f32(row[x]), (uint32_t)x));
   }
-  merge_top<S>(best, lists, s, top);  // top[0..s) of this slice (0 = empty)
+  merge_top<S>(best, s, top);  // top[0..s) of this slice (0 = empty)
   cluster_barrier();
   if (cta == 0) {
     for (int e = threadIdx.x; e < kCluster * s; e += kThreads) all[e] = ld_cluster_u64(&top[e % s], e / s);
@@ -145,7 +148,6 @@ __global__ void __launch_bounds__(kThreads)
     expand_rows_kernel(const T *__restrict__ logits, int n_front, int V, const int32_t *frontier,
                        int k, float temp, int32_t *pool_parent, int32_t *pool_tok, float *pool_conf,
                        float *pool_val, const int32_t *pool_count, int pool_cap, int32_t *status) {
-  __shared__ unsigned long long lists[kThreads * S];
   __shared__ unsigned long long top[32];
   __shared__ float red[kWarps];
   __shared__ float s_bcast;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int w = 0; w < kWarps; ++w) ss += red[w];
     s_bcast = ss;
   }
-  merge_top<S>(best, lists, k, top);  // contains __syncthreads
+  merge_top<S>(best, k, top);  // contains __syncthreads
   S_ = s_bcast;
   if (threadIdx.x < k) {
     const int x = (int)sv::key_index(top[threadIdx.x]);
@@ -254,8 +256,14 @@ int launch_topk(const void *rows, int n_rows, int row_len, int row_stride, int s
 int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
             int32_t *idx, float *val, cudaStream_t stream) {
   if (s > kMaxS) return SPEC_ERR_UNSUPPORTED;
-  if (dtype == SPEC_BF16)
+  // per-thread lists no longer than needed: s rounded up to 4, 8 or 16
+  if (dtype == SPEC_BF16) {
+    if (s <= 4) return launch_topk<__nv_bfloat16, 4>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
+    if (s <= 8) return launch_topk<__nv_bfloat16, 8>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
     return launch_topk<__nv_bfloat16, kMaxS>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
+  }
+  if (s <= 4) return launch_topk<float, 4>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
+  if (s <= 8) return launch_topk<float, 8>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
   return launch_topk<float, kMaxS>(rows, n_rows, row_len, row_stride, s, idx, val, stream);
 }
 

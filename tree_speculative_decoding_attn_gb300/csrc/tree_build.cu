@@ -14,29 +14,26 @@ namespace {
 constexpr int kMaxNodes = SPEC_MAX_NODES;
 
 // Emits depth/pos/mask/child links for one sequence's parents array held in
-// shared memory.  One thread per node; the walk is bounded because the
+// shared memory, with kids[v] = the set of v's children (N <= 64, so one
+// bit per node).  One thread per node; the walk is bounded because the
 // caller validated parent < node.
-__device__ void emit_tree_arrays(const int *par, int N, int i, int prefix, int64_t row,
-                                 int32_t *depth, int32_t *pos, uint64_t *anc, int32_t *first_child,
-                                 int32_t *next_sibling, int *depth_out) {
+__device__ void emit_tree_arrays(const int *par, const unsigned long long *kids, int i, int prefix,
+                                 int64_t row, int32_t *depth, int32_t *pos, uint64_t *anc,
+                                 int32_t *first_child, int32_t *next_sibling, int *depth_out) {
   uint64_t m = 0;
   int d = -1;
   for (int c = i; c != -1; c = par[c]) {
     m |= 1ull << c;
     ++d;
   }
-  int fc = -1, ns = -1;
-  for (int c = i + 1; c < N; ++c)
-    if (par[c] == i) {
-      fc = c;
-      break;
-    }
-  if (i > 0)
-    for (int c = i + 1; c < N; ++c)
-      if (par[c] == par[i]) {
-        ns = c;
-        break;
-      }
+  // first child: the lowest child; next sibling: the parent's lowest child above i
+  const unsigned long long own = kids[i];
+  const int fc = own ? __ffsll((long long)own) - 1 : -1;
+  int ns = -1;
+  if (i > 0) {
+    const unsigned long long later = i >= 63 ? 0ull : kids[par[i]] & (~0ull << (i + 1));
+    ns = later ? __ffsll((long long)later) - 1 : -1;
+  }
   depth[row + i] = d;
   pos[row + i] = prefix + d;
   anc[row + i] = m;
@@ -52,14 +49,23 @@ __global__ void __launch_bounds__(kMaxNodes)
                         int N, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
                         int32_t *first_child, int32_t *next_sibling, int32_t *status) {
   __shared__ int par[kMaxNodes];
+  __shared__ unsigned long long kids[kMaxNodes];
   __shared__ int bad;
   const int b = blockIdx.x, i = threadIdx.x;
+  // every load that does not depend on the tree walk is issued up front
+  const int p = i < N ? parents[i] : 0;
+  const int P = prefix_len[b];
+  const int r = tok && i > 0 && i < N ? rank[i] : 0;
+  const int t0 = tok && i == 0 ? root_tok[b] : -1;
   if (i == 0) bad = 0;
+  kids[i] = 0ull;
   __syncthreads();
   if (i < N) {
-    const int p = parents[i];
     par[i] = p;
-    if (i == 0 ? p != -1 : (p < 0 || p >= i)) atomicOr(&bad, 1);
+    if (i == 0 ? p != -1 : (p < 0 || p >= i))
+      atomicOr(&bad, 1);
+    else if (i > 0)
+      atomicOr(&kids[p], 1ull << i);
   }
   __syncthreads();
   if (bad) {
@@ -69,13 +75,12 @@ __global__ void __launch_bounds__(kMaxNodes)
   if (i >= N) return;
   const int64_t row = (int64_t)b * N;
   int d;
-  emit_tree_arrays(par, N, i, prefix_len[b], row, depth, pos, anc, first_child, next_sibling, &d);
+  emit_tree_arrays(par, kids, i, P, row, depth, pos, anc, first_child, next_sibling, &d);
   if (tok) {
     int t = -1;
     if (i == 0) {
-      t = root_tok[b];
+      t = t0;
     } else {
-      const int r = rank[i];
       if (d - 1 < cand_levels && r >= 0 && r < cand_s)
         t = cand_tok[((int64_t)b * cand_levels + (d - 1)) * cand_s + r];
       else
@@ -210,10 +215,14 @@ __global__ void __launch_bounds__(kDynThreads)
     if (pool_index) pool_index[row + ni] = my_pool;
     if (val_out) val_out[row + ni] = val[my_pool];
   }
+  __shared__ unsigned long long kids[kMaxNodes];
+  if (t < N) kids[t] = 0ull;
+  __syncthreads();
+  if (t > 0 && t < N) atomicOr(&kids[new_par[t]], 1ull << t);
   __syncthreads();
   if (t < N) {
     int d;
-    emit_tree_arrays(new_par, N, t, prefix_len[b], (int64_t)b * N, depth, pos, anc, first_child,
+    emit_tree_arrays(new_par, kids, t, prefix_len[b], (int64_t)b * N, depth, pos, anc, first_child,
                      next_sibling, &d);
   }
 }
