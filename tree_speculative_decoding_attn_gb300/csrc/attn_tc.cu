@@ -7,10 +7,8 @@
 //
 // Query row r of a (sequence, KV head) is node r / G, head kvh*G + r % G, so
 // the G heads of a GQA group and all tree nodes share every K/V tile.  One
-// CTA owns one 128-row query tile.  With more than 128 rows per KV head the
-// query tiles of a (sequence, KV head) run as a two-CTA cluster: each CTA
-// TMA-loads one 64-dim half of every K and V tile and multicasts it to both,
-// so each tile leaves HBM / L2 once and fills both CTAs' shared memory.
+// CTA owns the (at most 128) query rows of a (sequence, KV head, split);
+// more rows per KV head are served by the SM-pair kernel (attn_tc2.cu).
 //
 //   warp 0      TMA producers, lane 0: Q once, then K; lane 1: V.  Tiles of
 //               128 keys x 128 dims, 128-byte swizzle, through two rings
@@ -89,7 +87,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                    const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
@@ -109,11 +106,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / Hkv, kvh = bh % Hkv;
   const int row0 = qt * 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
-  constexpr uint16_t kPair = (uint16_t)((1u << CL) - 1u);
-
-  // Both CTAs of a cluster share (sequence, split), so they take these
-  // early exits together, before any cluster-wide synchronisation.
   const int P = prefix_len[b];
   if (P < 0 || P > max_prefix || P > s_max) {
     if (threadIdx.x == 0) sv::report(status, SPEC_DEV_CAPACITY);
@@ -140,11 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q, 1);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars->kfull[s], 1);
-      mbar_init(&bars->kempty[s], CL);  // one MMA commit from each CTA of the cluster
+      mbar_init(&bars->kempty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars->vfull[s], 1);
-      mbar_init(&bars->vempty[s], CL);
+      mbar_init(&bars->vempty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->sfull[i], 1);
@@ -163,7 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(&bars->tmem, 512);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // partner barriers initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = bars->tmem;
 
@@ -191,12 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_expect_tx(&full[s], kTile);
-        if (CL > 1) {
-          tma_load_2d_mc(ring + s * kTile + rank * kHalf, m, 64 * rank, row, &full[s], kPair);
-        } else {
-          tma_load_2d(ring + s * kTile, m, 0, row, &full[s]);
-          tma_load_2d(ring + s * kTile + kHalf, m, 64, row, &full[s]);
-        }
+        tma_load_2d(ring + s * kTile, m, 0, row, &full[s]);
+        tma_load_2d(ring + s * kTile + kHalf, m, 64, row, &full[s]);
         ++issued;
       }
       if (bars->abort)  // let the copies into this CTA land before it exits
@@ -220,10 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     const uint32_t qa = smem_u32(sQ), ka = smem_u32(sK), va = smem_u32(sV);
-    auto release = [&](uint64_t *bar) {
-      if (CL > 1) mma_commit_mc(bar, kPair);
-      else mma_commit(bar);
-    };
+    auto release = [&](uint64_t *bar) { mma_commit(bar); };
     // S(j) = Q K(j)^T into S buffer j % 2
     auto issue_s = [&](int j) -> bool {
       const int s = j % kKStages;
@@ -472,9 +456,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  // the partner's multicast copies into this CTA and its commits to this
-  // CTA's barriers are complete once it has passed its own __syncthreads
-  if (CL > 1) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -514,50 +495,28 @@ int make_map(CUtensorMap *m, const void *base, cuuint32_t rank, const cuuint64_t
   return r == CUDA_SUCCESS ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-template <int CL>
 int launch_tc(dim3 grid, cudaStream_t stream, const CUtensorMap &mq, const CUtensorMap &mkc, const CUtensorMap &mvc,
               const CUtensorMap &mkt, const CUtensorMap &mvt, const int32_t *prefix_len, const uint64_t *anc,
               void *out, void *ws, const SvAttnShape &s, const SvAttnPlan &p, float scale, int32_t *status) {
-  if (cudaFuncSetAttribute(attn_tc_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+  if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, attn_tc_kernel<CL>, mq, mkc, mvc, mkt, mvt, prefix_len, anc, (__nv_bfloat16 *)out, (float *)ws,
-      s.n_nodes, s.hq, s.hkv, s.s_max, s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status);
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
-}
-
-// Query tiles per (sequence, KV head): pairs run as two-CTA clusters.
-inline int tc_cluster(int R) { return R > 128 ? 2 : 1; }
-inline int tc_qtiles(int R) {
-  const int t = (R + 127) / 128;
-  return tc_cluster(R) == 2 ? (t + 1) / 2 * 2 : t;
+  attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
+      mq, mkc, mvc, mkt, mvt, prefix_len, anc, (__nv_bfloat16 *)out, (float *)ws, s.n_nodes, s.hq, s.hkv, s.s_max,
+      s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 // Modelled time of one split count, in units of one K/V tile streamed by
-// one cluster slot: clusters are dispatched in launch order (query-tile
-// pair fastest, then split, then sequence x KV head) onto the free slots;
+// one SM: CTAs are dispatched in launch order (split fastest, then
+// sequence x KV head) onto the free SMs;
 // each streams its prefix chunk, the tree tile on the last split, and about
 // one tile's worth of set-up.  Split partials cost their write and re-read
 // plus a combine launch.  `prefix` holds each sequence's prefix length, or
 // is null for "every sequence at max_prefix".
 double tc_split_cost(const SvAttnShape &s, const int32_t *prefix, int splits) {
   const int G = s.hq / s.hkv, R = s.n_nodes * G;
-  const int cl = tc_cluster(R);
-  const int pairs = tc_qtiles(R) / cl;
-  const int slots = kSms / cl;
+  const int slots = kSms;
   int chunk = (s.max_prefix + splits - 1) / splits;
   chunk = (chunk + kBN - 1) / kBN * kBN;
   // min-heap of slot finish times (small arrays: slots <= 152)
@@ -569,12 +528,10 @@ double tc_split_cost(const SvAttnShape &s, const int32_t *prefix, int splits) {
       const int k0 = sp * chunk, k1 = P < k0 + chunk ? P : k0 + chunk;
       const int tiles = k1 > k0 ? (k1 - k0 + kBN - 1) / kBN : 0;
       const double work = tiles + (sp == splits - 1 ? 2.0 : (tiles ? 1.0 : 0.1));
-      for (int pr = 0; pr < pairs; ++pr) {
-        int best = 0;
-        for (int i = 1; i < slots; ++i)
-          if (finish[i] < finish[best]) best = i;
-        finish[best] += work;
-      }
+      int best = 0;
+      for (int i = 1; i < slots; ++i)
+        if (finish[i] < finish[best]) best = i;
+      finish[best] += work;
     }
   }
   double makespan = 0.0;
@@ -606,7 +563,7 @@ int tc_best_splits(const SvAttnShape &s, const int32_t *prefix) {
 bool sv_attn_tc_supported(const SvAttnShape &s) {
   if (s.dtype != SPEC_BF16 || s.head_dim != kD) return false;
   const int G = s.hq / s.hkv;
-  return G <= 128 && (128 % G) == 0;
+  return G <= 128 && (128 % G) == 0 && s.n_nodes * G <= 128;
 }
 
 int sv_attn_tc_ragged_splits(const SvAttnShape &s, const int32_t *host_prefix) {
@@ -661,9 +618,6 @@ int sv_attn_tc(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const v
     if (make_map(&mkt, kt, 2, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
     if (make_map(&mvt, vt, 2, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
   }
-  const int R = s.n_nodes * G;
-  const dim3 grid(tc_qtiles(R), p.splits, s.batch * s.hkv);
-  return tc_cluster(R) == 2
-             ? launch_tc<2>(grid, stream, mq, mkc, mvc, mkt, mvt, prefix_len, anc, out, ws, s, p, scale, status)
-             : launch_tc<1>(grid, stream, mq, mkc, mvc, mkt, mvt, prefix_len, anc, out, ws, s, p, scale, status);
+  const dim3 grid(1, p.splits, s.batch * s.hkv);  // at most 128 query rows: one query tile
+  return launch_tc(grid, stream, mq, mkc, mvc, mkt, mvt, prefix_len, anc, out, ws, s, p, scale, status);
 }

@@ -71,17 +71,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
         "r"(smem_u32(bar))
       : "memory");
 }
-// 2D tile load delivered to the same shared-memory offset (and the same
-// mbarrier offset) in every CTA of `cta_mask` within the cluster.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
-        "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -159,16 +148,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 #undef SV_R16
 #define SV_W(i) "r"(r[i])
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-      ::"r"(taddr), SV_W(0), SV_W(1), SV_W(2), SV_W(3), SV_W(4), SV_W(5), SV_W(6), SV_W(7), SV_W(8), SV_W(9),
-        SV_W(10), SV_W(11), SV_W(12), SV_W(13), SV_W(14), SV_W(15), SV_W(16), SV_W(17), SV_W(18), SV_W(19),
-        SV_W(20), SV_W(21), SV_W(22), SV_W(23), SV_W(24), SV_W(25), SV_W(26), SV_W(27), SV_W(28), SV_W(29),
-        SV_W(30), SV_W(31)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
@@ -271,15 +250,6 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return *reinterpret_cast<float2 *>(&d);
 }
 
-// Arrive once on `bar` at the same offset in every CTA of `cta_mask` when
-// every tcgen05 operation this thread issued so far has completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
 
 // ---- CTA pairs (tcgen05 cta_group::2) ----------------------------------------
 // Shared::cluster address of the same shared-memory offset in CTA `rank`.
@@ -319,39 +289,10 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// One poll that suspends for at most `hint_ns` while the phase is pending.
-__device__ __forceinline__ bool mbar_poll_cluster(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait_cluster(bar, parity)) return true;
   return false;
-}
-// Tile loads of the odd CTA of a pair into its own shared memory whose
-// completion is counted on an mbarrier of the even CTA (shared::cluster
-// address `bar_cluster`): the pair's consumer waits on one barrier.
-__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map, int c0, int c1,
-                                                 uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_4d_pair(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
-                                                 uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-        "r"(bar_cluster)
-      : "memory");
 }
 // Pair TMEM allocation: one warp of each CTA of the pair executes these
 // together; both CTAs receive the same column address.
