@@ -30,16 +30,20 @@ constexpr int kKC = 64;                     // K elements per chunk (one 128-byt
 constexpr uint32_t kWTile = 128 * kKC * 2;  // 16 KB
 constexpr uint32_t kWaitLimit = 1u << 22;
 
+// With up to 64 tree rows two CTAs share an SM (half the ring each, the
+// same bytes in flight per SM), so a vocabulary of a few hundred tiles is
+// resident in one wave instead of running 1.6 waves of one CTA per SM.
 template <int NT>
 struct GemmCfg {
   static constexpr uint32_t kHTile = NT * kKC * 2;
   static constexpr uint32_t kStage = kWTile + kHTile;
-  static constexpr int kStages = (192 * 1024) / kStage;
+  static constexpr int kCtasPerSm = NT <= 64 ? 2 : 1;
+  static constexpr int kStages = ((kCtasPerSm == 2 ? 104 : 192) * 1024) / kStage;
   static constexpr uint32_t kSmem = kStages * kStage + 256 + 1024;
 };
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, GemmCfg<NT>::kCtasPerSm)
     lm_head_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h, int R, int V,
                       int hidden, float *__restrict__ out, int32_t *status) {
   using C = GemmCfg<NT>;
