@@ -55,6 +55,56 @@ __device__ __forceinline__ void insert_key(unsigned long long (&best)[S], unsign
   }
 }
 
+// Bitonic sorting network on S keys (S a power of two), descending: every
+// stage is S/2 independent compare-exchanges.
+template <int S>
+__device__ __forceinline__ void bitonic_sort_desc(unsigned long long (&a)[S]) {
+#pragma unroll
+  for (int k = 2; k <= S; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1)
+#pragma unroll
+      for (int i = 0; i < S; ++i) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long x = a[i], y = a[l];
+          const bool sw = (i & k) == 0 ? x < y : x > y;
+          a[i] = sw ? y : x;
+          a[l] = sw ? x : y;
+        }
+      }
+}
+// Sorts a bitonic sequence of S keys descending.
+template <int S>
+__device__ __forceinline__ void bitonic_merge_desc(unsigned long long (&a)[S]) {
+#pragma unroll
+  for (int j = S >> 1; j > 0; j >>= 1)
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      const int l = i ^ j;
+      if (l > i) {
+        const unsigned long long x = a[i], y = a[l];
+        a[i] = x > y ? x : y;
+        a[l] = x > y ? y : x;
+      }
+    }
+}
+// Folds a batch of S keys (any order; consumed) into the sorted top-S list:
+// the batch is sorted, the pairwise maxima of the list and the reversed
+// batch form a bitonic sequence holding the top S of both, which is sorted.
+template <int S>
+__device__ __forceinline__ void fold_batch(unsigned long long (&best)[S], unsigned long long (&c)[S], bool first) {
+  bitonic_sort_desc<S>(c);
+  if (first) {
+#pragma unroll
+    for (int i = 0; i < S; ++i) best[i] = c[i];
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < S; ++i) best[i] = best[i] > c[S - 1 - i] ? best[i] : c[S - 1 - i];
+  bitonic_merge_desc<S>(best);
+}
+
 // Top-s of the CTA from the per-thread sorted lists (keys are unique; 0 =
 // empty).  Each warp takes its own top-s by s warp-wide maxima of the list
 // heads, the winning lane popping its head (no block barrier per round);
@@ -115,10 +165,15 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int j = 0; j < S; ++j) best[j] = 0ull;
   const T *row = rows + (int64_t)blockIdx.y * row_stride;
-  if ((lo % (16 / (int)sizeof(T))) == 0) {
-    for_row(row + lo, hi - lo, [&](int x, float v) { insert_key<S>(best, sv::rank_key(v, (uint32_t)(lo + x))); });
-  } else {
-    for (int x = lo + threadIdx.x; x < hi; x += kThreads) insert_key<S>(best, sv::rank_key(sv::to_f32(row[x]), (uint32_t)x));
+  // batches of S keys per thread (coalesced: element lo + threadIdx.x + j kThreads)
+  for (int base = lo + threadIdx.x; base < hi; base += S * kThreads) {
+    unsigned long long c[S];
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const int x = base + j * kThreads;
+      c[j] = x < hi ? sv::rank_key(sv::to_f32(row[x]), (uint32_t)x) : 0ull;
+    }
+    fold_batch<S>(best, c, base == lo + (int)threadIdx.x);
   }
   merge_top<S>(best, s, top);  // top[0..s) of this slice (0 = empty)
   cluster_barrier();
