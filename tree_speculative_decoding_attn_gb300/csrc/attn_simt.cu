@@ -117,34 +117,60 @@ __global__ void __launch_bounds__(kWarps * 32)
       stage_rows<T, D, D>(sV, vc + kv_base + (int64_t)t0 * D, nvalid);
     }
     __syncthreads();
+    // The warp's rows go through each step together, so their dot products,
+    // reductions and P.V updates are independent chains, and every staged
+    // K/V value is read once for all of them.
+    constexpr int RW = kRowsPerWarp;
+    const float *kr = sK + lane * (D + 1);
+    const float *qw = sQ + warp * RW * D;
+    float sc[RW];
 #pragma unroll
-    for (int k = 0; k < kRowsPerWarp; ++k) {
-      const float *qr = sQ + (warp * kRowsPerWarp + k) * D;
-      bool vis = lane < nvalid;
-      if (tree) vis = vis && ((am[k] >> (t0 + lane)) & 1ull);
-      float s = -INFINITY;
-      if (vis) {
-        float dot = 0.f;
-        const float *kr = sK + lane * (D + 1);
-#pragma unroll 16
-        for (int d = 0; d < D; ++d) dot = fmaf(qr[d], kr[d], dot);
-        s = dot * scale_log2;
-      }
-      const float mn = fmaxf(m[k], sv::warp_max(s));
-      if (mn == -INFINITY) continue;  // nothing visible yet for this row
-      const float p = vis ? exp2f(s - mn) : 0.f;
-      const float corr = exp2f(m[k] - mn);
-      l[k] = l[k] * corr + sv::warp_sum(p);
+    for (int k = 0; k < RW; ++k) sc[k] = 0.f;
+#pragma unroll 8
+    for (int d = 0; d < D; ++d) {
+      const float kd = kr[d];
+#pragma unroll
+      for (int k = 0; k < RW; ++k) sc[k] = fmaf(qw[k * D + d], kd, sc[k]);
+    }
+    float mx[RW], p[RW];
+#pragma unroll
+    for (int k = 0; k < RW; ++k) {
+      const bool vis = lane < nvalid && (!tree || ((am[k] >> (t0 + lane)) & 1ull));
+      sc[k] = vis ? sc[k] * scale_log2 : -INFINITY;
+      mx[k] = sc[k];
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < RW; ++k) mx[k] = fmaxf(mx[k], __shfl_xor_sync(0xffffffffu, mx[k], o));
+#pragma unroll
+    for (int k = 0; k < RW; ++k) {
+      const float mn = fmaxf(m[k], mx[k]);
+      const bool live = mn != -INFINITY;  // something visible so far
+      p[k] = live && sc[k] != -INFINITY ? exp2f(sc[k] - mn) : 0.f;
+      const float corr = live ? exp2f(m[k] - mn) : 1.f;  // 0 when m was -inf
+      mx[k] = p[k];                                      // reused for the row sum
+      l[k] *= corr;
 #pragma unroll
       for (int dd = 0; dd < DL; ++dd) acc[k][dd] *= corr;
-      for (int j = 0; j < nvalid; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, p, j);
-        if (pj != 0.f) {
-#pragma unroll
-          for (int dd = 0; dd < DL; ++dd) acc[k][dd] = fmaf(pj, sV[j * D + lane + 32 * dd], acc[k][dd]);
-        }
-      }
       m[k] = mn;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < RW; ++k) mx[k] += __shfl_xor_sync(0xffffffffu, mx[k], o);
+#pragma unroll
+    for (int k = 0; k < RW; ++k) l[k] += mx[k];
+    for (int j = 0; j < nvalid; ++j) {
+      float v[DL];
+#pragma unroll
+      for (int dd = 0; dd < DL; ++dd) v[dd] = sV[j * D + lane + 32 * dd];
+#pragma unroll
+      for (int k = 0; k < RW; ++k) {
+        const float pj = __shfl_sync(0xffffffffu, p[k], j);
+#pragma unroll
+        for (int dd = 0; dd < DL; ++dd) acc[k][dd] = fmaf(pj, v[dd], acc[k][dd]);
+      }
     }
   }
 
@@ -239,7 +265,7 @@ SvAttnPlan sv_attn_simt_plan(const SvAttnShape &s, int num_splits) {
   p.use_tc = 0;
   const int R = s.n_nodes * (s.hq / s.hkv);
   const int base = ((R + kRowsPerCta - 1) / kRowsPerCta) * s.batch * s.hkv;
-  const int max_useful = s.max_prefix > 0 ? (s.max_prefix + 255) / 256 : 1;
+  const int max_useful = s.max_prefix > 0 ? (s.max_prefix + kKeyTile - 1) / kKeyTile : 1;
   int splits = num_splits > 0 ? num_splits : (2 * kSms + base - 1) / base;
   splits = splits < 1 ? 1 : (splits > max_useful ? max_useful : splits);
   if (splits > 64) splits = 64;
