@@ -9,13 +9,15 @@
 // (min(1, p/q); on rejection sample the target minus the drafter), with
 // the point-mass proposal of a deterministic tree sibling.
 //
-// One cluster of kCluster CTAs per sequence walks the tree from the root.
-// Each visited node's vocabulary row is reduced in slices: CTA c reduces the
-// c-th slice with 16-byte loads, the kCluster partial results are exchanged
-// through distributed shared memory and combined in CTA order, so every CTA
-// of the cluster holds the same totals and takes the same decisions without
-// a broadcast.  Only the rows on the walk are read (plus, for typical
-// acceptance, the rows of every node reachable through valid children).
+// One cluster of nc = 8 CTAs per sequence.
+// The cluster walks the tree from the root: each visited node's vocabulary
+// row is reduced in slices (CTA c reduces the c-th slice with 16-byte loads),
+// the nc partial results are exchanged through distributed shared memory and
+// combined in CTA order, so every CTA of the cluster holds the same totals
+// and takes the same decisions without a broadcast.  Only the rows on the
+// walk are read (plus, for typical acceptance, the rows of every node
+// reachable through valid children).  Logits are scaled by 1/T as a product;
+// the softmax exponentials use the fast exp.
 #include <math.h>
 
 #include "common.cuh"
@@ -26,7 +28,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNodes = SPEC_MAX_NODES;
-constexpr int kCluster = 8;
+constexpr int kMaxCluster = 8;  // CTAs per sequence
 
 struct Red {
   float f[kWarps];
@@ -99,6 +101,7 @@ __device__ unsigned long long block_max_u64(unsigned long long v, Red &r) {
 struct ClusterOps {
   Red &r;
   int parity;
+  uint32_t nc;  // CTAs in the cluster
 
   __device__ float max(float v) {
     v = block_reduce(v, -INFINITY, r, [](float a, float b) { return fmaxf(a, b); });
@@ -106,7 +109,7 @@ struct ClusterOps {
     cluster_barrier();
     if (threadIdx.x == 0) {
       float m = -INFINITY;
-      for (uint32_t c = 0; c < kCluster; ++c) m = fmaxf(m, ld_remote_f32(&r.xf[parity][0], c));
+      for (uint32_t c = 0; c < nc; ++c) m = fmaxf(m, ld_remote_f32(&r.xf[parity][0], c));
       r.cf[0] = m;
     }
     __syncthreads();
@@ -126,7 +129,7 @@ struct ClusterOps {
     cluster_barrier();
     if (threadIdx.x == 0) {
       float sa = 0.f, sb = 0.f;
-      for (uint32_t c = 0; c < kCluster; ++c) {
+      for (uint32_t c = 0; c < nc; ++c) {
         sa += ld_remote_f32(&r.xf[parity][0], c);
         sb += ld_remote_f32(&r.xf[parity][1], c);
       }
@@ -145,7 +148,7 @@ struct ClusterOps {
     cluster_barrier();
     if (threadIdx.x == 0) {
       unsigned long long m = 0ull;
-      for (uint32_t c = 0; c < kCluster; ++c) {
+      for (uint32_t c = 0; c < nc; ++c) {
         const unsigned long long w = ld_remote_u64(&r.xu[parity], c);
         m = w > m ? w : m;
       }
@@ -161,25 +164,39 @@ struct ClusterOps {
 
 // Visit every element of this CTA's slice [lo, hi) of a logits row:
 // f(x, value) with x the column.  16-byte loads when the slice start is
-// aligned and its length a multiple of the vector width.
+// aligned and its length a multiple of the vector width, issued kBatch at a
+// time per thread before any is used, so a CTA keeps kThreads * kBatch * 16
+// bytes in flight.
+constexpr int kBatch = 8;
 template <typename T, typename F>
 __device__ __forceinline__ void for_slice(const T *row, int lo, int hi, F &&f) {
   constexpr int kVec = 16 / sizeof(T);
   if (((hi - lo) % kVec) == 0 && (reinterpret_cast<uintptr_t>(row + lo) & 15) == 0) {
     const int nv = (hi - lo) / kVec;
-    for (int vi = threadIdx.x; vi < nv; vi += kThreads) {
-      const uint4 u = *reinterpret_cast<const uint4 *>(row + lo + (int64_t)vi * kVec);
-      float v[kVec];
-      if constexpr (sizeof(T) == 2) {
-        sv::bf16x8_to_f32(u, v);
-      } else {
-        v[0] = __uint_as_float(u.x);
-        v[1] = __uint_as_float(u.y);
-        v[2] = __uint_as_float(u.z);
-        v[3] = __uint_as_float(u.w);
+    const uint4 *src = reinterpret_cast<const uint4 *>(row + lo);
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
+      uint4 u[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int vi = v0 + i * kThreads;
+        u[i] = vi < nv ? src[vi] : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int j = 0; j < kVec; ++j) f(lo + vi * kVec + j, v[j]);
+      for (int i = 0; i < kBatch; ++i) {
+        const int vi = v0 + i * kThreads;
+        if (vi >= nv) break;
+        float v[kVec];
+        if constexpr (sizeof(T) == 2) {
+          sv::bf16x8_to_f32(u[i], v);
+        } else {
+          v[0] = __uint_as_float(u[i].x);
+          v[1] = __uint_as_float(u[i].y);
+          v[2] = __uint_as_float(u[i].z);
+          v[3] = __uint_as_float(u[i].w);
+        }
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) f(lo + vi * kVec + j, v[j]);
+      }
     }
   } else {
     for (int x = lo + threadIdx.x; x < hi; x += kThreads) f(x, sv::to_f32(row[x]));
@@ -203,11 +220,14 @@ __global__ void __launch_bounds__(kThreads)
 
   const uint32_t cta = blockIdx.x;  // rank in the cluster (cluster spans x)
   const int b = blockIdx.y;
-  const int slice = ((V + kCluster - 1) / kCluster + 7) / 8 * 8;
+  const int nc = (int)gridDim.x;  // the cluster spans x
+  const int slice = ((V + nc - 1) / nc + 7) / 8 * 8;
   const int lo = min(V, (int)cta * slice), hi = min(V, lo + slice);
-  ClusterOps cl{red, 0};
+  ClusterOps cl{red, 0, (uint32_t)nc};
 
   const int64_t row0 = (int64_t)b * N;
+  // 1/T once: logits are scaled by a product, not a division per element
+  const float inv_t = 1.f / temp;
   for (int i = threadIdx.x; i < N; i += kThreads) {
     s_fc[i] = first_child[row0 + i];
     s_ns[i] = next_sibling[row0 + i];
@@ -233,7 +253,7 @@ __global__ void __launch_bounds__(kThreads)
   };
   auto row_max_z = [&](const T *row) -> float {
     float m = -INFINITY;
-    for_slice(row, lo, hi, [&](int, float v) { m = fmaxf(m, v / temp); });
+    for_slice(row, lo, hi, [&](int, float v) { m = fmaxf(m, v * inv_t); });
     return cl.max(m);
   };
 
@@ -273,8 +293,8 @@ __global__ void __launch_bounds__(kThreads)
       const float m = row_max_z(row);
       float S = 0.f, Q = 0.f;
       for_slice(row, lo, hi, [&](int, float x) {
-        const float z = x / temp - m;
-        const float e = expf(z);
+        const float z = x * inv_t - m;
+        const float e = __expf(z);
         S += e;
         Q = fmaf(e, z, Q);
       });
@@ -288,7 +308,7 @@ __global__ void __launch_bounds__(kThreads)
             sv::report(status, SPEC_DEV_BAD_TOKEN);
             continue;
           }
-          const float p = expf(sv::to_f32(row[x]) / temp - m) / S;
+          const float p = __expf(sv::to_f32(row[x]) * inv_t - m) / S;
           s_ok[c] = p > thr;
         }
       }
@@ -315,7 +335,7 @@ __global__ void __launch_bounds__(kThreads)
       const T *row = base + (int64_t)v * V;
       const float m = row_max_z(row);
       float S = 0.f, unused = 0.f;
-      for_slice(row, lo, hi, [&](int, float x) { S += expf(x / temp - m); });
+      for_slice(row, lo, hi, [&](int, float x) { S += __expf(x * inv_t - m); });
       cl.sum2(S, unused);
       if (threadIdx.x == 0) {
         int nxt = -1;
@@ -330,7 +350,7 @@ __global__ void __launch_bounds__(kThreads)
             sv::report(status, SPEC_DEV_BAD_TOKEN);
             seen = true;
           } else if (!seen) {
-            ex = expf(sv::to_f32(row[x]) / temp - m);
+            ex = __expf(sv::to_f32(row[x]) * inv_t - m);
             r = ex / (S - removed);
           }
           const sv::u32x4 w = sv::philox4x32_10(sv::u32x4{(uint32_t)c, 0u, (uint32_t)b, st}, k0, k1);
@@ -363,7 +383,7 @@ __global__ void __launch_bounds__(kThreads)
             sv::philox4x32_10(sv::u32x4{(uint32_t)x, 256u + (uint32_t)v, (uint32_t)b, st}, k0, k1);
         const float up = ((float)(w.x >> 9) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
         const float g = -logf(-logf(up));
-        const float key = val / temp + g;
+        const float key = val * inv_t + g;
         const unsigned long long k = sv::rank_key(key, (uint32_t)x);
         best = k > best ? k : best;
       });
@@ -392,13 +412,14 @@ int launch_accept(int mode, const void *logits, int batch, int n_nodes, int voca
                   const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
                   float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
                   int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
+  const int nc = kMaxCluster;  // CTAs per sequence (the kernel reads it from gridDim.x)
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kCluster, batch);
+  cfg.gridDim = dim3(nc, batch);
   cfg.blockDim = dim3(kThreads);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.x = nc;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
