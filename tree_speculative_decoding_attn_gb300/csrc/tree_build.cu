@@ -109,22 +109,30 @@ __global__ void __launch_bounds__(kDynThreads)
                          uint64_t *anc, int32_t *first_child, int32_t *next_sibling, int32_t *pool_index,
                          float *val_out, int32_t *status) {
   extern __shared__ __align__(16) unsigned char smem[];
-  unsigned long long *key = reinterpret_cast<unsigned long long *>(smem);  // [M]
-  int *ppar = reinterpret_cast<int *>(key + M);                          // [M]
+  int M2 = 1;  // M rounded up to a power of two: the sort width
+  while (M2 < M) M2 <<= 1;
+  unsigned long long *key = reinterpret_cast<unsigned long long *>(smem);  // [M2]
+  int *ppar = reinterpret_cast<int *>(key + M2);                         // [M]
   float *val = reinterpret_cast<float *>(ppar + M);                      // [M]
+  float *conf = val + M;                                                 // [M]
+  int *pdep = reinterpret_cast<int *>(conf + M);                         // [M]
   __shared__ int kept[kMaxNodes];       // pool index of kept slot r (sorted by key)
   __shared__ int kept_new[kMaxNodes];   // new (breadth-first) index of kept slot r
   __shared__ int new_par[kMaxNodes];    // parents by new index
-  __shared__ int bad;
+  __shared__ int bad, s_dmax;
 
   const int b = blockIdx.x, t = threadIdx.x;
   const int64_t prow = (int64_t)b * M;
-  if (t == 0) bad = 0;
+  if (t == 0) {
+    bad = 0;
+    s_dmax = 0;
+  }
   __syncthreads();
   for (int i = t; i < M; i += kDynThreads) {
     const int p = pool_parent[prow + i];
     const float c = pool_conf[prow + i];
     ppar[i] = p;
+    conf[i] = c;
     if (i == 0 ? p != -1 : (p < 0 || p >= i || !(c >= 0.f && c <= 1.f))) atomicOr(&bad, 1);
   }
   __syncthreads();
@@ -132,38 +140,59 @@ __global__ void __launch_bounds__(kDynThreads)
     if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
     return;
   }
-  // 1. path values and depths
+  // 1. depths (parent walk in shared memory), then path values level by
+  // level: v[i] = v[parent] * conf[i] multiplies in root-to-node order, the
+  // parent's value being complete one level earlier
+  int dmax_t = 0;
   for (int i = t; i < M; i += kDynThreads) {
-    int chain[kMaxPoolDepth];
-    int d = 0;
-    int c = i;
+    int d = 0, c = i;
     while (c > 0 && d < kMaxPoolDepth) {
-      chain[d++] = c;
       c = ppar[c];
+      ++d;
     }
     if (c != 0) {
       atomicOr(&bad, 1);
       d = 0;
     }
-    float v = 1.0f;
-    for (int j = d - 1; j >= 0; --j) v = __fmul_rn(v, pool_conf[prow + chain[j]]);
-    val[i] = v;
-    // v >= 0, so clearing the sign bit only maps -0 to +0
-    key[i] = ((unsigned long long)(0xFFFFFFFFu - (__float_as_uint(v) & 0x7FFFFFFFu)) << 32) |
-             ((unsigned long long)d << 16) | (unsigned long long)i;
+    pdep[i] = d;
+    dmax_t = max(dmax_t, d);
   }
+  if (dmax_t > 0) atomicMax(&s_dmax, dmax_t);
   __syncthreads();
   if (bad) {
     if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
     return;
   }
-  // 2. keep the N smallest keys
-  for (int i = t; i < M; i += kDynThreads) {
-    const unsigned long long k = key[i];
-    int r = 0;
-    for (int j = 0; j < M; ++j) r += key[j] < k;
-    if (r < N) kept[r] = i;
+  if (t == 0) val[0] = 1.0f;
+  for (int d = 1; d <= s_dmax; ++d) {
+    __syncthreads();  // level d - 1 complete
+    for (int i = t; i < M; i += kDynThreads)
+      if (pdep[i] == d) val[i] = __fmul_rn(val[ppar[i]], conf[i]);
   }
+  __syncthreads();
+  for (int i = t; i < M2; i += kDynThreads) {
+    // v >= 0, so clearing the sign bit only maps -0 to +0; padding sorts last
+    key[i] = i < M ? ((unsigned long long)(0xFFFFFFFFu - (__float_as_uint(val[i]) & 0x7FFFFFFFu)) << 32) |
+                         ((unsigned long long)pdep[i] << 16) | (unsigned long long)i
+                   : ~0ull;
+  }
+  __syncthreads();
+  // 2. keep the N smallest keys: bitonic sort of the (unique) keys, ascending
+  for (int k = 2; k <= M2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < M2; i += kDynThreads) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = key[i], c = key[l];
+          if ((a > c) == ((i & k) == 0)) {
+            key[i] = c;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  if (t < N) kept[t] = (int)(key[t] & 0xFFFFull);  // pool index of the t-th smallest key
   __syncthreads();
   // parent closure check and breadth-first renumbering (N <= 64 threads):
   // each kept slot's parent slot and depth are looked up once, then every
@@ -172,7 +201,7 @@ __global__ void __launch_bounds__(kDynThreads)
   int my_pool = -1, my_depth = 0, my_pslot = -1;
   if (t < N) {
     my_pool = kept[t];
-    my_depth = (int)((key[my_pool] >> 16) & 0xFFFF);
+    my_depth = pdep[my_pool];
     if (t > 0) {
       const int pp = ppar[my_pool];
       for (int r = 0; r < N; ++r)
@@ -198,7 +227,7 @@ __global__ void __launch_bounds__(kDynThreads)
       for (int r = 0; r < N; ++r) {
         if (r == t || kept_depth[r] != d) continue;
         const int upar = r == 0 ? -1 : kept_new[kept_pslot[r]];  // assigned on an earlier level
-        if (upar < mp || (upar == mp && key[kept[r]] < key[my_pool])) ++before;
+        if (upar < mp || (upar == mp && r < t)) ++before;  // kept slots are in key order
       }
       kept_new[t] = base + before;
       new_par[base + before] = mp;
@@ -246,7 +275,9 @@ int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const 
                      int32_t *first_child, int32_t *next_sibling, int32_t *pool_index, float *val,
                      int32_t *status, cudaStream_t stream) {
   if (M > kMaxPool) return SPEC_ERR_UNSUPPORTED;
-  const size_t smem = (size_t)M * (8 + 4 + 4);
+  size_t M2 = 1;
+  while (M2 < (size_t)M) M2 <<= 1;
+  const size_t smem = M2 * 8 + (size_t)M * (4 + 4 + 4 + 4);  // key (sort width), parent, value, conf, depth
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(build_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
