@@ -86,7 +86,10 @@ def test_lm_head(R, d, V):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("V,s", [(1000, 10), (32000, 10), (128256, 16), (17, 1), (33, 16)])
+# (V, s): per-thread lists of 4, 8 and 16 keys; rows that fill one partial
+# batch per thread and rows that fold many batches per thread
+@pytest.mark.parametrize("V,s", [(1000, 10), (32000, 10), (128256, 16), (17, 1), (33, 16), (40000, 4), (9000, 7),
+                                 (200000, 6), (3000, 12)])
 def test_topk_bit_exact(dtype, V, s):
     g = synth.stream(V + s, "topk")
     rows = np.round(synth.gaussian(g, (6, V), 2.0, False) * 4) / 4   # plenty of exact ties
