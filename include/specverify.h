@@ -229,6 +229,12 @@ int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front
  * hq % hkv == 0; (hq / hkv) * n_nodes <= 512.  Softmax and accumulation
  * are float32.  A prefix_len above max_prefix sets SPEC_DEV_CAPACITY and
  * that sequence's output is left unwritten.
+ * bf16 with head_dim 128 and more than 128 query rows per KV head
+ * ((hq / hkv) * n_nodes > 128, hq / hkv dividing 128) runs on pairs of
+ * SMs with a persistent grid that balances its own work: num_splits is
+ * ignored there (tree_attn_plan_splits returns 1) and the workspace holds
+ * the partial rows of the row groups cut between SM pairs.  Calls that
+ * may overlap on the GPU need separate workspaces.
  * ------------------------------------------------------------------ */
 size_t tree_attn_workspace_bytes(int dtype, int batch, int n_nodes, int hq, int hkv,
                                  int head_dim, int max_prefix, int num_splits);
