@@ -539,7 +539,10 @@ double tc_split_cost(const SvAttnShape &s, const int32_t *prefix, int splits) {
   if (splits > 1) {
     const double tile_bytes = (double)kBN * kD * 2 * 2 * slots;  // bytes moved per unit of time
     const double partial = 2.0 * s.batch * s.hkv * splits * R * sv_partial_stride(kD) * 4.0;
-    makespan += partial / tile_bytes + 4.0;
+    // the combine launch, plus about one tile per split for the partial rows'
+    // write-back and merge (measured on the 32-head, 2048-key shape: three
+    // splits beat four)
+    makespan += partial / tile_bytes + 4.0 + splits;
   }
   return makespan;
 }
