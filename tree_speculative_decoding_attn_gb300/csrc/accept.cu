@@ -9,7 +9,7 @@
 // (min(1, p/q); on rejection sample the target minus the drafter), with
 // the point-mass proposal of a deterministic tree sibling.
 //
-// One cluster of nc = 8 CTAs per sequence.
+// One cluster of nc CTAs per sequence (8; 4 at batch >= 32).
 // The cluster walks the tree from the root: each visited node's vocabulary
 // row is reduced in slices (CTA c reduces the c-th slice with 16-byte loads),
 // the nc partial results are exchanged through distributed shared memory and
@@ -28,7 +28,7 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNodes = SPEC_MAX_NODES;
-constexpr int kMaxCluster = 8;  // CTAs per sequence
+constexpr int kMaxCluster = 8;  // CTAs per sequence (4 at batch >= 32)
 
 struct Red {
   float f[kWarps];
@@ -412,7 +412,9 @@ int launch_accept(int mode, const void *logits, int batch, int n_nodes, int voca
                   const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
                   float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
                   int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
-  const int nc = kMaxCluster;  // CTAs per sequence (the kernel reads it from gridDim.x)
+  // CTAs per sequence (the kernel reads it from gridDim.x): at batch >= 32
+  // four, so every sequence's cluster is resident in one wave
+  const int nc = batch >= 32 ? 4 : kMaxCluster;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nc, batch);
   cfg.blockDim = dim3(kThreads);
