@@ -93,14 +93,26 @@ __global__ void __launch_bounds__(kMaxNodes)
 // ---------------------------------------------------------------------------
 // Confidence-product rerank.  One CTA per sequence.
 //   1. val[i] = val[parent] * conf[i] in root-to-node order (float32).
-//   2. rank of every pool node under (val desc, depth asc, index asc) by
-//      counting; the n lowest ranks are kept (the root has rank 0).
+//   2. the pool sorted by (val desc, depth asc, index asc); the n first
+//      nodes are kept (the root comes first).
 //   3. breadth-first renumbering, level by level: (new parent, val desc,
 //      index asc).
 // ---------------------------------------------------------------------------
-constexpr int kDynThreads = 1024;
+constexpr int kDynThreads = 512;
 constexpr int kMaxPool = 4096;
 constexpr int kMaxPoolDepth = 64;
+
+// Bitonic compare-exchange steps with partner distance j0, j0/2, .., 1 of
+// the merge of width k, for element i held in a register; the partner
+// i ^ j lies in the same warp because j < 32.  Ascending where i & k == 0.
+__device__ __forceinline__ unsigned long long bitonic_steps_reg(unsigned long long a, int i, int k, int j0) {
+  for (int j = j0; j > 0; j >>= 1) {
+    const unsigned long long c = __shfl_xor_sync(0xffffffffu, a, j);
+    const bool keep_min = ((i & j) == 0) == ((i & k) == 0);
+    a = keep_min ? (c < a ? c : a) : (c < a ? a : c);
+  }
+  return a;
+}
 
 __global__ void __launch_bounds__(kDynThreads)
     build_dynamic_kernel(const int32_t *__restrict__ pool_parent, const int32_t *__restrict__ pool_tok,
@@ -116,7 +128,6 @@ __global__ void __launch_bounds__(kDynThreads)
   float *val = reinterpret_cast<float *>(ppar + M);                      // [M]
   float *conf = val + M;                                                 // [M]
   int *pdep = reinterpret_cast<int *>(conf + M);                         // [M]
-  __shared__ int kept[kMaxNodes];       // pool index of kept slot r (sorted by key)
   __shared__ int kept_new[kMaxNodes];   // new (breadth-first) index of kept slot r
   __shared__ int new_par[kMaxNodes];    // parents by new index
   __shared__ int bad, s_dmax;
@@ -169,17 +180,35 @@ __global__ void __launch_bounds__(kDynThreads)
     for (int i = t; i < M; i += kDynThreads)
       if (pdep[i] == d) val[i] = __fmul_rn(val[ppar[i]], conf[i]);
   }
+  __shared__ int lvl_count[kMaxPoolDepth + 2];  // kept nodes per depth
+  __shared__ __align__(16) unsigned lkey[kMaxNodes];  // sort keys of one level
+  for (int i = t; i < kMaxPoolDepth + 2; i += kDynThreads) lvl_count[i] = 0;
   __syncthreads();
+  // conf is dead once the values are formed: it becomes the map from pool
+  // index to kept slot (-1: not kept)
+  int *slot_of = reinterpret_cast<int *>(conf);
   for (int i = t; i < M2; i += kDynThreads) {
     // v >= 0, so clearing the sign bit only maps -0 to +0; padding sorts last
     key[i] = i < M ? ((unsigned long long)(0xFFFFFFFFu - (__float_as_uint(val[i]) & 0x7FFFFFFFu)) << 32) |
                          ((unsigned long long)pdep[i] << 16) | (unsigned long long)i
                    : ~0ull;
+    if (i < M) slot_of[i] = -1;
   }
   __syncthreads();
-  // 2. keep the N smallest keys: bitonic sort of the (unique) keys, ascending
-  for (int k = 2; k <= M2; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
+  // 2. keep the N smallest keys: bitonic sort of the (unique) keys,
+  // ascending.  Steps with partner distance >= 32 exchange through shared
+  // memory; the shorter ones run on registers.  Merges up to width 32 run
+  // entirely on registers (over a whole warp: past M2 the lanes hold
+  // padding that only ever meets padding).
+  const int M2w = M2 < 32 ? 32 : M2;
+  for (int i = t; i < M2w; i += kDynThreads) {
+    unsigned long long a = i < M2 ? key[i] : ~0ull;
+    for (int k = 2; k <= 32 && k <= M2; k <<= 1) a = bitonic_steps_reg(a, i, k, k >> 1);
+    if (i < M2) key[i] = a;
+  }
+  __syncthreads();
+  for (int k = 64; k <= M2; k <<= 1) {
+    for (int j = k >> 1; j >= 32; j >>= 1) {
       for (int i = t; i < M2; i += kDynThreads) {
         const int l = i ^ j;
         if (l > i) {
@@ -192,42 +221,48 @@ __global__ void __launch_bounds__(kDynThreads)
       }
       __syncthreads();
     }
-  if (t < N) kept[t] = (int)(key[t] & 0xFFFFull);  // pool index of the t-th smallest key
-  __syncthreads();
-  // parent closure check and breadth-first renumbering (N <= 64 threads):
-  // each kept slot's parent slot and depth are looked up once, then every
-  // level is numbered by counting the predecessors of each node on it
-  __shared__ int kept_pslot[kMaxNodes], kept_depth[kMaxNodes];
+    for (int i = t; i < M2; i += kDynThreads) key[i] = bitonic_steps_reg(key[i], i, k, 16);
+    __syncthreads();
+  }
+  // kept slot t = the t-th smallest key; its parent's slot through the map
   int my_pool = -1, my_depth = 0, my_pslot = -1;
   if (t < N) {
-    my_pool = kept[t];
+    my_pool = (int)(key[t] & 0xFFFFull);
     my_depth = pdep[my_pool];
-    if (t > 0) {
-      const int pp = ppar[my_pool];
-      for (int r = 0; r < N; ++r)
-        if (kept[r] == pp) my_pslot = r;
-      if (my_pslot < 0) atomicOr(&bad, 1);
-    }
-    kept_pslot[t] = my_pslot;
-    kept_depth[t] = my_depth;
+    slot_of[my_pool] = t;
+    atomicAdd(&lvl_count[min(my_depth, kMaxPoolDepth + 1)], 1);
+  }
+  __syncthreads();
+  if (t > 0 && t < N) {
+    my_pslot = slot_of[ppar[my_pool]];
+    if (my_pslot < 0) atomicOr(&bad, 1);  // the kept set is not closed under parents
   }
   __syncthreads();
   if (bad) {
     if (t == 0) sv::report(status, SPEC_DEV_BAD_POOL);
     return;
   }
+  // breadth-first renumbering, one level per round: a node's place on its
+  // level is the number of level nodes with a smaller (new parent, slot);
+  // slots are in key order, so this orders siblings by value
   int base = 0;
-  for (int d = 0; d < kMaxPoolDepth; ++d) {
-    int here = 0;  // kept nodes at depth d (uniform across threads)
-    for (int r = 0; r < N; ++r) here += kept_depth[r] == d;
+  for (int d = 0; d <= kMaxPoolDepth; ++d) {
+    const int here = lvl_count[d];
     if (here == 0) break;
+    int mp = -1;
+    unsigned mine = 0xFFFFFFFFu;
     if (t < N && my_depth == d) {
-      const int mp = (t == 0) ? -1 : kept_new[my_pslot];
+      mp = t == 0 ? -1 : kept_new[my_pslot];  // the parent was numbered one level up
+      mine = ((unsigned)(mp + 1) << 6) | (unsigned)t;
+    }
+    if (t < kMaxNodes) lkey[t] = mine;
+    __syncthreads();
+    if (t < N && my_depth == d) {
       int before = 0;
-      for (int r = 0; r < N; ++r) {
-        if (r == t || kept_depth[r] != d) continue;
-        const int upar = r == 0 ? -1 : kept_new[kept_pslot[r]];  // assigned on an earlier level
-        if (upar < mp || (upar == mp && r < t)) ++before;  // kept slots are in key order
+#pragma unroll
+      for (int r = 0; r < kMaxNodes; r += 4) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(&lkey[r]);
+        before += (q.x < mine) + (q.y < mine) + (q.z < mine) + (q.w < mine);
       }
       kept_new[t] = base + before;
       new_par[base + before] = mp;
