@@ -314,10 +314,11 @@ int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab
  *       r <- r with tok[c] removed, renormalised.  If no child is
  *       accepted the bonus is a sample of r ("Drafters: ...", section "Why
  *       the answer does not change").  Uniforms: Philox4x32-10 with key
- *       `seed`; accept draw counter (c, 0, b, step), sampling counter
- *       (x, 256 + v, b, step); u = (word0 >> 8) * 2^-24.  Sampling is the
- *       exponential race argmax_x (logits/T + Gumbel(u'_x)) over the
- *       tokens not removed, u' = ((word0 >> 9) + 0.5) * 2^-23.
+ *       `seed`; accept draw counter (c, 0, b, step), u = (word0 >> 8) *
+ *       2^-24.  Sampling is the exponential race argmax_x (logits/T +
+ *       Gumbel(u'_x)) over the tokens not removed, u' = ((w >> 9) + 0.5) *
+ *       2^-23 with w = word (x mod 4) of counter (x div 4, 256 + v, b,
+ *       step).
  *       Requires temperature > 0.
  * Outputs: acc_len [batch] (accepted nodes, root excluded), acc_path
  * [batch, path_cap] (node ids root first, -1 after), bonus [batch].

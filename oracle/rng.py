@@ -13,7 +13,8 @@ published generator separately) draws the identical numbers:
 * accept draw for child node c of sequence b at step t:
   counter (c, 0, b, t), key (seed_lo, seed_hi), word 0;
 * race draw for token x when sampling at stop node v:
-  counter (x, 256 + v, b, t), same key, word 0.
+  counter (x div 4, 256 + v, b, t), same key, word x mod 4 (one call of
+  the generator serves four consecutive tokens).
 
 A 32-bit word w maps to u = (w >> 8) * 2^-24 in [0, 1) (exact in float32);
 for the race the open-interval form u' = ((w >> 9) + 0.5) * 2^-23 is used
@@ -57,5 +58,7 @@ def uniform_accept(seed: int, b: int, step: int, child):
 
 def uniform_race(seed: int, b: int, step: int, node: int, tokens):
     """u' in (0,1) for the sampling race over ``tokens`` at stop node ``node``."""
-    w = philox4x32_10((tokens, 256 + node, b, step), _key(seed))[0]
+    t = np.asarray(tokens, np.int64)
+    words = philox4x32_10((t >> 2, 256 + node, b, step), _key(seed))
+    w = np.choose(t & 3, words)
     return ((w >> np.uint32(9)).astype(np.float64) + 0.5) * 2.0 ** -23

@@ -6,7 +6,10 @@ import torch
 def dev(x, dtype=None):
     """numpy -> CUDA tensor; float32 arrays become ``dtype`` (bf16 values
     produced by synth.round_bf16 convert exactly)."""
-    t = torch.from_numpy(np.ascontiguousarray(x))
+    a = np.ascontiguousarray(x)
+    if not a.flags.writeable:  # e.g. a broadcast view: torch wants its own copy
+        a = a.copy()
+    t = torch.from_numpy(a)
     if dtype is not None:
         t = t.to(dtype)
     return t.cuda()

@@ -102,9 +102,13 @@ def test_typical_matches_oracle(si, eps, delta, bf16):
 @pytest.mark.parametrize("si", [0, 1, 2, 3])
 @pytest.mark.parametrize("bf16", [False, True])
 @pytest.mark.parametrize("temperature", [1.0, 0.7])
-def test_reject_matches_oracle(si, bf16, temperature):
+@pytest.mark.parametrize("V", [3000, 3001])
+def test_reject_matches_oracle(si, bf16, temperature, V):
+    """V = 3001 leaves odd rows unaligned, so those rows are visited one
+    column at a time (the sampling race picks each token's Philox word
+    singly there)."""
     shape = SHAPES[si]
-    B, V = 5, 3000
+    B = 5
     t = _tree_batch(shape, B, V, 30 + si)
     lg = _logits(shape, t, B, V, 40 + si, bf16)
     cap = shape.n_levels + 1
@@ -113,6 +117,31 @@ def test_reject_matches_oracle(si, bf16, temperature):
         assert got[3] == 0
         ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 0x1234ABCD5678, step,
                                 temperature, cap)
+        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+
+
+@pytest.mark.parametrize("B", [1, 20, 40])
+@pytest.mark.parametrize("mode", [sv.GREEDY, sv.TYPICAL, sv.REJECT])
+def test_every_cluster_size(B, mode):
+    """16, 8 and 4 CTAs per sequence (batch 1, 20, 40), bf16, a vocabulary
+    that splits unevenly over the CTAs."""
+    shape = SHAPES[2]
+    V = 20011
+    t = _tree_batch(shape, B, V, 60 + B)
+    lg = _logits(shape, t, B, V, 70 + B, True)
+    cap = shape.n_levels + 1
+    got = _accept(mode, lg, t, cap, bf16=True, temperature=1.0, eps=0.3, delta=0.09, seed=99, step=B)
+    assert got[3] == 0
+    if mode == sv.GREEDY:
+        ref = ACC.accept_greedy(lg, t["tok"], t["first_child"], t["next_sibling"], cap)
+        for g_, r_ in zip(got[:3], ref):
+            np.testing.assert_array_equal(g_, r_)
+    elif mode == sv.TYPICAL:
+        ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], 0.3, 0.09, 1.0,
+                                 cap)
+        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+    else:
+        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 99, B, 1.0, cap)
         _compare_with_near_ties(got[:3], ref[:3], ref[3])
 
 

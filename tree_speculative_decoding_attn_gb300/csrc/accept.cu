@@ -9,16 +9,22 @@
 // (min(1, p/q); on rejection sample the target minus the drafter), with
 // the point-mass proposal of a deterministic tree sibling.
 //
-// One cluster of nc CTAs per sequence (8; 4 at batch >= 32).
-// The cluster walks the tree from the root: each visited node's vocabulary
-// row is reduced in slices (CTA c reduces the c-th slice with 16-byte loads),
-// the nc partial results are exchanged through distributed shared memory and
-// combined in CTA order, so every CTA of the cluster holds the same totals
-// and takes the same decisions without a broadcast.  Only the rows on the
-// walk are read (plus, for typical acceptance, the rows of every node
-// reachable through valid children).  Logits are scaled by 1/T as a product;
-// the softmax exponentials use the fast exp.
+// One cluster of nc CTAs per sequence (16 at batch < 16, 8 below 32, else
+// 4).  The cluster walks the tree from the root: each visited node's
+// vocabulary row is reduced in slices (CTA c reduces the c-th slice with
+// 16-byte loads), the nc partial results are exchanged through distributed
+// shared memory and combined in the same fixed order in every CTA, so all
+// CTAs hold the same totals and take the same decisions without a
+// broadcast.  Only the rows on the walk are read (plus, for typical
+// acceptance, the rows of every node reachable through valid children).
+// The softmax statistics of a row (max, sum of exponentials and, for the
+// entropy, their first moment) come from one online pass.  A node's
+// children are examined by one warp in parallel; only the rejection rule's
+// residual bookkeeping runs serially, on values already in shared memory.
+#include <float.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -28,19 +34,59 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxNodes = SPEC_MAX_NODES;
-constexpr int kMaxCluster = 8;  // CTAs per sequence (4 at batch >= 32)
+
+// Softmax statistics of a set of scaled logits z: m = max z, S = sum
+// exp(z - m), Q = sum exp(z - m) (z - m).  S == 0 marks the empty set.
+struct Stats {
+  float m, S, Q;
+};
+__device__ __forceinline__ Stats stats_empty() { return Stats{-FLT_MAX, 0.f, 0.f}; }
+// The union of two disjoint sets: both are brought to the larger max
+// (exp(z - m') = exp(m - m') exp(z - m), and z - m' = (z - m) + (m - m')).
+__device__ __forceinline__ Stats stats_merge(Stats a, Stats b) {
+  if (!(b.S > 0.f)) return a;
+  if (!(a.S > 0.f)) return b;
+  const float mn = fmaxf(a.m, b.m), da = a.m - mn, db = b.m - mn;
+  const float ea = __expf(da), eb = __expf(db);
+  return Stats{mn, fmaf(ea, a.S, eb * b.S), fmaf(ea, fmaf(da, a.S, a.Q), eb * fmaf(db, b.S, b.Q))};
+}
+// One more element z (kQ: keep the first moment as well).
+template <bool kQ>
+__device__ __forceinline__ void stats_add(Stats &s, float z) {
+  if (z > s.m) {  // new max: rescale what is there
+    if (s.S > 0.f) {
+      const float d = s.m - z, e = __expf(d);
+      if (kQ) s.Q = e * fmaf(d, s.S, s.Q);
+      s.S *= e;
+    }
+    s.m = z;
+  }
+  const float d = z - s.m, e = __expf(d);
+  s.S += e;
+  if (kQ) s.Q = fmaf(e, d, s.Q);
+}
+__device__ __forceinline__ Stats shfl_stats(Stats s, int o) {
+  return Stats{__shfl_xor_sync(0xffffffffu, s.m, o), __shfl_xor_sync(0xffffffffu, s.S, o),
+               __shfl_xor_sync(0xffffffffu, s.Q, o)};
+}
+// Butterfly over a warp.  Lane 0 ends with the union of all lanes' sets,
+// combined in a fixed order: warps holding the same inputs get the same
+// lane-0 value bit for bit (other lanes may differ in rounding).
+__device__ __forceinline__ Stats warp_stats(Stats s) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s = stats_merge(s, shfl_stats(s, o));
+  return s;
+}
 
 struct Red {
-  float f[kWarps];
-  unsigned long long u[kWarps];
-  float bf;
-  unsigned long long bu;
+  Stats ws[kWarps];              // per-warp partials
+  unsigned long long wu[kWarps];
   // cluster exchange slots, double-buffered by reduction parity: a slot is
   // rewritten two reductions later, after every CTA has passed the barrier
   // that follows its last read of it
-  float xf[2][2];
+  Stats xs[2];
   unsigned long long xu[2];
-  float cf[2];
+  Stats cs;                      // the cluster's result
   unsigned long long cu;
 };
 
@@ -63,126 +109,86 @@ __device__ __forceinline__ unsigned long long ld_remote_u64(const void *local, u
   return v;
 }
 
-template <typename Op>
-__device__ float block_reduce(float v, float ident, Red &r, Op op) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float w = threadIdx.x < kWarps ? r.f[threadIdx.x] : ident;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) w = op(w, __shfl_xor_sync(0xffffffffu, w, o));
-    if (threadIdx.x == 0) r.bf = w;
-  }
-  __syncthreads();
-  const float out = r.bf;
-  __syncthreads();
-  return out;
-}
-
-__device__ unsigned long long block_max_u64(unsigned long long v, Red &r) {
-  v = sv::warp_max_u64(v);
-  if ((threadIdx.x & 31) == 0) r.u[threadIdx.x >> 5] = v;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    unsigned long long w = threadIdx.x < kWarps ? r.u[threadIdx.x] : 0ull;
-    w = sv::warp_max_u64(w);
-    if (threadIdx.x == 0) r.bu = w;
-  }
-  __syncthreads();
-  const unsigned long long out = r.bu;
-  __syncthreads();
-  return out;
-}
-
-// Cluster-wide reductions: every CTA gets the identical result (partials
-// combined in CTA order).  All threads of all CTAs must call them together.
+// Cluster-wide reductions: every CTA gets the identical result.  Warp
+// partials go through shared memory to warp 0, which combines them, posts
+// the CTA's partial, and after the cluster barrier reads all nc partials
+// at once (lane c reads CTA c) and combines them by the same butterfly in
+// every CTA.  All threads of all CTAs must call them together.
 struct ClusterOps {
   Red &r;
   int parity;
-  uint32_t nc;  // CTAs in the cluster
+  uint32_t nc;  // CTAs in the cluster (<= 32)
 
-  __device__ float max(float v) {
-    v = block_reduce(v, -INFINITY, r, [](float a, float b) { return fmaxf(a, b); });
-    if (threadIdx.x == 0) r.xf[parity][0] = v;
+  __device__ Stats stats(Stats s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    s = warp_stats(s);
+    if (lane == 0) r.ws[w] = s;
+    __syncthreads();
+    if (w == 0) {
+      Stats c = lane < kWarps ? r.ws[lane] : stats_empty();
+      c = warp_stats(c);
+      if (lane == 0) r.xs[parity] = c;
+    }
     cluster_barrier();
-    if (threadIdx.x == 0) {
-      float m = -INFINITY;
-      for (uint32_t c = 0; c < nc; ++c) m = fmaxf(m, ld_remote_f32(&r.xf[parity][0], c));
-      r.cf[0] = m;
+    if (w == 0) {
+      Stats c = stats_empty();
+      if (lane < (int)nc)
+        c = Stats{ld_remote_f32(&r.xs[parity].m, lane), ld_remote_f32(&r.xs[parity].S, lane),
+                  ld_remote_f32(&r.xs[parity].Q, lane)};
+      c = warp_stats(c);
+      if (lane == 0) r.cs = c;
     }
     __syncthreads();
-    const float out = r.cf[0];
-    __syncthreads();
+    const Stats out = r.cs;
     parity ^= 1;
     return out;
   }
-  // two sums at once
-  __device__ void sum2(float &a, float &b) {
-    a = block_reduce(a, 0.f, r, [](float x, float y) { return x + y; });
-    b = block_reduce(b, 0.f, r, [](float x, float y) { return x + y; });
-    if (threadIdx.x == 0) {
-      r.xf[parity][0] = a;
-      r.xf[parity][1] = b;
-    }
-    cluster_barrier();
-    if (threadIdx.x == 0) {
-      float sa = 0.f, sb = 0.f;
-      for (uint32_t c = 0; c < nc; ++c) {
-        sa += ld_remote_f32(&r.xf[parity][0], c);
-        sb += ld_remote_f32(&r.xf[parity][1], c);
-      }
-      r.cf[0] = sa;
-      r.cf[1] = sb;
-    }
-    __syncthreads();
-    a = r.cf[0];
-    b = r.cf[1];
-    __syncthreads();
-    parity ^= 1;
-  }
   __device__ unsigned long long max_u64(unsigned long long v) {
-    v = block_max_u64(v, r);
-    if (threadIdx.x == 0) r.xu[parity] = v;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = sv::warp_max_u64_redux(v);
+    if (lane == 0) r.wu[w] = v;
+    __syncthreads();
+    if (w == 0) {
+      unsigned long long c = lane < kWarps ? r.wu[lane] : 0ull;
+      c = sv::warp_max_u64_redux(c);
+      if (lane == 0) r.xu[parity] = c;
+    }
     cluster_barrier();
-    if (threadIdx.x == 0) {
-      unsigned long long m = 0ull;
-      for (uint32_t c = 0; c < nc; ++c) {
-        const unsigned long long w = ld_remote_u64(&r.xu[parity], c);
-        m = w > m ? w : m;
-      }
-      r.cu = m;
+    if (w == 0) {
+      unsigned long long c = lane < (int)nc ? ld_remote_u64(&r.xu[parity], lane) : 0ull;
+      c = sv::warp_max_u64_redux(c);
+      if (lane == 0) r.cu = c;
     }
     __syncthreads();
     const unsigned long long out = r.cu;
-    __syncthreads();
     parity ^= 1;
     return out;
   }
 };
 
-// Visit every element of this CTA's slice [lo, hi) of a logits row:
-// f(x, value) with x the column.  16-byte loads when the slice start is
-// aligned and its length a multiple of the vector width, issued kBatch at a
-// time per thread before any is used, so a CTA keeps kThreads * kBatch * 16
-// bytes in flight.
+// Visit this CTA's slice [lo, hi) of a logits row.  Where the slice start
+// is 16-byte aligned and its length a multiple of the vector width, fv(x0,
+// v) gets kVec consecutive values from column x0 (x0 a multiple of kVec,
+// since lo is a multiple of 8); loads are issued kBatch at a time per
+// thread before any is used, so a CTA keeps kThreads * kBatch * 16 bytes in
+// flight (kB loads, for a caller that needs registers for its own work).
+// Otherwise f1(x, value) gets one column at a time.
 constexpr int kBatch = 8;
-template <typename T, typename F>
-__device__ __forceinline__ void for_slice(const T *row, int lo, int hi, F &&f) {
+template <int kB = kBatch, typename T, typename FV, typename F1>
+__device__ __forceinline__ void for_slice_v(const T *row, int lo, int hi, FV &&fv, F1 &&f1) {
   constexpr int kVec = 16 / sizeof(T);
   if (((hi - lo) % kVec) == 0 && (reinterpret_cast<uintptr_t>(row + lo) & 15) == 0) {
     const int nv = (hi - lo) / kVec;
     const uint4 *src = reinterpret_cast<const uint4 *>(row + lo);
-    for (int v0 = threadIdx.x; v0 < nv; v0 += kBatch * kThreads) {
-      uint4 u[kBatch];
+    for (int v0 = threadIdx.x; v0 < nv; v0 += kB * kThreads) {
+      uint4 u[kB];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
+      for (int i = 0; i < kB; ++i) {
         const int vi = v0 + i * kThreads;
         u[i] = vi < nv ? src[vi] : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
+      for (int i = 0; i < kB; ++i) {
         const int vi = v0 + i * kThreads;
         if (vi >= nv) break;
         float v[kVec];
@@ -194,17 +200,48 @@ __device__ __forceinline__ void for_slice(const T *row, int lo, int hi, F &&f) {
           v[2] = __uint_as_float(u[i].z);
           v[3] = __uint_as_float(u[i].w);
         }
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) f(lo + vi * kVec + j, v[j]);
+        fv(lo + vi * kVec, v);
       }
     }
   } else {
-    for (int x = lo + threadIdx.x; x < hi; x += kThreads) f(x, sv::to_f32(row[x]));
+    for (int x = lo + threadIdx.x; x < hi; x += kThreads) f1(x, sv::to_f32(row[x]));
   }
 }
-
+template <typename T, typename F>
+__device__ __forceinline__ void for_slice(const T *row, int lo, int hi, F &&f) {
+  constexpr int kVec = 16 / sizeof(T);
+  for_slice_v(
+      row, lo, hi,
+      [&](int x0, const float *v) {
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) f(x0 + j, v[j]);
+      },
+      f);
+}
+// The first column this thread visits in for_slice_v (hi if none).
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__device__ __forceinline__ int first_column(const T *row, int lo, int hi) {
+  constexpr int kVec = 16 / sizeof(T);
+  const bool vec = ((hi - lo) % kVec) == 0 && (reinterpret_cast<uintptr_t>(row + lo) & 15) == 0;
+  return min(hi, lo + (int)threadIdx.x * (vec ? kVec : 1));
+}
+
+// Uniform in (0, 1) for the sampling race from a 32-bit Philox word:
+// ((w >> 9) + 1/2) 2^-23, exact in float32.
+__device__ __forceinline__ float race_uniform(uint32_t w) {
+  return ((float)(w >> 9) + 0.5f) * 1.1920928955078125e-7f;
+}
+// Race key z + G, G = -log(-log u) a Gumbel variate.  The inner log keeps
+// full precision (u near 1 gives the largest G); the outer one takes the
+// fast log, whose absolute error is far below the keys' spacing.
+__device__ __forceinline__ float race_key(float z, uint32_t w) {
+  return z - __logf(-logf(race_uniform(w)));
+}
+
+// Two CTAs per SM (<= 64 registers), so that 4-CTA clusters of a batch
+// of 64 are all resident in one wave.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
     accept_kernel(int mode, const T *__restrict__ logits, int N, int V,
                   const int32_t *__restrict__ tok, const int32_t *__restrict__ parents,
                   const int32_t *__restrict__ first_child, const int32_t *__restrict__ next_sibling,
@@ -215,7 +252,10 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ int s_len, s_next, s_bonus;
   __shared__ int s_fc[kMaxNodes], s_ns[kMaxNodes], s_tok[kMaxNodes], s_par[kMaxNodes];
   __shared__ int s_ok[kMaxNodes], s_depth[kMaxNodes];
-  __shared__ int s_exc[kMaxNodes];
+  __shared__ int s_kid[kMaxNodes], s_nkid;   // children of the node being examined, in node order
+  __shared__ float s_kex[kMaxNodes];         // exp(z - m) of each child's token
+  __shared__ float s_ku[kMaxNodes];          // each child's accept draw
+  __shared__ int s_exc[kMaxNodes];           // tokens removed from the residual
   __shared__ int s_nexc;
 
   const uint32_t cta = blockIdx.x;  // rank in the cluster (cluster spans x)
@@ -223,6 +263,7 @@ __global__ void __launch_bounds__(kThreads)
   const int nc = (int)gridDim.x;  // the cluster spans x
   const int slice = ((V + nc - 1) / nc + 7) / 8 * 8;
   const int lo = min(V, (int)cta * slice), hi = min(V, lo + slice);
+  const int lane = threadIdx.x & 31;
   ClusterOps cl{red, 0, (uint32_t)nc};
 
   const int64_t row0 = (int64_t)b * N;
@@ -243,18 +284,34 @@ __global__ void __launch_bounds__(kThreads)
   const uint32_t st = (uint32_t)step;
   const T *base = logits + row0 * V;
 
+  // argmax with ties to the lowest column: each thread keeps its first
+  // largest value (it visits columns in increasing order), the cluster
+  // takes the largest (value, lowest column) key
   auto row_argmax = [&](const T *row) -> int {
-    unsigned long long best = 0ull;
+    float best = -INFINITY;
+    int bx = first_column(row, lo, hi);
     for_slice(row, lo, hi, [&](int x, float v) {
-      const unsigned long long k = sv::rank_key(v, (uint32_t)x);
-      best = k > best ? k : best;
+      if (v > best) {
+        best = v;
+        bx = x;
+      }
     });
-    return (int)sv::key_index(cl.max_u64(best));
+    return (int)sv::key_index(cl.max_u64(bx < hi ? sv::rank_key(best, (uint32_t)bx) : 0ull));
   };
-  auto row_max_z = [&](const T *row) -> float {
-    float m = -INFINITY;
-    for_slice(row, lo, hi, [&](int, float v) { m = fmaxf(m, v * inv_t); });
-    return cl.max(m);
+  // softmax statistics of z = logits / T over the row, one pass
+  auto row_stats = [&](const T *row, auto with_q) -> Stats {
+    Stats s = stats_empty();
+    for_slice(row, lo, hi, [&](int, float v) { stats_add<decltype(with_q)::value>(s, v * inv_t); });
+    return cl.stats(s);
+  };
+  // node v's children in node order into s_kid (thread 0; bounded walk)
+  auto list_children = [&](int v) {
+    if (threadIdx.x == 0) {
+      int n = 0;
+      for (int c = s_fc[v]; c >= 0 && c < N && n < kMaxNodes; c = s_ns[c]) s_kid[n++] = c;
+      s_nkid = n;
+    }
+    __syncthreads();
   };
 
   if (mode == SPEC_ACCEPT_GREEDY) {
@@ -263,7 +320,7 @@ __global__ void __launch_bounds__(kThreads)
       const int a = row_argmax(base + (int64_t)v * V);
       if (threadIdx.x == 0) {
         int nxt = -1;
-        for (int c = s_fc[v]; c >= 0 && c < N; c = s_ns[c])
+        for (int c = s_fc[v], n = 0; c >= 0 && c < N && n < kMaxNodes; c = s_ns[c], ++n)
           if (s_tok[c] == a) {
             nxt = c;
             break;
@@ -290,25 +347,18 @@ __global__ void __launch_bounds__(kThreads)
     for (int v = 0; v < N; ++v) {
       if (!s_ok[v] || s_fc[v] < 0) continue;  // uniform: shared flags, identical in every CTA
       const T *row = base + (int64_t)v * V;
-      const float m = row_max_z(row);
-      float S = 0.f, Q = 0.f;
-      for_slice(row, lo, hi, [&](int, float x) {
-        const float z = x * inv_t - m;
-        const float e = __expf(z);
-        S += e;
-        Q = fmaf(e, z, Q);
-      });
-      cl.sum2(S, Q);
-      if (threadIdx.x == 0) {
-        const float H = logf(S) - Q / S;
+      const Stats s = row_stats(row, std::true_type{});
+      list_children(v);
+      if (threadIdx.x < 32) {
+        const float H = logf(s.S) - s.Q / s.S;
         const float thr = fminf(eps, delta * expf(-H));
-        for (int c = s_fc[v]; c >= 0 && c < N; c = s_ns[c]) {
-          const int x = s_tok[c];
+        for (int j = lane; j < s_nkid; j += 32) {
+          const int c = s_kid[j], x = s_tok[c];
           if (x < 0 || x >= V) {
             sv::report(status, SPEC_DEV_BAD_TOKEN);
             continue;
           }
-          const float p = __expf(sv::to_f32(row[x]) * inv_t - m) / S;
+          const float p = __expf(sv::to_f32(row[x]) * inv_t - s.m) / s.S;
           s_ok[c] = p > thr;
         }
       }
@@ -333,39 +383,46 @@ __global__ void __launch_bounds__(kThreads)
     int v = 0;
     for (int guard = 0; guard < kMaxNodes; ++guard) {
       const T *row = base + (int64_t)v * V;
-      const float m = row_max_z(row);
-      float S = 0.f, unused = 0.f;
-      for_slice(row, lo, hi, [&](int, float x) { S += __expf(x * inv_t - m); });
-      cl.sum2(S, unused);
-      if (threadIdx.x == 0) {
-        int nxt = -1;
-        float removed = 0.f;
-        s_nexc = 0;
-        for (int c = s_fc[v]; c >= 0 && c < N; c = s_ns[c]) {
-          const int x = s_tok[c];
-          bool seen = false;
-          for (int e = 0; e < s_nexc; ++e) seen |= s_exc[e] == x;
-          float r = 0.f, ex = 0.f;
-          if (x < 0 || x >= V) {
-            sv::report(status, SPEC_DEV_BAD_TOKEN);
-            seen = true;
-          } else if (!seen) {
-            ex = __expf(sv::to_f32(row[x]) * inv_t - m);
-            r = ex / (S - removed);
-          }
+      const Stats s = row_stats(row, std::false_type{});
+      list_children(v);
+      if (threadIdx.x < 32) {
+        // every child's exp(z - m) and accept draw, in parallel
+        for (int j = lane; j < s_nkid; j += 32) {
+          const int c = s_kid[j], x = s_tok[c];
+          s_kex[j] = x >= 0 && x < V ? __expf(sv::to_f32(row[x]) * inv_t - s.m) : 0.f;
           const sv::u32x4 w = sv::philox4x32_10(sv::u32x4{(uint32_t)c, 0u, (uint32_t)b, st}, k0, k1);
-          const float u = (float)(w.x >> 8) * 5.9604644775390625e-8f;  // 2^-24
-          if (u < r) {
-            nxt = c;
-            break;
-          }
-          if (!seen) {
-            s_exc[s_nexc++] = x;
-            removed = removed + ex;
-          }
+          s_ku[j] = (float)(w.x >> 8) * 5.9604644775390625e-8f;  // 2^-24
         }
-        s_next = nxt;
-        if (nxt >= 0) s_path[s_len++] = nxt;
+        __syncwarp();
+        // the residual's bookkeeping, child after child: accept c iff
+        // u < r(tok c); otherwise tok c leaves the residual
+        if (lane == 0) {
+          int nxt = -1, nexc = 0;
+          float removed = 0.f;
+          for (int j = 0; j < s_nkid; ++j) {
+            const int c = s_kid[j], x = s_tok[c];
+            bool seen = false;
+            for (int e = 0; e < nexc; ++e) seen |= s_exc[e] == x;
+            float r = 0.f;
+            if (x < 0 || x >= V) {
+              sv::report(status, SPEC_DEV_BAD_TOKEN);
+              seen = true;
+            } else if (!seen) {
+              r = s_kex[j] / (s.S - removed);
+            }
+            if (s_ku[j] < r) {
+              nxt = c;
+              break;
+            }
+            if (!seen) {
+              s_exc[nexc++] = x;
+              removed = removed + s_kex[j];
+            }
+          }
+          s_nexc = nexc;
+          s_next = nxt;
+          if (nxt >= 0) s_path[s_len++] = nxt;
+        }
       }
       __syncthreads();
       if (s_next >= 0) {
@@ -373,21 +430,52 @@ __global__ void __launch_bounds__(kThreads)
         __syncthreads();
         continue;
       }
-      // residual sample: exponential race in log form over non-removed tokens
+      // residual sample: exponential race in log form over the tokens not
+      // removed.  One Philox call gives the draws of four consecutive
+      // tokens: token x uses word x % 4 of counter (x / 4, 256 + v, b, step).
       const int nexc = s_nexc;
-      unsigned long long best = 0ull;
-      for_slice(row, lo, hi, [&](int x, float val) {
-        for (int e = 0; e < nexc; ++e)
-          if (s_exc[e] == x) return;
+      float bk = -INFINITY;
+      int bx = hi;
+      auto race4 = [&](int x0, const float *z4, unsigned skip) {
         const sv::u32x4 w =
-            sv::philox4x32_10(sv::u32x4{(uint32_t)x, 256u + (uint32_t)v, (uint32_t)b, st}, k0, k1);
-        const float up = ((float)(w.x >> 9) + 0.5f) * 1.1920928955078125e-7f;  // 2^-23
-        const float g = -logf(-logf(up));
-        const float key = val * inv_t + g;
-        const unsigned long long k = sv::rank_key(key, (uint32_t)x);
-        best = k > best ? k : best;
-      });
-      best = cl.max_u64(best);
+            sv::philox4x32_10(sv::u32x4{(uint32_t)x0 >> 2, 256u + (uint32_t)v, (uint32_t)b, st}, k0, k1);
+        const uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+          if ((skip >> l) & 1u) continue;
+          const float key = race_key(z4[l] * inv_t, wd[l]);
+          if (key > bk) {
+            bk = key;
+            bx = x0 + l;
+          }
+        }
+      };
+      // (four loads in flight: the race's arithmetic hides the latency)
+      for_slice_v<4>(
+          row, lo, hi,
+          [&](int x0, const float *vals) {
+            constexpr int kVec = 16 / sizeof(T);
+            unsigned skip = 0;  // removed tokens among x0 .. x0 + kVec - 1
+            for (int e = 0; e < nexc; ++e) {
+              const unsigned d = (unsigned)(s_exc[e] - x0);
+              if (d < (unsigned)kVec) skip |= 1u << d;
+            }
+#pragma unroll
+            for (int q = 0; q < kVec / 4; ++q) race4(x0 + 4 * q, vals + 4 * q, skip >> (4 * q));
+          },
+          [&](int x, float val) {
+            for (int e = 0; e < nexc; ++e)
+              if (s_exc[e] == x) return;
+            const sv::u32x4 w =
+                sv::philox4x32_10(sv::u32x4{(uint32_t)x >> 2, 256u + (uint32_t)v, (uint32_t)b, st}, k0, k1);
+            const uint32_t wx = (x & 2) ? ((x & 1) ? w.w : w.z) : ((x & 1) ? w.y : w.x);
+            const float key = race_key(val * inv_t, wx);
+            if (key > bk) {
+              bk = key;
+              bx = x;
+            }
+          });
+      const unsigned long long best = cl.max_u64(bx < hi ? sv::rank_key(bk, (uint32_t)bx) : 0ull);
       if (threadIdx.x == 0) s_bonus = (int)sv::key_index(best);
       __syncthreads();
       break;
@@ -407,14 +495,42 @@ __global__ void __launch_bounds__(kThreads)
   cluster_barrier();  // partners' reads of this CTA's exchange slots are done
 }
 
+// CTAs per sequence (the kernel reads it from gridDim.x): enough to fill
+// the GPU at small batch, few enough that every cluster is resident in one
+// wave at large batch.  Sixteen is a non-portable cluster size; it is used
+// only where the device accepts it for this kernel.
+template <typename T>
+int cluster_size(int batch) {
+  if (batch >= 32) return 4;
+  if (batch >= 16) return 8;
+  if (cudaFuncSetAttribute(accept_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 8;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(16, batch);
+  cfg.blockDim = dim3(kThreads);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 16;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxPotentialClusterSize(&n, accept_kernel<T>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 8;
+  }
+  return n >= 16 ? 16 : 8;
+}
+
 template <typename T>
 int launch_accept(int mode, const void *logits, int batch, int n_nodes, int vocab, const int32_t *tok,
                   const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
                   float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
                   int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
-  // CTAs per sequence (the kernel reads it from gridDim.x): at batch >= 32
-  // four, so every sequence's cluster is resident in one wave
-  const int nc = batch >= 32 ? 4 : kMaxCluster;
+  const int nc = cluster_size<T>(batch);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nc, batch);
   cfg.blockDim = dim3(kThreads);

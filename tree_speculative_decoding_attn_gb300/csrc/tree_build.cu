@@ -128,12 +128,15 @@ __global__ void __launch_bounds__(kDynThreads)
   float *val = reinterpret_cast<float *>(ppar + M);                      // [M]
   float *conf = val + M;                                                 // [M]
   int *pdep = reinterpret_cast<int *>(conf + M);                         // [M]
+  int *ptok = pdep + M;                                                  // [M]
   __shared__ int kept_new[kMaxNodes];   // new (breadth-first) index of kept slot r
   __shared__ int new_par[kMaxNodes];    // parents by new index
   __shared__ int bad, s_dmax;
 
   const int b = blockIdx.x, t = threadIdx.x;
   const int64_t prow = (int64_t)b * M;
+  // every global load is issued here, so their latencies overlap
+  const int P = t < N ? prefix_len[b] : 0;
   if (t == 0) {
     bad = 0;
     s_dmax = 0;
@@ -142,6 +145,7 @@ __global__ void __launch_bounds__(kDynThreads)
   for (int i = t; i < M; i += kDynThreads) {
     const int p = pool_parent[prow + i];
     const float c = pool_conf[prow + i];
+    ptok[i] = pool_tok[prow + i];
     ppar[i] = p;
     conf[i] = c;
     if (i == 0 ? p != -1 : (p < 0 || p >= i || !(c >= 0.f && c <= 1.f))) atomicOr(&bad, 1);
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kDynThreads)
   if (t < N) {
     const int ni = kept_new[t];
     const int64_t row = (int64_t)b * N;
-    tok[row + ni] = pool_tok[prow + my_pool];
+    tok[row + ni] = ptok[my_pool];
     parents_out[row + ni] = new_par[ni];
     if (pool_index) pool_index[row + ni] = my_pool;
     if (val_out) val_out[row + ni] = val[my_pool];
@@ -286,7 +290,7 @@ __global__ void __launch_bounds__(kDynThreads)
   __syncthreads();
   if (t < N) {
     int d;
-    emit_tree_arrays(new_par, kids, t, prefix_len[b], (int64_t)b * N, depth, pos, anc, first_child,
+    emit_tree_arrays(new_par, kids, t, P, (int64_t)b * N, depth, pos, anc, first_child,
                      next_sibling, &d);
   }
 }
@@ -312,7 +316,7 @@ int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const 
   if (M > kMaxPool) return SPEC_ERR_UNSUPPORTED;
   size_t M2 = 1;
   while (M2 < (size_t)M) M2 <<= 1;
-  const size_t smem = M2 * 8 + (size_t)M * (4 + 4 + 4 + 4);  // key (sort width), parent, value, conf, depth
+  const size_t smem = M2 * 8 + (size_t)M * (4 + 4 + 4 + 4 + 4);  // key (sort width), parent, value, conf, depth, token
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(build_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
