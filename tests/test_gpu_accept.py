@@ -209,6 +209,39 @@ def test_commit_bitwise_with_canaries(dtype, layers):
     np.testing.assert_array_equal(host(plen), rlen)
 
 
+@pytest.mark.parametrize("mode", [sv.TYPICAL, sv.REJECT])
+def test_out_of_range_child_token_is_reported_and_never_accepted(mode):
+    shape = SHAPES[0]                                  # parents [-1, 0, 0, 1, 2]
+    B, V = 2, 1000
+    t = _tree_batch(shape, B, V, 80)
+    lg = _logits(shape, t, B, V, 81, False)
+    t["gpu"]["tok"][0, 1] = V + 5                      # sequence 0, node 1: no such token
+    cap = shape.n_levels + 1
+    got = _accept(mode, lg, t, cap, temperature=1.0, eps=0.0, delta=0.0, seed=5, step=0)
+    assert got[3] == sv.DEV_BAD_TOKEN
+    assert 1 not in got[1][0].tolist()
+
+
+def test_commit_bad_path_is_reported_and_skipped():
+    B, Hkv, S, N, D = 3, 2, 32, 8, 64
+    g = np.random.default_rng(9)
+    kc, vc = (g.standard_normal((B, Hkv, S, D)).astype(np.float32) for _ in range(2))
+    kt, vt = (g.standard_normal((B, Hkv, N, D)).astype(np.float32) for _ in range(2))
+    prefix = np.array([4, 5, 6], np.int32)
+    acc_len = np.array([2, 2, 1], np.int32)
+    acc_path = np.array([[0, 1, 3], [0, 9, 2], [0, 2, -1]], np.int32)   # node 9 does not exist (N = 8)
+    dkc, dvc = dev(kc), dev(vc)
+    plen, st = i32(prefix), zeros_i32(1)
+    sv.kv_commit(dkc, dvc, dev(kt), dev(vt), i32(acc_len), i32(acc_path), plen, plen, st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == sv.DEV_BAD_PATH
+    ok = np.array([True, False, True])
+    rk, rv, rlen = COM.kv_commit(kc, vc, kt, vt, prefix, np.where(ok, acc_len, -1), acc_path)
+    np.testing.assert_array_equal(host(dkc), rk)
+    np.testing.assert_array_equal(host(dvc), rv)
+    np.testing.assert_array_equal(host(plen), np.where(ok, rlen, prefix))
+
+
 # ---------------------------------------------------------------- expansion
 
 
