@@ -277,7 +277,7 @@ class GpuStep:
             1, None))
         self.stages.append(("kv_commit", lambda: sv.kv_commit(
             self.kc, self.vc, self.kt, self.vt, self.acc_len, self.acc_path, self.d_prefix, self.new_prefix,
-            self.status), 2, None))
+            self.status), 1, None))
 
     # ---- running ---------------------------------------------------------
     def launches_per_step(self):
