@@ -9,6 +9,7 @@ from scipy import stats
 from oracle import accept as ACC
 from oracle import attention as A
 from oracle import commit as C
+from oracle import expected as E
 from oracle import tree as T
 from tree_speculative_decoding_attn_gb300 import synth
 
@@ -48,6 +49,43 @@ def test_greedy_argmax_ties_go_to_lowest_id():
     tok = np.array([[0, 7, 3]])
     acc_len, acc_path, bonus = ACC.accept_greedy(logits, tok, fc, ns, 2)
     assert acc_path[0, :2].tolist() == [0, 2]       # the child holding token 3
+
+
+def test_greedy_mean_length_under_planted_agreement_matches_the_tree_form():
+    """Cartesian tree 3 x 2 x 2 with distinct sibling tokens, float32 target
+    logits N(0, 2) and planted agreement: at a node on level l the
+    generator raises one uniformly chosen child's token above the row max
+    with probability r_l; otherwise the argmax is uniform over the V tokens.
+    So the child of rank r is the argmax with probability r_l / n_l +
+    (1 - r_l) / V, and the mean accepted length (root excluded) over many
+    seeded sequences must match the tree form of the expected length minus
+    the root, within a 99% interval."""
+    branching, V, B = (3, 2, 2), 64, 10000
+    parents, rank, depth, level = [-1], [0], [0], [0]
+    for d, s in enumerate(branching, start=1):
+        nxt = []
+        for v in level:
+            for r in range(s):
+                parents.append(v); rank.append(r); depth.append(d); nxt.append(len(parents) - 1)
+        level = nxt
+    parents, rank, depth = np.array(parents), np.array(rank), np.array(depth)
+    N = len(parents)
+    cand = synth.candidate_tokens(11, B, len(branching) + 1, max(branching), V)
+    tok = np.empty((B, N), np.int64)
+    tok[:, 0] = 0
+    for i in range(1, N):
+        tok[:, i] = cand[:, depth[i] - 1, rank[i]]
+    lg = synth.target_logits(12, B, N, V, 2.0, bf16=False)
+    synth.plant_agreement(13, lg, parents, depth, tok, bf16=False)
+    _, fc, ns, _ = _tree_arrays(parents, B)
+    acc_len, _, _ = ACC.accept_greedy(lg, tok, fc, ns, path_cap=len(branching) + 1)
+    rates = synth.PLANT_RATES
+    p_rank = [[rates[d] / s + (1 - rates[d]) / V] * s for d, s in enumerate(branching)]
+    want = E.expected_len_tree(parents, rank, depth, p_rank) - 1.0
+    half = 2.576 * acc_len.std(ddof=1) / math.sqrt(B)
+    assert abs(acc_len.mean() - want) <= half, (acc_len.mean(), want, half)
+    # and the process is not degenerate: every length 0..3 occurs
+    assert set(np.unique(acc_len).tolist()) == {0, 1, 2, 3}
 
 
 def _tiny_model(seed, V=40, d=32, Hq=4, Hkv=2, Dh=8):
