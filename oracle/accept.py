@@ -209,3 +209,109 @@ def reject_outcome_probs(probs, tok, first_child, next_sibling):
 
     visit(0, (0,), 1.0)
     return out
+
+
+# ------------------------------------------------------------------------
+# Rejection with stochastic siblings (the children of a node drawn
+# independently from the drafter's distribution q at that node).
+#
+# "Drafters: ...", section "Why the answer does not change": keep a drafted
+# token x with probability min(1, p(x)/q(x)); on rejection continue from
+# the target with the drafter's probabilities subtracted, max(0, p - q)
+# renormalised.  Applied to the siblings one after another, each test uses
+# the residual left by the previous rejections: r <- norm(max(0, r - q)).
+# With the siblings independent draws from q this keeps the output
+# distribution the target's (pinned by exact enumeration in the tests).
+# q_v = softmax(draft_logits[v] / T), the same temperature as the target.
+# ------------------------------------------------------------------------
+
+
+def _residual_after_rejection(r, q):
+    """norm(max(0, r - q)); None when nothing is left (then the rejection
+    had probability 0)."""
+    res = np.maximum(r - q, 0.0)
+    z = res.sum()
+    return res / z if z > 0 else None
+
+
+def reject_stochastic_outcome_probs(probs, qprobs, tok, first_child, next_sibling):
+    """Exact distribution of (accepted path, bonus token) for one sequence
+    whose child tokens are given, by recursion over every accept/reject
+    branch (no random numbers).  ``probs[v]`` / ``qprobs[v]``: target and
+    drafter distributions at node v (float64).  Returns {(path, bonus): p}."""
+    out = {}
+
+    def visit(v, path, mass):
+        r = np.array(probs[v], np.float64)
+        r = r / r.sum()
+        q = np.array(qprobs[v], np.float64)
+        q = q / q.sum()
+        for c in _children(first_child, next_sibling, v):
+            x = int(tok[c])
+            a = 1.0 if q[x] <= 0 else min(1.0, r[x] / q[x])
+            if a > 0:
+                visit(c, path + (c,), mass * a)
+            if a >= 1.0:
+                return
+            mass *= 1.0 - a
+            r = _residual_after_rejection(r, q)
+            if r is None:
+                return
+        for x in np.nonzero(r)[0]:
+            key = (path, int(x))
+            out[key] = out.get(key, 0.0) + mass * r[x]
+
+    visit(0, (0,), 1.0)
+    return out
+
+
+def accept_reject_stochastic(logits, draft_logits, tok, first_child, next_sibling, seed, step, T, path_cap,
+                             dtype=np.float32):
+    """The RNG-driven walk of the rule above: child c with token x is kept
+    iff u_c < r(x) / q(x) (u_c the accept draw of the rejection rule); the
+    bonus is the exponential race argmax_x (log r(x) + G_x) over the tokens
+    with r(x) > 0, G_x = -log(-log u'_x).  Returns (acc_len, acc_path, bonus,
+    near_ties[B])."""
+    B, N, V = logits.shape
+    paths, bonus, near = [], [], np.zeros(B, np.int64)
+    for b in range(B):
+        v, path = 0, [0]
+        while True:
+            z = np.asarray(logits[b, v], dtype) / dtype(T)
+            e = np.exp(z - z.max())
+            r = e / e.sum(dtype=dtype)
+            zq = np.asarray(draft_logits[b, v], dtype) / dtype(T)
+            eq = np.exp(zq - zq.max())
+            q = eq / eq.sum(dtype=dtype)
+            chosen = -1
+            for c in _children(first_child[b], next_sibling[b], v):
+                x = int(tok[b, c])
+                ratio = np.inf if q[x] <= 0 else float(r[x] / q[x])
+                u = float(rng.uniform_accept(seed, b, step, c))
+                if np.isfinite(ratio) and abs(u - ratio) <= NEAR_REJECT * max(ratio, 1e-30):
+                    near[b] += 1
+                if u < ratio:
+                    chosen = c
+                    break
+                r = _residual_after_rejection(r.astype(np.float64), q.astype(np.float64))
+                if r is None:       # a rejection of probability 0 (rounding): nothing to sample from
+                    r = e / e.sum(dtype=dtype)
+                    break
+                r = r.astype(dtype)
+            if chosen == -1:
+                u = rng.uniform_race(seed, b, step, v, np.arange(V))
+                g = -np.log(-np.log(u.astype(dtype)))
+                with np.errstate(divide="ignore"):
+                    key = (np.log(r) + g).astype(dtype)
+                key[r <= 0] = -np.inf
+                x = int(np.argmax(key))
+                top2 = np.partition(key, -2)[-2:]
+                if abs(float(top2[1] - top2[0])) <= NEAR_REJECT * max(1.0, abs(float(top2[1]))):
+                    near[b] += 1
+                bonus.append(x)
+                break
+            v = chosen
+            path.append(v)
+        paths.append(path)
+    acc_len, acc_path, bon = _pack(paths, bonus, path_cap)
+    return acc_len, acc_path, bon, near

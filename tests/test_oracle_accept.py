@@ -365,6 +365,113 @@ def test_rejection_walk_frequencies_match_exact_enumeration():
     assert stats.chi2.sf(chi2, len(keys) - 1) > 1e-3
 
 
+def _contexts(parents, tok):
+    """Tokens on each node's path after the root."""
+    ctx = {}
+    for i in range(len(parents)):
+        path, u = [], i
+        while u > 0:
+            path.append(int(tok[u])); u = parents[u]
+        ctx[i] = tuple(path[::-1])
+    return ctx
+
+
+@pytest.mark.parametrize("V,parents", [(3, [-1, 0, 0]), (3, [-1, 0, 0, 1, 2]), (3, [-1, 0, 0, 0, 1, 1, 4]),
+                                       (4, [-1, 0, 1, 2]), (3, [-1, 0, 0, 0, 0])])
+def test_stochastic_sibling_rejection_preserves_the_target_distribution_exactly(V, parents):
+    """Siblings drawn independently from the drafter's q at their parent's
+    context, each tested against the residual the earlier rejections left:
+    averaged over every draw and every accept/reject branch, (accepted
+    tokens + bonus) extended by target sampling has exactly the target's
+    joint distribution ("Drafters: ...", section "Why the answer does not
+    change": min(1, p/q), then the target minus the drafter)."""
+    n = len(parents)
+    _, fc, ns, t = _tree_arrays(parents)
+    Lmax = int(t["depth"].max()) + 1
+    ptab = _target_table(10 * V + n, V, Lmax)
+    qtab = _target_table(10 * V + n + 1, V, Lmax)        # the drafter: another seeded model
+    joint = {}
+    for toks in itertools.product(range(V), repeat=n - 1):
+        tok = np.array((0,) + toks)
+        ctx = _contexts(parents, tok)
+        weight = 1.0
+        for i in range(1, n):
+            weight *= _softmax64(qtab[ctx[parents[i]]])[tok[i]]
+        probs = {i: _softmax64(ptab[ctx[i]]) for i in range(n)}
+        qprobs = {i: _softmax64(qtab[ctx[i]]) for i in range(n)}
+        out = ACC.reject_stochastic_outcome_probs(probs, qprobs, tok, fc[0], ns[0])
+        assert sum(out.values()) == pytest.approx(1.0, abs=1e-12)
+        for (path, bonus), pr in out.items():
+            frontier = {tuple(int(tok[i]) for i in path[1:]) + (bonus,): weight * pr}
+            while len(next(iter(frontier))) < Lmax:
+                nf = {}
+                for sq, pq in frontier.items():
+                    tp = _softmax64(ptab[sq])
+                    for x in range(V):
+                        nf[sq + (x,)] = nf.get(sq + (x,), 0.0) + pq * tp[x]
+                frontier = nf
+            for sq, pq in frontier.items():
+                joint[sq] = joint.get(sq, 0.0) + pq
+    for sq in itertools.product(range(V), repeat=Lmax):
+        ref = 1.0
+        for j in range(Lmax):
+            ref *= _softmax64(ptab[sq[:j]])[sq[j]]
+        assert joint.get(sq, 0.0) == pytest.approx(ref, abs=1e-12)
+
+
+@pytest.mark.parametrize("length", [1, 2, 3])
+def test_stochastic_rule_with_a_point_mass_drafter_is_the_deterministic_rule(length):
+    """On a chain, a drafter certain of each drafted token (q = point mass)
+    turns min(1, r/q) into r(x) and norm(max(0, r - q)) into r with x
+    removed: the two rules give the same outcome distribution."""
+    parents = list(range(-1, length))
+    V = 4
+    _, fc, ns, _t = _tree_arrays(parents)
+    g = np.random.default_rng(length)
+    for trial in range(5):
+        tok = np.concatenate([[0], g.integers(0, V, length)])
+        probs = {i: _softmax64(g.standard_normal(V) * 1.5) for i in range(length + 1)}
+        qprobs = {}
+        for i in range(length + 1):
+            q = np.full(V, 0.25)
+            if i < length:
+                q = np.zeros(V); q[tok[i + 1]] = 1.0
+            qprobs[i] = q
+        a = ACC.reject_stochastic_outcome_probs(probs, qprobs, tok, fc[0], ns[0])
+        b = ACC.reject_outcome_probs(probs, tok, fc[0], ns[0])
+        for k in set(a) | set(b):
+            assert a.get(k, 0.0) == pytest.approx(b.get(k, 0.0), abs=1e-12)
+
+
+@pytest.mark.slow
+def test_stochastic_rejection_walk_frequencies_match_exact_enumeration():
+    """The RNG-driven walk (float32 decisions, Philox draws) against the
+    exact outcome distribution for fixed drafted tokens, chi-square."""
+    parents = [-1, 0, 0, 1, 2]
+    V = 4
+    _, fc, ns, t = _tree_arrays(parents)
+    tok = np.array([[2, 0, 0, 3, 1]])                    # two siblings drew the same token
+    g = np.random.default_rng(6)
+    logits = (g.standard_normal((1, 5, V)) * 1.2).astype(np.float32)
+    draft = (g.standard_normal((1, 5, V)) * 1.2).astype(np.float32)
+    probs = {i: _softmax64(logits[0, i].astype(np.float64)) for i in range(5)}
+    qprobs = {i: _softmax64(draft[0, i].astype(np.float64)) for i in range(5)}
+    exact = ACC.reject_stochastic_outcome_probs(probs, qprobs, tok[0], fc[0], ns[0])
+    keys = sorted(k for k, v in exact.items() if v > 0)
+    counts = dict.fromkeys(keys, 0)
+    n_draws = 20000
+    for step in range(n_draws):
+        acc_len, acc_path, bonus, _ = ACC.accept_reject_stochastic(logits, draft, tok, fc, ns, seed=78, step=step,
+                                                                   T=1.0, path_cap=3)
+        key = (tuple(int(x) for x in acc_path[0, : acc_len[0] + 1]), int(bonus[0]))
+        counts[key] += 1
+    obs = np.array([counts[k] for k in keys], float)
+    exp_ = np.array([exact[k] for k in keys]) * n_draws
+    assert obs.sum() == n_draws
+    chi2 = ((obs - exp_) ** 2 / exp_).sum()
+    assert stats.chi2.sf(chi2, len(keys) - 1) > 1e-3
+
+
 def test_rejection_with_certain_target_accepts_and_leaf_bonus_is_target_sample():
     parents = [-1, 0, 1]
     _, fc, ns, t = _tree_arrays(parents)
