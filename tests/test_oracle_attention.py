@@ -53,7 +53,8 @@ def test_chain_tree_equals_causal_attention(G):
             np.testing.assert_allclose(o[b, :, h], ref, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("seed,n,caps", [(2, 5, None), (3, 24, (4, 3, 2)), (4, 40, (6, 3, 2, 2))])
+@pytest.mark.parametrize("seed,n,caps", [(2, 5, None), (3, 24, (4, 3, 2)), (4, 40, (6, 3, 2, 2)),
+                                         (5, 256, (8, 8, 4, 2))])
 def test_every_node_equals_attention_over_its_path(seed, n, caps):
     shape = synth.p4_example() if caps is None else synth.random_tree(seed, n, caps)
     B, Hkv, G, D, P = 2, 2, 2, 8, 11
