@@ -2,12 +2,17 @@
 """Throughput of the tree-verification step (Medusa / EAGLE) on GB300.
 
 One step = one pass of the whole hot path over one batch of synthetic
-inputs resident in HBM: Medusa heads -> top-s -> static tree -> tree
-attention (one layer) -> LM head over the tree -> greedy acceptance -> KV
-commit, for the Vicuna-7B-shaped workload (batch 1, 32 heads, head_dim 128,
-prefix 2048, 4 heads of hidden 4096, vocabulary 32000, 64-node tree).
-Other workloads: --workload {tiny_exact, vicuna7b_medusa, llama8b_eagle2,
-llama70b_serving, long_context}.
+inputs resident in HBM.  The default workload is 70B-shaped batched serving
+(batch 64, 64 query / 8 KV heads, head_dim 128, bf16, prefix 4096, a 32-node
+static tree of 4 levels, vocabulary 128256): static tree build -> tree
+attention (one layer) -> greedy acceptance -> batched KV commit.  Other
+workloads: --workload {tiny_exact, vicuna7b_medusa, llama8b_eagle2,
+llama70b_serving, long_context}; the default run also reports the full step
+rate of each of the other four under "workloads".
+
+Timing: the K steps are captured once as a CUDA graph; the graph is replayed
+back to back for at least --min-seconds (so the clock sampler sees the GPU
+under load) and the median replay, divided by K, is the step time.
 
 Prints one JSON line (rank 0).  N > 1 (torchrun) runs independent replicas
 (no collective on the data path; weak scaling).  ``--impl reference`` times
@@ -35,11 +40,11 @@ if "reference" in sys.argv and "--impl" in sys.argv:
 
 import numpy as np  # noqa: E402
 
-DEFAULT = "vicuna7b_medusa"
+DEFAULT = "llama70b_serving"
 L2_BYTES = 129 * 1024 * 1024
 
-# DRAM bytes (read + write) per call of a stage, from one ncu capture
-# (profiles/gemv_medusa_heads_vicuna7b.md), valid only while the kernel
+# DRAM bytes (read + write) per call of a stage, from one ncu capture of
+# that stage's kernel at the workload's shape, valid only while the kernel
 # source is the one the counters were taken on: (source, sha256 prefix,
 # bytes) keyed by (workload, stage).
 NCU_TRAFFIC = {
@@ -463,13 +468,14 @@ class OracleStep:
         return sum(parts.values()), parts
 
 
-def _cpu_baseline_subprocess(name: str, reps: int = 2):
+def _cpu_baseline_subprocess(name: str, reps: int = 3):
     """Run the oracle timing in a fresh single-threaded process (spawned,
     not forked from this CUDA process)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
             f"o = bench.OracleStep({name!r}); r = [o.step() for _ in range({reps})]; "
-            f"print(json.dumps({{'s': min(x[0] for x in r), 'sample': o.sample, 'parts': r[0][1]}}))")
+            f"import statistics; print(json.dumps({{'s': statistics.median(x[0] for x in r), 'reps': len(r), "
+            f"'sample': o.sample, 'parts': r[0][1]}}))")
     out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     if out.returncode != 0:
         return None, out.stderr[-400:]
@@ -509,46 +515,129 @@ def job_rate(steps_per_rank: int, world: int, max_seconds: float) -> float:
     return world * steps_per_rank / max_seconds
 
 
+def workload_config(w, world: int) -> dict:
+    """The ``config`` object of a bench line (both arms print the same one)."""
+    return {"workload": w.name, "batch": w.batch, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim,
+            "prefix": list(w.prefix), "n_nodes": w.n_nodes, "vocab": w.vocab, "accept": w.accept,
+            "tree": w.tree, "parallelism": f"replicas x{world}",
+            "l2": "inputs exceed L2 (weights and/or KV cache streamed each step)"}
+
+
 def run_reference(args):
     # rank 0 alone times the oracle; other ranks of a torchrun launch exit
     if int(os.environ.get("RANK", "0")) != 0:
         return
     from tree_speculative_decoding_attn_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    times = []
     o = OracleStep(args.workload)
     for _ in range(min(args.warmup, 1)):  # the oracle has nothing to warm beyond one pass
         o.step()
-    # every step is the same deterministic sample, so the timed oracle steps
-    # stop at a bounded budget of CPU time (the line says how many ran)
-    budget_s, spent = 150.0, 0.0
-    while len(times) < args.steps and (not times or spent < budget_s):
+    # each step runs the oracle on the same bounded sample of the workload;
+    # the timed steps stop at a bounded budget of CPU time (the line says how
+    # many ran)
+    budget_s, spent, measured, extrap = 150.0, 0.0, [], []
+    while len(measured) < args.steps and (not measured or spent < budget_s):
         t0 = time.perf_counter()
         s, _ = o.step()
-        spent += time.perf_counter() - t0
-        times.append(s)
-    sample = f"{o.sample}; {len(times)} of {args.steps} steps timed (identical deterministic steps)"
-    t = sum(times) / len(times)
-    val = 1.0 / t
+        dt = time.perf_counter() - t0
+        spent += dt
+        measured.append(dt)
+        extrap.append(s)
+    sample = f"{o.sample}; {len(measured)} of {args.steps} steps timed (identical deterministic steps)"
+    t_full = statistics.median(extrap)
+    val = 1.0 / t_full
     line = {"impl": "reference", "metric": "tree-verify steps/s", "value": val, "unit": "steps/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "n_gpus": args.gpus, "steps": len(measured), "warmup": args.warmup,
+            # wall time of one sampled oracle step (what the timed region ran)
+            "ms_per_step": statistics.median(measured) * 1e3,
+            # one whole-workload step, extrapolated from the sample; value = 1 / this
+            "ms_per_step_extrapolated": t_full * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "batch": w.batch, "prefix": list(w.prefix), "n_nodes": w.n_nodes},
+            "config": workload_config(w, 1),
             "cpu_baseline": {"value": val, "unit": "steps/s", "cores": 1, "kind": "oracle",
-                             "sample": sample + " (per step; extrapolated by sampled fraction)"},
+                             "sample": sample + " (value extrapolated from the sample by the sampled fraction "
+                                                "of each stage)"},
             "e2e": {"value": val, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def capture(step, steps: int, with_events: bool):
+    """CUDA graph of ``steps`` verify steps (optionally with a CUDA event
+    before every stage, as external record nodes); returns (graph, events)."""
+    import torch
+    n_st = len(step.stages)
+    evs = None
+    if with_events:
+        mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
+        evs = [[mk_ev() for _ in range(n_st + 1)] for _ in range(steps)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for k in range(steps):
+            step.run(evs[k] if evs else None)
+    torch.cuda.synchronize()
+    return graph, evs
+
+
+def replay_median(graph, min_seconds: float, min_replays: int = 5):
+    """Replays ``graph`` back to back for at least ``min_seconds``; returns
+    (median replay seconds, replays, wall seconds).  Each replay is timed by
+    CUDA events on the current stream."""
+    import torch
+    times, t_wall = [], time.perf_counter()
+    pend = []
+    while len(times) + len(pend) < min_replays or time.perf_counter() - t_wall < min_seconds:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); graph.replay(); e1.record()
+        pend.append((e0, e1))
+        if len(pend) >= 8:  # bound the queue; keeps the GPU busy back to back
+            pend[0][1].synchronize()
+            a, b = pend.pop(0)
+            times.append(a.elapsed_time(b) * 1e-3)
+    torch.cuda.synchronize()
+    times += [a.elapsed_time(b) * 1e-3 for a, b in pend]
+    return statistics.median(times), len(times), time.perf_counter() - t_wall
+
+
+def measure_workload(name: str, dev, steps: int, warmup: int, min_seconds: float):
+    """Full verify step of one workload: step rate (median graph replay),
+    per-stage times (from a second graph with stage events) and the
+    attention stage's HBM rate."""
+    import torch
+    from tree_speculative_decoding_attn_gb300 import specverify as sv
+    step = GpuStep(name, dev)
+    for _ in range(warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"{name}: device status {sv.spec_status_string(int(step.status.item()))}")
+    graph, _ = capture(step, steps, False)
+    t_rep, reps, _ = replay_median(graph, min_seconds)
+    sgraph, evs = capture(step, steps, True)
+    sgraph.replay()
+    torch.cuda.synchronize()
+    n_st = len(step.stages)
+    stage_s = {step.stages[i][0]: sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(steps)) * 1e-3 / steps
+               for i in range(n_st)}
+    del graph, sgraph
+    res = {"steps_per_s": steps / t_rep, "ms_per_step": t_rep / steps * 1e3, "replays": reps,
+           "stages_us": {k: v * 1e6 for k, v in stage_s.items()}, "gpu_launches_per_step": step.launches_per_step()}
+    if "tree_attn" in stage_s:
+        res["attention_gbps"] = step.attn_bytes / stage_s["tree_attn"] / 1e9
+    return step, res, stage_s, t_rep
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=DEFAULT)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="replay the captured K-step graph back to back for at least this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-attention", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the other workloads' step rates and the attention-only timings")
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling cases)")
     ap.add_argument("--attention-only", action="store_true",
                     help="time tree_attn_verify alone at the workload's shape (profiling runs)")
@@ -560,12 +649,12 @@ def main():
     dist, rank, local, ws = _dist()
     import torch
     from tree_speculative_decoding_attn_gb300 import specverify as sv
+    from tree_speculative_decoding_attn_gb300 import synth
     sv.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.batch:
         import dataclasses
-        from tree_speculative_decoding_attn_gb300 import synth
         synth.WORKLOADS[args.workload] = dataclasses.replace(synth.WORKLOADS[args.workload], batch=args.batch)
     hbm, tc_peak, peak_kind = _peaks()
     if args.attention_only:
@@ -573,54 +662,38 @@ def main():
         r.update(workload=args.workload, frac_hbm=r["gbps"] / hbm, peak_kind=peak_kind)
         print(json.dumps({"attention_only": r}), flush=True)
         return
-    step = GpuStep(args.workload, dev)
-    stream = torch.cuda.current_stream()
+    w = synth.WORKLOADS[args.workload]
 
-    # warm-up
+    # timed region: the K-step graph replayed for >= min_seconds, barrier and
+    # synchronize on both sides, clocks sampled throughout
+    step = GpuStep(args.workload, dev)
     for _ in range(args.warmup):
         step.run()
     torch.cuda.synchronize()
     assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
-
-    # timed region: K steps, per-stage events on the launch stream.  The K
-    # steps are captured once into a CUDA graph (events as external record
-    # nodes) and replayed as one launch, so host launch latency between the
-    # library's kernels is not part of the measurement; without graph event
-    # support the steps run eagerly.
-    n_st = len(step.stages)
-    try:
-        mk_ev = lambda: torch.cuda.Event(enable_timing=True, external=True)
-        evs = [[mk_ev() for _ in range(n_st + 1)] for _ in range(args.steps)]
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for k in range(args.steps):
-                step.run(evs[k])
-        mode = "cuda_graph"
-    except (TypeError, RuntimeError):
-        torch.cuda.synchronize()
-        graph = None
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_st + 1)] for _ in range(args.steps)]
-        mode = "eager"
+    graph, _ = capture(step, args.steps, False)
+    graph.replay()  # one untimed replay
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
-        if graph is not None:
-            graph.replay()
-        else:
-            for k in range(args.steps):
-                step.run(evs[k])
-        torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall
+        t_rep, reps, t_wall = replay_median(graph, args.min_seconds)
     if dist:
         dist.barrier()
     assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
-    total = evs[0][0].elapsed_time(evs[-1][-1]) * 1e-3
+    t_rep = job_max(t_rep, dist, dev)
+    steps_per_s = job_rate(args.steps, ws, t_rep)
+    del graph
+
+    # per-stage times: a second graph of the same K steps with a CUDA event
+    # before every stage (the events cost a little; the headline above has none)
+    sgraph, evs = capture(step, args.steps, True)
+    sgraph.replay()
+    torch.cuda.synchronize()
+    n_st = len(step.stages)
     stage_s = {step.stages[i][0]: sum(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                * 1e-3 / args.steps for i in range(n_st)}
-    total = job_max(total, dist, dev)
-    steps_per_s = job_rate(args.steps, ws, total)
+    del sgraph
     dyn, mean_acc = step.dynamic_bytes()
 
     # roofline for the dominant stage
@@ -632,7 +705,8 @@ def main():
     if dom_bytes:
         ach = dom_bytes / stage_s[dom] / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                "traffic": measured_traffic(args.workload, dom), "peak_kind": peak_kind, "bytes_per_launch": dom_bytes}
+                "traffic": measured_traffic(args.workload, dom), "peak_kind": peak_kind,
+                "bytes_per_launch": dom_bytes, "launch_us": stage_s[dom] * 1e6}
 
     # end-to-end leg through the public API: per-step H2D of this pass's
     # inputs from pinned memory, D2H of the accepted path
@@ -656,18 +730,28 @@ def main():
            "d2h_bytes_per_step": d2h_bytes}
 
     launches = step.launches_per_step()
-    attn_cfg = stage_s.get("tree_attn")
-    attention = {"workload": args.workload, "us": attn_cfg * 1e6, "gbps": step.attn_bytes / attn_cfg / 1e9,
-                 "frac_hbm": step.attn_bytes / attn_cfg / 1e9 / hbm}
-    extra = {}
-    if rank == 0 and not args.no_attention:
-        del step
-        torch.cuda.empty_cache()
+    attn_s = stage_s.get("tree_attn")
+    attention = {"workload": args.workload, "us": attn_s * 1e6, "gbps": step.attn_bytes / attn_s / 1e9,
+                 "frac_hbm": step.attn_bytes / attn_s / 1e9 / hbm, "bytes": step.attn_bytes}
+    del step
+    torch.cuda.empty_cache()
+
+    extra, extra_attn = {}, {}
+    if rank == 0 and not args.no_extra:
+        for nm in synth.WORKLOADS:
+            if nm == args.workload:
+                continue
+            st, res, _, _ = measure_workload(nm, dev, args.steps, 3, min_seconds=0.2)
+            if "attention_gbps" in res:
+                res["attention_frac_hbm"] = res["attention_gbps"] / hbm
+            extra[nm] = res
+            del st
+            torch.cuda.empty_cache()
         for nm in ("llama8b_eagle2", "llama70b_serving", "long_context"):
             r = attention_only(nm, dev, steps=20, warmup=3)
             r["frac_hbm"] = r["gbps"] / hbm
             r["frac_tensor"] = r["tflops"] / tc_peak
-            extra[nm] = r
+            extra_attn[nm] = r
             torch.cuda.empty_cache()
 
     cpu = None
@@ -675,27 +759,24 @@ def main():
         res, err = _cpu_baseline_subprocess(args.workload)
         if res:
             cpu = {"value": 1.0 / res["s"], "unit": "steps/s", "cores": 1, "kind": "oracle",
-                   "sample": res["sample"] + " (one step, extrapolated by sampled fraction of each stage)"}
+                   "sample": res["sample"] + f" (median of {res['reps']} steps, each extrapolated by the sampled "
+                                             "fraction of each stage)"}
         else:
             cpu = {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle", "sample": f"failed: {err}"}
 
     if rank == 0:
-        from tree_speculative_decoding_attn_gb300 import synth
-        w = synth.WORKLOADS[args.workload]
         line = {"metric": "tree-verify steps/s", "value": steps_per_s, "unit": "steps/s", "n_gpus": ws,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_rep / args.steps * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic (seeded; random weights)",
-                "config": {"workload": args.workload, "batch": w.batch, "hq": w.hq, "hkv": w.hkv,
-                           "head_dim": w.head_dim, "prefix": list(w.prefix), "n_nodes": w.n_nodes,
-                           "vocab": w.vocab, "accept": w.accept, "parallelism": f"replicas x{ws}",
-                           "launch": mode,
-                           "l2": "inputs exceed L2 (weights + KV streamed each step)"},
+                "config": workload_config(w, ws),
+                "timing": {"launch": "cuda_graph", "replays": reps, "replay_s_median": t_rep, "timed_wall_s": t_wall,
+                           "how": "median CUDA-event time of back-to-back replays of one K-step graph"},
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches * args.steps,
                 "stages_us": {k: v * 1e6 for k, v in stage_s.items()},
-                "mean_accepted": mean_acc, "attention": attention, "attention_full_shapes": extra,
-                "clocks": clocks.summary(), "wall_s": t_wall}
+                "mean_accepted": mean_acc, "attention": attention, "workloads": extra,
+                "attention_full_shapes": extra_attn, "clocks": clocks.summary()}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
