@@ -29,10 +29,14 @@ notes):
   among several valid branches the deepest valid node wins, ties to the
   lowest node index; the bonus is the greedy token at the stop node.
 * Decisions that compare floats (typical threshold, accept draw, sampling
-  race) are taken in ``dtype`` -- float32 by default, the kernel's
-  precision -- and every decision whose margin is below ``NEAR`` (relative)
-  is counted in ``near_ties``: there, either outcome is a correct result of
-  the rule within rounding.
+  race) are taken in ``dtype``, float64 by default.  Every decision whose
+  margin is below ``NEAR`` (relative) is reported by name in ``near``: a
+  kernel that takes it in float32 may take it the other way and still follow
+  the rule within rounding.  ``flip`` names decisions to take the other way,
+  so a test can check that a divergence sits exactly at a flagged decision.
+  Decision names: ("valid", c) typical validity of child c; ("accept", c)
+  the accept draw of child c; ("race", v) the sampling race at stop node v
+  (flipped: the runner-up wins).
 * Sampling from the residual uses the exponential race in its log form:
   argmax over non-removed x of z_x + G_x, z = logits / T and
   G_x = -log(-log u'_x) with u'_x from the counter-based generator.
@@ -85,27 +89,44 @@ def accept_greedy(logits, tok, first_child, next_sibling, path_cap):
     return _pack(paths, bonus, path_cap)
 
 
-def typical_threshold(row, eps, delta, T, dtype=np.float32):
-    """(p, thr) for one logits row: p = softmax(row / T),
-    thr = min(eps, delta * exp(-H)), H = -sum p ln p = ln S - sum(e z)/S with
-    z = row/T - max, e = exp(z), S = sum e."""
+def typical_threshold(row, eps, delta, T, dtype=np.float64):
+    """(p, thr) for one logits row: p = softmax(row / T) and
+    thr = min(eps, delta * exp(-H)) with the entropy H = -sum_x p(x) ln p(x)
+    (natural log; a zero probability contributes nothing)."""
     z = np.asarray(row, dtype) / dtype(T)
-    z = z - z.max()
-    e = np.exp(z)
-    S = e.sum(dtype=dtype)
-    H = np.log(S) - (e * z).sum(dtype=dtype) / S
+    e = np.exp(z - z.max())
+    p = e / e.sum(dtype=dtype)
+    nz = p > 0
+    H = -np.sum(p[nz] * np.log(p[nz]), dtype=dtype)
     thr = min(dtype(eps), dtype(delta) * np.exp(-H))
-    return e / S, thr
+    return p, thr
+
+
+def _race(z_or_logr, g, excluded_mask, flipped):
+    """Winner of the exponential race (lowest id among equal keys), the
+    runner-up when ``flipped``; also the top-two gap."""
+    key = z_or_logr + g
+    key[excluded_mask] = -np.inf
+    x = int(np.argmax(key))
+    k1 = key[x]
+    key2 = key.copy()
+    key2[x] = -np.inf
+    y = int(np.argmax(key2))
+    gap = float(k1 - key2[y])
+    near = gap <= NEAR_REJECT * max(1.0, abs(float(k1)))
+    return (y if flipped else x), near
 
 
 def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, T, path_cap,
-                   dtype=np.float32):
+                   dtype=np.float64, flip=()):
     """Node c (non-root) is valid iff p_parent(tok_c) > thr_parent; the
     accepted path is the root path of the deepest node whose whole path is
     valid (ties: lowest node index); bonus = argmax at that node.
-    Returns (acc_len, acc_path, bonus, near_ties[B])."""
+    Returns (acc_len, acc_path, bonus, near) with near[b] the list of
+    near-tie decisions of sequence b; ``flip`` holds (b, decision) pairs to
+    take the other way."""
     B, N, _ = logits.shape
-    paths, bonus, near = [], [], np.zeros(B, np.int64)
+    paths, bonus, near = [], [], [[] for _ in range(B)]
     for b in range(B):
         ok = np.zeros(N, bool)
         ok[0] = True
@@ -120,9 +141,10 @@ def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, 
             for c in kids:
                 depth[c] = depth[v] + 1
                 pc = p[int(tok[b, c])]
+                d = ("valid", c)
                 if abs(float(pc) - float(thr)) <= NEAR_TYPICAL * float(thr):
-                    near[b] += 1
-                ok[c] = bool(pc > thr)
+                    near[b].append(d)
+                ok[c] = bool(pc > thr) != ((b, d) in flip)
         reach = [i for i in range(N) if ok[i]]
         best = max(reach, key=lambda i: (depth[i], -i))
         path = []
@@ -138,11 +160,13 @@ def accept_typical(logits, tok, parents, first_child, next_sibling, eps, delta, 
 
 
 def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_cap,
-                  dtype=np.float32):
+                  dtype=np.float64, flip=()):
     """Rejection walk with point-mass sibling proposals and residual
-    resampling.  Returns (acc_len, acc_path, bonus, near_ties[B])."""
+    resampling.  Returns (acc_len, acc_path, bonus, near) with near[b] the
+    list of near-tie decisions of sequence b; ``flip`` holds (b, decision)
+    pairs to take the other way."""
     B, N, V = logits.shape
-    paths, bonus, near = [], [], np.zeros(B, np.int64)
+    paths, bonus, near = [], [], [[] for _ in range(B)]
     for b in range(B):
         v, path = 0, [0]
         while True:
@@ -156,9 +180,10 @@ def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_ca
                 x = int(tok[b, c])
                 r = dtype(0) if x in excluded else e[x] / (S - removed)
                 u = rng.uniform_accept(seed, b, step, c)
+                d = ("accept", c)
                 if abs(float(u) - float(r)) <= NEAR_REJECT * max(float(r), 1e-30):
-                    near[b] += 1
-                if u < r:
+                    near[b].append(d)
+                if bool(u < r) != ((b, d) in flip):
                     chosen = c
                     break
                 if x not in excluded:
@@ -167,12 +192,12 @@ def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_ca
             if chosen == -1:
                 u = rng.uniform_race(seed, b, step, v, np.arange(V))
                 g = -np.log(-np.log(u.astype(dtype)))
-                key = (z + g).astype(dtype)
-                key[excluded] = -np.inf
-                x = int(np.argmax(key))
-                top2 = np.partition(key, -2)[-2:]
-                if abs(float(top2[1] - top2[0])) <= NEAR_REJECT * max(1.0, abs(float(top2[1]))):
-                    near[b] += 1
+                mask = np.zeros(V, bool)
+                mask[excluded] = True
+                d = ("race", v)
+                x, is_near = _race(z, g, mask, (b, d) in flip)
+                if is_near:
+                    near[b].append(d)
                 bonus.append(x)
                 break
             v = chosen
@@ -266,14 +291,16 @@ def reject_stochastic_outcome_probs(probs, qprobs, tok, first_child, next_siblin
 
 
 def accept_reject_stochastic(logits, draft_logits, tok, first_child, next_sibling, seed, step, T, path_cap,
-                             dtype=np.float32):
+                             dtype=np.float64, flip=()):
     """The RNG-driven walk of the rule above: child c with token x is kept
-    iff u_c < r(x) / q(x) (u_c the accept draw of the rejection rule); the
-    bonus is the exponential race argmax_x (log r(x) + G_x) over the tokens
-    with r(x) > 0, G_x = -log(-log u'_x).  Returns (acc_len, acc_path, bonus,
-    near_ties[B])."""
+    iff u_c < r(x) / q(x) (u_c the accept draw of the rejection rule; a
+    token with q(x) = 0 is always kept); after a rejection
+    r <- norm(max(0, r - q)); the bonus is the exponential race
+    argmax_x (log r(x) + G_x) over the tokens with r(x) > 0,
+    G_x = -log(-log u'_x).  Returns (acc_len, acc_path, bonus, near) as
+    ``accept_reject``."""
     B, N, V = logits.shape
-    paths, bonus, near = [], [], np.zeros(B, np.int64)
+    paths, bonus, near = [], [], [[] for _ in range(B)]
     for b in range(B):
         v, path = 0, [0]
         while True:
@@ -288,9 +315,10 @@ def accept_reject_stochastic(logits, draft_logits, tok, first_child, next_siblin
                 x = int(tok[b, c])
                 ratio = np.inf if q[x] <= 0 else float(r[x] / q[x])
                 u = float(rng.uniform_accept(seed, b, step, c))
+                d = ("accept", c)
                 if np.isfinite(ratio) and abs(u - ratio) <= NEAR_REJECT * max(ratio, 1e-30):
-                    near[b] += 1
-                if u < ratio:
+                    near[b].append(d)
+                if bool(u < ratio) != ((b, d) in flip):
                     chosen = c
                     break
                 r = _residual_after_rejection(r.astype(np.float64), q.astype(np.float64))
@@ -302,12 +330,11 @@ def accept_reject_stochastic(logits, draft_logits, tok, first_child, next_siblin
                 u = rng.uniform_race(seed, b, step, v, np.arange(V))
                 g = -np.log(-np.log(u.astype(dtype)))
                 with np.errstate(divide="ignore"):
-                    key = (np.log(r) + g).astype(dtype)
-                key[r <= 0] = -np.inf
-                x = int(np.argmax(key))
-                top2 = np.partition(key, -2)[-2:]
-                if abs(float(top2[1] - top2[0])) <= NEAR_REJECT * max(1.0, abs(float(top2[1]))):
-                    near[b] += 1
+                    logr = np.log(r).astype(dtype)
+                d = ("race", v)
+                x, is_near = _race(logr, g, r <= 0, (b, d) in flip)
+                if is_near:
+                    near[b].append(d)
                 bonus.append(x)
                 break
             v = chosen

@@ -1,10 +1,13 @@
 """GPU parity: acceptance (greedy / typical / rejection), commit and the expansion round.
 
 Integer outputs are compared exactly.  The typical and rejection rules
-decide integers from float32 arithmetic; both sides take those decisions
-in float32, and a difference is allowed only for a sequence where the
-oracle flagged a near tie (decision margin below 1e-5 relative for the
-rejection draws and the sampling race, 1e-4 for the typical threshold).
+decide integers from floating-point arithmetic: the oracle takes those
+decisions in float64, the kernel in float32.  The oracle names every
+decision whose margin is below 1e-5 relative (rejection draws, sampling
+race) or 1e-4 (typical threshold).  A sequence may differ from the oracle
+only when re-running the oracle with exactly one such flagged decision
+taken the other way reproduces the GPU's result; those sequences are
+counted, printed, and must number zero on the full-size workloads.
 """
 import numpy as np
 import pytest
@@ -78,10 +81,27 @@ def test_greedy_bit_exact(si, bf16, V):
         np.testing.assert_array_equal(g_, r_)
 
 
-def _compare_with_near_ties(got, ref, near_per_seq):
+def _same(got, ref, b):
+    return got[0][b] == ref[0][b] and (got[1][b] == ref[1][b]).all() and got[2][b] == ref[2][b]
+
+
+def _compare_decisions(got, ref, near, rerun, label=""):
+    """Every sequence equals the oracle, or differs only at one decision the
+    oracle flagged as a near tie: the oracle re-run with that decision
+    flipped (``rerun(flip)``) must then equal the GPU.  Returns the number of
+    such excused sequences (also printed)."""
+    excused = 0
     for b in range(len(ref[0])):
-        same = got[0][b] == ref[0][b] and (got[1][b] == ref[1][b]).all() and got[2][b] == ref[2][b]
-        assert same or near_per_seq[b] > 0, f"sequence {b} differs without a near tie"
+        if _same(got, ref, b):
+            continue
+        hit = [d for d in near[b] if _same(got, rerun({(b, d)}), b)]
+        assert hit, (f"{label} sequence {b} differs from the oracle (gpu len {got[0][b]} path {got[1][b].tolist()} "
+                     f"bonus {got[2][b]}; oracle len {ref[0][b]} path {ref[1][b].tolist()} bonus {ref[2][b]}) "
+                     f"and no single flagged near tie {near[b]} explains it")
+        excused += 1
+    n_near = sum(len(x) for x in near)
+    print(f"{label}: {len(ref[0])} sequences, {n_near} near-tie decisions flagged, {excused} excused")
+    return excused
 
 
 @pytest.mark.parametrize("si", [0, 1, 2])
@@ -95,8 +115,10 @@ def test_typical_matches_oracle(si, eps, delta, bf16):
     cap = shape.n_levels + 1
     got = _accept(sv.TYPICAL, lg, t, cap, bf16=bf16, eps=eps, delta=delta, temperature=1.0)
     assert got[3] == 0
-    ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], eps, delta, 1.0, cap)
-    _compare_with_near_ties(got[:3], ref[:3], ref[3])
+    rerun = lambda flip: ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], eps,
+                                            delta, 1.0, cap, flip=flip)
+    ref = rerun(())
+    assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "typical") <= 1
 
 
 @pytest.mark.parametrize("si", [0, 1, 2, 3])
@@ -115,9 +137,10 @@ def test_reject_matches_oracle(si, bf16, temperature, V):
     for step in range(3):
         got = _accept(sv.REJECT, lg, t, cap, bf16=bf16, temperature=temperature, seed=0x1234ABCD5678, step=step)
         assert got[3] == 0
-        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 0x1234ABCD5678, step,
-                                temperature, cap)
-        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+        rerun = lambda flip: ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 0x1234ABCD5678,
+                                               step, temperature, cap, flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "reject") <= 1
 
 
 @pytest.mark.parametrize("B", [1, 20, 40])
@@ -137,12 +160,15 @@ def test_every_cluster_size(B, mode):
         for g_, r_ in zip(got[:3], ref):
             np.testing.assert_array_equal(g_, r_)
     elif mode == sv.TYPICAL:
-        ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], 0.3, 0.09, 1.0,
-                                 cap)
-        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+        rerun = lambda flip: ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], 0.3,
+                                                0.09, 1.0, cap, flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "typical") <= 1
     else:
-        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 99, B, 1.0, cap)
-        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+        rerun = lambda flip: ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], 99, B, 1.0, cap,
+                                               flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "reject") <= 1
 
 
 FULL_ACCEPT = [("llama70b_serving", sv.GREEDY), ("long_context", sv.TYPICAL), ("llama8b_eagle2", sv.REJECT)]
@@ -165,12 +191,15 @@ def test_accept_full_size(name, mode):
         for g_, r_ in zip(got[:3], ref):
             np.testing.assert_array_equal(g_, r_)
     elif mode == sv.TYPICAL:
-        ref = ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"], w.eps, w.delta,
-                                 1.0, cap)
-        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+        rerun = lambda flip: ACC.accept_typical(lg, t["tok"], t["parent"], t["first_child"], t["next_sibling"],
+                                                w.eps, w.delta, 1.0, cap, flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, name) == 0
     else:
-        ref = ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], w.seed, 7, 1.0, cap)
-        _compare_with_near_ties(got[:3], ref[:3], ref[3])
+        rerun = lambda flip: ACC.accept_reject(lg, t["tok"], t["first_child"], t["next_sibling"], w.seed, 7, 1.0,
+                                               cap, flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, name) == 0
     assert got[0].mean() > 0.5            # planted agreement gives non-trivial paths
 
 
@@ -264,10 +293,27 @@ def test_expand_round_matches_oracle():
     torch.cuda.synchronize()
     assert int(host(st)[0]) == 0
     rp, rt, rc, rv, rcnt, rnxt, near = X.expand_round(logits, front, par, tok, conf, val, count, k, 1.0, 6)
-    np.testing.assert_array_equal(host(dp), rp)
-    np.testing.assert_array_equal(host(dt), rt)
-    np.testing.assert_array_equal(host(dn), rcnt)
-    np.testing.assert_allclose(host(dc), rc, rtol=2e-6, atol=1e-9)
-    np.testing.assert_allclose(host(dv), rv, rtol=4e-6, atol=1e-9)
-    if near == 0:
-        np.testing.assert_array_equal(host(nxt), rnxt)
+    _check_expand(host(dp), host(dt), host(dc), host(dv), host(dn), host(nxt), count, rp, rt, rc, rv, rcnt, rnxt,
+                  near)
+
+
+def _check_expand(gp, gt, gc, gv, gn, gnxt, first_new, rp, rt, rc, rv, rcnt, rnxt, near):
+    """Pool entries exact (parents, tokens, count), confidences and values
+    within float32 rounding of the float64 oracle; every frontier slot equal
+    to the oracle's except slots the oracle flagged as value near ties; and
+    the GPU frontier is in any case the top of the GPU's own values (value
+    descending, ties to the lower pool index)."""
+    np.testing.assert_array_equal(gp, rp)
+    np.testing.assert_array_equal(gt, rt)
+    np.testing.assert_array_equal(gn, rcnt)
+    np.testing.assert_allclose(gc, rc, rtol=1e-5, atol=1e-12)
+    np.testing.assert_allclose(gv, rv, rtol=1e-5, atol=1e-12)
+    flagged = set(near)
+    for b in range(gnxt.shape[0]):
+        for j in range(gnxt.shape[1]):
+            if (b, j) not in flagged:
+                assert gnxt[b, j] == rnxt[b, j], f"frontier slot ({b}, {j})"
+        new = list(range(int(first_new[b]), int(gn[b])))
+        best = sorted(new, key=lambda m: (-float(gv[b, m]), m))[: gnxt.shape[1]]
+        assert gnxt[b].tolist() == best, f"sequence {b}: frontier is not the top of the GPU's own values"
+    print(f"expand: {len(flagged)} frontier slots flagged as value near ties")

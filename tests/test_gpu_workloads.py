@@ -1,0 +1,176 @@
+"""GPU parity of whole verify steps at the workloads' full shapes.
+
+Each bf16 workload is built exactly as ``bench.GpuStep`` builds it (same
+seeded inputs, same launches), run for one step, and every stage's output is
+checked against the oracle:
+
+* tree construction, top-s, acceptance and KV commit: exactly (the oracle's
+  integer stages read the GPU's upstream outputs, so a tolerance-level
+  difference in logits cannot legitimately change them); float-decided
+  acceptance may differ only at a decision the oracle flags as a near tie,
+  and on these seeded workloads no sequence may need that excuse;
+* Medusa heads and the LM head: every output element, |gpu - ref| <= 2e-2 +
+  1e-2 |ref|;
+* tree attention: every output of two whole (sequence, KV-head group)
+  blocks, the first and the last, with Q scaled by 4 (exact in bf16) so the
+  softmax is peaked and the outputs are far larger than the tolerance; then
+  again with the tree K scaled by 4 as well, so each node's ancestors carry
+  most of its softmax weight and a wrong mask bit moves the output by far
+  more than the tolerance.  Max-abs and normalised RMS errors are printed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+from _util import host
+from oracle import accept as ACC
+from oracle import attention as A
+from oracle import commit as COM
+from oracle import heads as H
+from oracle import tree as T
+from tree_speculative_decoding_attn_gb300 import specverify as sv
+from tree_speculative_decoding_attn_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 2e-2, 1e-2
+
+
+def _close(label, got, ref, min_std=None):
+    err = np.abs(got - ref)
+    excess = err - (ATOL + RTOL * np.abs(ref))
+    nrms = float(np.sqrt((err ** 2).mean()) / max(np.sqrt((ref ** 2).mean()), 1e-30))
+    print(f"{label}: {ref.size} outputs, max |err| {err.max():.3e}, normalised RMS err {nrms:.3e}, "
+          f"ref std {ref.std():.3f}")
+    assert (excess <= 0).all(), f"{label}: tolerance exceeded by {excess.max():.3e}"
+    if min_std is not None:
+        assert ref.std() > min_std, f"{label}: reference outputs too flat for the tolerance to bind"
+    return nrms
+
+
+def _stage(step, name):
+    return next(fn for nm, fn, _, _ in step.stages if nm == name)
+
+
+def _tree_reference(step):
+    """The oracle's tree arrays [B, N] for the tree this step built."""
+    w, B, N = step.w, step.w.batch, step.w.n_nodes
+    if w.tree == "dynamic":
+        dk = w.dynamic
+        par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], w.vocab)
+        trees = [T.rerank_dynamic(par[b], tok[b], conf[b], N, int(step.prefix[b])) for b in range(B)]
+        return {k: np.stack([t[k] for t in trees]) for k in
+                ("tok", "parent", "depth", "pos", "anc", "mask", "first_child", "next_sibling")}
+    cand = host(step.cand)
+    if w.medusa:  # the tree reads the GPU's own top-s of the head logits
+        idx, _ = H.topk(host(step.head_logits), cand.shape[-1])
+        np.testing.assert_array_equal(cand, idx)
+    return T.build_tree_static(step.shape.parents, step.shape.rank, cand, host(step.root), step.prefix)
+
+
+def _check_tree(step, ref):
+    got = dict(tok=host(step.tok), depth=host(step.depth), pos=host(step.pos), first_child=host(step.fc),
+               next_sibling=host(step.ns), anc=host(step.anc).view(np.uint64))
+    if step.w.tree == "dynamic":
+        got["parent"] = host(step.par_out)
+    for k, v in got.items():
+        np.testing.assert_array_equal(v, np.asarray(ref[k]).astype(v.dtype), err_msg=k)
+
+
+def _attention_blocks(step, ref_tree, label):
+    """Every output of (sequence 0, KV head 0) and (last sequence, last KV
+    head), all N nodes x G query heads."""
+    w = step.w
+    G = w.group
+    out = host(step.out)
+    nrms = []
+    for b, kvh in ((0, 0), (w.batch - 1, w.hkv - 1)):
+        P = int(step.prefix[b])
+        heads = list(range(kvh * G, (kvh + 1) * G))
+        q = host(step.q[b:b + 1])
+        kc, vc = host(step.kc[b:b + 1, :, :P]), host(step.vc[b:b + 1, :, :P])
+        kt, vt = host(step.kt[b:b + 1]), host(step.vt[b:b + 1])
+        ref = A.tree_attention(q, kc, vc, kt, vt, np.array([P]), ref_tree["mask"][b], heads=heads)
+        nrms.append(_close(f"{label} attention seq {b} kv head {kvh}", out[b][:, heads], ref[0][:, heads],
+                           min_std=0.1))
+    return nrms
+
+
+def _check_accept(step, ref_tree, logits):
+    w = step.w
+    got = (host(step.acc_len), host(step.acc_path), host(step.bonus))
+    cap = step.path_cap
+    par = ref_tree["parent"] if ref_tree["parent"].ndim == 2 else np.broadcast_to(ref_tree["parent"],
+                                                                                  ref_tree["tok"].shape)
+    tok, fc, ns = ref_tree["tok"], ref_tree["first_child"], ref_tree["next_sibling"]
+    if w.accept == "greedy":
+        ref = ACC.accept_greedy(logits, tok, fc, ns, cap)
+        for g_, r_ in zip(got, ref):
+            np.testing.assert_array_equal(g_, r_)
+        return got
+    if w.accept == "typical":
+        rerun = lambda flip: ACC.accept_typical(logits, tok, par, fc, ns, w.eps, w.delta, w.temperature, cap,
+                                                flip=flip)
+    else:
+        rerun = lambda flip: ACC.accept_reject(logits, tok, fc, ns, w.seed, 0, w.temperature, cap, flip=flip)
+    ref = rerun(())
+    excused = 0
+    for b in range(w.batch):
+        same = got[0][b] == ref[0][b] and (got[1][b] == ref[1][b]).all() and got[2][b] == ref[2][b]
+        if not same:
+            alt = [d for d in ref[3][b] if (lambda r: r[0][b] == got[0][b] and (r[1][b] == got[1][b]).all()
+                                            and r[2][b] == got[2][b])(rerun({(b, d)}))]
+            assert alt, f"sequence {b}: acceptance differs from the oracle with no flagged near tie"
+            excused += 1
+    print(f"{w.name} {w.accept}: {sum(len(x) for x in ref[3])} near-tie decisions flagged, {excused} excused")
+    assert excused == 0
+    return got
+
+
+def _check_commit(step, acc, kc_tail, vc_tail, lo):
+    """Rows prefix..prefix+L of every sequence hold the accepted path's tree
+    rows (bitwise); the rest of the tail region is unchanged; the new prefix
+    length is prefix + L + 1."""
+    acc_len, acc_path, _ = acc
+    kc, vc = host(step.kc[:, :, lo:]), host(step.vc[:, :, lo:])
+    kt, vt = host(step.kt), host(step.vt)
+    ref_k, ref_v, ref_len = COM.kv_commit(kc_tail, vc_tail, kt, vt, step.prefix - lo, acc_len, acc_path)
+    np.testing.assert_array_equal(kc.view(np.uint32), ref_k.view(np.uint32))
+    np.testing.assert_array_equal(vc.view(np.uint32), ref_v.view(np.uint32))
+    np.testing.assert_array_equal(host(step.new_prefix), ref_len + lo)
+
+
+@pytest.mark.parametrize("name", ["vicuna7b_medusa", "llama8b_eagle2", "llama70b_serving", "long_context"])
+def test_full_step_matches_oracle(name):
+    step = bench.GpuStep(name, torch.device("cuda", 0))
+    w = step.w
+    step.q.mul_(4.0)
+    lo = int(step.prefix.min())
+    kc_tail, vc_tail = host(step.kc[:, :, lo:]), host(step.vc[:, :, lo:])   # the region commit may write
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0, sv.spec_status_string(int(step.status.item()))
+
+    if w.medusa:
+        m = w.medusa
+        h, w1, w2, wlm = synth.medusa_inputs(w)
+        z, hl = H.medusa_heads(h, w1, None, w2)
+        _close(f"{name} medusa z", host(step.z), z)
+        _close(f"{name} medusa head logits", host(step.head_logits), hl)
+        _close(f"{name} lm head logits", host(step.logits).reshape(-1, w.vocab), H.lm_head(host(step.hid), wlm))
+        del w1, w2
+    ref_tree = _tree_reference(step)
+    _check_tree(step, ref_tree)
+    _attention_blocks(step, ref_tree, name)
+    acc = _check_accept(step, ref_tree, host(step.logits))
+    if w.planted:
+        assert acc[0].mean() > 0.5
+    _check_commit(step, acc, kc_tail, vc_tail, lo)
+
+    # tree keys scaled by 4: ancestors dominate each node's softmax
+    step.kt.mul_(4.0)
+    _stage(step, "tree_attn")()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    _attention_blocks(step, ref_tree, f"{name} (tree K x4)")

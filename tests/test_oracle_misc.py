@@ -93,6 +93,37 @@ def test_uniforms_range_and_uniformity():
     assert not np.array_equal(u[:100], R.uniform_accept(123, 0, 1, np.arange(100)))   # step matters
 
 
+def test_expand_round_hand_worked_example():
+    """A round computed by hand ("5.3 Medusa、EAGLE 与 MTP", section 5.2:
+    value = product of confidences along the path; the best-valued nodes
+    are expanded next).  Rows with equal maxima and entries of -200
+    (exp(-200) is negligible against 1) give exact probabilities 1/2 and
+    1/4, so every value below is exact:
+      frontier node 1 (value 1/2): probabilities (1/2, 1/2, 0, 0, 0) ->
+        children tokens 0, 1 (equal -> lower id first), value 1/4 each;
+      frontier node 2 (value 1/4): probabilities (0, 1/4, 1/4, 1/4, 1/4) ->
+        children tokens 1, 2, value 1/16 each.
+    Children go to pool slots 3, 4 (node 1) and 5, 6 (node 2); the next
+    frontier of three is 3, 4, 5 (equal values -> lower pool index)."""
+    logits = np.array([[[0, 0, -200, -200, -200], [-200, 0, 0, 0, 0]]], np.float64)
+    par = np.array([[-1, 0, 0, -1, -1, -1, -1]]); tok = np.array([[7, 3, 4, 0, 0, 0, 0]])
+    conf = np.array([[1.0, 0.5, 0.25, 0, 0, 0, 0]]); val = conf.copy()
+    p2, t2, c2, v2, cnt, nxt, near = X.expand_round(logits, np.array([[1, 2]]), par, tok, conf, val,
+                                                     np.array([3]), 2, 1.0, 3)
+    assert cnt.tolist() == [7]
+    assert p2[0].tolist() == [-1, 0, 0, 1, 1, 2, 2]
+    assert t2[0].tolist() == [7, 3, 4, 0, 1, 1, 2]
+    assert c2[0, 3:].tolist() == [0.5, 0.5, 0.25, 0.25]
+    assert v2[0, 3:].tolist() == [0.25, 0.25, 0.0625, 0.0625]
+    assert nxt[0].tolist() == [3, 4, 5]
+    assert (0, 2) in near and (0, 0) in near          # the exact ties are flagged
+    # temperature 2 halves the logits: probabilities unchanged for rows of 0 / -200 (to rounding)
+    _, _, c3, _, _, nxt3, _ = X.expand_round(logits, np.array([[1, 2]]), par, tok, conf, val, np.array([3]), 2,
+                                             2.0, 3)
+    np.testing.assert_allclose(c3[0, 3:], [0.5, 0.5, 0.25, 0.25], rtol=1e-12)
+    assert nxt3[0].tolist() == [3, 4, 5]
+
+
 def test_expand_round_brute_force():
     g = np.random.default_rng(0)
     B, F, V, k, M = 2, 3, 30, 4, 1 + 3 + 12
@@ -115,7 +146,7 @@ def test_expand_round_brute_force():
                 m = 4 + f * k + j
                 assert p2[b, m] == front[b, f] and t2[b, m] == order[j]
                 assert c2[b, m] == pytest.approx(prob[order[j]], rel=1e-5)
-                assert v2[b, m] == np.float32(val[b, front[b, f]] * c2[b, m])
+                assert v2[b, m] == pytest.approx(float(val[b, front[b, f]]) * prob[order[j]], rel=1e-12)
         new = list(range(4, 16))
         best = sorted(new, key=lambda m: (-float(v2[b, m]), m))[:5]
         assert nxt[b].tolist() == best
