@@ -48,7 +48,6 @@ L2_BYTES = 129 * 1024 * 1024
 # source is the one the counters were taken on: (source, sha256 prefix,
 # bytes) keyed by (workload, stage).
 NCU_TRAFFIC = {
-    ("vicuna7b_medusa", "medusa_heads"): ("csrc/heads.cu", "04c7e4bf72a021e3", 1183632896),
 }
 
 
@@ -228,13 +227,17 @@ class GpuStep:
         self.h = cu(h, bf)
         self.w1, self.w2, self.wlm = cu(w1, bf), cu(w2, bf), cu(wlm, bf)
         del w1, w2, wlm
-        self.z = torch.empty((B, K, d), dtype=torch.float32, device=self.dev)
+        self.z = torch.empty((B, K, d), dtype=bf, device=self.dev)
         self.head_logits = torch.empty((B, K, V), dtype=torch.float32, device=self.dev)
+        self.heads_ws = torch.empty(max(sv.spec_medusa_heads_workspace_bytes(B, K, d, V), 16), dtype=torch.uint8,
+                                    device=self.dev)
         self.cand = torch.empty((B, K, s), dtype=torch.int32, device=self.dev)
         self.h2d.append((self.h.cpu().pin_memory(), self.h))
-        heads_bytes = 2 * K * d * d + 2 * K * V * d + 2 * B * d + 4 * B * K * (d + V)
-        self.stages.append(("medusa_heads", lambda: sv.spec_medusa_heads(self.h, self.w1, None, self.w2, self.z,
-                                                                        self.head_logits), 2, heads_bytes))
+        # algorithmic bytes: both weight matrices once, h in, z out (bf16), logits out
+        heads_bytes = 2 * K * d * d + 2 * K * V * d + 2 * B * d + 2 * B * K * d + 4 * B * K * V
+        self.stages.append(("medusa_heads", lambda: sv.spec_medusa_heads(
+            self.h, self.w1, None, self.w2, self.z, self.head_logits, workspace=self.heads_ws,
+            dev_status=self.status), 2, heads_bytes))
         self.stages.append(("topk", lambda: sv.spec_topk(self.head_logits, s, self.cand), 1, 4 * B * K * V))
         self.stages.append(("build_tree", lambda: sv.spec_build_tree(
             self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos, self.anc,
@@ -268,7 +271,10 @@ class GpuStep:
         self.logits = torch.empty((B, N, V), dtype=torch.float32, device=self.dev)
         self.logits_bytes_row = V * 4
         self.h2d.append((self.hid.cpu().pin_memory(), self.hid))
-        self.stages.append(("lm_head", lambda: sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V)), 1,
+        self.lm_ws = torch.empty(max(sv.spec_lm_head_workspace_bytes(B * N, d, V), 16), dtype=torch.uint8,
+                                 device=self.dev)
+        self.stages.append(("lm_head", lambda: sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V),
+                                                               dev_status=self.status, workspace=self.lm_ws), 1,
                             2 * V * d + 2 * B * N * d + 4 * B * N * V))
 
     def _accept_commit_stages(self):

@@ -77,10 +77,18 @@ enum {
 enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
 
 /* acceptance modes */
-enum { SPEC_ACCEPT_GREEDY = 0, SPEC_ACCEPT_TYPICAL = 1, SPEC_ACCEPT_REJECT = 2 };
+enum {
+  SPEC_ACCEPT_GREEDY = 0,
+  SPEC_ACCEPT_TYPICAL = 1,
+  SPEC_ACCEPT_REJECT = 2,           /* siblings are deterministic drafts */
+  SPEC_ACCEPT_REJECT_STOCHASTIC = 3 /* siblings drawn from the drafter's q */
+};
 
-/* Largest tree the ancestor bitmask supports (one uint64 word per node). */
-#define SPEC_MAX_NODES 64
+/* Largest tree (nodes, root included).  The ancestor bitmask of a node is
+ * SPEC_MASK_WORDS(n_nodes) uint64 words: bit j % 64 of word j / 64 stands
+ * for node j.  Trees of up to 64 nodes therefore use one word per node. */
+#define SPEC_MAX_NODES 256
+#define SPEC_MASK_WORDS(n) (((n) + 63) / 64)
 
 /* Text for a host or device status code (static string, never NULL). */
 const char *spec_status_string(int status);
@@ -98,14 +106,25 @@ int spec_abi_version(void);
  *   w1     [n_heads, hidden, hidden]     bf16, nn.Linear layout [out, in]
  *   b1     [n_heads, hidden]             bf16, or NULL for no bias
  *   w2     [n_heads, vocab, hidden]      bf16
- *   z      [batch, n_heads, hidden]      f32 out: h + SiLU(W1 h + b1)
+ *   z      [batch, n_heads, hidden]      bf16 out: h + SiLU(W1 h + b1),
+ *                                        rounded to bf16 (the W2 operand)
  *   logits [batch, n_heads, vocab]       f32 out: W2 z (softmax omitted:
  *                                        it does not change the top-s)
- * Accumulation is float32.  Requires hidden % 8 == 0, 1 <= batch <= 8.
+ *   workspace  device scratch of spec_medusa_heads_workspace_bytes()
+ *              bytes (16-byte aligned; contents need not be initialised;
+ *              calls that may overlap on the GPU need separate ones)
+ * Both products run on the tensor cores with float32 accumulation; every
+ * SM streams an equal share of the weights, and the sum over hidden is
+ * taken in a fixed order, so results repeat bit for bit across calls.
+ * Requires hidden % 64 == 0; any batch >= 1 (blocks of 256 rows).  A
+ * device-side timeout (never expected) sets SPEC_DEV_TIMEOUT in dev_status
+ * (optional).  SPEC_ERR_CAPACITY: workspace too small.
  * ------------------------------------------------------------------ */
+size_t spec_medusa_heads_workspace_bytes(int batch, int n_heads, int hidden, int vocab);
 int spec_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2,
                       int batch, int n_heads, int hidden, int vocab,
-                      float *z, float *logits, spec_stream_t stream);
+                      void *z, float *logits, void *workspace, size_t workspace_bytes,
+                      int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
  * spec_topk -- top-s candidates per row ("Medusa and EAGLE ...
@@ -139,8 +158,9 @@ int spec_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stri
  *   prefix_len [batch] int32: committed cache length of each sequence
  * Outputs, all [batch, n_nodes]:
  *   tok (int32, may be NULL), depth (int32), pos_ids (int32) = prefix_len
- *   + depth, anc_mask (uint64: bit j of word i set iff node j is node i or
- *   an ancestor of it), first_child / next_sibling (int32, -1 = none;
+ *   + depth, anc_mask ([batch, n_nodes, SPEC_MASK_WORDS(n_nodes)] uint64:
+ *   the bit of node j in node i's words is set iff node j is node i or an
+ *   ancestor of it), first_child / next_sibling (int32, -1 = none;
  *   children in node order).
  * n_nodes <= SPEC_MAX_NODES.  A malformed parents array or a depth beyond
  * cand_levels sets SPEC_DEV_BAD_PARENTS.
@@ -219,14 +239,16 @@ int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front
  *   k_tree, v_tree   [batch, hkv, n_nodes, head_dim] dtype: this pass's
  *            K/V of the tree nodes (position ids already applied)
  *   prefix_len [batch] int32 (device), each <= max_prefix (host bound)
- *   anc_mask   [batch, n_nodes] uint64 (from spec_build_tree*)
+ *   anc_mask   [batch, n_nodes, SPEC_MASK_WORDS(n_nodes)] uint64 (from
+ *            spec_build_tree*)
  *   out      [batch, n_nodes, hq, head_dim]       dtype
  *   scale    softmax scale; <= 0 selects 1/sqrt(head_dim)
  *   num_splits  KV splits per (sequence, KV head); 0 = automatic
  *   workspace   device scratch of tree_attn_workspace_bytes() bytes
  *               (may be NULL when that size is 0)
- * dtype SPEC_F32 or SPEC_BF16; head_dim 64 or 128; n_nodes <= 64;
- * hq % hkv == 0; (hq / hkv) * n_nodes <= 512.  Softmax and accumulation
+ * dtype SPEC_F32 or SPEC_BF16; head_dim 64 or 128; n_nodes <= 256;
+ * hq % hkv == 0; (hq / hkv) * n_nodes <= 512 for trees of up to 64 nodes,
+ * <= 2048 above (those run on the CUDA-core kernel).  Softmax and accumulation
  * are float32.  A prefix_len above max_prefix sets SPEC_DEV_CAPACITY and
  * that sequence's output is left unwritten.
  * bf16 with head_dim 128 and more than 128 query rows per KV head
@@ -286,17 +308,24 @@ int tree_attn_verify_noalloc(const void *q, const void *k_cache, const void *v_c
  *   hid    [rows, hidden] bf16
  *   w      [vocab, hidden] bf16 (LM head weight)
  *   logits [rows, vocab]   f32 out = hid . w^T (float32 accumulation)
- * Requires hidden % 64 == 0.  Runs on the tensor cores; a device-side
- * timeout (never expected) sets SPEC_DEV_TIMEOUT in dev_status (optional).
+ *   workspace  device scratch of spec_lm_head_workspace_bytes() bytes
+ *              (as spec_medusa_heads)
+ * Requires hidden % 64 == 0; any rows >= 1 (blocks of 256 rows).  Runs on
+ * the tensor cores; a device-side timeout (never expected) sets
+ * SPEC_DEV_TIMEOUT in dev_status (optional).
  * ------------------------------------------------------------------ */
+size_t spec_lm_head_workspace_bytes(int rows, int hidden, int vocab);
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-                 int32_t *dev_status, spec_stream_t stream);
+                 void *workspace, size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
  * spec_accept -- accept the longest target-agreeing path.
  *
  *   logits  [batch, n_nodes, vocab] (f32 or bf16): target logits at each
  *           node (distribution of the token after it)
+ *   draft_logits [batch, n_nodes, vocab] (same dtype): the drafter's
+ *           logits at each node (SPEC_ACCEPT_REJECT_STOCHASTIC only; NULL
+ *           otherwise)
  *   tok, parents, first_child, next_sibling [batch, n_nodes] int32
  * Modes (p_v = softmax(logits[b,v] / temperature)):
  *   SPEC_ACCEPT_GREEDY  child c of v is accepted iff tok[c] == argmax
@@ -319,12 +348,22 @@ int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab
  *       Gumbel(u'_x)) over the tokens not removed, u' = ((w >> 9) + 0.5) *
  *       2^-23 with w = word (x mod 4) of counter (x div 4, 256 + v, b,
  *       step).
- *       Requires temperature > 0.
+ *   SPEC_ACCEPT_REJECT_STOCHASTIC  the children of v are independent
+ *       draws from the drafter's q_v = softmax(draft_logits[b,v] / T)
+ *       (SpecInfer-style multi-draft; "Medusa and EAGLE ... explained",
+ *       section "Medusa: heads, losses and trees"; "Drafters: ...", section
+ *       "Why the answer does not change"): child c is accepted iff u <
+ *       r(tok[c]) / q_v(tok[c]) (always when q_v(tok[c]) = 0); a rejection
+ *       sets r <- norm(max(0, r - q_v)); if no child is accepted the bonus
+ *       is the race over log r(x) + Gumbel(u'_x) for r(x) > 0.  Same draws
+ *       as SPEC_ACCEPT_REJECT.
+ *       REJECT modes require temperature > 0.
  * Outputs: acc_len [batch] (accepted nodes, root excluded), acc_path
  * [batch, path_cap] (node ids root first, -1 after), bonus [batch].
  * path_cap must exceed the tree depth.  Decisions use float32.
  * ------------------------------------------------------------------ */
-int spec_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
+int spec_accept(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
+                int n_nodes, int vocab,
                 const int32_t *tok, const int32_t *parents, const int32_t *first_child,
                 const int32_t *next_sibling, float temperature, float eps, float delta,
                 uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,

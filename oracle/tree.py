@@ -56,6 +56,17 @@ def mask_words(mask: np.ndarray) -> np.ndarray:
     return w
 
 
+def mask_words_multi(mask: np.ndarray) -> np.ndarray:
+    """Pack mask rows into ceil(N / 64) uint64 words per row: node j is bit
+    j % 64 of word j // 64.  Shape [..., N, words]."""
+    n = mask.shape[-1]
+    nw = (n + 63) // 64
+    w = np.zeros(mask.shape[:-1] + (nw,), dtype=np.uint64)
+    for j in range(n):
+        w[..., j // 64] |= mask[..., j].astype(np.uint64) << np.uint64(j % 64)
+    return w
+
+
 def child_links(parents):
     """first_child[v] and next_sibling[c] in node order (-1 = none)."""
     n = len(parents)
@@ -77,7 +88,7 @@ def build_tree(parents, prefix_len: int) -> dict:
     depth, mask = depth_and_mask(parents)
     first, nxt = child_links(parents)
     return dict(parent=np.asarray(parents, np.int64), depth=depth, mask=mask,
-                anc=mask_words(mask), pos=prefix_len + depth,
+                anc=mask_words(mask) if len(parents) <= 64 else mask_words_multi(mask), pos=prefix_len + depth,
                 first_child=first, next_sibling=nxt)
 
 

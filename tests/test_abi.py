@@ -40,7 +40,7 @@ def test_status_strings_without_gpu(built_lib):
     from tree_speculative_decoding_attn_gb300 import specverify as sv
     assert sv.spec_status_string(0) == "ok"
     assert "invalid" in sv.spec_status_string(1)
-    assert sv.spec_abi_version() == 1
+    assert sv.spec_abi_version() == 2
 
 
 def test_split_planner_is_host_only_and_sane(built_lib):
@@ -58,4 +58,4 @@ def test_split_planner_is_host_only_and_sane(built_lib):
     assert sv.tree_attn_plan_splits(bf, 2, 64, 32, 32, 128, [8192, 600]) > 1       # MHA: 64 rows per KV head
     assert 1 <= sv.tree_attn_plan_splits(torch.float32, 1, 5, 4, 4, 64, [128]) <= 64
     with pytest.raises(sv.SpecError):
-        sv.tree_attn_plan_splits(bf, 2, 65, 8, 8, 128, [10, 10])     # more than 64 tree nodes
+        sv.tree_attn_plan_splits(bf, 2, 257, 8, 8, 128, [10, 10])    # more than 256 tree nodes

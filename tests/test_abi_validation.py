@@ -44,8 +44,9 @@ def _attn(lib, q=P, kc=P, dtype=sv.BF16, B=2, N=32, hq=16, hkv=2, D=128, s_max=1
     (dict(dtype=7), UNS),
     (dict(hq=12, hkv=8), INV),                 # query heads not a multiple of KV heads
     (dict(D=96), UNS),
-    (dict(N=65), UNS),                         # more nodes than one 64-bit ancestor word
-    (dict(hq=128, hkv=8, N=64), UNS),          # 1024 query rows per KV head; 512 is the limit
+    (dict(N=257), UNS),                        # more nodes than the largest tree
+    (dict(hq=128, hkv=8, N=64), UNS),          # 1024 query rows per KV head; 512 is the limit up to 64 nodes
+    (dict(hq=16, hkv=1, N=200), UNS),          # 3200 rows per KV head; 2048 above 64 nodes
     (dict(B=0), INV),
     (dict(max_prefix=2048), CAP),              # prefix beyond the cache's capacity
     (dict(q=MIS), INV),
@@ -61,19 +62,23 @@ def test_tree_attn_verify_refuses(lib, kw, code):
 
 def test_workspace_query_is_zero_for_bad_shapes(lib):
     assert lib.tree_attn_workspace_bytes(sv.BF16, 2, 32, 12, 8, 128, 512, 0) == 0
-    assert lib.tree_attn_workspace_bytes(sv.BF16, 2, 65, 16, 2, 128, 512, 0) == 0
+    assert lib.tree_attn_workspace_bytes(sv.BF16, 2, 257, 16, 2, 128, 512, 0) == 0
     assert lib.tree_attn_workspace_bytes(sv.BF16, 1, 64, 32, 32, 128, 2048, 0) > 0
 
 
-def _accept(lib, mode=sv.GREEDY, logits=P, dtype=sv.BF16, B=2, N=16, V=1000, T=1.0, cap=8):
-    return lib.spec_accept(mode, logits, dtype, B, N, V, P, P, P, P, T, 0.3, 0.09, 1, 0, cap, P, P, P, NULL, NULL)
+def _accept(lib, mode=sv.GREEDY, logits=P, draft=NULL, dtype=sv.BF16, B=2, N=16, V=1000, T=1.0, cap=8):
+    return lib.spec_accept(mode, logits, draft, dtype, B, N, V, P, P, P, P, T, 0.3, 0.09, 1, 0, cap, P, P, P, NULL,
+                           NULL)
 
 
 @pytest.mark.parametrize("kw,code", [
     (dict(logits=NULL), INV),
-    (dict(mode=3), INV),
+    (dict(mode=4), INV),
+    (dict(mode=sv.REJECT_STOCHASTIC), INV),            # stochastic siblings need the drafter's logits
+    (dict(mode=sv.REJECT, draft=P), INV),              # ... and only that mode takes them
+    (dict(mode=sv.REJECT_STOCHASTIC, draft=P, T=0.0), INV),
     (dict(dtype=5), UNS),
-    (dict(N=65), UNS),
+    (dict(N=257), UNS),
     (dict(V=0), INV),
     (dict(cap=0), INV),
     (dict(mode=sv.TYPICAL, T=0.0), INV),
@@ -93,8 +98,8 @@ def _commit(lib, kc=P, elem=2, layers=1, B=2, hkv=2, s_max=64, N=16, D=128, cap=
     (dict(prefix=NULL), INV),
     (dict(elem=3), UNS),
     (dict(layers=0), INV),
-    (dict(N=65), UNS),
-    (dict(cap=66), UNS),
+    (dict(N=257), UNS),
+    (dict(cap=258), UNS),
     (dict(D=6), UNS),                          # a row of 12 bytes is not a whole number of 16-byte copies
     (dict(kc=MIS), INV),
 ])
@@ -105,7 +110,7 @@ def test_kv_commit_refuses(lib, kw, code):
 def test_build_tree_refuses(lib):
     # static: parents, rank, cand_tok, levels, s, root_tok, prefix_len, batch, n, tok, depth, pos, anc, fc, ns
     args = [P, P, P, 3, 4, P, P, 2, 16, P, P, P, P, P, P, NULL, NULL]
-    assert lib.spec_build_tree(*args[:7], 2, 65, *args[9:]) == UNS
+    assert lib.spec_build_tree(*args[:7], 2, 257, *args[9:]) == UNS
     assert lib.spec_build_tree(NULL, *args[1:]) == INV
     assert lib.spec_build_tree(P, NULL, *args[2:]) == INV          # candidate tokens without ranks
     assert lib.spec_build_tree(*args[:4], 0, *args[5:]) == INV     # zero candidates per level
@@ -114,13 +119,19 @@ def test_build_tree_refuses(lib):
                                                    NULL)
     assert dyn(10, 16) == INV
     assert dyn(4097, 16) == UNS
-    assert dyn(100, 65) == UNS
+    assert dyn(300, 257) == UNS
 
 
 def test_heads_topk_expand_lm_head_refuse(lib):
-    assert lib.spec_medusa_heads(P, P, NULL, P, 9, 4, 4096, 32000, P, P, NULL) == UNS    # batch above 8
-    assert lib.spec_medusa_heads(P, P, NULL, P, 1, 4, 4100, 32000, P, P, NULL) == INV    # hidden not a multiple of 8
-    assert lib.spec_medusa_heads(MIS, P, NULL, P, 1, 4, 4096, 32000, P, P, NULL) == INV
+    heads = lambda h=P, B=1, d=4096, ws=P, nbytes=1 << 30: lib.spec_medusa_heads(h, P, NULL, P, B, 4, d, 32000, P, P,
+                                                                                 ws, nbytes, NULL, NULL)
+    assert heads(B=0) == INV                                                              # no rows
+    assert heads(d=4100) == INV                                                           # hidden not a multiple of 64
+    assert heads(h=MIS) == INV                                                            # misaligned input
+    assert heads(ws=NULL) == INV                                                          # no workspace
+    assert heads(nbytes=16) == CAP                                                        # workspace too small
+    assert lib.spec_medusa_heads_workspace_bytes(64, 4, 4096, 32000) > 0
+    assert lib.spec_medusa_heads_workspace_bytes(0, 4, 4096, 32000) == 0
     assert lib.spec_topk(P, sv.F32, 4, 1000, 1000, 17, P, P, NULL) == UNS                # s above 16
     assert lib.spec_topk(P, sv.F32, 4, 1000, 999, 10, P, P, NULL) == INV                 # stride below the row
     assert lib.spec_topk(P, sv.F32, 4, 8, 8, 9, P, P, NULL) == INV                       # s above the row
@@ -128,7 +139,9 @@ def test_heads_topk_expand_lm_head_refuse(lib):
                                 NULL) == UNS
     assert lib.spec_tree_expand(P, sv.BF16, 2, 10, 1000, P, 10, 0.0, P, P, P, P, P, 512, P, 10, NULL,
                                 NULL) == INV
-    assert lib.spec_lm_head(P, P, 64, 100, 32000, P, NULL, NULL) == INV                   # hidden not a multiple of 64
+    assert lib.spec_lm_head(P, P, 64, 100, 32000, P, P, 1 << 30, NULL, NULL) == INV       # hidden not a multiple of 64
+    assert lib.spec_lm_head(P, P, 64, 4096, 32000, P, P, 16, NULL, NULL) == CAP          # workspace too small
+    assert lib.spec_lm_head(P, P, 64, 4096, 32000, P, NULL, 1 << 30, NULL, NULL) == INV  # no workspace
 
 
 def test_refusal_codes_have_their_texts(lib):

@@ -7,7 +7,10 @@
 // "Typical acceptance" (p(x) > min(eps, delta exp(-H)); the step's first
 // token is the greedy one).  Rejection: "Drafters: ...", same section
 // (min(1, p/q); on rejection sample the target minus the drafter), with
-// the point-mass proposal of a deterministic tree sibling.
+// the point-mass proposal of a deterministic tree sibling, or with siblings
+// drawn from the drafter's distribution q at their parent (SpecInfer-style
+// multi-draft verification, "Medusa and EAGLE ... explained", section
+// "Medusa: heads, losses and trees").
 //
 // One cluster of nc CTAs per sequence (16 at batch < 16, 8 below 32, else
 // 4).  The cluster walks the tree from the root: each visited node's
@@ -226,6 +229,36 @@ __device__ __forceinline__ int first_column(const T *row, int lo, int hi) {
   return min(hi, lo + (int)threadIdx.x * (vec ? kVec : 1));
 }
 
+// Visit this CTA's slice of two rows at the same columns (two rows of one
+// [.., V] layout: equal alignment): f(x, a[x], b[x]).
+template <typename T, typename F>
+__device__ __forceinline__ void for_slice2(const T *ra, const T *rb, int lo, int hi, F &&f) {
+  constexpr int kVec = 16 / sizeof(T);
+  if (((hi - lo) % kVec) == 0 && (reinterpret_cast<uintptr_t>(ra + lo) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(rb + lo) & 15) == 0) {
+    const int nv = (hi - lo) / kVec;
+    const uint4 *sa = reinterpret_cast<const uint4 *>(ra + lo);
+    const uint4 *sb = reinterpret_cast<const uint4 *>(rb + lo);
+    for (int vi = threadIdx.x; vi < nv; vi += kThreads) {
+      const uint4 ua = sa[vi], ub = sb[vi];
+      float a[kVec], c[kVec];
+      if constexpr (sizeof(T) == 2) {
+        sv::bf16x8_to_f32(ua, a);
+        sv::bf16x8_to_f32(ub, c);
+      } else {
+        a[0] = __uint_as_float(ua.x); a[1] = __uint_as_float(ua.y);
+        a[2] = __uint_as_float(ua.z); a[3] = __uint_as_float(ua.w);
+        c[0] = __uint_as_float(ub.x); c[1] = __uint_as_float(ub.y);
+        c[2] = __uint_as_float(ub.z); c[3] = __uint_as_float(ub.w);
+      }
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) f(lo + vi * kVec + j, a[j], c[j]);
+    }
+  } else {
+    for (int x = lo + threadIdx.x; x < hi; x += kThreads) f(x, sv::to_f32(ra[x]), sv::to_f32(rb[x]));
+  }
+}
+
 // Uniform in (0, 1) for the sampling race from a 32-bit Philox word:
 // ((w >> 9) + 1/2) 2^-23, exact in float32.
 __device__ __forceinline__ float race_uniform(uint32_t w) {
@@ -242,7 +275,7 @@ __device__ __forceinline__ float race_key(float z, uint32_t w) {
 // of 64 are all resident in one wave.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
-    accept_kernel(int mode, const T *__restrict__ logits, int N, int V,
+    accept_kernel(int mode, const T *__restrict__ logits, const T *__restrict__ draft, int N, int V,
                   const int32_t *__restrict__ tok, const int32_t *__restrict__ parents,
                   const int32_t *__restrict__ first_child, const int32_t *__restrict__ next_sibling,
                   float temp, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
@@ -255,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int s_kid[kMaxNodes], s_nkid;   // children of the node being examined, in node order
   __shared__ float s_kex[kMaxNodes];         // exp(z - m) of each child's token
   __shared__ float s_ku[kMaxNodes];          // each child's accept draw
+  __shared__ float s_kq[kMaxNodes];          // stochastic siblings: q(tok) of each child
   __shared__ int s_exc[kMaxNodes];           // tokens removed from the residual
   __shared__ int s_nexc;
 
@@ -379,6 +413,81 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     const int a = row_argmax(base + (int64_t)s_next * V);
     if (threadIdx.x == 0) s_bonus = a;
+  } else if (mode == SPEC_ACCEPT_REJECT_STOCHASTIC) {
+    const T *qbase = draft + row0 * V;
+    int v = 0;
+    for (int guard = 0; guard < kMaxNodes; ++guard) {
+      const T *row = base + (int64_t)v * V, *qrow = qbase + (int64_t)v * V;
+      const Stats sp = row_stats(row, std::false_type{});
+      const Stats sq = row_stats(qrow, std::false_type{});
+      list_children(v);
+      if (threadIdx.x < 32) {
+        for (int j = lane; j < s_nkid; j += 32) {
+          const int c = s_kid[j], x = s_tok[c];
+          const bool ok = x >= 0 && x < V;
+          if (!ok) sv::report(status, SPEC_DEV_BAD_TOKEN);
+          s_kex[j] = ok ? __expf(sv::to_f32(row[x]) * inv_t - sp.m) / sp.S : 0.f;
+          s_kq[j] = ok ? __expf(sv::to_f32(qrow[x]) * inv_t - sq.m) / sq.S : -1.f;  // -1: never accepted
+          const sv::u32x4 w = sv::philox4x32_10(sv::u32x4{(uint32_t)c, 0u, (uint32_t)b, st}, k0, k1);
+          s_ku[j] = (float)(w.x >> 8) * 5.9604644775390625e-8f;  // 2^-24
+        }
+      }
+      __syncthreads();
+      // children in node order; every CTA holds the same shared values and
+      // the same cluster sums, so all take the same branch
+      float cq = 0.f, D = 1.f;
+      int nxt = -1;
+      const int nk = s_nkid;
+      for (int j = 0; j < nk; ++j) {
+        const float pj = s_kex[j], qj = s_kq[j];
+        if (qj < 0.f) continue;  // bad token: reported, never accepted, residual unchanged
+        // accept iff u < r(x) / q(x); q(x) = 0 (a token the drafter cannot
+        // propose) is always kept
+        if (!(qj > 0.f) || s_ku[j] * (D * qj) < fmaxf(pj - cq * qj, 0.f)) {
+          nxt = s_kid[j];
+          break;
+        }
+        const float c2 = cq + D;
+        float part = 0.f;
+        for_slice2(row, qrow, lo, hi, [&](int, float zp, float zq) {
+          part += fmaxf(__expf(zp * inv_t - sp.m) / sp.S - c2 * (__expf(zq * inv_t - sq.m) / sq.S), 0.f);
+        });
+        const float D2 = cl.stats(Stats{0.f, part, 0.f}).S;
+        if (!(D2 > 0.f)) {  // nothing left (rounding): sample from the target itself
+          cq = 0.f;
+          D = 1.f;
+          break;
+        }
+        cq = c2;
+        D = D2;
+      }
+      if (threadIdx.x == 0 && nxt >= 0) s_path[s_len++] = nxt;
+      if (nxt >= 0) {
+        v = nxt;
+        __syncthreads();
+        continue;
+      }
+      // residual sample: exponential race argmax_x log r(x) + G over the
+      // tokens with r(x) > 0 (same draws as the point-mass rule)
+      float bk = -INFINITY;
+      int bx = hi;
+      for_slice2(row, qrow, lo, hi, [&](int x, float zp, float zq) {
+        const float r = __expf(zp * inv_t - sp.m) / sp.S - cq * (__expf(zq * inv_t - sq.m) / sq.S);
+        if (!(r > 0.f)) return;
+        const sv::u32x4 w =
+            sv::philox4x32_10(sv::u32x4{(uint32_t)x >> 2, 256u + (uint32_t)v, (uint32_t)b, st}, k0, k1);
+        const uint32_t wx = (x & 2) ? ((x & 1) ? w.w : w.z) : ((x & 1) ? w.y : w.x);
+        const float key = race_key(__logf(r), wx);
+        if (key > bk) {
+          bk = key;
+          bx = x;
+        }
+      });
+      const unsigned long long best = cl.max_u64(bx < hi ? sv::rank_key(bk, (uint32_t)bx) : 0ull);
+      if (threadIdx.x == 0) s_bonus = (int)sv::key_index(best);
+      __syncthreads();
+      break;
+    }
   } else {  // SPEC_ACCEPT_REJECT
     int v = 0;
     for (int guard = 0; guard < kMaxNodes; ++guard) {
@@ -526,7 +635,8 @@ int cluster_size(int batch) {
 }
 
 template <typename T>
-int launch_accept(int mode, const void *logits, int batch, int n_nodes, int vocab, const int32_t *tok,
+int launch_accept(int mode, const void *logits, const void *draft, int batch, int n_nodes, int vocab,
+                  const int32_t *tok,
                   const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
                   float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
                   int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
@@ -542,7 +652,8 @@ int launch_accept(int mode, const void *logits, int batch, int n_nodes, int voca
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, accept_kernel<T>, mode, (const T *)logits, n_nodes, vocab, tok, parents,
+  return cudaLaunchKernelEx(&cfg, accept_kernel<T>, mode, (const T *)logits, (const T *)draft, n_nodes, vocab,
+                            tok, parents,
                             first_child, next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
                             acc_path, bonus, status) == cudaSuccess
              ? SPEC_OK
@@ -551,16 +662,16 @@ int launch_accept(int mode, const void *logits, int batch, int n_nodes, int voca
 
 }  // namespace
 
-int sv_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
+int sv_accept(int mode, const void *logits, const void *draft, int dtype, int batch, int n_nodes, int vocab,
               const int32_t *tok, const int32_t *parents, const int32_t *first_child,
               const int32_t *next_sibling, float temperature, float eps, float delta,
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
               int32_t *bonus, int32_t *status, cudaStream_t stream) {
   if (dtype == SPEC_BF16)
-    return launch_accept<__nv_bfloat16>(mode, logits, batch, n_nodes, vocab, tok, parents, first_child,
+    return launch_accept<__nv_bfloat16>(mode, logits, draft, batch, n_nodes, vocab, tok, parents, first_child,
                                         next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
                                         acc_path, bonus, status, stream);
-  return launch_accept<float>(mode, logits, batch, n_nodes, vocab, tok, parents, first_child, next_sibling,
+  return launch_accept<float>(mode, logits, draft, batch, n_nodes, vocab, tok, parents, first_child, next_sibling,
                               temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus, status,
                               stream);
 }

@@ -54,7 +54,7 @@ __device__ __forceinline__ void stage_rows(float *dst, const T *src, int nrows) 
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, int MW>
 __global__ void __launch_bounds__(kWarps * 32)
     attn_simt_kernel(const T *__restrict__ q, const T *__restrict__ kc, const T *__restrict__ vc,
                      const T *__restrict__ kt, const T *__restrict__ vt,
@@ -85,11 +85,14 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 
   float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DL];
-  uint64_t am[kRowsPerWarp];
+  // the row's ancestor mask: MW words of 64 nodes (ceil(N / 64) stored per node)
+  const int nw = (N + 63) >> 6;
+  uint64_t am[kRowsPerWarp][MW];
 #pragma unroll
   for (int k = 0; k < kRowsPerWarp; ++k) {
     const int r = rg * kRowsPerCta + warp * kRowsPerWarp + k;
-    am[k] = r < R ? anc[(int64_t)b * N + r / G] : 0ull;
+#pragma unroll
+    for (int w = 0; w < MW; ++w) am[k][w] = r < R && w < nw ? anc[((int64_t)b * N + r / G) * nw + w] : 0ull;
     m[k] = -INFINITY;
     l[k] = 0.f;
 #pragma unroll
@@ -133,9 +136,14 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int k = 0; k < RW; ++k) sc[k] = fmaf(qw[k * D + d], kd, sc[k]);
     }
     float mx[RW], p[RW];
+    // a 32-key tree tile lies inside one mask word (t0 is a multiple of 32)
 #pragma unroll
     for (int k = 0; k < RW; ++k) {
-      const bool vis = lane < nvalid && (!tree || ((am[k] >> (t0 + lane)) & 1ull));
+      uint64_t word = am[k][0];
+#pragma unroll
+      for (int w = 1; w < MW; ++w)
+        if ((t0 >> 6) == w) word = am[k][w];
+      const bool vis = lane < nvalid && (!tree || ((word >> ((t0 & 63) + lane)) & 1ull));
       sc[k] = vis ? sc[k] * scale_log2 : -INFINITY;
       mx[k] = sc[k];
     }
@@ -240,10 +248,10 @@ int launch_simt(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const 
                 cudaStream_t stream) {
   const int R = s.n_nodes * (s.hq / s.hkv);
   dim3 grid((R + kRowsPerCta - 1) / kRowsPerCta, p.splits, s.batch * s.hkv);
-  attn_simt_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(
-      (const T *)q, (const T *)kc, (const T *)vc, (const T *)kt, (const T *)vt, prefix_len, anc,
-      (T *)out, s.n_nodes, s.hq, s.hkv, s.s_max, s.max_prefix, p.splits, p.chunk,
-      scale * 1.4426950408889634f, (float *)ws, status);
+  auto kern = s.n_nodes <= 64 ? attn_simt_kernel<T, D, 1> : attn_simt_kernel<T, D, 4>;
+  kern<<<grid, kWarps * 32, 0, stream>>>((const T *)q, (const T *)kc, (const T *)vc, (const T *)kt, (const T *)vt,
+                                         prefix_len, anc, (T *)out, s.n_nodes, s.hq, s.hkv, s.s_max, s.max_prefix,
+                                         p.splits, p.chunk, scale * 1.4426950408889634f, (float *)ws, status);
   return sv_launch_status();
 }
 

@@ -566,7 +566,7 @@ int tc_best_splits(const SvAttnShape &s, const int32_t *prefix) {
 bool sv_attn_tc_supported(const SvAttnShape &s) {
   if (s.dtype != SPEC_BF16 || s.head_dim != kD) return false;
   const int G = s.hq / s.hkv;
-  return G <= 128 && (128 % G) == 0 && s.n_nodes * G <= 128;
+  return s.n_nodes <= 64 && G <= 128 && (128 % G) == 0 && s.n_nodes * G <= 128;
 }
 
 int sv_attn_tc_ragged_splits(const SvAttnShape &s, const int32_t *host_prefix) {

@@ -1117,7 +1117,7 @@ int tc2_clusters() {
 bool sv_attn_tc2_supported(const SvAttnShape &s) {
   if (s.dtype != SPEC_BF16 || s.head_dim != kD || s.hkv < 1) return false;
   const int G = s.hq / s.hkv;
-  return G <= 128 && (128 % G) == 0 && s.n_nodes * G > 128;
+  return s.n_nodes <= 64 && G <= 128 && (128 % G) == 0 && s.n_nodes * G > 128;
 }
 
 size_t sv_attn_tc2_ws_bytes() {

@@ -52,11 +52,22 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
 int sv_attn_combine(const SvAttnShape &s, const SvAttnPlan &p, const void *ws, void *out,
                     const int32_t *prefix_len, cudaStream_t stream);
 
+// Weight-streaming tensor-core GEMM (Medusa heads, LM head): launch
+// geometry and workspace share of one GEMM.
+struct SvGemmPlan {
+  int nt, mt;              // activation rows per MMA (N), 128-row MMAs per tile
+  int nk, tiles_pg, n_tiles, n_ctas, rows_per_launch;
+  long long units;         // (tile, 64-wide K chunk) pairs
+  size_t counter_bytes, partial_bytes;
+};
+SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows);
+size_t sv_medusa_heads_ws_bytes(int batch, int n_heads, int hidden, int vocab);
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
-                    int n_heads, int hidden, int vocab, float *z, float *logits,
-                    cudaStream_t stream);
-int sv_lm_head_tc(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-                  int32_t *status, cudaStream_t stream);
+                    int n_heads, int hidden, int vocab, void *z, float *logits, void *ws,
+                    int32_t *status, cudaStream_t stream);
+size_t sv_lm_head_ws_bytes(int rows, int hidden, int vocab);
+int sv_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
+               void *ws, int32_t *status, cudaStream_t stream);
 int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
             int32_t *idx, float *val, cudaStream_t stream);
 int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,
@@ -64,7 +75,7 @@ int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vo
                    int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
                    int pool_cap, int32_t *next_frontier, int n_next, int32_t *status,
                    cudaStream_t stream);
-int sv_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
+int sv_accept(int mode, const void *logits, const void *draft, int dtype, int batch, int n_nodes, int vocab,
               const int32_t *tok, const int32_t *parents, const int32_t *first_child,
               const int32_t *next_sibling, float temperature, float eps, float delta,
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,

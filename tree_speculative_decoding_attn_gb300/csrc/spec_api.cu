@@ -44,16 +44,28 @@ const char *spec_status_string(int status) {
   }
 }
 
-int spec_abi_version(void) { return 1; }
+int spec_abi_version(void) { return 2; }
+
+static bool gemm_shape_ok(int rows, int groups, int hidden, int m) {
+  return rows >= 1 && groups >= 1 && m >= 1 && hidden >= 64 && hidden % 64 == 0;
+}
+
+size_t spec_medusa_heads_workspace_bytes(int batch, int n_heads, int hidden, int vocab) {
+  if (!gemm_shape_ok(batch, n_heads, hidden, vocab)) return 0;
+  return sv_medusa_heads_ws_bytes(batch, n_heads, hidden, vocab);
+}
 
 int spec_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
-                      int n_heads, int hidden, int vocab, float *z, float *logits,
-                      spec_stream_t stream) {
-  if (!h || !w1 || !w2 || !z || !logits) return SPEC_ERR_INVALID_ARG;
-  if (batch < 1 || n_heads < 1 || hidden < 8 || vocab < 1 || hidden % 8) return SPEC_ERR_INVALID_ARG;
-  if (batch > 8) return SPEC_ERR_UNSUPPORTED;
-  if (!aligned16(h) || !aligned16(w1) || !aligned16(w2) || !aligned16(z)) return SPEC_ERR_INVALID_ARG;
-  return sv_medusa_heads(h, w1, b1, w2, batch, n_heads, hidden, vocab, z, logits, cs(stream));
+                      int n_heads, int hidden, int vocab, void *z, float *logits, void *workspace,
+                      size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream) {
+  if (!h || !w1 || !w2 || !z || !logits || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(batch, n_heads, hidden, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(w1) || !aligned16(w2) || !aligned16(z) || !aligned16(workspace) ||
+      (b1 && !aligned16(b1)))
+    return SPEC_ERR_INVALID_ARG;
+  if (workspace_bytes < sv_medusa_heads_ws_bytes(batch, n_heads, hidden, vocab)) return SPEC_ERR_CAPACITY;
+  return sv_medusa_heads(h, w1, b1, w2, batch, n_heads, hidden, vocab, z, logits, workspace, dev_status,
+                         cs(stream));
 }
 
 int spec_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
@@ -121,7 +133,8 @@ static int attn_check(int dtype, int batch, int n_nodes, int hq, int hkv, int he
     return SPEC_ERR_INVALID_ARG;
   if (hq % hkv) return SPEC_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return SPEC_ERR_UNSUPPORTED;
-  if (n_nodes > SPEC_MAX_NODES || (hq / hkv) * n_nodes > 512) return SPEC_ERR_UNSUPPORTED;
+  if (n_nodes > SPEC_MAX_NODES || (hq / hkv) * n_nodes > (n_nodes <= 64 ? 512 : 2048))
+    return SPEC_ERR_UNSUPPORTED;
   if (max_prefix > s_max) return SPEC_ERR_CAPACITY;
   return SPEC_OK;
 }
@@ -178,29 +191,37 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache, co
   return sv_attn_combine(s, p, workspace, out, prefix_len, cs(stream));
 }
 
-int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
-                 int32_t *dev_status, spec_stream_t stream) {
-  if (!hid || !w || !logits) return SPEC_ERR_INVALID_ARG;
-  if (rows < 1 || vocab < 1 || hidden < 64 || hidden % 64) return SPEC_ERR_INVALID_ARG;
-  if (!aligned16(hid) || !aligned16(w)) return SPEC_ERR_INVALID_ARG;
-  return sv_lm_head_tc(hid, w, rows, hidden, vocab, logits, dev_status, cs(stream));
+size_t spec_lm_head_workspace_bytes(int rows, int hidden, int vocab) {
+  if (!gemm_shape_ok(rows, 1, hidden, vocab)) return 0;
+  return sv_lm_head_ws_bytes(rows, hidden, vocab);
 }
 
-int spec_accept(int mode, const void *logits, int dtype, int batch, int n_nodes, int vocab,
-                const int32_t *tok, const int32_t *parents, const int32_t *first_child,
+int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
+                 void *workspace, size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream) {
+  if (!hid || !w || !logits || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (!gemm_shape_ok(rows, 1, hidden, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(hid) || !aligned16(w) || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  if (workspace_bytes < sv_lm_head_ws_bytes(rows, hidden, vocab)) return SPEC_ERR_CAPACITY;
+  return sv_lm_head(hid, w, rows, hidden, vocab, logits, workspace, dev_status, cs(stream));
+}
+
+int spec_accept(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
+                int n_nodes, int vocab, const int32_t *tok, const int32_t *parents, const int32_t *first_child,
                 const int32_t *next_sibling, float temperature, float eps, float delta,
                 uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
                 int32_t *bonus, int32_t *dev_status, spec_stream_t stream) {
   if (!logits || !tok || !parents || !first_child || !next_sibling || !acc_len || !acc_path || !bonus)
     return SPEC_ERR_INVALID_ARG;
-  if (mode != SPEC_ACCEPT_GREEDY && mode != SPEC_ACCEPT_TYPICAL && mode != SPEC_ACCEPT_REJECT)
+  if (mode != SPEC_ACCEPT_GREEDY && mode != SPEC_ACCEPT_TYPICAL && mode != SPEC_ACCEPT_REJECT &&
+      mode != SPEC_ACCEPT_REJECT_STOCHASTIC)
     return SPEC_ERR_INVALID_ARG;
+  if ((mode == SPEC_ACCEPT_REJECT_STOCHASTIC) != (draft_logits != nullptr)) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
   if (batch < 1 || n_nodes < 1 || vocab < 1 || path_cap < 1) return SPEC_ERR_INVALID_ARG;
   if (n_nodes > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
   if (mode != SPEC_ACCEPT_GREEDY && !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
   if (mode == SPEC_ACCEPT_GREEDY) temperature = 1.f;
-  return sv_accept(mode, logits, dtype, batch, n_nodes, vocab, tok, parents, first_child,
+  return sv_accept(mode, logits, draft_logits, dtype, batch, n_nodes, vocab, tok, parents, first_child,
                    next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len, acc_path,
                    bonus, dev_status, cs(stream));
 }

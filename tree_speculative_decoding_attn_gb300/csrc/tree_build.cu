@@ -14,42 +14,57 @@ namespace {
 constexpr int kMaxNodes = SPEC_MAX_NODES;
 
 // Emits depth/pos/mask/child links for one sequence's parents array held in
-// shared memory, with kids[v] = the set of v's children (N <= 64, so one
-// bit per node).  One thread per node; the walk is bounded because the
-// caller validated parent < node.
-__device__ void emit_tree_arrays(const int *par, const unsigned long long *kids, int i, int prefix,
+// shared memory, with kids[v * MW + w] = word w of the set of v's children
+// (MW words of 64 bits; trees of up to 64 * MW nodes).  The ancestor mask of
+// node i is written as `nw` = ceil(N / 64) words.  One thread per node; the
+// walk is bounded because the caller validated parent < node.
+template <int MW>
+__device__ void emit_tree_arrays(const int *par, const unsigned long long *kids, int i, int nw, int prefix,
                                  int64_t row, int32_t *depth, int32_t *pos, uint64_t *anc,
                                  int32_t *first_child, int32_t *next_sibling, int *depth_out) {
-  uint64_t m = 0;
+  uint64_t m[MW];
+#pragma unroll
+  for (int w = 0; w < MW; ++w) m[w] = 0;
   int d = -1;
   for (int c = i; c != -1; c = par[c]) {
-    m |= 1ull << c;
+#pragma unroll
+    for (int w = 0; w < MW; ++w)
+      if ((c >> 6) == w) m[w] |= 1ull << (c & 63);
     ++d;
   }
   // first child: the lowest child; next sibling: the parent's lowest child above i
-  const unsigned long long own = kids[i];
-  const int fc = own ? __ffsll((long long)own) - 1 : -1;
+  int fc = -1;
+#pragma unroll
+  for (int w = MW - 1; w >= 0; --w)
+    if (kids[i * MW + w]) fc = w * 64 + __ffsll((long long)kids[i * MW + w]) - 1;
   int ns = -1;
   if (i > 0) {
-    const unsigned long long later = i >= 63 ? 0ull : kids[par[i]] & (~0ull << (i + 1));
-    ns = later ? __ffsll((long long)later) - 1 : -1;
+    const int p = par[i];
+#pragma unroll
+    for (int w = MW - 1; w >= 0; --w) {
+      const int lo = i + 1 - w * 64;  // first bit of word w above i
+      const unsigned long long k = kids[p * MW + w];
+      const unsigned long long later = lo <= 0 ? k : lo >= 64 ? 0ull : k & (~0ull << lo);
+      if (later) ns = w * 64 + __ffsll((long long)later) - 1;
+    }
   }
   depth[row + i] = d;
   pos[row + i] = prefix + d;
-  anc[row + i] = m;
+  for (int w = 0; w < nw; ++w) anc[(row + i) * nw + w] = w < MW ? m[w] : 0ull;
   first_child[row + i] = fc;
   next_sibling[row + i] = ns;
   *depth_out = d;
 }
 
-__global__ void __launch_bounds__(kMaxNodes)
+template <int MW>
+__global__ void __launch_bounds__(64 * MW)
     build_static_kernel(const int32_t *__restrict__ parents, const int32_t *__restrict__ rank,
                         const int32_t *__restrict__ cand_tok, int cand_levels, int cand_s,
                         const int32_t *__restrict__ root_tok, const int32_t *__restrict__ prefix_len,
                         int N, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
                         int32_t *first_child, int32_t *next_sibling, int32_t *status) {
-  __shared__ int par[kMaxNodes];
-  __shared__ unsigned long long kids[kMaxNodes];
+  __shared__ int par[64 * MW];
+  __shared__ unsigned long long kids[64 * MW * MW];
   __shared__ int bad;
   const int b = blockIdx.x, i = threadIdx.x;
   // every load that does not depend on the tree walk is issued up front
@@ -58,14 +73,15 @@ __global__ void __launch_bounds__(kMaxNodes)
   const int r = tok && i > 0 && i < N ? rank[i] : 0;
   const int t0 = tok && i == 0 ? root_tok[b] : -1;
   if (i == 0) bad = 0;
-  kids[i] = 0ull;
+#pragma unroll
+  for (int w = 0; w < MW; ++w) kids[i * MW + w] = 0ull;
   __syncthreads();
   if (i < N) {
     par[i] = p;
     if (i == 0 ? p != -1 : (p < 0 || p >= i))
       atomicOr(&bad, 1);
     else if (i > 0)
-      atomicOr(&kids[p], 1ull << i);
+      atomicOr(&kids[p * MW + (i >> 6)], 1ull << (i & 63));
   }
   __syncthreads();
   if (bad) {
@@ -75,7 +91,7 @@ __global__ void __launch_bounds__(kMaxNodes)
   if (i >= N) return;
   const int64_t row = (int64_t)b * N;
   int d;
-  emit_tree_arrays(par, kids, i, P, row, depth, pos, anc, first_child, next_sibling, &d);
+  emit_tree_arrays<MW>(par, kids, i, (N + 63) >> 6, P, row, depth, pos, anc, first_child, next_sibling, &d);
   if (tok) {
     int t = -1;
     if (i == 0) {
@@ -114,6 +130,7 @@ __device__ __forceinline__ unsigned long long bitonic_steps_reg(unsigned long lo
   return a;
 }
 
+template <int MW>
 __global__ void __launch_bounds__(kDynThreads)
     build_dynamic_kernel(const int32_t *__restrict__ pool_parent, const int32_t *__restrict__ pool_tok,
                          const float *__restrict__ pool_conf, int M, const int32_t *__restrict__ prefix_len,
@@ -257,14 +274,14 @@ __global__ void __launch_bounds__(kDynThreads)
     unsigned mine = 0xFFFFFFFFu;
     if (t < N && my_depth == d) {
       mp = t == 0 ? -1 : kept_new[my_pslot];  // the parent was numbered one level up
-      mine = ((unsigned)(mp + 1) << 6) | (unsigned)t;
+      mine = ((unsigned)(mp + 1) << 8) | (unsigned)t;
     }
-    if (t < kMaxNodes) lkey[t] = mine;
+    if (t < 64 * MW) lkey[t] = mine;
     __syncthreads();
     if (t < N && my_depth == d) {
       int before = 0;
 #pragma unroll
-      for (int r = 0; r < kMaxNodes; r += 4) {
+      for (int r = 0; r < 64 * MW; r += 4) {
         const uint4 q = *reinterpret_cast<const uint4 *>(&lkey[r]);
         before += (q.x < mine) + (q.y < mine) + (q.z < mine) + (q.w < mine);
       }
@@ -283,15 +300,16 @@ __global__ void __launch_bounds__(kDynThreads)
     if (pool_index) pool_index[row + ni] = my_pool;
     if (val_out) val_out[row + ni] = val[my_pool];
   }
-  __shared__ unsigned long long kids[kMaxNodes];
-  if (t < N) kids[t] = 0ull;
+  __shared__ unsigned long long kids[kMaxNodes * MW];
+  if (t < N)
+    for (int w = 0; w < MW; ++w) kids[t * MW + w] = 0ull;
   __syncthreads();
-  if (t > 0 && t < N) atomicOr(&kids[new_par[t]], 1ull << t);
+  if (t > 0 && t < N) atomicOr(&kids[new_par[t] * MW + (t >> 6)], 1ull << (t & 63));
   __syncthreads();
   if (t < N) {
     int d;
-    emit_tree_arrays(new_par, kids, t, P, (int64_t)b * N, depth, pos, anc, first_child,
-                     next_sibling, &d);
+    emit_tree_arrays<MW>(new_par, kids, t, (N + 63) >> 6, P, (int64_t)b * N, depth, pos, anc, first_child,
+                         next_sibling, &d);
   }
 }
 
@@ -302,9 +320,14 @@ int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *
                     int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
                     int32_t *first_child, int32_t *next_sibling, int32_t *status,
                     cudaStream_t stream) {
-  build_static_kernel<<<batch, kMaxNodes, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s,
-                                                       root_tok, prefix_len, n, tok, depth, pos, anc,
-                                                       first_child, next_sibling, status);
+  if (n <= 64)
+    build_static_kernel<1><<<batch, 64, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s, root_tok,
+                                                     prefix_len, n, tok, depth, pos, anc, first_child,
+                                                     next_sibling, status);
+  else
+    build_static_kernel<4><<<batch, 256, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s, root_tok,
+                                                      prefix_len, n, tok, depth, pos, anc, first_child,
+                                                      next_sibling, status);
   return sv_launch_status();
 }
 
@@ -317,12 +340,11 @@ int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const 
   size_t M2 = 1;
   while (M2 < (size_t)M) M2 <<= 1;
   const size_t smem = M2 * 8 + (size_t)M * (4 + 4 + 4 + 4 + 4);  // key (sort width), parent, value, conf, depth, token
+  auto kern = n <= 64 ? build_dynamic_kernel<1> : build_dynamic_kernel<4>;
   if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(build_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem) != cudaSuccess)
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  build_dynamic_kernel<<<batch, kDynThreads, smem, stream>>>(
-      pool_parent, pool_tok, pool_conf, M, prefix_len, n, tok, parents_out, depth, pos, anc,
-      first_child, next_sibling, pool_index, val, status);
+  kern<<<batch, kDynThreads, smem, stream>>>(pool_parent, pool_tok, pool_conf, M, prefix_len, n, tok, parents_out,
+                                             depth, pos, anc, first_child, next_sibling, pool_index, val, status);
   return sv_launch_status();
 }

@@ -20,8 +20,13 @@ LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA = range(5)
 DEV_OK, DEV_BAD_PARENTS, DEV_CAPACITY, DEV_BAD_PATH, DEV_BAD_POOL, DEV_BAD_TOKEN, DEV_TIMEOUT, DEV_INTERNAL = range(8)
 F32, BF16 = 0, 1
-GREEDY, TYPICAL, REJECT = 0, 1, 2
-MAX_NODES = 64
+GREEDY, TYPICAL, REJECT, REJECT_STOCHASTIC = 0, 1, 2, 3
+MAX_NODES = 256
+
+
+def mask_words(n_nodes):
+    """uint64 words of one node's ancestor mask."""
+    return (n_nodes + 63) // 64
 
 _lib = None
 
@@ -29,7 +34,8 @@ _vp, _i, _f, _u64, _sz = C.c_void_p, C.c_int, C.c_float, C.c_uint64, C.c_size_t
 _SIGS = {
     "spec_status_string": ([_i], C.c_char_p),
     "spec_abi_version": ([], _i),
-    "spec_medusa_heads": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "spec_medusa_heads_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "spec_medusa_heads": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp, _vp], _i),
     "spec_topk": ([_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
     "spec_build_tree": ([_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i),
     "spec_build_tree_dynamic": ([_vp, _vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
@@ -41,9 +47,10 @@ _SIGS = {
                           _vp, _sz, _vp, _vp], _i),
     "tree_attn_verify_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                   _i, _vp, _vp], _i),
-    "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp, _vp], _i),
-    "spec_accept": ([_i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp, _vp,
-                     _vp, _vp], _i),
+    "spec_lm_head_workspace_bytes": ([_i, _i, _i], _sz),
+    "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp, _vp], _i),
+    "spec_accept": ([_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp,
+                     _vp, _vp, _vp], _i),
     "kv_commit": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
 }
 
@@ -115,15 +122,30 @@ def spec_abi_version() -> int:
 # ---------------------------------------------------------------- entry points
 
 
-def spec_medusa_heads(h, w1, b1, w2, z, logits):
+def spec_medusa_heads_workspace_bytes(batch, n_heads, hidden, vocab):
+    return int(load().spec_medusa_heads_workspace_bytes(batch, n_heads, hidden, vocab))
+
+
+def _scratch(nbytes, like):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=like.device)
+
+
+def spec_medusa_heads(h, w1, b1, w2, z, logits, workspace=None, dev_status=None):
+    """z (bf16) and logits (float32) of every head; ``workspace`` (uint8,
+    at least spec_medusa_heads_workspace_bytes) is allocated per call when
+    not given."""
     B, d = h.shape
     K, V = w2.shape[0], w2.shape[1]
-    for t in (h, w1, w2):
+    for t in (h, w1, w2, z):
         _want(t, torch.bfloat16)
     _want(b1, torch.bfloat16)
-    _want(z, torch.float32); _want(logits, torch.float32)
-    _check("spec_medusa_heads", load().spec_medusa_heads(_p(h), _p(w1), _p(b1), _p(w2), B, K, d, V,
-                                                         _p(z), _p(logits), _stream()))
+    _want(logits, torch.float32)
+    if workspace is None:
+        workspace = _scratch(spec_medusa_heads_workspace_bytes(B, K, d, V), h)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_medusa_heads", load().spec_medusa_heads(_p(h), _p(w1), _p(b1), _p(w2), B, K, d, V, _p(z),
+                                                         _p(logits), _p(workspace), ws_bytes, _p(dev_status),
+                                                         _stream()))
 
 
 def spec_topk(rows, s, idx_out, val_out=None, row_len=None):
@@ -223,19 +245,29 @@ def tree_attn_verify_noalloc(q, k_cache, v_cache, k_tree, v_tree, prefix_len, an
         _stream()))
 
 
-def spec_lm_head(hid, w, logits, dev_status=None):
+def spec_lm_head_workspace_bytes(rows, hidden, vocab):
+    return int(load().spec_lm_head_workspace_bytes(rows, hidden, vocab))
+
+
+def spec_lm_head(hid, w, logits, dev_status=None, workspace=None):
     R, d = hid.shape
     V = w.shape[0]
     _want(hid, torch.bfloat16); _want(w, torch.bfloat16); _want(logits, torch.float32)
-    _check("spec_lm_head", load().spec_lm_head(_p(hid), _p(w), R, d, V, _p(logits), _p(dev_status), _stream()))
+    if workspace is None:
+        workspace = _scratch(spec_lm_head_workspace_bytes(R, d, V), hid)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_lm_head", load().spec_lm_head(_p(hid), _p(w), R, d, V, _p(logits), _p(workspace), ws_bytes,
+                                               _p(dev_status), _stream()))
 
 
 def spec_accept(mode, logits, tok, parents, first_child, next_sibling, acc_len, acc_path, bonus,
-                temperature=1.0, eps=0.0, delta=0.0, seed=0, step=0, dev_status=None):
+                temperature=1.0, eps=0.0, delta=0.0, seed=0, step=0, dev_status=None, draft_logits=None):
     B, N, V = logits.shape
     _want(logits, torch.float32, torch.bfloat16)
+    if draft_logits is not None and (draft_logits.dtype != logits.dtype or draft_logits.shape != logits.shape):
+        raise TypeError("draft_logits must match logits in dtype and shape")
     _check("spec_accept", load().spec_accept(
-        int(mode), _p(logits), _DT[logits.dtype], B, N, V, _p(tok), _p(parents), _p(first_child),
+        int(mode), _p(logits), _p(draft_logits), _DT[logits.dtype], B, N, V, _p(tok), _p(parents), _p(first_child),
         _p(next_sibling), float(temperature), float(eps), float(delta), int(seed), int(step),
         acc_path.shape[1], _p(acc_len), _p(acc_path), _p(bonus), _p(dev_status), _stream()))
 

@@ -138,6 +138,25 @@ def random_tree(seed: int, n: int, caps) -> TreeShape:
     return _bfs_shape(par, rank, level)
 
 
+def dense_tree(branching, n: int) -> TreeShape:
+    """The Cartesian tree with ``branching[l]`` children per node on level l,
+    breadth-first (children by rank), cut after its first ``n`` nodes: every
+    node of level l + 1 before any of level l + 2 (the dense trees of the
+    multi-candidate Medusa setting)."""
+    par, rank, level = [-1], [0], [0]
+    head = 0
+    while len(par) < n and head < len(par):
+        v = head
+        head += 1
+        if level[v] >= len(branching):
+            continue
+        for r in range(branching[level[v]]):
+            if len(par) == n:
+                break
+            par.append(v); rank.append(r); level.append(level[v] + 1)
+    return TreeShape(np.array(par, np.int32), np.array(rank, np.int32), np.array(level, np.int32))
+
+
 def candidate_tokens(seed: int, batch: int, n_levels: int, s: int, vocab: int) -> np.ndarray:
     """cand_tok[b, l, r]: token proposed with rank r for level l+1 (distinct per row)."""
     g = stream(seed, "cand_tok")
