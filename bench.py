@@ -277,15 +277,30 @@ class GpuStep:
                                                                dev_status=self.status, workspace=self.lm_ws), 1,
                             2 * V * d + 2 * B * N * d + 4 * B * N * V))
 
+    def lm_head_logits(self):
+        """The unfused LM head's float32 logits of this step's tree rows
+        (reference for tests of the fused stage)."""
+        w = self.w
+        B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
+        self.sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V), dev_status=self.status)
+        return self.logits
+
     def _accept_commit_stages(self):
         sv, w = self.sv, self.w
         mode = {"greedy": sv.GREEDY, "typical": sv.TYPICAL, "reject": sv.REJECT}[w.accept]
         parents = self.par_out if w.tree == "dynamic" else self.parents_b
         self.step_counter = 0
-        self.stages.append(("accept", lambda: sv.spec_accept(
+        if getattr(self, "fused_accept", False):
+            B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
+            self.stages.append(("lm_head_accept", lambda: sv.spec_lm_head_accept(
+                mode, self.hid.view(B, N, d), self.wlm, self.tok, parents, self.fc, self.ns, self.acc_len,
+                self.acc_path, self.bonus, temperature=w.temperature, eps=w.eps, delta=w.delta,
+                dev_status=self.status, workspace=self.lm_ws), 2, 2 * V * d + 2 * B * N * d))
+        else:
+            self.stages.append(("accept", lambda: sv.spec_accept(
             mode, self.logits, self.tok, parents, self.fc, self.ns, self.acc_len, self.acc_path, self.bonus,
-            temperature=w.temperature, eps=w.eps, delta=w.delta, seed=w.seed, step=0, dev_status=self.status),
-            1, None))
+                temperature=w.temperature, eps=w.eps, delta=w.delta, seed=w.seed, step=0, dev_status=self.status),
+                1, None))
         self.stages.append(("kv_commit", lambda: sv.kv_commit(
             self.kc, self.vc, self.kt, self.vt, self.acc_len, self.acc_path, self.d_prefix, self.new_prefix,
             self.status), 1, None))
@@ -308,7 +323,7 @@ class GpuStep:
         esz = 2 if self.tdt == self.torch.bfloat16 else 4
         rows = int((L + 1).sum())
         out = {}
-        if self.w.accept == "typical":
+        if self.w.accept == "typical" or getattr(self, "fused_accept", False):
             out["accept"] = None
         else:
             out["accept"] = rows * self.logits_bytes_row

@@ -70,7 +70,8 @@ enum {
   SPEC_DEV_BAD_POOL = 4,     /* pool parent not earlier / confidence > 1    */
   SPEC_DEV_BAD_TOKEN = 5,    /* token id outside [0, vocab)                 */
   SPEC_DEV_TIMEOUT = 6,      /* a bounded device-side wait gave up          */
-  SPEC_DEV_INTERNAL = 7      /* a kernel's own layout precondition failed   */
+  SPEC_DEV_INTERNAL = 7,     /* a kernel's own layout precondition failed   */
+  SPEC_DEV_BAD_BLOCK = 8     /* a block-table entry outside the block pool  */
 };
 
 /* dtype codes */
@@ -171,6 +172,28 @@ int spec_build_tree(const int32_t *parents, const int32_t *rank, const int32_t *
                     int32_t *tok, int32_t *depth, int32_t *pos_ids, uint64_t *anc_mask,
                     int32_t *first_child, int32_t *next_sibling, int32_t *dev_status,
                     spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_build_tree_batch -- one tree per sequence, of up to n_nodes nodes
+ * each, in one launch (ragged multi-tree batching of serving: requests with
+ * different tree budgets and shapes; "5.3 Medusa、EAGLE 与 MTP", section 8,
+ * closing remarks on batching trees of different requests).
+ *   parents  [batch, n_nodes] int32: sequence b's parents array (rules of
+ *            spec_build_tree) over its first n_valid[b] entries
+ *   n_valid  [batch] int32 (1 .. n_nodes), or NULL for all n_nodes: entries
+ *            at and past it are absent nodes (padding)
+ *   tok_in   [batch, n_nodes] int32 tokens copied to `tok`, or NULL (then
+ *            `tok` is not written)
+ * Outputs as spec_build_tree.  An absent node is nobody's child, has depth
+ * 0, position prefix_len, a mask of itself only and no child links, so
+ * attention, acceptance and commit never reach it (its attention output is
+ * computed but meaningless).
+ * ------------------------------------------------------------------ */
+int spec_build_tree_batch(const int32_t *parents, const int32_t *n_valid, const int32_t *tok_in,
+                          const int32_t *prefix_len, int batch, int n_nodes, int32_t *tok,
+                          int32_t *depth, int32_t *pos_ids, uint64_t *anc_mask,
+                          int32_t *first_child, int32_t *next_sibling, int32_t *dev_status,
+                          spec_stream_t stream);
 
 /* --------------------------------------------------------------------
  * spec_build_tree_dynamic -- EAGLE-2 style tree from a drafted pool.
@@ -277,6 +300,28 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache,
                      int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
+ * tree_attn_verify_paged -- tree_attn_verify over a paged prefix cache
+ * (block tables of paged KV: "5.3 Medusa、EAGLE 与 MTP", section 8, closing
+ * remarks).
+ *   k_pages, v_pages [num_blocks, hkv, block_size, head_dim]: the block pool
+ *   block_table [batch, max_blocks] int32: prefix positions
+ *            [j * block_size, (j + 1) * block_size) of sequence b are rows of
+ *            block block_table[b, j]; entries past the prefix are not read
+ *   block_size  a multiple of 128 (one 128-key tile never spans blocks)
+ * Everything else as tree_attn_verify, with each sequence's capacity
+ * max_blocks * block_size in place of s_max; the workspace size is
+ * tree_attn_workspace_bytes() of the same shape.  A block id outside
+ * [0, num_blocks) sets SPEC_DEV_BAD_BLOCK (those keys read as zeros).
+ * ------------------------------------------------------------------ */
+int tree_attn_verify_paged(const void *q, const void *k_pages, const void *v_pages,
+                           const int32_t *block_table, int block_size, int num_blocks,
+                           int max_blocks, const void *k_tree, const void *v_tree,
+                           const int32_t *prefix_len, const uint64_t *anc_mask, void *out,
+                           int dtype, int batch, int n_nodes, int hq, int hkv, int head_dim,
+                           int max_prefix, float scale, int num_splits, void *workspace,
+                           size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
  * tree_attn_verify_noalloc -- tree_attn_verify without a caller workspace.
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot allocate device memory: a plugin inside a host runtime that
@@ -317,6 +362,42 @@ int tree_attn_verify_noalloc(const void *q, const void *k_cache, const void *v_c
 size_t spec_lm_head_workspace_bytes(int rows, int hidden, int vocab);
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
                  void *workspace, size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * spec_lm_head_accept -- LM head over the tree nodes fused with greedy or
+ * typical acceptance: the target logits never reach device memory.
+ * "Medusa, explained", step 6 (one pass scores every node) and step 7 /
+ * section "Typical acceptance"; "Drafters: ...", section "Why the answer
+ * does not change".
+ *
+ *   hid    [batch, n_nodes, hidden] bf16: the final hidden state of every
+ *          tree node
+ *   w      [vocab, hidden] bf16: LM-head weight
+ *   tok, parents, first_child, next_sibling [batch, n_nodes] int32 (as
+ *          spec_accept)
+ *   mode   SPEC_ACCEPT_GREEDY or SPEC_ACCEPT_TYPICAL with the rules of
+ *          spec_accept applied to logits = hid . w^T (float32 accumulation
+ *          on the tensor cores).  The rejection modes need the full
+ *          residual row: use spec_lm_head + spec_accept
+ *          (SPEC_ERR_UNSUPPORTED here).
+ *   workspace  device scratch of spec_lm_head_accept_workspace_bytes()
+ *          bytes (16-byte aligned, uninitialised; separate per overlapping
+ *          call): per (node, 32 vocabulary rows) softmax statistics
+ *          records, about hidden / 256 times smaller than the logits.
+ * The greedy argmax is taken over the same float32 values spec_lm_head
+ * would write, so greedy results equal spec_lm_head + spec_accept bit for
+ * bit.  Typical: a child's probability uses its own logit recomputed as a
+ * float32 dot product; entropy and normaliser come from the records.
+ * Outputs as spec_accept.  dev_status: SPEC_DEV_BAD_TOKEN,
+ * SPEC_DEV_BAD_PARENTS, SPEC_DEV_CAPACITY (path_cap), SPEC_DEV_TIMEOUT.
+ * ------------------------------------------------------------------ */
+size_t spec_lm_head_accept_workspace_bytes(int batch, int n_nodes, int hidden, int vocab);
+int spec_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n_nodes, int hidden,
+                        int vocab, const int32_t *tok, const int32_t *parents,
+                        const int32_t *first_child, const int32_t *next_sibling,
+                        float temperature, float eps, float delta, int path_cap,
+                        int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
  * spec_accept -- accept the longest target-agreeing path.
@@ -389,6 +470,27 @@ int kv_commit(void *k_cache, void *v_cache, const void *k_tree, const void *v_tr
               int head_dim, const int32_t *acc_len, const int32_t *acc_path, int path_cap,
               const int32_t *prefix_len, int32_t *prefix_len_out, int32_t *dev_status,
               spec_stream_t stream);
+
+/* --------------------------------------------------------------------
+ * kv_commit_paged -- kv_commit into a paged cache: the accepted path is an
+ * append to each sequence's block list (block tables of paged KV: "5.3
+ * Medusa、EAGLE 与 MTP", section 8).
+ *   k_pages, v_pages [n_layers, num_blocks, hkv, block_size, head_dim]
+ *   block_table [batch, max_blocks] int32 (one table for every layer); the
+ *            blocks holding positions prefix_len .. prefix_len + acc_len
+ *            must already be assigned (the caller's allocator)
+ * Row prefix_len[b] + j of sequence b is row (prefix_len[b] + j) %
+ * block_size of block block_table[b, (prefix_len[b] + j) / block_size].
+ * Every destination block is checked first: a block id outside
+ * [0, num_blocks) sets SPEC_DEV_BAD_BLOCK and that sequence is neither
+ * copied nor advanced.  Otherwise as kv_commit.
+ * ------------------------------------------------------------------ */
+int kv_commit_paged(void *k_pages, void *v_pages, const int32_t *block_table, int block_size,
+                    int num_blocks, int max_blocks, const void *k_tree, const void *v_tree,
+                    int elem_bytes, int n_layers, int batch, int hkv, int n_nodes, int head_dim,
+                    const int32_t *acc_len, const int32_t *acc_path, int path_cap,
+                    const int32_t *prefix_len, int32_t *prefix_len_out, int32_t *dev_status,
+                    spec_stream_t stream);
 
 #ifdef __cplusplus
 }

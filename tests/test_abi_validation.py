@@ -148,3 +148,37 @@ def test_refusal_codes_have_their_texts(lib):
     assert _attn(lib, q=NULL) == INV and lib.spec_status_string(INV) == b"invalid argument"
     assert _attn(lib, D=96) == UNS and b"unsupported" in lib.spec_status_string(UNS)
     assert _attn(lib, max_prefix=2048) == CAP and b"capacity" in lib.spec_status_string(CAP)
+
+
+def test_paged_batch_and_fused_entry_points_refuse(lib):
+    # tree_attn_verify_paged(q, kp, vp, table, bs, nb, max_blocks, kt, vt, prefix, anc, out, dtype, B, N, hq, hkv,
+    #                        D, max_prefix, scale, splits, ws, ws_bytes, status, stream)
+    paged = lambda bs=128, nb=8, mb=4, table=P, mp=256, N=16: lib.tree_attn_verify_paged(
+        P, P, P, table, bs, nb, mb, P, P, P, P, P, sv.BF16, 2, N, 16, 2, 128, mp, 0.0, 0, P, 1 << 30, NULL, NULL)
+    assert paged(bs=64) == INV                   # blocks must hold whole 128-key tiles
+    assert paged(table=NULL) == INV
+    assert paged(nb=0) == INV
+    assert paged(mp=600) == CAP                  # prefix beyond max_blocks * block_size
+    assert paged(N=257) == UNS
+    # kv_commit_paged(kp, vp, table, bs, nb, mb, kt, vt, esz, layers, B, hkv, N, D, len, path, cap, prefix, out, st, s)
+    commit = lambda esz=2, table=P, D=128, cap=8: lib.kv_commit_paged(
+        P, P, table, 128, 8, 4, P, P, esz, 1, 2, 2, 16, D, P, P, cap, P, NULL, NULL, NULL)
+    assert commit(table=NULL) == INV
+    assert commit(esz=3) == UNS
+    assert commit(D=6) == UNS
+    assert commit(cap=300) == UNS
+    # spec_build_tree_batch(parents, n_valid, tok_in, prefix, B, N, tok, depth, pos, anc, fc, ns, status, stream)
+    batch = lambda par=P, N=16, tok_in=NULL, tok=NULL: lib.spec_build_tree_batch(
+        par, NULL, tok_in, P, 2, N, tok, P, P, P, P, P, NULL, NULL)
+    assert batch(par=NULL) == INV
+    assert batch(N=257) == UNS
+    assert batch(tok_in=P) == INV                # tokens given but nowhere to copy them
+    # spec_lm_head_accept(mode, hid, w, B, N, hidden, V, tok, par, fc, ns, T, eps, delta, cap, len, path, bonus,
+    #                     ws, ws_bytes, status, stream)
+    fused = lambda mode=sv.GREEDY, d=4096, ws_bytes=1 << 30, T=1.0: lib.spec_lm_head_accept(
+        mode, P, P, 1, 64, d, 32000, P, P, P, P, T, 0.3, 0.09, 6, P, P, P, P, ws_bytes, NULL, NULL)
+    assert fused(mode=sv.REJECT) == UNS          # rejection needs the whole residual row
+    assert fused(mode=sv.REJECT_STOCHASTIC) == UNS
+    assert fused(d=4100) == INV
+    assert fused(mode=sv.TYPICAL, T=0.0) == INV
+    assert fused(ws_bytes=16) == CAP

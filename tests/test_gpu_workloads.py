@@ -158,6 +158,10 @@ def test_full_step_matches_oracle(name):
         z, hl = H.medusa_heads(h, w1, None, w2)
         _close(f"{name} medusa z", host(step.z), z)
         _close(f"{name} medusa head logits", host(step.head_logits), hl)
+        # the step's LM head is fused with the acceptance; its reference is
+        # acceptance on the unfused LM head's logits (same GEMM schedule)
+        step.lm_head_logits()
+        torch.cuda.synchronize()
         _close(f"{name} lm head logits", host(step.logits).reshape(-1, w.vocab), H.lm_head(host(step.hid), wlm))
         del w1, w2
     ref_tree = _tree_reference(step)

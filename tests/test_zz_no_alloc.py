@@ -23,10 +23,10 @@ pytestmark = pytest.mark.gpu
 TOL = (2e-2, 1e-2)
 
 
-def _inputs(seed, B=1, hq=32, hkv=32, D=128, P=2048, n=64):
+def _inputs(seed, B=1, hq=32, hkv=32, D=128, P=2048, n=64, caps=(10, 10, 10, 10)):
     w = synth.Workload("noalloc", seed, batch=B, hq=hq, hkv=hkv, head_dim=D, dtype="bf16", prefix=(P, P),
-                       n_nodes=n, n_levels=5, vocab=10, accept="greedy", tree="random")
-    shape = synth.random_tree(seed, n, (10, 10, 10, 10))
+                       n_nodes=n, n_levels=len(caps) + 1, vocab=10, accept="greedy", tree="random")
+    shape = synth.random_tree(seed, n, caps)
     prefix = synth.prefix_lengths(w)
     q, kc, vc, kt, vt = synth.attention_inputs(w, prefix, q_scale=2.0)
     anc = np.broadcast_to(T.mask_words(T.depth_and_mask(shape.parents)[1]), (B, n)).copy()
@@ -49,6 +49,29 @@ def test_noalloc_matches_workspace_entry_point_twice():
                             num_splits=splits, workspace=ws, dev_status=st)
         sv.tree_attn_verify_noalloc(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], got,
                                     x["max_prefix"], num_splits=splits, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(host(st)[0]) == 0, f"call {call}"
+        ok, excess = within(host(got), host(ref), *TOL)
+        assert ok, f"call {call}: max excess {excess}"
+
+
+def test_noalloc_sm_pair_path_matches_twice():
+    """The 70B serving shape (64 query / 8 KV heads, 32 nodes: 256 query rows
+    per KV head) runs on the SM-pair kernel, whose partial rows of cut row
+    groups and cut descriptors also live in the fixed array."""
+    B, hq, hkv, n = 16, 64, 8, 32
+    for call, seed in enumerate((21, 22)):
+        x = _inputs(seed, B=B, hq=hq, hkv=hkv, P=1000 + 300 * call, n=n, caps=(4, 3, 2))
+        need = sv.tree_attn_workspace_bytes(torch.bfloat16, B, n, hq, hkv, 128, x["max_prefix"])
+        assert 0 < need <= sv.NOALLOC_SCRATCH_BYTES
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        ref = torch.empty_like(x["q"])
+        got = torch.full_like(x["q"], float("nan"))
+        st = zeros_i32(1)
+        sv.tree_attn_verify(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], ref, x["max_prefix"],
+                            workspace=ws, dev_status=st)
+        sv.tree_attn_verify_noalloc(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], got,
+                                    x["max_prefix"], dev_status=st)
         torch.cuda.synchronize()
         assert int(host(st)[0]) == 0, f"call {call}"
         ok, excess = within(host(got), host(ref), *TOL)

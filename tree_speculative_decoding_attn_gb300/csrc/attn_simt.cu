@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kWarps * 32)
                      const T *__restrict__ kt, const T *__restrict__ vt,
                      const int32_t *__restrict__ prefix_len, const uint64_t *__restrict__ anc,
                      T *__restrict__ out, int N, int Hq, int Hkv, int s_max, int max_prefix,
-                     int splits, int chunk, float scale_log2, float *ws, int32_t *status) {
+                     int splits, int chunk, float scale_log2, float *ws, int32_t *status, const sv::KvPages pg) {
   constexpr int DL = D / 32;  // output dims per lane
   __shared__ float sK[kKeyTile * (D + 1)];
   __shared__ float sV[kKeyTile * D];
@@ -116,8 +116,12 @@ __global__ void __launch_bounds__(kWarps * 32)
       stage_rows<T, D, D + 1>(sK, kt + kt_base + (int64_t)t0 * D, nvalid);
       stage_rows<T, D, D>(sV, vt + kt_base + (int64_t)t0 * D, nvalid);
     } else {
-      stage_rows<T, D, D + 1>(sK, kc + kv_base + (int64_t)t0 * D, nvalid);
-      stage_rows<T, D, D>(sV, vc + kv_base + (int64_t)t0 * D, nvalid);
+      // a 32-key tile lies inside one cache block (block sizes are multiples of 32)
+      const int row = pg.table ? sv::kv_row(pg, b, Hkv, kvh, s_max, t0, status) : 0;
+      const T *ks = pg.table ? kc + (int64_t)(row < 0 ? 0 : row) * D : kc + kv_base + (int64_t)t0 * D;
+      const T *vs = pg.table ? vc + (int64_t)(row < 0 ? 0 : row) * D : vc + kv_base + (int64_t)t0 * D;
+      stage_rows<T, D, D + 1>(sK, ks, row < 0 ? 0 : nvalid);
+      stage_rows<T, D, D>(sV, vs, row < 0 ? 0 : nvalid);
     }
     __syncthreads();
     // The warp's rows go through each step together, so their dot products,
@@ -251,7 +255,8 @@ int launch_simt(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const 
   auto kern = s.n_nodes <= 64 ? attn_simt_kernel<T, D, 1> : attn_simt_kernel<T, D, 4>;
   kern<<<grid, kWarps * 32, 0, stream>>>((const T *)q, (const T *)kc, (const T *)vc, (const T *)kt, (const T *)vt,
                                          prefix_len, anc, (T *)out, s.n_nodes, s.hq, s.hkv, s.s_max, s.max_prefix,
-                                         p.splits, p.chunk, scale * 1.4426950408889634f, (float *)ws, status);
+                                         p.splits, p.chunk, scale * 1.4426950408889634f, (float *)ws, status,
+                                         sv::KvPages{s.block_table, s.block_size, s.max_blocks, s.num_blocks});
   return sv_launch_status();
 }
 

@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_vt, const int32_t *__restrict__ prefix_len,
                    const uint64_t *__restrict__ anc, __nv_bfloat16 *__restrict__ out, float *__restrict__ ws,
                    int N, int Hq, int Hkv, int s_max, int max_prefix, int splits, int chunk, float scale_log2,
-                   int32_t *status) {
+                   int32_t *status, const sv::KvPages pg) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sQ = smem;
@@ -162,9 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producers
     // lane 0 streams Q then K, lane 1 streams V: the two rings refill
     // independently (K is released by S, V only after the softmax and PV)
+    // (a 128-key tile lies inside one cache block: block sizes are multiples
+    // of 128; a bad block id gives row -1, which TMA reads as zeros)
     auto tile_row = [&](int j, bool &tree) {
       tree = with_tree && j == n_tiles - 1;
-      return tree ? bh * N : bh * s_max + k0 + j * kBN;
+      return tree ? bh * N : sv::kv_row(pg, b, Hkv, kvh, s_max, k0 + j * kBN, status);
     };
     auto stream_ring = [&](bool is_v) {
       const int n_st = is_v ? kVStages : kKStages;
@@ -503,7 +505,8 @@ int launch_tc(dim3 grid, cudaStream_t stream, const CUtensorMap &mq, const CUten
     return SPEC_ERR_CUDA;
   attn_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
       mq, mkc, mvc, mkt, mvt, prefix_len, anc, (__nv_bfloat16 *)out, (float *)ws, s.n_nodes, s.hq, s.hkv, s.s_max,
-      s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status);
+      s.max_prefix, p.splits, p.chunk, scale * 1.4426950408889634f, status,
+      sv::KvPages{s.block_table, s.block_size, s.max_blocks, s.num_blocks});
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -606,8 +609,10 @@ int sv_attn_tc(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const v
     if (make_map(&mq, q, 4, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
   }
   {
-    // (at least one row so the map is valid when no prefix tile is ever loaded)
-    const cuuint64_t rows = (cuuint64_t)s.batch * s.hkv * s.s_max;
+    // (at least one row so the map is valid when no prefix tile is ever
+    // loaded; a paged cache is one pool of blocks)
+    const cuuint64_t rows = s.block_table ? (cuuint64_t)s.num_blocks * s.hkv * s.block_size
+                                          : (cuuint64_t)s.batch * s.hkv * s.s_max;
     const cuuint64_t dims[2] = {(cuuint64_t)kD, rows > 0 ? rows : 1};
     const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)kBN};

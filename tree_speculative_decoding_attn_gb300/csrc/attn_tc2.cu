@@ -117,6 +117,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(256, 128, 0, 1);  // V MN-major (di
 struct Sched {
   const int32_t *prefix_len;
   int batch, hkv, pairs, n_nodes, s_max, max_prefix, n_clusters;
+  sv::KvPages pg;                                          // prefix cache addressing
   __device__ int gpb() const { return hkv * pairs; }  // row groups per sequence
 };
 
@@ -477,7 +478,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // warm L2 with this CTA's half of tile g + kPrefetch
           const int pbh = cpf.b * s.hkv + cpf.gi / pairs;
           const bool ptree = cpf.t == 0;
-          const int prow = ptree ? pbh * N : pbh * s.s_max + (cpf.t - 1) * kBN;
+          const int prow = ptree ? pbh * N : sv::kv_row(s.pg, cpf.b, s.hkv, cpf.gi / pairs, s.s_max, (cpf.t - 1) * kBN,
+                                                        nullptr);
           if (is_v) {
             tma_prefetch_2d(ptree ? &tm_vt : &tm_vc, 64 * (int)rank, prow);
           } else {
@@ -509,7 +511,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         const bool tree = c.t == 0;
-        const int row0 = tree ? bh * N : bh * s.s_max + (c.t - 1) * kBN;
+        // (a 128-key tile lies inside one cache block: block sizes are
+        // multiples of 128; a bad block id gives row -1, read as zeros)
+        const int row0 = tree ? bh * N : sv::kv_row(s.pg, c.b, s.hkv, kvh, s.s_max, (c.t - 1) * kBN, status);
         if (is_v) {
           mbar_expect_tx(land, kVBytes);
           tma_load_2d(sV + st * kVBytes, tree ? &tm_vt : &tm_vc, 64 * (int)rank, row0, land);
@@ -1150,8 +1154,10 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
     if (make_map(&mo, out, 5, dims, strides, box) != SPEC_OK) return SPEC_ERR_CUDA;
   }
   {
-    // (at least one row so the map is valid when no prefix tile is ever loaded)
-    const cuuint64_t rows = (cuuint64_t)s.batch * s.hkv * s.s_max;
+    // (at least one row so the map is valid when no prefix tile is ever
+    // loaded; a paged cache is one pool of blocks)
+    const cuuint64_t rows = s.block_table ? (cuuint64_t)s.num_blocks * s.hkv * s.block_size
+                                          : (cuuint64_t)s.batch * s.hkv * s.s_max;
     const cuuint64_t dims[2] = {(cuuint64_t)kD, rows > 0 ? rows : 1};
     const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
     const cuuint32_t kbox[2] = {64, 64}, vbox[2] = {64, (cuuint32_t)kBN};
@@ -1174,6 +1180,7 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
   sc.s_max = s.s_max;
   sc.max_prefix = s.max_prefix;
   sc.n_clusters = C;
+  sc.pg = sv::KvPages{s.block_table, s.block_size, s.max_blocks, s.num_blocks};
   if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
     return SPEC_ERR_CUDA;

@@ -110,6 +110,28 @@ __device__ __forceinline__ u32x4 philox4x32_10(u32x4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// Prefix cache addressing.  Contiguous: [batch, hkv, s_max, D], row
+// (b * hkv + h) * s_max + key.  Paged: blocks [num_blocks, hkv, block_size,
+// D] and a block table [batch, max_blocks]; key k of sequence b lives in
+// block table[b][k / block_size] at row k % block_size, i.e. at row
+// (block * hkv + h) * block_size + k % block_size of the pool.
+struct KvPages {
+  const int32_t *table;  // null: contiguous cache
+  int block_size, max_blocks, num_blocks;
+};
+// Row of (sequence b, KV head h, prefix key `key`), or -1 for a block id
+// outside the pool (reported as SPEC_DEV_BAD_BLOCK; callers read zeros).
+__device__ __forceinline__ int kv_row(const KvPages &pg, int b, int hkv, int h, int s_max, int key,
+                                      int32_t *status) {
+  if (!pg.table) return (b * hkv + h) * s_max + key;
+  const int blk = __ldg(pg.table + (int64_t)b * pg.max_blocks + key / pg.block_size);
+  if (blk < 0 || blk >= pg.num_blocks) {
+    report(status, SPEC_DEV_BAD_BLOCK);
+    return -1;
+  }
+  return (blk * hkv + h) * pg.block_size + key % pg.block_size;
+}
+
 }  // namespace sv
 
 // Launch wrapper status helper (host).

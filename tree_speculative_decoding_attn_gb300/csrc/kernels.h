@@ -10,6 +10,12 @@ int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *
                     int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
                     int32_t *first_child, int32_t *next_sibling, int32_t *status, cudaStream_t stream);
 
+int sv_build_batch(const int32_t *parents, int par_stride, const int32_t *n_valid, const int32_t *tok_in,
+                   const int32_t *rank, const int32_t *cand_tok, int cand_levels, int cand_s,
+                   const int32_t *root_tok, const int32_t *prefix_len, int batch, int n, int32_t *tok,
+                   int32_t *depth, int32_t *pos, uint64_t *anc, int32_t *first_child, int32_t *next_sibling,
+                   int32_t *status, cudaStream_t stream);
+
 int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const float *pool_conf,
                      int M, const int32_t *prefix_len, int batch, int n, int32_t *tok,
                      int32_t *parents_out, int32_t *depth, int32_t *pos, uint64_t *anc,
@@ -23,6 +29,10 @@ int sv_build_dynamic(const int32_t *pool_parent, const int32_t *pool_tok, const 
 inline constexpr int sv_partial_stride(int head_dim) { return head_dim + 4; }
 struct SvAttnShape {
   int dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix;
+  // paged prefix cache (block_table null: contiguous [batch, hkv, s_max, D];
+  // paged: s_max = max_blocks * block_size is each sequence's capacity)
+  const int32_t *block_table;
+  int block_size, max_blocks, num_blocks;
 };
 struct SvAttnPlan {
   int use_tc;        // 2 = pair (cta_group::2) kernel, 1 = tcgen05 kernel, 0 = CUDA-core kernel
@@ -61,6 +71,13 @@ struct SvGemmPlan {
   size_t counter_bytes, partial_bytes;
 };
 SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows);
+// One weight-streaming GEMM (all row blocks).  epi: 0 float32 logits, 1
+// bf16 SiLU + residual, 2 softmax statistics records (float4 per 32 W rows
+// and activation row: max logit, sum exp, first moment, argmax).
+int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, int M, int K, int G, int rows,
+             int epi, float *out, void *zout, const void *res, const void *bias, int *counters, float *partial,
+             bool counters_clear, bool pdl, int32_t *status, cudaStream_t stream, float inv_t = 1.f,
+             void *stats = nullptr);
 size_t sv_medusa_heads_ws_bytes(int batch, int n_heads, int hidden, int vocab);
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,
                     int n_heads, int hidden, int vocab, void *z, float *logits, void *ws,
@@ -68,6 +85,12 @@ int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w
 size_t sv_lm_head_ws_bytes(int rows, int hidden, int vocab);
 int sv_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
                void *ws, int32_t *status, cudaStream_t stream);
+size_t sv_lm_head_accept_ws_bytes(int batch, int n_nodes, int hidden, int vocab);
+int sv_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n_nodes, int hidden, int vocab,
+                      const int32_t *tok, const int32_t *parents, const int32_t *first_child,
+                      const int32_t *next_sibling, float temperature, float eps, float delta, int path_cap,
+                      int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *ws, int32_t *status,
+                      cudaStream_t stream);
 int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
             int32_t *idx, float *val, cudaStream_t stream);
 int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,
@@ -80,7 +103,14 @@ int sv_accept(int mode, const void *logits, const void *draft, int dtype, int ba
               const int32_t *next_sibling, float temperature, float eps, float delta,
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
               int32_t *bonus, int32_t *status, cudaStream_t stream);
+// kv_commit; `pages` (table null: contiguous) addresses a paged cache
+// [n_layers, num_blocks, hkv, block_size, D] with s_max = max_blocks *
+// block_size.
+struct SvPages {
+  const int32_t *table;
+  int block_size, max_blocks, num_blocks;
+};
 int sv_kv_commit(void *kc, void *vc, const void *kt, const void *vt, int elem_bytes, int n_layers,
                  int batch, int hkv, int s_max, int n_nodes, int head_dim, const int32_t *acc_len,
                  const int32_t *acc_path, int path_cap, const int32_t *prefix_len,
-                 int32_t *prefix_len_out, int32_t *status, cudaStream_t stream);
+                 int32_t *prefix_len_out, int32_t *status, cudaStream_t stream, SvPages pages = SvPages{});

@@ -196,6 +196,42 @@ size_t spec_lm_head_workspace_bytes(int rows, int hidden, int vocab) {
   return sv_lm_head_ws_bytes(rows, hidden, vocab);
 }
 
+int tree_attn_verify_paged(const void *q, const void *k_pages, const void *v_pages, const int32_t *block_table,
+                           int block_size, int num_blocks, int max_blocks, const void *k_tree, const void *v_tree,
+                           const int32_t *prefix_len, const uint64_t *anc_mask, void *out, int dtype, int batch,
+                           int n_nodes, int hq, int hkv, int head_dim, int max_prefix, float scale, int num_splits,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream) {
+  if (!q || !k_pages || !v_pages || !block_table || !k_tree || !v_tree || !prefix_len || !anc_mask || !out)
+    return SPEC_ERR_INVALID_ARG;
+  if (block_size < 128 || block_size % 128 || num_blocks < 1 || max_blocks < 1) return SPEC_ERR_INVALID_ARG;
+  if ((long long)max_blocks * block_size > (1 << 30) || (long long)num_blocks * hkv * block_size > (1 << 30))
+    return SPEC_ERR_UNSUPPORTED;
+  const int s_max = max_blocks * block_size;
+  int rc = attn_check(dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix);
+  if (rc != SPEC_OK) return rc;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_tree) || !aligned16(v_tree) ||
+      !aligned16(out))
+    return SPEC_ERR_INVALID_ARG;
+  SvAttnShape s{dtype, batch, n_nodes, hq, hkv, head_dim, s_max, max_prefix};
+  s.block_table = block_table;
+  s.block_size = block_size;
+  s.max_blocks = max_blocks;
+  s.num_blocks = num_blocks;
+  const SvAttnPlan p = sv_attn_plan(s, num_splits);
+  if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned16(workspace)))
+    return SPEC_ERR_CAPACITY;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)head_dim);
+  if (p.use_tc == 2)
+    return sv_attn_tc2(s, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale, workspace,
+                       workspace_bytes, dev_status, cs(stream));
+  rc = p.use_tc ? sv_attn_tc(s, p, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale,
+                             workspace, dev_status, cs(stream))
+                : sv_attn_simt(s, p, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale,
+                               workspace, dev_status, cs(stream));
+  if (rc != SPEC_OK || p.splits == 1) return rc;
+  return sv_attn_combine(s, p, workspace, out, prefix_len, cs(stream));
+}
+
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,
                  void *workspace, size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream) {
   if (!hid || !w || !logits || !workspace) return SPEC_ERR_INVALID_ARG;
@@ -203,6 +239,34 @@ int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab
   if (!aligned16(hid) || !aligned16(w) || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
   if (workspace_bytes < sv_lm_head_ws_bytes(rows, hidden, vocab)) return SPEC_ERR_CAPACITY;
   return sv_lm_head(hid, w, rows, hidden, vocab, logits, workspace, dev_status, cs(stream));
+}
+
+size_t spec_lm_head_accept_workspace_bytes(int batch, int n_nodes, int hidden, int vocab) {
+  if (batch < 1 || n_nodes < 1 || n_nodes > SPEC_MAX_NODES || !gemm_shape_ok(batch * n_nodes, 1, hidden, vocab))
+    return 0;
+  return sv_lm_head_accept_ws_bytes(batch, n_nodes, hidden, vocab);
+}
+
+int spec_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n_nodes, int hidden, int vocab,
+                        const int32_t *tok, const int32_t *parents, const int32_t *first_child,
+                        const int32_t *next_sibling, float temperature, float eps, float delta, int path_cap,
+                        int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *workspace,
+                        size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream) {
+  if (!hid || !w || !tok || !parents || !first_child || !next_sibling || !acc_len || !acc_path || !bonus ||
+      !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  if (mode == SPEC_ACCEPT_REJECT || mode == SPEC_ACCEPT_REJECT_STOCHASTIC) return SPEC_ERR_UNSUPPORTED;
+  if (mode != SPEC_ACCEPT_GREEDY && mode != SPEC_ACCEPT_TYPICAL) return SPEC_ERR_INVALID_ARG;
+  if (batch < 1 || n_nodes < 1 || path_cap < 1) return SPEC_ERR_INVALID_ARG;
+  if (n_nodes > SPEC_MAX_NODES || path_cap > SPEC_MAX_NODES + 1) return SPEC_ERR_UNSUPPORTED;
+  if (!gemm_shape_ok(batch * n_nodes, 1, hidden, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (!aligned16(hid) || !aligned16(w) || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  if (mode == SPEC_ACCEPT_TYPICAL && !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
+  if (mode == SPEC_ACCEPT_GREEDY) temperature = 1.f;
+  if (workspace_bytes < sv_lm_head_accept_ws_bytes(batch, n_nodes, hidden, vocab)) return SPEC_ERR_CAPACITY;
+  return sv_lm_head_accept(mode, hid, w, batch, n_nodes, hidden, vocab, tok, parents, first_child, next_sibling,
+                           temperature, eps, delta, path_cap, acc_len, acc_path, bonus, workspace, dev_status,
+                           cs(stream));
 }
 
 int spec_accept(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
@@ -224,6 +288,41 @@ int spec_accept(int mode, const void *logits, const void *draft_logits, int dtyp
   return sv_accept(mode, logits, draft_logits, dtype, batch, n_nodes, vocab, tok, parents, first_child,
                    next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len, acc_path,
                    bonus, dev_status, cs(stream));
+}
+
+int spec_build_tree_batch(const int32_t *parents, const int32_t *n_valid, const int32_t *tok_in,
+                          const int32_t *prefix_len, int batch, int n_nodes, int32_t *tok, int32_t *depth,
+                          int32_t *pos_ids, uint64_t *anc_mask, int32_t *first_child, int32_t *next_sibling,
+                          int32_t *dev_status, spec_stream_t stream) {
+  if (!parents || !prefix_len || !depth || !pos_ids || !anc_mask || !first_child || !next_sibling)
+    return SPEC_ERR_INVALID_ARG;
+  if (batch < 1 || n_nodes < 1 || (tok_in && !tok)) return SPEC_ERR_INVALID_ARG;
+  if (n_nodes > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
+  return sv_build_batch(parents, n_nodes, n_valid, tok_in, nullptr, nullptr, 0, 1, nullptr, prefix_len, batch,
+                        n_nodes, tok_in ? tok : nullptr, depth, pos_ids, anc_mask, first_child, next_sibling,
+                        dev_status, cs(stream));
+}
+
+int kv_commit_paged(void *k_pages, void *v_pages, const int32_t *block_table, int block_size, int num_blocks,
+                    int max_blocks, const void *k_tree, const void *v_tree, int elem_bytes, int n_layers,
+                    int batch, int hkv, int n_nodes, int head_dim, const int32_t *acc_len,
+                    const int32_t *acc_path, int path_cap, const int32_t *prefix_len, int32_t *prefix_len_out,
+                    int32_t *dev_status, spec_stream_t stream) {
+  if (!k_pages || !v_pages || !block_table || !k_tree || !v_tree || !acc_len || !acc_path || !prefix_len)
+    return SPEC_ERR_INVALID_ARG;
+  if (elem_bytes != 2 && elem_bytes != 4) return SPEC_ERR_UNSUPPORTED;
+  if (block_size < 1 || num_blocks < 1 || max_blocks < 1 || n_layers < 1 || batch < 1 || hkv < 1 ||
+      n_nodes < 1 || head_dim < 1 || path_cap < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (n_nodes > SPEC_MAX_NODES || path_cap > SPEC_MAX_NODES + 1) return SPEC_ERR_UNSUPPORTED;
+  if ((head_dim * elem_bytes) % 16) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)max_blocks * block_size > (1 << 30) || (long long)num_blocks * hkv * block_size > (1 << 30))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(k_pages) || !aligned16(v_pages) || !aligned16(k_tree) || !aligned16(v_tree))
+    return SPEC_ERR_INVALID_ARG;
+  return sv_kv_commit(k_pages, v_pages, k_tree, v_tree, elem_bytes, n_layers, batch, hkv, max_blocks * block_size,
+                      n_nodes, head_dim, acc_len, acc_path, path_cap, prefix_len, prefix_len_out, dev_status,
+                      cs(stream), SvPages{block_table, block_size, max_blocks, num_blocks});
 }
 
 int kv_commit(void *k_cache, void *v_cache, const void *k_tree, const void *v_tree, int elem_bytes,

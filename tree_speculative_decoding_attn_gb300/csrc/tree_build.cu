@@ -38,7 +38,7 @@ __device__ void emit_tree_arrays(const int *par, const unsigned long long *kids,
   for (int w = MW - 1; w >= 0; --w)
     if (kids[i * MW + w]) fc = w * 64 + __ffsll((long long)kids[i * MW + w]) - 1;
   int ns = -1;
-  if (i > 0) {
+  if (i > 0 && par[i] >= 0) {
     const int p = par[i];
 #pragma unroll
     for (int w = MW - 1; w >= 0; --w) {
@@ -56,9 +56,16 @@ __device__ void emit_tree_arrays(const int *par, const unsigned long long *kids,
   *depth_out = d;
 }
 
+// One CTA per sequence.  parents: shared [N] (par_stride 0) or per sequence
+// [batch, N] (par_stride N).  n_valid (optional, [batch]): nodes at and past
+// it are absent (a smaller tree padded to N): they are nobody's child and
+// get depth 0, position prefix_len, a mask of themselves and no links.
+// Tokens: tok_in [batch, N] copied when given, else the static candidate
+// table (cand_tok), else not written.
 template <int MW>
 __global__ void __launch_bounds__(64 * MW)
-    build_static_kernel(const int32_t *__restrict__ parents, const int32_t *__restrict__ rank,
+    build_static_kernel(const int32_t *__restrict__ parents, int par_stride, const int32_t *__restrict__ n_valid,
+                        const int32_t *__restrict__ tok_in, const int32_t *__restrict__ rank,
                         const int32_t *__restrict__ cand_tok, int cand_levels, int cand_s,
                         const int32_t *__restrict__ root_tok, const int32_t *__restrict__ prefix_len,
                         int N, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
@@ -68,20 +75,25 @@ __global__ void __launch_bounds__(64 * MW)
   __shared__ int bad;
   const int b = blockIdx.x, i = threadIdx.x;
   // every load that does not depend on the tree walk is issued up front
-  const int p = i < N ? parents[i] : 0;
+  const int nv = n_valid ? n_valid[b] : N;
+  const int p = i < N ? parents[(int64_t)b * par_stride + i] : 0;
   const int P = prefix_len[b];
-  const int r = tok && i > 0 && i < N ? rank[i] : 0;
-  const int t0 = tok && i == 0 ? root_tok[b] : -1;
-  if (i == 0) bad = 0;
+  const int r = tok && !tok_in && i > 0 && i < N ? rank[i] : 0;
+  const int t0 = tok && !tok_in && i == 0 ? root_tok[b] : -1;
+  const int tin = tok && tok_in && i < N ? tok_in[(int64_t)b * N + i] : -1;
+  if (i == 0) bad = nv < 1 || nv > N;
 #pragma unroll
   for (int w = 0; w < MW; ++w) kids[i * MW + w] = 0ull;
   __syncthreads();
   if (i < N) {
-    par[i] = p;
-    if (i == 0 ? p != -1 : (p < 0 || p >= i))
+    par[i] = i < nv ? p : -1;
+    if (i >= nv) {
+      // absent node
+    } else if (i == 0 ? p != -1 : (p < 0 || p >= i)) {
       atomicOr(&bad, 1);
-    else if (i > 0)
+    } else if (i > 0) {
       atomicOr(&kids[p * MW + (i >> 6)], 1ull << (i & 63));
+    }
   }
   __syncthreads();
   if (bad) {
@@ -92,10 +104,14 @@ __global__ void __launch_bounds__(64 * MW)
   const int64_t row = (int64_t)b * N;
   int d;
   emit_tree_arrays<MW>(par, kids, i, (N + 63) >> 6, P, row, depth, pos, anc, first_child, next_sibling, &d);
-  if (tok) {
+  if (tok && tok_in) {
+    tok[row + i] = tin;
+  } else if (tok) {
     int t = -1;
     if (i == 0) {
       t = t0;
+    } else if (i >= nv) {
+      t = -1;
     } else {
       if (d - 1 < cand_levels && r >= 0 && r < cand_s)
         t = cand_tok[((int64_t)b * cand_levels + (d - 1)) * cand_s + r];
@@ -320,14 +336,23 @@ int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *
                     int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
                     int32_t *first_child, int32_t *next_sibling, int32_t *status,
                     cudaStream_t stream) {
+  return sv_build_batch(parents, 0, nullptr, nullptr, rank, cand_tok, cand_levels, cand_s, root_tok, prefix_len,
+                        batch, n, tok, depth, pos, anc, first_child, next_sibling, status, stream);
+}
+
+int sv_build_batch(const int32_t *parents, int par_stride, const int32_t *n_valid, const int32_t *tok_in,
+                   const int32_t *rank, const int32_t *cand_tok, int cand_levels, int cand_s,
+                   const int32_t *root_tok, const int32_t *prefix_len, int batch, int n, int32_t *tok,
+                   int32_t *depth, int32_t *pos, uint64_t *anc, int32_t *first_child, int32_t *next_sibling,
+                   int32_t *status, cudaStream_t stream) {
   if (n <= 64)
-    build_static_kernel<1><<<batch, 64, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s, root_tok,
-                                                     prefix_len, n, tok, depth, pos, anc, first_child,
-                                                     next_sibling, status);
+    build_static_kernel<1><<<batch, 64, 0, stream>>>(parents, par_stride, n_valid, tok_in, rank, cand_tok,
+                                                     cand_levels, cand_s, root_tok, prefix_len, n, tok, depth, pos,
+                                                     anc, first_child, next_sibling, status);
   else
-    build_static_kernel<4><<<batch, 256, 0, stream>>>(parents, rank, cand_tok, cand_levels, cand_s, root_tok,
-                                                      prefix_len, n, tok, depth, pos, anc, first_child,
-                                                      next_sibling, status);
+    build_static_kernel<4><<<batch, 256, 0, stream>>>(parents, par_stride, n_valid, tok_in, rank, cand_tok,
+                                                      cand_levels, cand_s, root_tok, prefix_len, n, tok, depth, pos,
+                                                      anc, first_child, next_sibling, status);
   return sv_launch_status();
 }
 

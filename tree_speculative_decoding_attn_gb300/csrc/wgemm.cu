@@ -54,7 +54,7 @@ constexpr int kThreads = 192;
 constexpr int kKC = 64;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint32_t kSmemBudget = 216 * 1024;
-enum { kEpiF32 = 0, kEpiSiluRes = 1 };
+enum { kEpiF32 = 0, kEpiSiluRes = 1, kEpiStats = 2 };
 
 template <int NT, int MT>
 struct Cfg {
@@ -69,21 +69,34 @@ struct Cfg {
   static constexpr uint32_t kSmem = kStages * kStage + 1024 + 256;
 };
 
+// One GEMM of a launch.  A launch runs one or two of them ("phases") over
+// the same activation rows and reduction length; with two, every CTA first
+// takes its share of phase 0, then its share of phase 1, and phase 1 reads
+// phase 0's bf16 output as its X operand (the Medusa W1 -> W2 chain).
+struct Phase {
+  int M, tiles_pg, n_tiles, x_grouped, epi;
+  long long units;             // n_tiles * nk
+  float *out;                  // kEpiF32: [*, G, M] float32
+  __nv_bfloat16 *zout;         // kEpiSiluRes: [*, G, M] bf16
+  const __nv_bfloat16 *res;    // kEpiSiluRes: [*, M]
+  const __nv_bfloat16 *bias;   // kEpiSiluRes: [G, M] or null
+  float *partial;              // [2 * n_ctas][ceil(rows / 4)][kM][4] float32
+  int *counters;               // [n_tiles * 4] (one per tile and epilogue warp), zero at launch
+};
+
 struct WArgs {
-  int M, K, G;           // W rows per group, reduction length, groups
-  int rows;              // valid activation rows of this launch (<= NT)
-  int r0;                // first activation row of this launch
-  int x_grouped;         // 1: group g reads X group g; 0: X group 0
-  int nk, tiles_pg, n_tiles, n_ctas;
-  long long units;       // n_tiles * nk
-  float *out;            // kEpiF32: [*, G, M] float32
-  __nv_bfloat16 *zout;   // kEpiSiluRes: [*, G, M] bf16
-  const __nv_bfloat16 *res;   // kEpiSiluRes: [*, M]
-  const __nv_bfloat16 *bias;  // kEpiSiluRes: [G, M] or null
-  float *partial;        // [2 * n_ctas][rows][kM] float32
-  int *counters;         // [n_tiles * 4] (one per tile and epilogue warp), zero at launch
+  Phase ph[2];
+  int nphase;
+  int K, G;                    // reduction length, groups (heads)
+  int rows;                    // valid activation rows of this launch (<= NT)
+  int r0;                      // first activation row of this launch
+  int nk, n_ctas;
   int32_t *status;
   int pdl_wait;
+  float inv_t;                 // kEpiStats: 1 / temperature
+  float4 *stats;               // kEpiStats: [*, rec_stride] records of 32 W rows
+  int rec_stride;              // kEpiStats: records per activation row (tiles * MT * 4)
+  int *xready;                 // chained phases: count of phase-0 (tile, quarter) results stored
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long units, long long ctas) {
@@ -94,22 +107,63 @@ __device__ __forceinline__ int cta_of_unit(long long x, long long units, long lo
   return (int)(((x + 1) * ctas - 1) / units);
 }
 
-template <int NT, int MT, int EPI>
-__device__ __forceinline__ void store_final(const WArgs &a, int g, int m, int r, float acc) {
-  if (r >= a.rows || m >= a.M) return;
-  const long long o = ((long long)(a.r0 + r) * a.G + g) * a.M + m;
-  if constexpr (EPI == kEpiF32) {
-    a.out[o] = acc;
+// kEpiStats: softmax statistics of the 32 W rows a warp holds for activation
+// row r (warp-collective: r is the same in every lane).  Record =
+// (max logit, sum exp(z - zmax), sum exp(z - zmax) (z - zmax), argmax) with
+// z = logit / T and zmax = max logit / T; argmax ties go to the lowest W row,
+// -1 (and a zero sum) when none of the 32 rows exists.
+// (kept out of line: it is warp-collective and called from several loops,
+// and inlining it everywhere bloats the kernel's instruction footprint)
+__device__ __noinline__ void store_stats(const WArgs &a, const Phase &ph, int m, int rec, int r, float acc) {
+  if (r >= a.rows) return;
+  const bool valid = m < ph.M;
+  const unsigned long long best = sv::warp_max_u64_redux(valid ? sv::rank_key(acc, (uint32_t)m) : 0ull);
+  const float mx = sv::key_value(best);
+  const float zmax = mx * a.inv_t, z = acc * a.inv_t;
+  const float e = valid ? __expf(z - zmax) : 0.f;
+  const float S = sv::warp_sum(e), Q = sv::warp_sum(e * (z - zmax));
+  if ((threadIdx.x & 31) == 0)
+    a.stats[(long long)(a.r0 + r) * a.rec_stride + rec] =
+        make_float4(mx, S, Q, __int_as_float(best ? (int)sv::key_index(best) : -1));
+}
+
+__device__ __forceinline__ void store_final(const WArgs &a, const Phase &ph, int g, int m, int r, float acc) {
+  if (r >= a.rows || m >= ph.M) return;
+  const long long o = ((long long)(a.r0 + r) * a.G + g) * ph.M + m;
+  if (ph.epi == kEpiF32) {
+    ph.out[o] = acc;
   } else {
-    float x = acc + (a.bias ? __bfloat162float(a.bias[(long long)g * a.M + m]) : 0.f);
+    float x = acc + (ph.bias ? __bfloat162float(ph.bias[(long long)g * ph.M + m]) : 0.f);
     x = x / (1.f + __expf(-x));
-    a.zout[o] = __float2bfloat16_rn(__bfloat162float(a.res[(long long)(a.r0 + r) * a.M + m]) + x);
+    ph.zout[o] = __float2bfloat16_rn(__bfloat162float(ph.res[(long long)(a.r0 + r) * ph.M + m]) + x);
   }
 }
 
-template <int NT, int MT, int EPI>
+// Store (or reduce into statistics) 4 consecutive rows of one W row.
+__device__ __forceinline__ void store4(const WArgs &a, const Phase &ph, int g, int m, int rec, int r, float4 v) {
+  if (ph.epi == kEpiStats) {
+    store_stats(a, ph, m, rec, r, v.x);
+    store_stats(a, ph, m, rec, r + 1, v.y);
+    store_stats(a, ph, m, rec, r + 2, v.z);
+    store_stats(a, ph, m, rec, r + 3, v.w);
+  } else {
+    store_final(a, ph, g, m, r, v.x);
+    store_final(a, ph, g, m, r + 1, v.y);
+    store_final(a, ph, g, m, r + 2, v.z);
+    store_final(a, ph, g, m, r + 3, v.w);
+  }
+}
+
+// The CTA's units of phase p: [lo, hi).
+__device__ __forceinline__ void phase_range(const WArgs &a, int p, int c, long long &lo, long long &hi) {
+  lo = range_start(c, a.ph[p].units, a.n_ctas);
+  hi = range_start(c + 1, a.ph[p].units, a.n_ctas);
+}
+
+template <int NT, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
-    wgemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, const WArgs a) {
+    wgemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_x0,
+                 const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x1, const WArgs a) {
   using C = Cfg<NT, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -123,7 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  const long long u0 = range_start(c, a.units, a.n_ctas), u1 = range_start(c + 1, a.units, a.n_ctas);
+  long long lo0, hi0, lo1 = 0, hi1 = 0;
+  phase_range(a, 0, c, lo0, hi0);
+  if (a.nphase > 1) phase_range(a, 1, c, lo1, hi1);
+  const long long n0 = hi0 - lo0, n_it = n0 + (hi1 - lo1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -137,8 +194,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    tma_prefetch_desc(&tm_w);
-    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w0);
+    tma_prefetch_desc(&tm_x0);
+    if (a.nphase > 1) {
+      tma_prefetch_desc(&tm_w1);
+      tma_prefetch_desc(&tm_x1);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -151,41 +212,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      const long long n_it = u1 - u0;
-      const long long pre = a.pdl_wait ? (n_it < C::kStages ? n_it : C::kStages) : 0;
-      // the first ring's weight chunks do not depend on the previous kernel
-      for (long long i = 0; i < pre; ++i) {
-        const long long u = u0 + i;
-        const int t = (int)(u / a.nk), k = (int)(u % a.nk);
-        uint8_t *st = smem + i * C::kStage;
-        mbar_expect_tx(&full[i], C::kStage);
-        tma_load_3d_hint(st, &tm_w, k * kKC, (t % a.tiles_pg) * C::kM, t / a.tiles_pg, &full[i], pol);
-      }
-      if (a.pdl_wait) grid_dep_wait();
-      long long issued = 0;
-      for (long long i = 0; i < n_it; ++i) {
+      // item i of this CTA: phase 0 units first, then phase 1
+      auto item = [&](long long i, int &p, int &t, int &k) {
+        p = i < n0 ? 0 : 1;
+        const long long u = p == 0 ? lo0 + i : lo1 + (i - n0);
+        t = (int)(u / a.nk);
+        k = (int)(u % a.nk);
+      };
+      auto load_w = [&](long long i) {
+        int p, t, k;
+        item(i, p, t, k);
         const int s = (int)(i % C::kStages);
-        if (i >= pre) {
+        mbar_expect_tx(&full[s], C::kStage);
+        tma_load_3d_hint(smem + s * C::kStage, p ? &tm_w1 : &tm_w0, k * kKC, (t % a.ph[p].tiles_pg) * C::kM,
+                         t / a.ph[p].tiles_pg, &full[s], pol);
+      };
+      auto load_x = [&](long long i) {
+        int p, t, k;
+        item(i, p, t, k);
+        const int s = (int)(i % C::kStages);
+        tma_load_3d(smem + s * C::kStage + C::kWBytes, p ? &tm_x1 : &tm_x0, k * kKC,
+                    a.ph[p].x_grouped ? t / a.ph[p].tiles_pg : 0, a.r0, &full[s]);
+      };
+      // the first ring's weight chunks do not depend on the previous kernel
+      const long long pre = a.pdl_wait ? (n_it < C::kStages ? n_it : C::kStages) : 0;
+      for (long long i = 0; i < pre; ++i) load_w(i);
+      if (a.pdl_wait) grid_dep_wait();
+      long long w_issued = pre, issued = 0;
+      bool x_ok = a.nphase < 2;  // phase 1's X is phase 0's output
+      for (long long i = 0; i < n_it; ++i) {
+        if (i >= w_issued) {
+          const int s = (int)(i % C::kStages);
           if (!mbar_wait(&empty[s], (uint32_t)((i / C::kStages) & 1) ^ 1u, kWaitLimit) || *abort_flag) {
             *abort_flag = 1;
             sv::report(a.status, SPEC_DEV_TIMEOUT);
             break;
           }
+          load_w(i);
+          w_issued = i + 1;
         }
-        const long long u = u0 + i;
-        const int t = (int)(u / a.nk), k = (int)(u % a.nk);
-        const int g = t / a.tiles_pg;
-        uint8_t *st = smem + s * C::kStage;
-        if (i >= pre) {
-          mbar_expect_tx(&full[s], C::kStage);
-          tma_load_3d_hint(st, &tm_w, k * kKC, (t % a.tiles_pg) * C::kM, g, &full[s], pol);
+        if (i >= n0 && !x_ok) {
+          // first phase-1 chunk: wait (bounded) until every phase-0 result
+          // is stored, meanwhile keeping the weight stream going into every
+          // ring slot the MMAs free; then make those generic-proxy stores
+          // visible to TMA
+          const int target = a.ph[0].n_tiles * 4;
+          uint32_t spins = 0;
+          while (true) {
+            while (w_issued < n_it && w_issued < i + C::kStages) {
+              const long long j = w_issued;
+              if (j >= C::kStages && !mbar_test(&empty[j % C::kStages], (uint32_t)((j / C::kStages) & 1) ^ 1u))
+                break;
+              load_w(j);
+              w_issued = j + 1;
+            }
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.xready) : "memory");
+            if (v >= target || *abort_flag) break;
+            if (++spins > kWaitLimit) break;
+            __nanosleep(64);
+          }
+          if (spins > kWaitLimit || *abort_flag) {
+            *abort_flag = 1;
+            sv::report(a.status, SPEC_DEV_TIMEOUT);
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          x_ok = true;
         }
-        tma_load_3d(st + C::kWBytes, &tm_x, k * kKC, a.x_grouped ? g : 0, a.r0, &full[s]);
+        load_x(i);
         issued = i + 1;
       }
-      if (*abort_flag)  // let this CTA's own copies land before it exits
-        for (long long i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+      if (*abort_flag) {  // let this CTA's own copies land before it exits
+        const long long last = w_issued > issued ? w_issued : issued;
+        for (long long i = last > C::kStages ? last - C::kStages : 0; i < last; ++i) {
+          // a stage whose X was never issued completes only its W bytes: give
+          // it the missing transaction count so the wait can end
+          if (i >= issued) mbar_complete_tx_local(&full[i % C::kStages], C::kXBytes);
           mbar_wait(&full[i % C::kStages], (uint32_t)((i / C::kStages) & 1), kWaitLimit);
+        }
+      }
     }
   } else if (warp == 1) {
     constexpr uint32_t idesc = idesc_bf16_f32(128, NT, 0, 0);
@@ -193,35 +299,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     long long it = 0;
     int seg = 0;
-    for (long long u = u0; u < u1 && ok; ++seg) {
-      const int klo = (int)(u % a.nk);
-      const int khi = (int)((u1 - u) < (long long)(a.nk - klo) ? klo + (u1 - u) : a.nk);
-      const int buf = seg & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, kWaitLimit)))) break;
-      tc_fence_after();
-      const uint32_t dacc = tmem + (uint32_t)(buf * C::kAccCols);
-      for (int k = klo; k < khi; ++k, ++it) {
-        const int s = (int)(it % C::kStages);
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1), kWaitLimit)) &&
-                   !*abort_flag))
-          break;
+    for (int p = 0; p < a.nphase && ok; ++p) {
+      const long long ulo = p ? lo1 : lo0, uhi = p ? hi1 : hi0;
+      for (long long u = ulo; u < uhi && ok; ++seg) {
+        const int klo = (int)(u % a.nk);
+        const int khi = (int)((uhi - u) < (long long)(a.nk - klo) ? klo + (uhi - u) : a.nk);
+        const int buf = seg & 1;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, kWaitLimit)))) break;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t wa = base + (uint32_t)s * C::kStage, xa = wa + C::kWBytes;
+        const uint32_t dacc = tmem + (uint32_t)(buf * C::kAccCols);
+        for (int k = klo; k < khi; ++k, ++it) {
+          const int s = (int)(it % C::kStages);
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1), kWaitLimit)) &&
+                     !*abort_flag))
+            break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t wa = base + (uint32_t)s * C::kStage, xa = wa + C::kWBytes;
 #pragma unroll
-          for (int kk = 0; kk < kKC / 16; ++kk)
+            for (int kk = 0; kk < kKC / 16; ++kk)
 #pragma unroll
-            for (int j = 0; j < MT; ++j)
-              mma_ss(dacc + j * NT, smem_desc_sw128(wa + j * (128 * kKC * 2) + kk * 32, 16, 1024),
-                     smem_desc_sw128(xa + kk * 32, 16, 1024), idesc, (k > klo || kk > 0));
-          mma_commit(&empty[s]);
+              for (int j = 0; j < MT; ++j)
+                mma_ss(dacc + j * NT, smem_desc_sw128(wa + j * (128 * kKC * 2) + kk * 32, 16, 1024),
+                       smem_desc_sw128(xa + kk * 32, 16, 1024), idesc, (k > klo || kk > 0));
+            mma_commit(&empty[s]);
+          }
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) mma_commit(&acc_full[buf]);
         __syncwarp();
+        u += khi - klo;
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(&acc_full[buf]);
-      __syncwarp();
-      u += khi - klo;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -234,86 +343,154 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int ml = quarter * 32 + lane;  // W row within a 128-row sub-tile
     const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int rows4 = (a.rows + 3) >> 2;
     int seg = 0;
-    for (long long u = u0; u < u1; ++seg) {
-      const int t = (int)(u / a.nk), klo = (int)(u % a.nk);
-      const int khi = (int)((u1 - u) < (long long)(a.nk - klo) ? klo + (u1 - u) : a.nk);
-      const int g = t / a.tiles_pg, mt = t % a.tiles_pg;
-      const bool whole = klo == 0 && khi == a.nk;
-      const int buf = seg & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (seg >> 1) & 1, kWaitLimit)) ||
-          __any_sync(0xffffffffu, *abort_flag != 0)) {
-        *abort_flag = 1;
-        sv::report(a.status, SPEC_DEV_TIMEOUT);
-        break;
-      }
-      tc_fence_after();
-      float *slot = a.partial + (long long)(2 * c + (u == u0 ? 0 : 1)) * a.rows * C::kM;
+    bool live = true;
+    for (int p = 0; p < a.nphase && live; ++p) {
+      const Phase &ph = a.ph[p];
+      const long long ulo = p ? lo1 : lo0, uhi = p ? hi1 : hi0;
+      // this quarter's results of phase 0 count toward phase 1's X readiness
+      const bool feeds = p == 0 && a.nphase > 1;
+      for (long long u = ulo; u < uhi; ++seg) {
+        const int t = (int)(u / a.nk), klo = (int)(u % a.nk);
+        const int khi = (int)((uhi - u) < (long long)(a.nk - klo) ? klo + (uhi - u) : a.nk);
+        const int g = t / ph.tiles_pg, mt = t % ph.tiles_pg;
+        const bool whole = klo == 0 && khi == a.nk;
+        const int buf = seg & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (seg >> 1) & 1, kWaitLimit)) ||
+            __any_sync(0xffffffffu, *abort_flag != 0)) {
+          *abort_flag = 1;
+          sv::report(a.status, SPEC_DEV_TIMEOUT);
+          live = false;
+          break;
+        }
+        tc_fence_after();
+        // partial slot layout: [rows / 4][kM][4] floats, so four rows of one
+        // W row are one 16-byte vector (for the reducer's loads)
+        float4 *slot = reinterpret_cast<float4 *>(ph.partial) + (long long)(2 * c + (u == ulo ? 0 : 1)) * rows4 * C::kM;
 #pragma unroll 1
-      for (int j = 0; j < MT; ++j) {
+        for (int j = 0; j < MT; ++j) {
 #pragma unroll 1
-        for (int cc = 0; cc < NT / C::kCW; ++cc) {
-          if (cc * C::kCW >= a.rows) break;  // warp-uniform
-          uint32_t acc[32];
-          const uint32_t ta = tq + (uint32_t)(buf * C::kAccCols + j * NT + cc * C::kCW);
-          if constexpr (C::kCW == 32) {
-            tmem_ld32(ta, acc);
-          } else {
-            tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(acc));
-          }
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < C::kCW; ++i) {
-            const int r = cc * C::kCW + i;
+          for (int cc = 0; cc < NT / C::kCW; ++cc) {
+            if (cc * C::kCW >= a.rows) break;  // warp-uniform
+            const uint32_t ta = tq + (uint32_t)(buf * C::kAccCols + j * NT + cc * C::kCW);
+            if (whole && ph.epi == kEpiStats) {
+              // statistics: one TMEM column (activation row) at a time, a
+              // rolled loop (small code; this path is not bandwidth-bound)
+              const int m = mt * C::kM + j * 128 + ml;
+              const int rec = (mt * MT + j) * 4 + quarter;
+#pragma unroll 1
+              for (int i = 0; i < C::kCW && cc * C::kCW + i < a.rows; ++i) {
+                uint32_t v;
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(ta + (uint32_t)i));
+                tmem_wait_ld();
+                store_stats(a, ph, m, rec, cc * C::kCW + i, __uint_as_float(v));
+              }
+              continue;
+            }
+            uint32_t acc[32];
+            if constexpr (C::kCW == 32) {
+              tmem_ld32(ta, acc);
+            } else {
+              tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(acc));
+            }
+            tmem_wait_ld();
+            const int m = mt * C::kM + j * 128 + ml;
             if (whole) {
-              store_final<NT, MT, EPI>(a, g, mt * C::kM + j * 128 + ml, r, __uint_as_float(acc[i]));
-            } else if (r < a.rows) {
-              slot[(long long)r * C::kM + j * 128 + ml] = __uint_as_float(acc[i]);
+              const int rec = (mt * MT + j) * 4 + quarter;
+#pragma unroll
+              for (int i = 0; i < C::kCW; i += 4)
+                store4(a, ph, g, m, rec, cc * C::kCW + i,
+                       make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]), __uint_as_float(acc[i + 2]),
+                                   __uint_as_float(acc[i + 3])));
+            } else {
+#pragma unroll
+              for (int i = 0; i < C::kCW; i += 4) {
+                const int r = cc * C::kCW + i;
+                if (r < a.rows)
+                  slot[(long long)(r >> 2) * C::kM + j * 128 + ml] =
+                      make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]), __uint_as_float(acc[i + 2]),
+                                  __uint_as_float(acc[i + 3]));
+              }
             }
           }
         }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      if (!whole) {
-        // ticket per (tile, quarter): the warp that brings the last
-        // contributor's rows of this quarter reduces them; no warp waits
-        __threadfence();
+        tc_fence_before();
         __syncwarp();
-        int ticket = 0;
-        if (lane == 0) ticket = atomicAdd(&a.counters[4 * t + quarter], 1);
-        ticket = __shfl_sync(0xffffffffu, ticket, 0);
-        const long long tu = (long long)t * a.nk;
-        const int c_first = cta_of_unit(tu, a.units, a.n_ctas);
-        const int c_last = cta_of_unit(tu + a.nk - 1, a.units, a.n_ctas);
-        if (ticket == c_last - c_first) {
+        if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        bool stored = whole;
+        if (!whole) {
+          // ticket per (tile, quarter): the warp that brings the last
+          // contributor's rows of this quarter reduces them; no warp waits
           __threadfence();
-          // 16 rows at a time, each contributor's 16 loads issued together
+          __syncwarp();
+          int ticket = 0;
+          if (lane == 0) ticket = atomicAdd(&ph.counters[4 * t + quarter], 1);
+          ticket = __shfl_sync(0xffffffffu, ticket, 0);
+          const long long tu = (long long)t * a.nk;
+          const int c_first = cta_of_unit(tu, ph.units, a.n_ctas);
+          const int c_last = cta_of_unit(tu + a.nk - 1, ph.units, a.n_ctas);
+          if (ticket == c_last - c_first) {
+            stored = true;
+            __threadfence();
+            // Entries (sub-tile j, 4 rows) x contributors in one index space,
+            // 16 loads in flight per round; each entry's contributions are
+            // summed in CTA order.  Only the first contributor can have
+            // started before the tile (slot 2c + 1); the others start inside
+            // it (2c).
+            const float4 *part = reinterpret_cast<const float4 *>(ph.partial);
+            const int nc = c_last - c_first + 1;
+            const int slot_first = 2 * c_first + (range_start(c_first, ph.units, a.n_ctas) >= tu ? 0 : 1);
+            const int n_ent = MT * rows4;
+            const int per = nc >= 16 ? 1 : 16 / nc;
 #pragma unroll 1
-          for (int j = 0; j < MT; ++j) {
+            for (int e0 = 0; e0 < n_ent; e0 += per) {
+              float4 sum[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-            for (int r0 = 0; r0 < a.rows; r0 += 16) {
-              float sum[16];
+              for (int k0 = 0; k0 < per * nc; k0 += 16) {  // more than one round only when nc > 16
+                float4 v[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) sum[i] = 0.f;
-#pragma unroll 1
-              for (int cq = c_first; cq <= c_last; ++cq) {
-                const int sl = 2 * cq + (range_start(cq, a.units, a.n_ctas) >= tu ? 0 : 1);
-                const float *src = a.partial + ((long long)sl * a.rows + r0) * C::kM + j * 128 + ml;
-                float v[16];
+                for (int i = 0; i < 16; ++i) {
+                  const int k = k0 + i, e = e0 + k / nc, cq = k % nc;
+                  v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                  if (k < per * nc && e < n_ent) {
+                    const int sl = cq == 0 ? slot_first : 2 * (c_first + cq);
+                    const int j = e / rows4, q = e % rows4;
+                    v[i] = __ldcg(part + ((long long)sl * rows4 + q) * C::kM + j * 128 + ml);
+                  }
+                }
+                // (static register indices only: entry t takes the loads with k / nc == t)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = r0 + i < a.rows ? __ldcg(src + (long long)i * C::kM) : 0.f;
+                for (int i = 0; i < 16; ++i) {
+                  const int k = k0 + i, el = k / nc;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) sum[i] += v[i];
+                  for (int tt = 0; tt < 16; ++tt)
+                    if (el == tt && k < per * nc) {
+                      sum[tt].x += v[i].x;
+                      sum[tt].y += v[i].y;
+                      sum[tt].z += v[i].z;
+                      sum[tt].w += v[i].w;
+                    }
+                }
               }
 #pragma unroll
-              for (int i = 0; i < 16; ++i) store_final<NT, MT, EPI>(a, g, mt * C::kM + j * 128 + ml, r0 + i, sum[i]);
+              for (int el = 0; el < 16; ++el) {
+                if (el >= per || e0 + el >= n_ent) break;
+                const int e = e0 + el, j = e / rows4;
+                store4(a, ph, g, mt * C::kM + j * 128 + ml, (mt * MT + j) * 4 + quarter, (e % rows4) * 4, sum[el]);
+              }
             }
           }
         }
+        if (feeds && stored) {  // this (tile, quarter) of phase 0 is final
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) atomicAdd(a.xready, 1);
+        }
+        u += khi - klo;
       }
-      u += khi - klo;
     }
   }
   tc_fence_before();
@@ -386,17 +563,16 @@ SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows) {
   p.n_ctas = (int)(p.units < sms ? p.units : sms);
   p.rows_per_launch = rl;
   p.counter_bytes = align256((size_t)p.n_tiles * 16);
-  p.partial_bytes = align256((size_t)2 * p.n_ctas * rl * km * 4);
+  p.partial_bytes = align256((size_t)2 * p.n_ctas * ((rl + 3) / 4 * 4) * km * 4);
   return p;
 }
 
 namespace {
 
-template <int NT, int MT, int EPI>
-int launch_t(const SvGemmPlan &p, const CUtensorMap &mw, const CUtensorMap &mx, const WArgs &a, bool pdl,
-             cudaStream_t stream) {
+template <int NT, int MT>
+int launch_t(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream) {
   using C = Cfg<NT, MT>;
-  auto kern = wgemm_kernel<NT, MT, EPI>;
+  auto kern = wgemm_kernel<NT, MT>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
     return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -409,20 +585,36 @@ int launch_t(const SvGemmPlan &p, const CUtensorMap &mw, const CUtensorMap &mx, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, mw, mx, a) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], a) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
-template <int EPI>
-int launch_nt(const SvGemmPlan &p, const CUtensorMap &mw, const CUtensorMap &mx, const WArgs &a, bool pdl,
-              cudaStream_t stream) {
+int launch_nt(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream) {
   switch (p.nt) {
-    case 16: return launch_t<16, 2, EPI>(p, mw, mx, a, pdl, stream);
-    case 32: return launch_t<32, 2, EPI>(p, mw, mx, a, pdl, stream);
-    case 64: return launch_t<64, 2, EPI>(p, mw, mx, a, pdl, stream);
-    case 128: return launch_t<128, 2, EPI>(p, mw, mx, a, pdl, stream);
-    default: return launch_t<256, 1, EPI>(p, mw, mx, a, pdl, stream);
+    case 16: return launch_t<16, 2>(p, maps, a, pdl, stream);
+    case 32: return launch_t<32, 2>(p, maps, a, pdl, stream);
+    case 64: return launch_t<64, 2>(p, maps, a, pdl, stream);
+    case 128: return launch_t<128, 2>(p, maps, a, pdl, stream);
+    default: return launch_t<256, 1>(p, maps, a, pdl, stream);
   }
+}
+
+Phase make_phase(const SvGemmPlan &p, int M, int x_grouped, int epi, float *out, void *zout, const void *res,
+                 const void *bias, int *counters, float *partial) {
+  Phase ph{};
+  ph.M = M;
+  ph.tiles_pg = p.tiles_pg;
+  ph.n_tiles = p.n_tiles;
+  ph.x_grouped = x_grouped;
+  ph.epi = epi;
+  ph.units = p.units;
+  ph.out = out;
+  ph.zout = reinterpret_cast<__nv_bfloat16 *>(zout);
+  ph.res = reinterpret_cast<const __nv_bfloat16 *>(res);
+  ph.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
+  ph.counters = counters;
+  ph.partial = partial;
+  return ph;
 }
 
 }  // namespace
@@ -435,60 +627,115 @@ int launch_nt(const SvGemmPlan &p, const CUtensorMap &mw, const CUtensorMap &mx,
 // on the stream (only its X loads wait for that kernel).
 int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, int M, int K, int G, int rows,
              int epi, float *out, void *zout, const void *res, const void *bias, int *counters, float *partial,
-             bool counters_clear, bool pdl, int32_t *status, cudaStream_t stream) {
+             bool counters_clear, bool pdl, int32_t *status, cudaStream_t stream, float inv_t, void *stats) {
   const int km = 128 * p.mt;
   if (p.n_ctas < 1) return SPEC_ERR_CUDA;
-  CUtensorMap mw, mx;
-  if (map3(&mw, w, K, M, G, km, 1) != SPEC_OK) return SPEC_ERR_CUDA;
-  if (map3(&mx, x, K, x_grouped ? G : 1, rows, 1, p.nt) != SPEC_OK) return SPEC_ERR_CUDA;
+  CUtensorMap maps[4];
+  if (map3(&maps[0], w, K, M, G, km, 1) != SPEC_OK) return SPEC_ERR_CUDA;
+  if (map3(&maps[1], x, K, x_grouped ? G : 1, rows, 1, p.nt) != SPEC_OK) return SPEC_ERR_CUDA;
+  maps[2] = maps[0];
+  maps[3] = maps[1];
   for (int r0 = 0; r0 < rows; r0 += p.rows_per_launch) {
     if (r0 > 0 || !counters_clear)
       if (cudaMemsetAsync(counters, 0, p.counter_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     WArgs a{};
-    a.M = M; a.K = K; a.G = G;
+    a.ph[0] = make_phase(p, M, x_grouped, epi, out, zout, res, bias, counters, partial);
+    a.nphase = 1;
+    a.K = K;
+    a.G = G;
     a.rows = rows - r0 < p.rows_per_launch ? rows - r0 : p.rows_per_launch;
-    a.r0 = r0; a.x_grouped = x_grouped;
-    a.nk = p.nk; a.tiles_pg = p.tiles_pg; a.n_tiles = p.n_tiles; a.n_ctas = p.n_ctas; a.units = p.units;
-    a.out = out; a.zout = reinterpret_cast<__nv_bfloat16 *>(zout);
-    a.res = reinterpret_cast<const __nv_bfloat16 *>(res);
-    a.bias = reinterpret_cast<const __nv_bfloat16 *>(bias);
-    a.partial = partial; a.counters = counters; a.status = status;
+    a.r0 = r0;
+    a.nk = p.nk;
+    a.n_ctas = p.n_ctas;
+    a.status = status;
     const bool dep = pdl && r0 == 0 && counters_clear;
     a.pdl_wait = dep ? 1 : 0;
-    const int rc = epi == kEpiF32 ? launch_nt<kEpiF32>(p, mw, mx, a, dep, stream)
-                                  : launch_nt<kEpiSiluRes>(p, mw, mx, a, dep, stream);
+    a.inv_t = inv_t;
+    a.stats = reinterpret_cast<float4 *>(stats);
+    a.rec_stride = p.tiles_pg * p.mt * 4;
+    const int rc = launch_nt(p, maps, a, dep, stream);
     if (rc != SPEC_OK) return rc;
   }
   return sv_launch_status();
 }
 
-// Medusa heads: z = h + SiLU(W1 h + b1) (bf16), then logits = W2 z (float32).
-// Workspace: both GEMMs' counters side by side (one memset clears them),
-// then each GEMM's partial slots.  With a single row block the second GEMM
-// launches as a programmatic dependent of the first: its weight stream starts
-// while the first drains, and only its z loads wait.
+// Medusa heads: z = h + SiLU(W1 h + b1) (bf16), then logits = W2 z (float32),
+// in one persistent launch per block of up to 256 rows: every CTA streams its
+// share of W1, then its share of W2; a CTA's first W2 chunks are in flight
+// while the last W1 results are stored, and its first z load waits (bounded)
+// until all of them are.  Workspace: both phases' counters and the readiness
+// count side by side (one memset clears them), then each phase's partial
+// slots.
+namespace {
+struct HeadsLayout {
+  SvGemmPlan p1, p2;
+  size_t c1, c2, ready, pa1, pa2, total;
+};
+HeadsLayout heads_layout(int batch, int n_heads, int hidden, int vocab) {
+  HeadsLayout l{};
+  l.p1 = sv_wgemm_plan(hidden, hidden, n_heads, batch);
+  l.p2 = sv_wgemm_plan(vocab, hidden, n_heads, batch);
+  l.c1 = 0;
+  l.c2 = l.p1.counter_bytes;
+  l.ready = l.c2 + l.p2.counter_bytes;
+  l.pa1 = l.ready + 256;
+  l.pa2 = l.pa1 + l.p1.partial_bytes;
+  l.total = l.pa2 + l.p2.partial_bytes;
+  return l;
+}
+}  // namespace
+
 size_t sv_medusa_heads_ws_bytes(int batch, int n_heads, int hidden, int vocab) {
-  const SvGemmPlan p1 = sv_wgemm_plan(hidden, hidden, n_heads, batch);
-  const SvGemmPlan p2 = sv_wgemm_plan(vocab, hidden, n_heads, batch);
-  return p1.counter_bytes + p2.counter_bytes + p1.partial_bytes + p2.partial_bytes;
+  return heads_layout(batch, n_heads, hidden, vocab).total;
 }
 
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch, int n_heads,
                     int hidden, int vocab, void *z, float *logits, void *ws, int32_t *status, cudaStream_t stream) {
-  const SvGemmPlan p1 = sv_wgemm_plan(hidden, hidden, n_heads, batch);
-  const SvGemmPlan p2 = sv_wgemm_plan(vocab, hidden, n_heads, batch);
+  const HeadsLayout l = heads_layout(batch, n_heads, hidden, vocab);
+  if (l.p1.n_ctas < 1 || l.p2.n_ctas < 1) return SPEC_ERR_CUDA;
+  if (l.p1.nt != l.p2.nt) return SPEC_ERR_CUDA;  // same rows: same tile shape
   uint8_t *base = reinterpret_cast<uint8_t *>(ws);
-  int *c1 = reinterpret_cast<int *>(base), *c2 = reinterpret_cast<int *>(base + p1.counter_bytes);
-  float *pa1 = reinterpret_cast<float *>(base + p1.counter_bytes + p2.counter_bytes);
-  float *pa2 = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(pa1) + p1.partial_bytes);
-  const bool single = batch <= p1.rows_per_launch;
-  if (single && cudaMemsetAsync(base, 0, p1.counter_bytes + p2.counter_bytes, stream) != cudaSuccess)
-    return SPEC_ERR_CUDA;
-  int rc = sv_wgemm(p1, w1, h, 0, hidden, hidden, n_heads, batch, kEpiSiluRes, nullptr, z, h, b1, c1, pa1, single,
-                    false, status, stream);
-  if (rc != SPEC_OK) return rc;
-  return sv_wgemm(p2, w2, z, 1, vocab, hidden, n_heads, batch, kEpiF32, logits, nullptr, nullptr, nullptr, c2, pa2,
-                  single, single, status, stream);
+  if (l.p1.n_ctas != l.p2.n_ctas) {
+    // fewer W1 chunks than CTAs: one grid would leave CTAs without W1 work
+    // (stream-K assumes none); two launches, the second dependent on the first
+    if (cudaMemsetAsync(base, 0, l.ready, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    int rc = sv_wgemm(l.p1, w1, h, 0, hidden, hidden, n_heads, batch, kEpiSiluRes, nullptr, z, h, b1,
+                      reinterpret_cast<int *>(base + l.c1), reinterpret_cast<float *>(base + l.pa1), true, false,
+                      status, stream);
+    if (rc != SPEC_OK) return rc;
+    return sv_wgemm(l.p2, w2, z, 1, vocab, hidden, n_heads, batch, kEpiF32, logits, nullptr, nullptr, nullptr,
+                    reinterpret_cast<int *>(base + l.c2), reinterpret_cast<float *>(base + l.pa2), true, true, status,
+                    stream);
+  }
+  const int km = 128 * l.p1.mt;
+  CUtensorMap maps[4];
+  if (map3(&maps[0], w1, hidden, hidden, n_heads, km, 1) != SPEC_OK) return SPEC_ERR_CUDA;
+  if (map3(&maps[1], h, hidden, 1, batch, 1, l.p1.nt) != SPEC_OK) return SPEC_ERR_CUDA;
+  if (map3(&maps[2], w2, hidden, vocab, n_heads, km, 1) != SPEC_OK) return SPEC_ERR_CUDA;
+  if (map3(&maps[3], z, hidden, n_heads, batch, 1, l.p1.nt) != SPEC_OK) return SPEC_ERR_CUDA;
+  const int n_ctas = l.p2.n_ctas;  // both phases are split over the whole grid
+  const SvGemmPlan &p = l.p2;
+  for (int r0 = 0; r0 < batch; r0 += l.p1.rows_per_launch) {
+    if (cudaMemsetAsync(base, 0, l.pa1, stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    WArgs a{};
+    a.ph[0] = make_phase(l.p1, hidden, 0, kEpiSiluRes, nullptr, z, h, b1, reinterpret_cast<int *>(base + l.c1),
+                         reinterpret_cast<float *>(base + l.pa1));
+    a.ph[1] = make_phase(l.p2, vocab, 1, kEpiF32, logits, nullptr, nullptr, nullptr,
+                         reinterpret_cast<int *>(base + l.c2), reinterpret_cast<float *>(base + l.pa2));
+    a.nphase = 2;
+    a.K = hidden;
+    a.G = n_heads;
+    a.rows = batch - r0 < l.p1.rows_per_launch ? batch - r0 : l.p1.rows_per_launch;
+    a.r0 = r0;
+    a.nk = l.p1.nk;
+    a.n_ctas = n_ctas;
+    a.status = status;
+    a.xready = reinterpret_cast<int *>(base + l.ready);
+    a.inv_t = 1.f;
+    const int rc = launch_nt(p, maps, a, false, stream);
+    if (rc != SPEC_OK) return rc;
+  }
+  return sv_launch_status();
 }
 
 size_t sv_lm_head_ws_bytes(int rows, int hidden, int vocab) {

@@ -18,7 +18,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libspecverify.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA = range(5)
-DEV_OK, DEV_BAD_PARENTS, DEV_CAPACITY, DEV_BAD_PATH, DEV_BAD_POOL, DEV_BAD_TOKEN, DEV_TIMEOUT, DEV_INTERNAL = range(8)
+(DEV_OK, DEV_BAD_PARENTS, DEV_CAPACITY, DEV_BAD_PATH, DEV_BAD_POOL, DEV_BAD_TOKEN, DEV_TIMEOUT, DEV_INTERNAL,
+ DEV_BAD_BLOCK) = range(9)
 F32, BF16 = 0, 1
 GREEDY, TYPICAL, REJECT, REJECT_STOCHASTIC = 0, 1, 2, 3
 MAX_NODES = 256
@@ -40,17 +41,25 @@ _SIGS = {
     "spec_build_tree": ([_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i),
     "spec_build_tree_dynamic": ([_vp, _vp, _vp, _i, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                  _vp, _vp, _vp], _i),
+    "spec_build_tree_batch": ([_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i),
     "spec_tree_expand": ([_vp, _i, _i, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp], _i),
     "tree_attn_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "tree_attn_plan_splits": ([_i, _i, _i, _i, _i, _i, _vp], _i),
     "tree_attn_verify": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
                           _vp, _sz, _vp, _vp], _i),
+    "tree_attn_verify_paged": ([_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                _i, _f, _i, _vp, _sz, _vp, _vp], _i),
     "tree_attn_verify_noalloc": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                                   _i, _vp, _vp], _i),
     "spec_lm_head_workspace_bytes": ([_i, _i, _i], _sz),
     "spec_lm_head": ([_vp, _vp, _i, _i, _i, _vp, _vp, _sz, _vp, _vp], _i),
+    "spec_lm_head_accept_workspace_bytes": ([_i, _i, _i, _i], _sz),
+    "spec_lm_head_accept": ([_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _i, _vp, _vp, _vp, _vp, _sz,
+                             _vp, _vp], _i),
     "spec_accept": ([_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp,
                      _vp, _vp, _vp], _i),
+    "kv_commit_paged": ([_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp,
+                         _vp], _i),
     "kv_commit": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
 }
 
@@ -170,6 +179,19 @@ def spec_build_tree(parents, rank, cand_tok, root_tok, prefix_len, tok, depth, p
         _p(depth), _p(pos_ids), _p(anc_mask), _p(first_child), _p(next_sibling), _p(dev_status), _stream()))
 
 
+def spec_build_tree_batch(parents, prefix_len, depth, pos_ids, anc_mask, first_child, next_sibling, n_valid=None,
+                          tok_in=None, tok=None, dev_status=None):
+    """One tree per sequence: parents [B, N] (first n_valid[b] entries
+    valid), tokens copied from tok_in when given."""
+    B, N = parents.shape
+    for t in (parents, n_valid, tok_in, tok, prefix_len, depth, pos_ids, first_child, next_sibling, dev_status):
+        _want(t, torch.int32)
+    _want(anc_mask, torch.int64)
+    _check("spec_build_tree_batch", load().spec_build_tree_batch(
+        _p(parents), _p(n_valid), _p(tok_in), _p(prefix_len), B, N, _p(tok), _p(depth), _p(pos_ids), _p(anc_mask),
+        _p(first_child), _p(next_sibling), _p(dev_status), _stream()))
+
+
 def spec_build_tree_dynamic(pool_parent, pool_tok, pool_conf, prefix_len, tok, parents_out, depth, pos_ids,
                             anc_mask, first_child, next_sibling, pool_index=None, val=None, dev_status=None):
     B, M = pool_parent.shape
@@ -224,6 +246,24 @@ def tree_attn_verify(q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, 
         ws_bytes, _p(dev_status), _stream()))
 
 
+def tree_attn_verify_paged(q, k_pages, v_pages, block_table, k_tree, v_tree, prefix_len, anc_mask, out, max_prefix,
+                           scale=0.0, num_splits=0, workspace=None, dev_status=None):
+    """tree_attn_verify over a paged prefix cache: k_pages/v_pages
+    [num_blocks, Hkv, block_size, D], block_table [B, max_blocks] int32."""
+    B, N, Hq, D = q.shape
+    nb, Hkv, bs = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    _want(q, torch.float32, torch.bfloat16)
+    for t in (k_pages, v_pages, k_tree, v_tree, out):
+        if t.dtype != q.dtype:
+            raise TypeError("q, pages, tree K/V and out must share one dtype")
+    _want(anc_mask, torch.int64); _want(prefix_len, torch.int32); _want(block_table, torch.int32)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tree_attn_verify_paged", load().tree_attn_verify_paged(
+        _p(q), _p(k_pages), _p(v_pages), _p(block_table), bs, nb, block_table.shape[1], _p(k_tree), _p(v_tree),
+        _p(prefix_len), _p(anc_mask), _p(out), _DT[q.dtype], B, N, Hq, Hkv, D, int(max_prefix), float(scale),
+        int(num_splits), _p(workspace), ws_bytes, _p(dev_status), _stream()))
+
+
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -260,6 +300,26 @@ def spec_lm_head(hid, w, logits, dev_status=None, workspace=None):
                                                _p(dev_status), _stream()))
 
 
+def spec_lm_head_accept_workspace_bytes(batch, n_nodes, hidden, vocab):
+    return int(load().spec_lm_head_accept_workspace_bytes(batch, n_nodes, hidden, vocab))
+
+
+def spec_lm_head_accept(mode, hid, w, tok, parents, first_child, next_sibling, acc_len, acc_path, bonus,
+                        temperature=1.0, eps=0.0, delta=0.0, dev_status=None, workspace=None):
+    """LM head fused with greedy / typical acceptance.  hid [B, N, hidden]
+    bf16, w [V, hidden] bf16; outputs as spec_accept."""
+    B, N, d = hid.shape
+    V = w.shape[0]
+    _want(hid, torch.bfloat16); _want(w, torch.bfloat16)
+    if workspace is None:
+        workspace = _scratch(spec_lm_head_accept_workspace_bytes(B, N, d, V), hid)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_lm_head_accept", load().spec_lm_head_accept(
+        int(mode), _p(hid), _p(w), B, N, d, V, _p(tok), _p(parents), _p(first_child), _p(next_sibling),
+        float(temperature), float(eps), float(delta), acc_path.shape[1], _p(acc_len), _p(acc_path), _p(bonus),
+        _p(workspace), ws_bytes, _p(dev_status), _stream()))
+
+
 def spec_accept(mode, logits, tok, parents, first_child, next_sibling, acc_len, acc_path, bonus,
                 temperature=1.0, eps=0.0, delta=0.0, seed=0, step=0, dev_status=None, draft_logits=None):
     B, N, V = logits.shape
@@ -283,3 +343,19 @@ def kv_commit(k_cache, v_cache, k_tree, v_tree, acc_len, acc_path, prefix_len, p
         _p(k_cache), _p(v_cache), _p(k_tree), _p(v_tree), k_cache.element_size(), L, B, Hkv, S, N, D,
         _p(acc_len), _p(acc_path), acc_path.shape[1], _p(prefix_len), _p(prefix_len_out), _p(dev_status),
         _stream()))
+
+
+def kv_commit_paged(k_pages, v_pages, block_table, k_tree, v_tree, acc_len, acc_path, prefix_len,
+                    prefix_len_out=None, dev_status=None):
+    """kv_commit into a paged cache [L, num_blocks, Hkv, block_size, D] (or
+    without the layer axis) addressed by block_table [B, max_blocks]."""
+    if k_pages.dim() == 4:
+        L, (nb, Hkv, bs, D) = 1, k_pages.shape
+    else:
+        L, nb, Hkv, bs, D = k_pages.shape
+    B, N = block_table.shape[0], k_tree.shape[-2]
+    _want(block_table, torch.int32)
+    _check("kv_commit_paged", load().kv_commit_paged(
+        _p(k_pages), _p(v_pages), _p(block_table), bs, nb, block_table.shape[1], _p(k_tree), _p(v_tree),
+        k_pages.element_size(), L, B, Hkv, N, D, _p(acc_len), _p(acc_path), acc_path.shape[1], _p(prefix_len),
+        _p(prefix_len_out), _p(dev_status), _stream()))
