@@ -8,9 +8,9 @@
 // min(eps, delta exp(-H)); the step's first token is the greedy one);
 // "Drafters: ...", section "Why the answer does not change".
 //
-// 1. The GEMM (wgemm.cu, statistics epilogue) writes, per tree node and per
-//    32 consecutive vocabulary rows, (max logit, sum exp(z - zmax), sum
-//    exp(z - zmax)(z - zmax), argmax) with z = logit / T.
+// 1. The GEMM (statistics epilogue) writes, per tree node, vocabulary tile and
+//    epilogue warp (the 32 * MT vocabulary rows that warp holds), (max logit,
+//    sum exp(z - zmax), sum exp(z - zmax)(z - zmax), argmax) with z = logit / T.
 // 2. fold_kernel, one CTA per (node, sequence): merges the node's records in
 //    a fixed order into (max, S, Q, argmax) and, for typical acceptance,
 //    computes each child's logit as the dot product of the node's hidden
@@ -231,7 +231,7 @@ Layout layout(int batch, int n_nodes, int hidden, int vocab) {
   Layout l{};
   const int rows = batch * n_nodes;
   l.p = sv_wgemm_plan(vocab, hidden, 1, rows);
-  const int rec = l.p.tiles_pg * l.p.mt * 4;
+  const int rec = l.p.tiles_pg * 4;  // one record per (row, tile, epilogue warp)
   l.fold_counters = l.p.counter_bytes;
   l.partial = l.fold_counters + align256((size_t)batch * 4);
   l.stats = l.partial + l.p.partial_bytes;
@@ -273,7 +273,7 @@ int sv_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, fold_kernel, mode, reinterpret_cast<const float4 *>(base + l.stats),
-                         l.p.tiles_pg * l.p.mt * 4, reinterpret_cast<const __nv_bfloat16 *>(hid),
+                         l.p.tiles_pg * 4, reinterpret_cast<const __nv_bfloat16 *>(hid),
                          reinterpret_cast<const __nv_bfloat16 *>(w), n_nodes, hidden, vocab, tok, parents,
                          first_child, next_sibling, inv_t, eps, delta, path_cap,
                          reinterpret_cast<RowStat *>(base + l.rowstat), reinterpret_cast<float *>(base + l.childp),
