@@ -246,6 +246,58 @@ int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front
                      spec_stream_t stream);
 
 /* --------------------------------------------------------------------
+ * spec_eagle_round -- one drafting round of an EAGLE-2 style draft: the
+ * draft layer applied to the frontier nodes, then spec_tree_expand on its
+ * distributions ("Medusa and EAGLE ... explained", section "EAGLE:
+ * autoregression over features": [feature ; embedding of the next token]
+ * -> FC (2d -> d) -> one decoder layer -> next feature -> the target's LM
+ * head; "5.3 Medusa、EAGLE 与 MTP", sections 4.1 and 5.2).
+ *
+ * Weights (bf16, nn.Linear layout [out, in]):
+ *   fc [hidden, 2*hidden]; ln1, ln2, lnf [hidden] (RMSNorm gains);
+ *   qkv [(hq + 2*hkv) * head_dim, hidden]; o [hidden, hq * head_dim];
+ *   gate_up [2, ffn, hidden]; down [hidden, ffn]; lm [vocab, hidden] (the
+ *   target's LM head); emb [vocab, hidden] (the target's embedding).
+ * The decoder layer is a pre-norm block: x1 = x + W_o attn(RMSNorm(x)),
+ * out = x1 + W_down(SiLU(W_gate n) * W_up n), n = RMSNorm(x1), RMSNorm eps
+ * 1e-6; rotary embedding rotate-half, base 10000, position = prefix_len +
+ * depth; the predicted feature passes RMSNorm(lnf) before the LM head.
+ *
+ *   k_prefix, v_prefix [batch, hkv, s_max, head_dim]: the draft layer's cache
+ *            of the verified prefix (rotary applied), prefix_len [batch]
+ *   k_nodes, v_nodes  [batch, hkv, pool_cap, head_dim]: draft K/V of pool
+ *            nodes; this round writes its frontier nodes' rows
+ *   feat     [batch, pool_cap + 1, hidden]: node features; slot pool_cap is
+ *            the target's feature of the last verified position (the root's
+ *            parent); this round writes its frontier nodes' rows
+ *   frontier [batch, n_front] pool indices (all at depth `depth`; round 1:
+ *            the root alone at depth 0)
+ *   pool_*, pool_count, next_frontier, k, temperature: as spec_tree_expand
+ *   draft_logits  [batch, n_front, vocab] f32 out (may be NULL: kept in the
+ *            workspace)
+ *   workspace  spec_eagle_round_workspace_bytes() bytes
+ * A frontier node attends to the prefix cache and to its ancestors and
+ * itself in the draft tree (at most 64 nodes per round: n_front * (depth +
+ * 1) <= 64).  Requires hidden, hq * head_dim and ffn multiples of 64,
+ * head_dim 64 or 128, hq % hkv == 0.  Malformed pools or frontiers set
+ * SPEC_DEV_BAD_POOL.
+ * ------------------------------------------------------------------ */
+typedef struct spec_eagle_weights {
+  const void *fc, *ln1, *qkv, *o, *ln2, *gate_up, *down, *lnf, *lm, *emb;
+} spec_eagle_weights;
+size_t spec_eagle_round_workspace_bytes(int batch, int n_front, int hidden, int hq, int hkv,
+                                        int head_dim, int ffn, int vocab, int s_max,
+                                        int max_prefix);
+int spec_eagle_round(const spec_eagle_weights *w, int batch, int hidden, int hq, int hkv,
+                     int head_dim, int ffn, int vocab, const void *k_prefix, const void *v_prefix,
+                     int s_max, const int32_t *prefix_len, int max_prefix, void *k_nodes,
+                     void *v_nodes, void *feat, const int32_t *frontier, int n_front, int depth,
+                     int k, float temperature, int32_t *pool_parent, int32_t *pool_tok,
+                     float *pool_conf, float *pool_val, int32_t *pool_count, int pool_cap,
+                     int32_t *next_frontier, int n_next, float *draft_logits, void *workspace,
+                     size_t workspace_bytes, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
  * tree_attn_verify -- attention of every tree node over the shared prefix
  * KV and its own ancestors ("5.3 Medusa、EAGLE 与 MTP", sections 3.1 and 8;
  * "Medusa, explained", step 6; "Medusa and EAGLE ... explained", section

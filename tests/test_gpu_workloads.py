@@ -58,7 +58,17 @@ def _tree_reference(step):
     w, B, N = step.w, step.w.batch, step.w.n_nodes
     if w.tree == "dynamic":
         dk = w.dynamic
-        par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], w.vocab)
+        if dk.get("draft"):
+            # the pool drafted on the GPU this step (the drafting rounds have
+            # their own parity test); the rerank is checked exactly on it
+            par, tok, conf = (host(x) for x in step.pool)
+            M = par.shape[1]
+            assert (host(step.e_cnt) == M).all()
+            for b in range(B):
+                assert par[b, 0] == -1 and all(0 <= par[b, i] < i for i in range(1, M))
+                assert ((conf[b, 1:] >= 0) & (conf[b, 1:] <= 1)).all()
+        else:
+            par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], w.vocab)
         trees = [T.rerank_dynamic(par[b], tok[b], conf[b], N, int(step.prefix[b])) for b in range(B)]
         return {k: np.stack([t[k] for t in trees]) for k in
                 ("tok", "parent", "depth", "pos", "anc", "mask", "first_child", "next_sibling")}

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "specverify.h"
+
 int sv_build_static(const int32_t *parents, const int32_t *rank, const int32_t *cand_tok,
                     int cand_levels, int cand_s, const int32_t *root_tok, const int32_t *prefix_len,
                     int batch, int n, int32_t *tok, int32_t *depth, int32_t *pos, uint64_t *anc,
@@ -59,6 +61,9 @@ size_t sv_attn_tc2_ws_bytes();
 int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void *vc, const void *kt,
                 const void *vt, const int32_t *prefix_len, const uint64_t *anc, void *out,
                 float scale, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
+int sv_attn_run(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const void *kc, const void *vc,
+                const void *kt, const void *vt, const int32_t *prefix_len, const uint64_t *anc, void *out,
+                float scale, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream);
 int sv_attn_combine(const SvAttnShape &s, const SvAttnPlan &p, const void *ws, void *out,
                     const int32_t *prefix_len, cudaStream_t stream);
 
@@ -91,6 +96,15 @@ int sv_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n
                       const int32_t *next_sibling, float temperature, float eps, float delta, int path_cap,
                       int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *ws, int32_t *status,
                       cudaStream_t stream);
+typedef spec_eagle_weights SvEagleWeights;
+size_t sv_eagle_round_ws_bytes(int batch, int n_front, int hidden, int hq, int hkv, int head_dim, int ffn,
+                               int vocab, int s_max, int max_prefix);
+int sv_eagle_round(const SvEagleWeights &w, int batch, int hidden, int hq, int hkv, int head_dim, int ffn, int vocab,
+                   const void *k_prefix, const void *v_prefix, int s_max, const int32_t *prefix_len, int max_prefix,
+                   void *k_nodes, void *v_nodes, void *feat, const int32_t *frontier, int n_front, int depth, int k,
+                   float temperature, int32_t *pool_parent, int32_t *pool_tok, float *pool_conf, float *pool_val,
+                   int32_t *pool_count, int pool_cap, int32_t *next_frontier, int n_next, float *logits_out,
+                   void *ws, int32_t *status, cudaStream_t stream);
 int sv_topk(const void *rows, int dtype, int n_rows, int row_len, int row_stride, int s,
             int32_t *idx, float *val, cudaStream_t stream);
 int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vocab,

@@ -31,6 +31,20 @@ SvAttnPlan sv_attn_plan(const SvAttnShape &s, int num_splits) {
   return sv_attn_simt_plan(s, num_splits);
 }
 
+// Run the planned attention kernel (and its combine) for shape s.
+int sv_attn_run(const SvAttnShape &s, const SvAttnPlan &p, const void *q, const void *kc, const void *vc,
+                const void *kt, const void *vt, const int32_t *prefix_len, const uint64_t *anc, void *out,
+                float scale, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t stream) {
+  if (p.use_tc == 2) {
+    if (p.ws_bytes == 0) return SPEC_ERR_CUDA;
+    return sv_attn_tc2(s, q, kc, vc, kt, vt, prefix_len, anc, out, scale, ws, ws_bytes, status, stream);
+  }
+  const int rc = p.use_tc ? sv_attn_tc(s, p, q, kc, vc, kt, vt, prefix_len, anc, out, scale, ws, status, stream)
+                          : sv_attn_simt(s, p, q, kc, vc, kt, vt, prefix_len, anc, out, scale, ws, status, stream);
+  if (rc != SPEC_OK || p.splits == 1) return rc;
+  return sv_attn_combine(s, p, ws, out, prefix_len, stream);
+}
+
 extern "C" {
 
 const char *spec_status_string(int status) {
@@ -178,17 +192,8 @@ int tree_attn_verify(const void *q, const void *k_cache, const void *v_cache, co
   if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned16(workspace)))
     return SPEC_ERR_CAPACITY;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)head_dim);
-  if (p.use_tc == 2) {
-    if (p.ws_bytes == 0) return SPEC_ERR_CUDA;
-    return sv_attn_tc2(s, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out, scale,
-                       workspace, workspace_bytes, dev_status, cs(stream));
-  }
-  rc = p.use_tc ? sv_attn_tc(s, p, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out,
-                             scale, workspace, dev_status, cs(stream))
-                : sv_attn_simt(s, p, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask,
-                               out, scale, workspace, dev_status, cs(stream));
-  if (rc != SPEC_OK || p.splits == 1) return rc;
-  return sv_attn_combine(s, p, workspace, out, prefix_len, cs(stream));
+  return sv_attn_run(s, p, q, k_cache, v_cache, k_tree, v_tree, prefix_len, anc_mask, out, scale, workspace,
+                     workspace_bytes, dev_status, cs(stream));
 }
 
 size_t spec_lm_head_workspace_bytes(int rows, int hidden, int vocab) {
@@ -221,15 +226,50 @@ int tree_attn_verify_paged(const void *q, const void *k_pages, const void *v_pag
   if (p.ws_bytes > 0 && (!workspace || workspace_bytes < p.ws_bytes || !aligned16(workspace)))
     return SPEC_ERR_CAPACITY;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)head_dim);
-  if (p.use_tc == 2)
-    return sv_attn_tc2(s, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale, workspace,
-                       workspace_bytes, dev_status, cs(stream));
-  rc = p.use_tc ? sv_attn_tc(s, p, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale,
-                             workspace, dev_status, cs(stream))
-                : sv_attn_simt(s, p, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale,
-                               workspace, dev_status, cs(stream));
-  if (rc != SPEC_OK || p.splits == 1) return rc;
-  return sv_attn_combine(s, p, workspace, out, prefix_len, cs(stream));
+  return sv_attn_run(s, p, q, k_pages, v_pages, k_tree, v_tree, prefix_len, anc_mask, out, scale, workspace,
+                     workspace_bytes, dev_status, cs(stream));
+}
+
+static bool eagle_shape_ok(int batch, int n_front, int hidden, int hq, int hkv, int head_dim, int ffn, int vocab) {
+  return batch >= 1 && n_front >= 1 && hidden >= 64 && hidden % 64 == 0 && hq >= 1 && hkv >= 1 && hq % hkv == 0 &&
+         (head_dim == 64 || head_dim == 128) && (hq * head_dim) % 64 == 0 && ffn >= 64 && ffn % 64 == 0 &&
+         vocab >= 1;
+}
+
+size_t spec_eagle_round_workspace_bytes(int batch, int n_front, int hidden, int hq, int hkv, int head_dim, int ffn,
+                                        int vocab, int s_max, int max_prefix) {
+  if (!eagle_shape_ok(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab) || max_prefix < 0 || s_max < max_prefix)
+    return 0;
+  return sv_eagle_round_ws_bytes(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab, s_max, max_prefix);
+}
+
+int spec_eagle_round(const spec_eagle_weights *w, int batch, int hidden, int hq, int hkv, int head_dim, int ffn,
+                     int vocab, const void *k_prefix, const void *v_prefix, int s_max, const int32_t *prefix_len,
+                     int max_prefix, void *k_nodes, void *v_nodes, void *feat, const int32_t *frontier, int n_front,
+                     int depth, int k, float temperature, int32_t *pool_parent, int32_t *pool_tok,
+                     float *pool_conf, float *pool_val, int32_t *pool_count, int pool_cap, int32_t *next_frontier,
+                     int n_next, float *draft_logits, void *workspace, size_t workspace_bytes,
+                     int32_t *dev_status, spec_stream_t stream) {
+  if (!w || !w->fc || !w->ln1 || !w->qkv || !w->o || !w->ln2 || !w->gate_up || !w->down || !w->lnf || !w->lm ||
+      !w->emb || !k_prefix || !v_prefix || !prefix_len || !k_nodes || !v_nodes || !feat || !frontier ||
+      !pool_parent || !pool_tok || !pool_conf || !pool_val || !pool_count || !next_frontier || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  if (!eagle_shape_ok(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab)) return SPEC_ERR_INVALID_ARG;
+  if (depth < 0 || max_prefix < 0 || s_max < max_prefix || pool_cap < 1 || n_next < 1 || k < 1 || vocab < k ||
+      !(temperature > 0.f))
+    return SPEC_ERR_INVALID_ARG;
+  if ((long long)n_front * (depth + 1) > 64 || k > 16 || n_front * k > 1024) return SPEC_ERR_UNSUPPORTED;
+  const void *ptrs[] = {w->fc, w->ln1, w->qkv, w->o, w->ln2, w->gate_up, w->down, w->lnf, w->lm, w->emb,
+                        k_prefix, v_prefix, k_nodes, v_nodes, feat, workspace};
+  for (const void *q : ptrs)
+    if (!aligned16(q)) return SPEC_ERR_INVALID_ARG;
+  if (workspace_bytes <
+      sv_eagle_round_ws_bytes(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab, s_max, max_prefix))
+    return SPEC_ERR_CAPACITY;
+  return sv_eagle_round(*w, batch, hidden, hq, hkv, head_dim, ffn, vocab, k_prefix, v_prefix, s_max, prefix_len,
+                        max_prefix, k_nodes, v_nodes, feat, frontier, n_front, depth, k, temperature, pool_parent,
+                        pool_tok, pool_conf, pool_val, pool_count, pool_cap, next_frontier, n_next, draft_logits,
+                        workspace, dev_status, cs(stream));
 }
 
 int spec_lm_head(const void *hid, const void *w, int rows, int hidden, int vocab, float *logits,

@@ -43,6 +43,9 @@ _SIGS = {
                                  _vp, _vp, _vp], _i),
     "spec_build_tree_batch": ([_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp], _i),
     "spec_tree_expand": ([_vp, _i, _i, _i, _i, _vp, _i, _f, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp], _i),
+    "spec_eagle_round_workspace_bytes": ([_i] * 10, _sz),
+    "spec_eagle_round": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _f,
+                          _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _sz, _vp, _vp], _i),
     "tree_attn_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i], _sz),
     "tree_attn_plan_splits": ([_i, _i, _i, _i, _i, _i, _vp], _i),
     "tree_attn_verify": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _i,
@@ -210,6 +213,46 @@ def spec_tree_expand(draft_logits, frontier, k, temperature, pool_parent, pool_t
         _p(draft_logits), _DT[draft_logits.dtype], B, F, V, _p(frontier), k, float(temperature),
         _p(pool_parent), _p(pool_tok), _p(pool_conf), _p(pool_val), _p(pool_count), pool_parent.shape[1],
         _p(next_frontier), next_frontier.shape[1], _p(dev_status), _stream()))
+
+
+EAGLE_WEIGHTS = ("fc", "ln1", "qkv", "o", "ln2", "gate_up", "down", "lnf", "lm", "emb")
+
+
+class _EagleWeights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in EAGLE_WEIGHTS]
+
+
+def spec_eagle_round_workspace_bytes(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab, s_max, max_prefix):
+    return int(load().spec_eagle_round_workspace_bytes(batch, n_front, hidden, hq, hkv, head_dim, ffn, vocab, s_max,
+                                                       max_prefix))
+
+
+def spec_eagle_round(weights, k_prefix, v_prefix, prefix_len, max_prefix, k_nodes, v_nodes, feat, frontier, depth, k,
+                     temperature, pool_parent, pool_tok, pool_conf, pool_val, pool_count, next_frontier,
+                     draft_logits=None, workspace=None, dev_status=None):
+    """One EAGLE drafting round; ``weights`` maps the names in EAGLE_WEIGHTS
+    to bf16 tensors (layouts in the C header)."""
+    B, _, d = feat.shape
+    hkv, S, D = k_prefix.shape[1], k_prefix.shape[2], k_prefix.shape[3]
+    hq = weights["o"].shape[1] // D
+    ffn = weights["down"].shape[1]
+    V = weights["lm"].shape[0]
+    F = frontier.shape[1]
+    for n in EAGLE_WEIGHTS:
+        _want(weights[n], torch.bfloat16)
+    for t in (k_prefix, v_prefix, k_nodes, v_nodes, feat):
+        _want(t, torch.bfloat16)
+    _want(draft_logits, torch.float32)
+    w = _EagleWeights(*[_p(weights[n]).value for n in EAGLE_WEIGHTS])
+    if workspace is None:
+        workspace = _scratch(spec_eagle_round_workspace_bytes(B, F, d, hq, hkv, D, ffn, V, S, int(max_prefix)), feat)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("spec_eagle_round", load().spec_eagle_round(
+        C.c_void_p(C.addressof(w)), B, d, hq, hkv, D, ffn, V, _p(k_prefix), _p(v_prefix), S, _p(prefix_len),
+        int(max_prefix), _p(k_nodes), _p(v_nodes), _p(feat), _p(frontier), F, int(depth), int(k), float(temperature),
+        _p(pool_parent), _p(pool_tok), _p(pool_conf), _p(pool_val), _p(pool_count), pool_parent.shape[1],
+        _p(next_frontier), next_frontier.shape[1], _p(draft_logits), _p(workspace), ws_bytes, _p(dev_status),
+        _stream()))
 
 
 def tree_attn_workspace_bytes(dtype, batch, n_nodes, hq, hkv, head_dim, max_prefix, num_splits=0):

@@ -315,7 +315,7 @@ WORKLOADS = {
     "llama8b_eagle2": Workload(
         "llama8b_eagle2", 1002, batch=8, hq=32, hkv=8, head_dim=128, dtype="bf16",
         prefix=(512, 8192), n_nodes=60, n_levels=6, vocab=128256, accept="reject", tree="dynamic",
-        dynamic=dict(k=10, frontier=10, rounds=5)),
+        dynamic=dict(k=10, frontier=10, rounds=5, draft=dict(ffn=14336, w_std=0.02))),
     "llama70b_serving": Workload(
         "llama70b_serving", 1003, batch=64, hq=64, hkv=8, head_dim=128, dtype="bf16",
         prefix=(4096, 4096), n_nodes=32, n_levels=4, vocab=128256, accept="greedy", tree="random",
