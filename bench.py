@@ -153,8 +153,11 @@ class GpuStep:
         # tree
         if w.tree == "dynamic":
             dk = w.dynamic
-            par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
-            self.pool = [cu(par), cu(tok), cu(conf)]
+            if dk.get("draft"):
+                self._eagle_setup()         # the pool is drafted on the GPU each step
+            else:
+                par, tok, conf = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
+                self.pool = [cu(par), cu(tok), cu(conf)]
             self.path_cap = dk["rounds"] + 2
             self.shape = None
         else:
@@ -205,8 +208,11 @@ class GpuStep:
                                       synth.node_tokens_from_table(self.shape, cand, synth.root_tokens(w)),
                                       bf16=w.dtype == "bf16")
             elif w.planted:
-                # plant on the tree the GPU builds from the seeded pool (deterministic)
-                self.stages[0][1]()
+                # plant on the tree the GPU builds from the (drafted) pool (deterministic)
+                for nm, fn, _, _ in self.stages:
+                    fn()
+                    if nm == "build_tree":
+                        break
                 torch.cuda.synchronize()
                 synth.plant_agreement(w.seed, lg, self.par_out.cpu().numpy(), self.depth.cpu().numpy(),
                                       self.tok.cpu().numpy(), bf16=True)
@@ -243,8 +249,67 @@ class GpuStep:
             self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos, self.anc,
             self.fc, self.ns, self.status), 1, None))
 
+    def _eagle_setup(self):
+        """EAGLE-2 drafting on the GPU: random draft-layer weights of the
+        target's shape (drawn on the device from a seeded generator), the
+        draft layer's prefix cache, and a pool grown by `rounds` drafting
+        rounds from the root: k children per frontier node, the next frontier
+        the `frontier` new nodes of highest path value."""
+        torch, sv, w = self.torch, self.sv, self.w
+        dk, dr = w.dynamic, w.dynamic["draft"]
+        dev, bf = self.dev, torch.bfloat16
+        B, hq, hkv, D, V = w.batch, w.hq, w.hkv, w.head_dim, w.vocab
+        d, ffn, k, F, R = hq * D, dr["ffn"], dk["k"], dk["frontier"], dk["rounds"]
+        M = 1 + k + (R - 1) * F * k
+        gen = torch.Generator(device=dev).manual_seed(w.seed + 77)
+        rnd = lambda *shape, std=1.0, mean=0.0: (torch.randn(shape, generator=gen, device=dev) * std + mean).to(bf)
+        sd = dr["w_std"]
+        self.eagle_w = dict(fc=rnd(d, 2 * d, std=sd), ln1=rnd(d, std=0.05, mean=1.0), qkv=rnd((hq + 2 * hkv) * D, d, std=sd),
+                            o=rnd(d, hq * D, std=sd), ln2=rnd(d, std=0.05, mean=1.0), gate_up=rnd(2, ffn, d, std=sd),
+                            down=rnd(d, ffn, std=sd), lnf=rnd(d, std=0.05, mean=1.0), lm=rnd(V, d, std=sd),
+                            emb=rnd(V, d))
+        S = self.s_max
+        self.e_kp, self.e_vp = rnd(B, hkv, S, D), rnd(B, hkv, S, D)
+        self.e_kn = torch.zeros((B, hkv, M, D), dtype=bf, device=dev)
+        self.e_vn = torch.zeros_like(self.e_kn)
+        self.e_feat = torch.zeros((B, M + 1, d), dtype=bf, device=dev)
+        self.e_feat[:, M] = rnd(B, d)
+        root = torch.from_numpy(self.synth.root_tokens(w)).to(dev)
+        i32 = lambda *sh: torch.zeros(sh, dtype=torch.int32, device=dev)
+        self.e_par0 = torch.full((B, M), -1, dtype=torch.int32, device=dev)
+        self.e_tok0 = i32(B, M)
+        self.e_tok0[:, 0] = root
+        self.e_conf0 = torch.zeros((B, M), dtype=torch.float32, device=dev)
+        self.e_conf0[:, 0] = 1.0
+        self.e_cnt0 = torch.ones(B, dtype=torch.int32, device=dev)
+        self.pool = [self.e_par0.clone(), self.e_tok0.clone(), self.e_conf0.clone()]
+        self.e_val, self.e_cnt = self.e_conf0.clone(), self.e_cnt0.clone()
+        self.e_front = [i32(B, 1), i32(B, F), i32(B, F)]
+        self.e_ws = torch.empty(sv.spec_eagle_round_workspace_bytes(B, F, d, hq, hkv, D, ffn, V, S, self.max_prefix),
+                                dtype=torch.uint8, device=dev)
+        self.e_rounds = R
+        # this layer's weight and cache bytes streamed per round (algorithmic)
+        self.eagle_round_bytes = 2 * (d * 2 * d + (hq + 2 * hkv) * D * d + d * hq * D + 2 * ffn * d + d * ffn + V * d) \
+            + hkv * D * 2 * 2 * (int(self.prefix.sum()))
+
+    def _eagle_rounds(self):
+        sv, w = self.sv, self.w
+        par, tok, conf = self.pool
+        par.copy_(self.e_par0); tok.copy_(self.e_tok0); conf.copy_(self.e_conf0)
+        self.e_val.copy_(self.e_conf0); self.e_cnt.copy_(self.e_cnt0)
+        front = self.e_front[0]
+        for r in range(self.e_rounds):
+            nxt = self.e_front[1 + (r % 2)]
+            sv.spec_eagle_round(self.eagle_w, self.e_kp, self.e_vp, self.d_prefix, self.max_prefix, self.e_kn,
+                                self.e_vn, self.e_feat, front, r, w.dynamic["k"], w.temperature, par, tok, conf,
+                                self.e_val, self.e_cnt, nxt, workspace=self.e_ws, dev_status=self.status)
+            front = nxt
+
     def _static_or_dynamic_build(self, cu):
         sv, synth, w = self.sv, self.synth, self.w
+        if w.tree == "dynamic" and w.dynamic.get("draft"):
+            self.stages.append(("eagle_draft", self._eagle_rounds, 20 * self.e_rounds,
+                                self.eagle_round_bytes * self.e_rounds))
         if w.tree == "dynamic":
             par, tok, conf = self.pool
             self.stages.append(("build_tree", lambda: sv.spec_build_tree_dynamic(
@@ -404,7 +469,10 @@ class OracleStep:
         desc = []
         if w.tree == "dynamic":
             dk = w.dynamic
+            # (a host-drawn pool of the same shape stands in for the drafting
+            # rounds, which the oracle does not time)
             self.pool = synth.candidate_pool(w.seed, B, dk["k"], dk["frontier"], dk["rounds"], V)
+            desc.append("drafting rounds not timed (pool drawn)")
         else:
             self.shape = synth.tree_shape(w)
             self.s = w.medusa["topk"] if w.medusa else (max(w.caps) if w.caps else 2)
