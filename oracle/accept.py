@@ -178,7 +178,14 @@ def accept_reject(logits, tok, first_child, next_sibling, seed, step, T, path_ca
             chosen = -1
             for c in _children(first_child[b], next_sibling[b], v):
                 x = int(tok[b, c])
-                r = dtype(0) if x in excluded else e[x] / (S - removed)
+                # the residual's mass is at least x's own; the last token left
+                # in the vocabulary holds all of it (r = 1)
+                if x in excluded:
+                    r = dtype(0)
+                elif len(excluded) + 1 == V:
+                    r = dtype(1)
+                else:
+                    r = e[x] / max(S - removed, e[x])
                 u = rng.uniform_accept(seed, b, step, c)
                 d = ("accept", c)
                 if abs(float(u) - float(r)) <= NEAR_REJECT * max(float(r), 1e-30):

@@ -251,6 +251,58 @@ def test_out_of_range_child_token_is_reported_and_never_accepted(mode):
     assert 1 not in got[1][0].tolist()
 
 
+def _raw_accept(mode, lg, tok, parents, fc, ns, cap, **kw):
+    B = lg.shape[0]
+    acc_len, acc_path, bonus, st = zeros_i32(B), zeros_i32(B, cap), zeros_i32(B), zeros_i32(1)
+    bc = lambda a: i32(np.broadcast_to(np.asarray(a, np.int32), (B, len(a))).copy())
+    sv.spec_accept(mode, dev(lg), bc(tok), bc(parents), bc(fc), bc(ns), acc_len, acc_path, bonus, dev_status=st,
+                   **kw)
+    torch.cuda.synchronize()
+    return host(acc_len), host(acc_path), host(bonus), int(host(st)[0])
+
+
+def test_typical_reports_parents_that_disagree_with_the_child_links():
+    """Node 3 is linked as a child of node 1 but its parents[] entry is -1;
+    node 4 (under node 3) is the deepest accepted node.  The path along
+    parents[] cannot reach the root: reported, and the root alone is
+    accepted with the root row's argmax as the bonus."""
+    V = 64
+    tok = [5, 7, 9, 11, 13]
+    parents = [-1, 0, 1, -1, 3]
+    fc = [1, 2, -1, 4, -1]
+    ns = [-1, -1, 3, -1, -1]
+    g = np.random.default_rng(11)
+    lg = g.standard_normal((2, 5, V)).astype(np.float32)
+    lg[:, 1, 9] = -1e4                                   # node 2 (token 9 under node 1) fails the threshold
+    got = _raw_accept(sv.TYPICAL, lg, tok, parents, fc, ns, 3, eps=0.0, delta=0.0, temperature=1.0)
+    assert got[3] == sv.DEV_BAD_PARENTS
+    np.testing.assert_array_equal(got[0], [0, 0])
+    np.testing.assert_array_equal(got[1], [[0, -1, -1]] * 2)
+    np.testing.assert_array_equal(got[2], lg[:, 0].argmax(-1))
+
+
+@pytest.mark.parametrize("V", [2, 3, 4])
+def test_reject_children_covering_the_vocabulary(V):
+    """The root's children hold every token of a tiny vocabulary: the last
+    child is the only mass left, so some child is always accepted and the
+    residual is never sampled empty; every step equals the oracle."""
+    tok = [0] + list(range(V))
+    parents = [-1] + [0] * V
+    fc = [1] + [-1] * V
+    ns = [-1] + list(range(2, V + 1)) + [-1]
+    B = 8
+    g = np.random.default_rng(20 + V)
+    lg = (g.standard_normal((B, V + 1, V)) * 1.5).astype(np.float32)
+    bt = lambda a: np.broadcast_to(np.asarray(a, np.int32), (B, len(a)))
+    for step in range(16):
+        got = _raw_accept(sv.REJECT, lg, tok, parents, fc, ns, 2, temperature=1.0, seed=31, step=step)
+        assert got[3] == 0
+        assert (got[0] == 1).all() and ((got[2] >= 0) & (got[2] < V)).all()
+        rerun = lambda flip: ACC.accept_reject(lg, bt(tok), bt(fc), bt(ns), 31, step, 1.0, 2, flip=flip)
+        ref = rerun(())
+        assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "reject (whole vocabulary)") == 0
+
+
 def test_commit_bad_path_is_reported_and_skipped():
     B, Hkv, S, N, D = 3, 2, 32, 8, 64
     g = np.random.default_rng(9)

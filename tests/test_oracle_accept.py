@@ -365,6 +365,26 @@ def test_rejection_walk_frequencies_match_exact_enumeration():
     assert stats.chi2.sf(chi2, len(keys) - 1) > 1e-3
 
 
+@pytest.mark.parametrize("V", [2, 3])
+def test_rejection_children_covering_the_vocabulary_always_accept_one(V):
+    """Exact arithmetic: after every other token is removed, the last child
+    holds the whole residual and is accepted with probability 1, so the walk
+    never samples an empty residual; the first child's acceptance frequency
+    is p(tok 0) (here checked against its exact value over many steps)."""
+    parents = [-1] + [0] * V
+    _, fc, ns, _ = _tree_arrays(parents)
+    tok = np.array([[0] + list(range(V))])
+    logits = np.array([[[0.3, -0.2, 0.9][:V]] * (V + 1)], np.float32)
+    p = _softmax64(logits[0, 0].astype(np.float64))
+    first = 0
+    n = 4000
+    for step in range(n):
+        acc_len, acc_path, bonus, _ = ACC.accept_reject(logits, tok, fc, ns, seed=3, step=step, T=1.0, path_cap=2)
+        assert acc_len[0] == 1 and 0 <= bonus[0] < V
+        first += int(acc_path[0, 1] == 1)
+    assert abs(first / n - p[0]) < 4 * np.sqrt(p[0] * (1 - p[0]) / n)
+
+
 def _contexts(parents, tok):
     """Tokens on each node's path after the root."""
     ctx = {}

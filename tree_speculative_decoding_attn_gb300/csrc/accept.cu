@@ -402,12 +402,32 @@ __global__ void __launch_bounds__(kThreads, 2)
       int best = 0;
       for (int i = 1; i < N; ++i)
         if (s_ok[i] && s_depth[i] > s_depth[best]) best = i;
-      int d = s_depth[best];  // root-first path of `best`
-      s_len = d + 1;
-      for (int u = best; d >= 0; --d) {
-        s_path[d] = u;
-        u = s_par[u];
+      // root-first path of `best` along parents[]: every step must go to an
+      // earlier node and end at the root, else parents[] disagrees with the
+      // child links (reported; the root alone is accepted)
+      const int d = s_depth[best];
+      bool good = true;
+      for (int u = best, k = d; k >= 0; --k) {
+        if (u < 0 || u >= N || (k == 0) != (u == 0)) {
+          good = false;
+          break;
+        }
+        s_path[k] = u;
+        if (k > 0) {
+          const int p = s_par[u];
+          if (p < 0 || p >= u) {
+            good = false;
+            break;
+          }
+          u = p;
+        }
       }
+      if (!good) {
+        sv::report(status, SPEC_DEV_BAD_PARENTS);
+        best = 0;
+        s_path[0] = 0;
+      }
+      s_len = good ? d + 1 : 1;
       s_next = best;
     }
     __syncthreads();
@@ -484,7 +504,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       });
       const unsigned long long best = cl.max_u64(bx < hi ? sv::rank_key(bk, (uint32_t)bx) : 0ull);
-      if (threadIdx.x == 0) s_bonus = (int)sv::key_index(best);
+      const int a = best ? (int)sv::key_index(best) : row_argmax(row);  // empty residual: the argmax
+      if (threadIdx.x == 0) s_bonus = a;
       __syncthreads();
       break;
     }
@@ -517,7 +538,9 @@ __global__ void __launch_bounds__(kThreads, 2)
               sv::report(status, SPEC_DEV_BAD_TOKEN);
               seen = true;
             } else if (!seen) {
-              r = s_kex[j] / (s.S - removed);
+              // the residual's mass is at least this token's own; the last
+              // token left in the vocabulary holds all of it
+              r = nexc + 1 >= V ? 1.f : s_kex[j] / fmaxf(s.S - removed, s_kex[j]);
             }
             if (s_ku[j] < r) {
               nxt = c;
@@ -585,7 +608,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
           });
       const unsigned long long best = cl.max_u64(bx < hi ? sv::rank_key(bk, (uint32_t)bx) : 0ull);
-      if (threadIdx.x == 0) s_bonus = (int)sv::key_index(best);
+      // an empty residual (not reached in exact arithmetic): the row's argmax
+      const int a = best ? (int)sv::key_index(best) : row_argmax(row);
+      if (threadIdx.x == 0) s_bonus = a;
       __syncthreads();
       break;
     }
