@@ -308,7 +308,9 @@ class GpuStep:
     def _static_or_dynamic_build(self, cu):
         sv, synth, w = self.sv, self.synth, self.w
         if w.tree == "dynamic" and w.dynamic.get("draft"):
-            self.stages.append(("eagle_draft", self._eagle_rounds, 20 * self.e_rounds,
+            # per round: 6 GEMMs, 4 stream-K fixups (the GEMMs of d-row weights), 9 row kernels,
+            # tree build, attention + merge, expansion (2)
+            self.stages.append(("eagle_draft", self._eagle_rounds, 24 * self.e_rounds,
                                 self.eagle_round_bytes * self.e_rounds))
         if w.tree == "dynamic":
             par, tok, conf = self.pool

@@ -278,8 +278,9 @@ int spec_tree_expand(const void *draft_logits, int dtype, int batch, int n_front
  *   workspace  spec_eagle_round_workspace_bytes() bytes
  * A frontier node attends to the prefix cache and to its ancestors and
  * itself in the draft tree (at most 64 nodes per round: n_front * (depth +
- * 1) <= 64).  Requires hidden, hq * head_dim and ffn multiples of 64,
- * head_dim 64 or 128, hq % hkv == 0.  Malformed pools or frontiers set
+ * 1) <= 64).  Requires hidden (at most 8192), hq * head_dim and ffn
+ * multiples of 64, head_dim 64 or 128, hq % hkv == 0, pool_cap <= 4000
+ * (else SPEC_ERR_UNSUPPORTED).  Malformed pools or frontiers set
  * SPEC_DEV_BAD_POOL.
  * ------------------------------------------------------------------ */
 typedef struct spec_eagle_weights {

@@ -80,31 +80,53 @@ __global__ void __launch_bounds__(kThreads)
 
 // y = RMSNorm(x (+ add)) w, bf16; with `add` the sum is also written back to
 // x_out (float32, the residual stream) and, optionally, as bf16 to feat_out
-// at the frontier node's slot.
+// at the frontier node's slot.  d is a multiple of 8 (16-byte rows); the
+// row stays in registers between the two passes.
+constexpr int kRmsVec = 8;  // float4 per thread: d <= 4 * kRmsVec * kThreads = 8192
 __global__ void __launch_bounds__(kThreads)
     rmsnorm_kernel(const float *__restrict__ x, const float *__restrict__ add, float *__restrict__ x_out,
                    const __nv_bfloat16 *__restrict__ w, int d, __nv_bfloat16 *__restrict__ y,
                    __nv_bfloat16 *__restrict__ feat_out, const int32_t *__restrict__ frontier, int F, int pool_cap) {
   __shared__ float red[kThreads / 32];
   const int r = blockIdx.x;
-  const float *xr = x + (int64_t)r * d;
-  const float *ar = add ? add + (int64_t)r * d : nullptr;
+  const float4 *xr = reinterpret_cast<const float4 *>(x + (int64_t)r * d);
+  const float4 *ar = add ? reinterpret_cast<const float4 *>(add + (int64_t)r * d) : nullptr;
+  const int n4 = d / 4;
+  float4 v[kRmsVec];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += kThreads) {
-    const float v = xr[i] + (ar ? ar[i] : 0.f);
-    ss = fmaf(v, v, ss);
+#pragma unroll
+  for (int q = 0; q < kRmsVec; ++q) {
+    const int i = (int)threadIdx.x + q * kThreads;
+    v[q] = i < n4 ? xr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ar && i < n4) {
+      const float4 a = ar[i];
+      v[q].x += a.x;
+      v[q].y += a.y;
+      v[q].z += a.z;
+      v[q].w += a.w;
+    }
+    ss = fmaf(v[q].x, v[q].x, fmaf(v[q].y, v[q].y, fmaf(v[q].z, v[q].z, fmaf(v[q].w, v[q].w, ss))));
   }
   const float inv = rsqrtf(block_sum(ss, red) / (float)d + kRmsEps);
   __nv_bfloat16 *fo = nullptr;
   if (feat_out) {
-    const int b = r / F, v = frontier[r];
-    if (v >= 0 && v < pool_cap) fo = feat_out + ((int64_t)b * (pool_cap + 1) + v) * d;
+    const int b = r / F, fv = frontier[r];
+    if (fv >= 0 && fv < pool_cap) fo = feat_out + ((int64_t)b * (pool_cap + 1) + fv) * d;
   }
-  for (int i = threadIdx.x; i < d; i += kThreads) {
-    const float v = xr[i] + (ar ? ar[i] : 0.f);
-    if (x_out) x_out[(int64_t)r * d + i] = v;
-    if (fo) fo[i] = __float2bfloat16_rn(v);
-    y[(int64_t)r * d + i] = __float2bfloat16_rn(v * inv * __bfloat162float(w[i]));
+#pragma unroll
+  for (int q = 0; q < kRmsVec; ++q) {
+    const int i = (int)threadIdx.x + q * kThreads;
+    if (i >= n4) break;
+    if (x_out) reinterpret_cast<float4 *>(x_out + (int64_t)r * d)[i] = v[q];
+    if (fo) {
+      reinterpret_cast<__nv_bfloat162 *>(fo)[2 * i] = __floats2bfloat162_rn(v[q].x, v[q].y);
+      reinterpret_cast<__nv_bfloat162 *>(fo)[2 * i + 1] = __floats2bfloat162_rn(v[q].z, v[q].w);
+    }
+    const __nv_bfloat162 w01 = reinterpret_cast<const __nv_bfloat162 *>(w)[2 * i];
+    const __nv_bfloat162 w23 = reinterpret_cast<const __nv_bfloat162 *>(w)[2 * i + 1];
+    __nv_bfloat162 *yr = reinterpret_cast<__nv_bfloat162 *>(y + (int64_t)r * d);
+    yr[2 * i] = __floats2bfloat162_rn(v[q].x * inv * __low2float(w01), v[q].y * inv * __high2float(w01));
+    yr[2 * i + 1] = __floats2bfloat162_rn(v[q].z * inv * __low2float(w23), v[q].w * inv * __high2float(w23));
   }
 }
 
@@ -119,10 +141,14 @@ __global__ void __launch_bounds__(kThreads)
   extern __shared__ int sm[];
   int *mark = sm;                 // [pool_cap]: 0 absent, 1 ancestor, 2 frontier
   int *newi = sm + pool_cap;      // [pool_cap]: compact index
-  __shared__ int s_n, s_bad;
+  int *pp = sm + 2 * pool_cap;    // [pool_cap]: the pool's parents (walked from shared memory)
+  __shared__ int s_n, s_bad, s_run, s_wc[kThreads / 32];
   const int b = blockIdx.x;
-  const int32_t *pp = pool_parent + (int64_t)b * pool_cap;
-  for (int i = threadIdx.x; i < pool_cap; i += kThreads) mark[i] = 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < pool_cap; i += kThreads) {
+    mark[i] = 0;
+    pp[i] = pool_parent[(int64_t)b * pool_cap + i];
+  }
   if (threadIdx.x == 0) s_bad = 0;
   __syncthreads();
   for (int f = threadIdx.x; f < F; f += kThreads) {
@@ -148,11 +174,26 @@ __global__ void __launch_bounds__(kThreads)
       u = pp[u];
     }
   }
+  // ancestors numbered in pool order: a block-wide count of the marked
+  // entries before each one
+  if (threadIdx.x == 0) s_run = 0;
   __syncthreads();
+  for (int c0 = 0; c0 < pool_cap; c0 += kThreads) {
+    const int i = c0 + (int)threadIdx.x;
+    const bool is_anc = i < pool_cap && mark[i] == 1;
+    const unsigned bal = __ballot_sync(0xffffffffu, is_anc);
+    if (lane == 0) s_wc[warp] = __popc(bal);
+    __syncthreads();
+    int off = s_run;
+    for (int w = 0; w < warp; ++w) off += s_wc[w];
+    if (is_anc) newi[i] = off + __popc(bal & ((1u << lane) - 1u));
+    __syncthreads();
+    if (threadIdx.x == 0)
+      for (int w = 0; w < kThreads / 32; ++w) s_run += s_wc[w];
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    int n = 0;
-    for (int i = 0; i < pool_cap; ++i)
-      if (mark[i] == 1) newi[i] = n++;
+    int n = s_run;
     for (int f = 0; f < F; ++f) {
       const int v = frontier[(int64_t)b * F + f];
       if (v >= 0 && v < pool_cap && mark[v] == 2) {
@@ -196,26 +237,34 @@ __global__ void __launch_bounds__(kThreads)
 
 // Rotary embedding (rotate-half: dims i and i + D/2 by pos * base^(-2i/D))
 // of the frontier rows' Q and K at position prefix_len + depth; Q goes to
-// its compact row, K and V to the node cache slot of the frontier node.
+// its compact row, K and V to the node cache slot of the frontier node.  The
+// D/2 angles of the row's position are taken once per row, in double, then
+// rounded to float cosines and sines.
+constexpr int kMaxHalf = 128;
 __global__ void __launch_bounds__(kThreads)
     rope_kernel(const float *__restrict__ qkv, int F, int hq, int hkv, int D, const int32_t *__restrict__ frontier,
                 const int32_t *__restrict__ cidx, int C, const int32_t *__restrict__ prefix_len, int depth,
                 int pool_cap, __nv_bfloat16 *__restrict__ qc, __nv_bfloat16 *__restrict__ k_nodes,
                 __nv_bfloat16 *__restrict__ v_nodes) {
+  __shared__ float2 cs[kMaxHalf];
   const int r = blockIdx.x, b = r / F, f = r % F;
   const int v = frontier[r];
   if (v < 0 || v >= pool_cap) return;
   const int ci = cidx[(int64_t)b * F + f];
-  const double pos = (double)(prefix_len[b] + depth);
   const int half = D / 2;
+  for (int i = threadIdx.x; i < half; i += kThreads) {
+    double sn, c;
+    sincos((double)(prefix_len[b] + depth) * pow(kRopeBase, -2.0 * i / D), &sn, &c);
+    cs[i] = make_float2((float)c, (float)sn);
+  }
+  __syncthreads();
   const float *row = qkv + (int64_t)r * (hq + 2 * hkv) * D;
+#pragma unroll 4
   for (int e = threadIdx.x; e < (hq + 2 * hkv) * half; e += kThreads) {
     const int h = e / half, i = e % half;
     const float x1 = row[h * D + i], x2 = row[h * D + i + half];
     if (h < hq + hkv) {
-      double sn, cs;
-      sincos(pos * pow(kRopeBase, -2.0 * i / D), &sn, &cs);
-      const float c = (float)cs, s = (float)sn;
+      const float c = cs[i].x, s = cs[i].y;
       const float y1 = x1 * c - x2 * s, y2 = x2 * c + x1 * s;
       __nv_bfloat16 *dst = h < hq ? qc + (((int64_t)b * C + ci) * hq + h) * D
                                   : k_nodes + (((int64_t)b * hkv + (h - hq)) * pool_cap + v) * D;
@@ -263,15 +312,18 @@ __global__ void __launch_bounds__(kThreads)
   for (int i = threadIdx.x; i < hqd / 8; i += kThreads) dst[i] = src[i];
 }
 
-// act = SiLU(gate) * up from the [R, 2, f] float32 product, bf16.
+// act = SiLU(gate) * up from the [R, 2, f] float32 product, bf16; grid
+// (chunks of 4 * kThreads, R), f a multiple of 4.
 __global__ void __launch_bounds__(kThreads)
     swiglu_kernel(const float *__restrict__ gu, int f, __nv_bfloat16 *__restrict__ act) {
-  const int r = blockIdx.x;
-  const float *g = gu + (int64_t)r * 2 * f, *u = g + f;
-  for (int i = threadIdx.x; i < f; i += kThreads) {
-    const float x = g[i];
-    act[(int64_t)r * f + i] = __float2bfloat16_rn(x / (1.f + __expf(-x)) * u[i]);
-  }
+  const int r = blockIdx.y, i = (int)(blockIdx.x * kThreads + threadIdx.x);
+  if (4 * i >= f) return;
+  const float4 g = reinterpret_cast<const float4 *>(gu + (int64_t)r * 2 * f)[i];
+  const float4 u = reinterpret_cast<const float4 *>(gu + (int64_t)r * 2 * f + f)[i];
+  auto silu = [](float x) { return x / (1.f + __expf(-x)); };
+  __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(act + (int64_t)r * f);
+  dst[2 * i] = __floats2bfloat162_rn(silu(g.x) * u.x, silu(g.y) * u.y);
+  dst[2 * i + 1] = __floats2bfloat162_rn(silu(g.z) * u.z, silu(g.w) * u.w);
 }
 
 struct Layout {
@@ -372,7 +424,7 @@ int sv_eagle_round(const SvEagleWeights &w, int batch, int hidden, int hq, int h
                                              nullptr, F, pool_cap);
   if ((rc = gemm(w.qkv, bf(l.n1), (hq + 2 * hkv) * D, d, 1, f32(l.qkv))) != SPEC_OK) return rc;
   // the round's draft tree, its Q / K / V and masks
-  compact_kernel<<<B, kThreads, (size_t)2 * pool_cap * sizeof(int), stream>>>(
+  compact_kernel<<<B, kThreads, (size_t)3 * pool_cap * sizeof(int), stream>>>(
       pool_parent, frontier, F, pool_cap, C, i32(l.cpar), i32(l.nval), i32(l.cpool), i32(l.cidx), status);
   if (cudaMemsetAsync(at(l.qc), 0, (size_t)B * C * hq * D * 2, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   rope_kernel<<<R, kThreads, 0, stream>>>(f32(l.qkv), F, hq, hkv, D, frontier, i32(l.cidx), C, prefix_len, depth,
@@ -396,7 +448,7 @@ int sv_eagle_round(const SvEagleWeights &w, int batch, int hidden, int hq, int h
                                              reinterpret_cast<const __nv_bfloat16 *>(w.ln2), d, bf(l.n2), nullptr,
                                              nullptr, F, pool_cap);
   if ((rc = gemm(w.gate_up, bf(l.n2), ffn, d, 2, f32(l.gu))) != SPEC_OK) return rc;
-  swiglu_kernel<<<R, kThreads, 0, stream>>>(f32(l.gu), ffn, bf(l.act));
+  swiglu_kernel<<<dim3((ffn / 4 + kThreads - 1) / kThreads, R), kThreads, 0, stream>>>(f32(l.gu), ffn, bf(l.act));
   if ((rc = gemm(w.down, bf(l.act), d, ffn, 1, f32(l.dn))) != SPEC_OK) return rc;
   // the node's feature (f = h1 + down) and the final norm before the LM head
   rmsnorm_kernel<<<R, kThreads, 0, stream>>>(f32(l.dn), f32(l.h1), nullptr,

@@ -74,6 +74,7 @@ struct SvGemmPlan {
   int nk, tiles_pg, n_tiles, n_ctas, rows_per_launch;
   long long units;         // (tile, 64-wide K chunk) pairs
   size_t counter_bytes, partial_bytes;
+  bool defer;              // cut tiles summed by a dependent fixup launch (single-phase GEMMs)
 };
 SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows);
 // One weight-streaming GEMM (all row blocks).  epi: 0 float32 logits, 1

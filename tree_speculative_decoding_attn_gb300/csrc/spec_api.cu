@@ -231,7 +231,7 @@ int tree_attn_verify_paged(const void *q, const void *k_pages, const void *v_pag
 }
 
 static bool eagle_shape_ok(int batch, int n_front, int hidden, int hq, int hkv, int head_dim, int ffn, int vocab) {
-  return batch >= 1 && n_front >= 1 && hidden >= 64 && hidden % 64 == 0 && hq >= 1 && hkv >= 1 && hq % hkv == 0 &&
+  return batch >= 1 && n_front >= 1 && hidden >= 64 && hidden % 64 == 0 && hidden <= 8192 && hq >= 1 && hkv >= 1 && hq % hkv == 0 &&
          (head_dim == 64 || head_dim == 128) && (hq * head_dim) % 64 == 0 && ffn >= 64 && ffn % 64 == 0 &&
          vocab >= 1;
 }
@@ -258,7 +258,8 @@ int spec_eagle_round(const spec_eagle_weights *w, int batch, int hidden, int hq,
   if (depth < 0 || max_prefix < 0 || s_max < max_prefix || pool_cap < 1 || n_next < 1 || k < 1 || vocab < k ||
       !(temperature > 0.f))
     return SPEC_ERR_INVALID_ARG;
-  if ((long long)n_front * (depth + 1) > 64 || k > 16 || n_front * k > 1024) return SPEC_ERR_UNSUPPORTED;
+  if ((long long)n_front * (depth + 1) > 64 || k > 16 || n_front * k > 1024 || pool_cap > 4000)
+    return SPEC_ERR_UNSUPPORTED;
   const void *ptrs[] = {w->fc, w->ln1, w->qkv, w->o, w->ln2, w->gate_up, w->down, w->lnf, w->lm, w->emb,
                         k_prefix, v_prefix, k_nodes, v_nodes, feat, workspace};
   for (const void *q : ptrs)

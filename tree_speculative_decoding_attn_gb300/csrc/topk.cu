@@ -20,41 +20,6 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxS = 16;  // largest s / k (per-thread sorted list length)
 
-template <typename T, typename F>
-__device__ __forceinline__ void for_row(const T *row, int V, F &&f) {
-  constexpr int kVec = 16 / sizeof(T);
-  if ((V % kVec) == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
-    for (int vi = threadIdx.x; vi < V / kVec; vi += kThreads) {
-      const uint4 u = sv::ldg_stream(row + (int64_t)vi * kVec);
-      float v[kVec];
-      if constexpr (sizeof(T) == 2) {
-        sv::bf16x8_to_f32(u, v);
-      } else {
-        v[0] = __uint_as_float(u.x);
-        v[1] = __uint_as_float(u.y);
-        v[2] = __uint_as_float(u.z);
-        v[3] = __uint_as_float(u.w);
-      }
-#pragma unroll
-      for (int j = 0; j < kVec; ++j) f(vi * kVec + j, v[j]);
-    }
-  } else {
-    for (int x = threadIdx.x; x < V; x += kThreads) f(x, sv::to_f32(row[x]));
-  }
-}
-
-// Keep the S largest keys seen by this thread, sorted descending.
-template <int S>
-__device__ __forceinline__ void insert_key(unsigned long long (&best)[S], unsigned long long k) {
-  if (k <= best[S - 1]) return;
-#pragma unroll
-  for (int j = 0; j < S; ++j) {
-    const unsigned long long hi = best[j] > k ? best[j] : k;
-    k = best[j] > k ? k : best[j];
-    best[j] = hi;
-  }
-}
-
 // Bitonic sorting network on S keys (S a power of two), descending: every
 // stage is S/2 independent compare-exchanges.
 template <int S>
@@ -194,70 +159,171 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// Expansion round, part 1: one CTA per (sequence, frontier node): top-k
-// tokens of the draft row, their softmax probabilities (float32), children
-// appended to the pool.
+// Expansion round, part 1: one cluster of kCluster CTAs per (sequence,
+// frontier node) row.  CTA c reads the c-th slice of the draft row once,
+// keeping its top-k keys and the online softmax statistics (running max of
+// z = logit / T and the sum of exp(z - max)); CTA 0 merges the slices'
+// lists and statistics through distributed shared memory and appends the k
+// children (token, probability, path value) to the pool.
 // ---------------------------------------------------------------------------
-template <typename T, int S>
+struct Soft {
+  float m, s;  // max of z, sum of exp(z - m)
+};
+__device__ __forceinline__ Soft soft_merge(Soft a, Soft b) {
+  const float m = fmaxf(a.m, b.m);
+  if (m == -INFINITY) return Soft{m, 0.f};
+  return Soft{m, (a.m == -INFINITY ? 0.f : a.s * expf(a.m - m)) + (b.m == -INFINITY ? 0.f : b.s * expf(b.m - m))};
+}
+__device__ __forceinline__ void soft_add(Soft &a, float z) {
+  if (z > a.m) {
+    a.s = (a.m == -INFINITY ? 0.f : a.s * expf(a.m - z)) + 1.f;
+    a.m = z;
+  } else if (z > -INFINITY) {
+    a.s += expf(z - a.m);
+  }
+}
+
+// A warp's top-k list: lane i < k holds the i-th largest key offered so far
+// (descending; 0 = empty), the other lanes 0.  warp_offer offers one key per
+// lane: the lanes whose key beats the list's k-th entry are inserted one at
+// a time (a ballot finds the insertion point, a shuffle shifts the tail), so
+// the common case -- no lane beats it -- costs one compare and one ballot.
+struct WarpTop {
+  unsigned long long l = 0ull;   // this lane's entry
+  unsigned long long thr = 0ull; // the k-th entry (warp-uniform)
+};
+__device__ __forceinline__ void warp_offer(WarpTop &w, unsigned long long key, int k) {
+  const int lane = threadIdx.x & 31;
+  unsigned bal = __ballot_sync(0xffffffffu, key > w.thr);
+  while (bal) {
+    const int src = __ffs(bal) - 1;
+    bal &= bal - 1u;
+    const unsigned long long kk = __shfl_sync(0xffffffffu, key, src);
+    if (kk <= w.thr) continue;  // (uniform) beaten since the ballot
+    const int pos = __popc(__ballot_sync(0xffffffffu, lane < k && w.l > kk));
+    const unsigned long long up = __shfl_up_sync(0xffffffffu, w.l, 1);
+    if (lane > pos && lane < k) w.l = up;
+    if (lane == pos) w.l = kk;
+    w.thr = __shfl_sync(0xffffffffu, w.l, k - 1);
+  }
+}
+
+template <typename T>
 __global__ void __launch_bounds__(kThreads)
     expand_rows_kernel(const T *__restrict__ logits, int n_front, int V, const int32_t *frontier,
                        int k, float temp, int32_t *pool_parent, int32_t *pool_tok, float *pool_conf,
                        float *pool_val, const int32_t *pool_count, int pool_cap, int32_t *status) {
-  __shared__ unsigned long long top[32];
-  __shared__ float red[kWarps];
-  __shared__ float s_bcast;
-  const int b = blockIdx.x / n_front, f = blockIdx.x % n_front;
+  __shared__ unsigned long long cand[kWarps * kMaxS];
+  __shared__ unsigned long long top[kMaxS];
+  __shared__ unsigned long long all[kCluster * kMaxS];
+  __shared__ Soft red[kWarps];
+  __shared__ unsigned long long s_soft;  // this CTA's (m, s), read by CTA 0
+  __shared__ Soft s_tot;
+  const uint32_t cta = blockIdx.x;       // rank in the cluster (cluster spans x)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.y, b = r / n_front, f = r % n_front;
   const int base = pool_count[b];
+  // (every CTA of the cluster takes the same branch: same inputs)
   if (base + n_front * k > pool_cap) {
-    if (threadIdx.x == 0) sv::report(status, SPEC_DEV_CAPACITY);
+    if (cta == 0 && threadIdx.x == 0) sv::report(status, SPEC_DEV_CAPACITY);
     return;
   }
   const int src = frontier[(int64_t)b * n_front + f];
   if (src < 0 || src >= base) {
-    if (threadIdx.x == 0) sv::report(status, SPEC_DEV_BAD_POOL);
+    if (cta == 0 && threadIdx.x == 0) sv::report(status, SPEC_DEV_BAD_POOL);
     return;
   }
-  const T *row = logits + ((int64_t)b * n_front + f) * V;
-  unsigned long long best[S];
+  const T *row = logits + (int64_t)r * V;
+  const int slice = ((V + kCluster - 1) / kCluster + 7) / 8 * 8;
+  const int lo = min(V, (int)cta * slice), hi = min(V, lo + slice);
+  const float inv_t = 1.f / temp;
+  WarpTop wt;
+  Soft st{-INFINITY, 0.f};
+  // every lane of a warp calls visit together (key 0 and z = -inf: no element)
+  auto visit = [&](bool in, int x, float v) {
+    warp_offer(wt, in ? sv::rank_key(v, (uint32_t)x) : 0ull, k);
+    if (in) soft_add(st, v * inv_t);
+  };
+  constexpr int kVec = 16 / sizeof(T);
+  constexpr int kUnroll = sizeof(T) == 2 ? 2 : 4;
+  int vec_end = lo;
+  if ((reinterpret_cast<uintptr_t>(row + lo) & 15) == 0) {
+    vec_end = lo + (hi - lo) / kVec * kVec;
+    // several 16-byte loads in flight per thread; warp-uniform trip count
+    for (int x0 = lo + (int)threadIdx.x * kVec; __any_sync(0xffffffffu, x0 < vec_end);
+         x0 += kUnroll * kThreads * kVec) {
+      uint4 u[kUnroll];
 #pragma unroll
-  for (int j = 0; j < S; ++j) best[j] = 0ull;
-  float m = -INFINITY;
-  for_row(row, V, [&](int x, float v) {
-    insert_key<S>(best, sv::rank_key(v, (uint32_t)x));
-    m = fmaxf(m, v / temp);
-  });
-  m = sv::warp_max(m);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+      for (int q = 0; q < kUnroll; ++q) {
+        const int x = x0 + q * kThreads * kVec;
+        u[q] = x < vec_end ? sv::ldg_stream(row + x) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < kUnroll; ++q) {
+        const int x = x0 + q * kThreads * kVec;
+        float v[kVec];
+        if constexpr (sizeof(T) == 2) {
+          sv::bf16x8_to_f32(u[q], v);
+        } else {
+          v[0] = __uint_as_float(u[q].x);
+          v[1] = __uint_as_float(u[q].y);
+          v[2] = __uint_as_float(u[q].z);
+          v[3] = __uint_as_float(u[q].w);
+        }
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) visit(x < vec_end, x + e, v[e]);
+      }
+    }
+  }
+  for (int x = vec_end + (int)threadIdx.x; __any_sync(0xffffffffu, x < hi); x += kThreads)
+    visit(x < hi, x, x < hi ? sv::to_f32(row[x]) : 0.f);
+  // the CTA's statistics (warps in order) and its top-k (rank by counting)
+#pragma unroll
+  for (int o = 16; o; o >>= 1) st = soft_merge(st, Soft{__shfl_xor_sync(0xffffffffu, st.m, o),
+                                                         __shfl_xor_sync(0xffffffffu, st.s, o)});
+  if (lane == 0) red[warp] = st;
+  if (lane < k) cand[warp * k + lane] = wt.l;
+  if (threadIdx.x < k) top[threadIdx.x] = 0ull;
   __syncthreads();
+  if (threadIdx.x < kWarps * k) {
+    const unsigned long long key = cand[threadIdx.x];
+    int rank = 0;
+    for (int e = 0; e < kWarps * k; ++e) rank += cand[e] > key;
+    if (key != 0ull && rank < k) top[rank] = key;
+  }
   if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, red[w]);
-    s_bcast = mm;
+    Soft t = red[0];
+    for (int w = 1; w < kWarps; ++w) t = soft_merge(t, red[w]);
+    s_soft = ((unsigned long long)__float_as_uint(t.s) << 32) | __float_as_uint(t.m);
   }
-  __syncthreads();
-  m = s_bcast;
-  float S_ = 0.f;
-  for_row(row, V, [&](int, float v) { S_ += expf(v / temp - m); });
-  S_ = sv::warp_sum(S_);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = S_;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float ss = 0.f;
-    for (int w = 0; w < kWarps; ++w) ss += red[w];
-    s_bcast = ss;
+  cluster_barrier();
+  if (cta == 0) {
+    for (int e = threadIdx.x; e < kCluster * k; e += kThreads) all[e] = ld_cluster_u64(&top[e % k], e / k);
+    if (threadIdx.x == 0) {
+      Soft t{-INFINITY, 0.f};
+      for (int c = 0; c < kCluster; ++c) {
+        const unsigned long long w = ld_cluster_u64(&s_soft, c);
+        t = soft_merge(t, Soft{__uint_as_float((uint32_t)w), __uint_as_float((uint32_t)(w >> 32))});
+      }
+      s_tot = t;
+    }
+    __syncthreads();
+    const Soft t = s_tot;
+    for (int e = threadIdx.x; e < kCluster * k; e += kThreads) {
+      const unsigned long long key = all[e];
+      int rank = 0;
+      for (int g = 0; g < kCluster * k; ++g) rank += all[g] > key;
+      if (key == 0ull || rank >= k) continue;
+      const int x = (int)sv::key_index(key);
+      const float p = expf(sv::key_value(key) * inv_t - t.m) / t.s;
+      const int64_t slot = (int64_t)b * pool_cap + base + f * k + rank;
+      pool_parent[slot] = src;
+      pool_tok[slot] = x;
+      pool_conf[slot] = p;
+      pool_val[slot] = __fmul_rn(pool_val[(int64_t)b * pool_cap + src], p);
+    }
   }
-  merge_top<S>(best, k, top);  // contains __syncthreads
-  S_ = s_bcast;
-  if (threadIdx.x < k) {
-    const int x = (int)sv::key_index(top[threadIdx.x]);
-    const float p = expf(sv::to_f32(row[x]) / temp - m) / S_;
-    const int64_t slot = (int64_t)b * pool_cap + base + f * k + threadIdx.x;
-    pool_parent[slot] = src;
-    pool_tok[slot] = x;
-    pool_conf[slot] = p;
-    pool_val[slot] = __fmul_rn(pool_val[(int64_t)b * pool_cap + src], p);
-  }
+  cluster_barrier();  // remote reads done before any CTA of the cluster exits
 }
 
 // Part 2: one CTA per sequence ranks the n_front * k new children by
@@ -327,18 +393,27 @@ int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vo
                    int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
                    int pool_cap, int32_t *next_frontier, int n_next, int32_t *status,
                    cudaStream_t stream) {
-  const int grid = batch * n_front;
   if (k > kMaxS) return SPEC_ERR_UNSUPPORTED;
-  if (dtype == SPEC_BF16)
-    expand_rows_kernel<__nv_bfloat16, kMaxS><<<grid, kThreads, 0, stream>>>(
-        (const __nv_bfloat16 *)logits, n_front, vocab, frontier, k, temperature, pool_parent,
-        pool_tok, pool_conf, pool_val, pool_count, pool_cap, status);
-  else
-    expand_rows_kernel<float, kMaxS><<<grid, kThreads, 0, stream>>>(
-        (const float *)logits, n_front, vocab, frontier, k, temperature, pool_parent, pool_tok,
-        pool_conf, pool_val, pool_count, pool_cap, status);
-  int rc = sv_launch_status();
-  if (rc != SPEC_OK) return rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster, batch * n_front);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      dtype == SPEC_BF16
+          ? cudaLaunchKernelEx(&cfg, expand_rows_kernel<__nv_bfloat16>, (const __nv_bfloat16 *)logits, n_front,
+                               vocab, frontier, k, temperature, pool_parent, pool_tok, pool_conf, pool_val, pool_count,
+                               pool_cap, status)
+          : cudaLaunchKernelEx(&cfg, expand_rows_kernel<float>, (const float *)logits, n_front, vocab, frontier,
+                               k, temperature, pool_parent, pool_tok, pool_conf, pool_val, pool_count, pool_cap,
+                               status);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
   expand_select_kernel<<<batch, 1024, 0, stream>>>(n_front * k, pool_val, pool_count, pool_cap,
                                                    next_frontier, n_next);
   return sv_launch_status();

@@ -69,12 +69,63 @@ SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows) {
   const int sms = sm_count();
   p.n_ctas = (int)(p.units < sms ? p.units : sms);
   p.rows_per_launch = rl;
+  // at least two CTAs per tile on average: every tile is cut, and the
+  // partials are summed by the fixup launch
+  p.defer = (long long)p.n_tiles * 2 <= p.n_ctas;
   p.counter_bytes = align256((size_t)p.n_tiles * 16);
   p.partial_bytes = align256((size_t)2 * p.n_ctas * ((rl + 3) / 4 * 4) * km * 4);
   return p;
 }
 
 namespace {
+
+// Sums the partials of the tiles a deferred launch cut, in CTA order, and
+// stores the epilogue's result (the in-kernel reduction's arithmetic, spread
+// over the whole GPU: thread = (tile, 4 activation rows, W row)).
+template <int EPI>
+__global__ void __launch_bounds__(256) wgemm_fixup_kernel(const WArgs a, int kM) {
+  grid_dep_wait();  // every contributor's partial is stored
+  const Phase &ph = a.ph[0];
+  const int rows4 = (a.rows + 3) >> 2;
+  const long long n = (long long)ph.n_tiles * rows4 * kM;
+  const float4 *part = reinterpret_cast<const float4 *>(ph.partial);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int mm = (int)(i % kM);
+    const long long tq = i / kM;
+    const int q = (int)(tq % rows4), t = (int)(tq / rows4);
+    const long long tu = (long long)t * a.nk;
+    const int c_first = cta_of_unit(tu, ph.units, a.n_ctas);
+    const int c_last = cta_of_unit(tu + a.nk - 1, ph.units, a.n_ctas);
+    if (c_first == c_last) continue;  // a whole tile: stored by the GEMM itself
+    const int slot_first = 2 * c_first + (range_start(c_first, ph.units, a.n_ctas) >= tu ? 0 : 1);
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = c_first; c <= c_last; ++c) {
+      const int sl = c == c_first ? slot_first : 2 * c;
+      const float4 v = __ldcg(part + ((long long)sl * rows4 + q) * kM + mm);
+      sum.x += v.x;
+      sum.y += v.y;
+      sum.z += v.z;
+      sum.w += v.w;
+    }
+    store4<EPI>(a, ph, t / ph.tiles_pg, (t % ph.tiles_pg) * kM + mm, 0, 4 * q, sum);
+  }
+}
+
+template <int EPI>
+int launch_fixup(const SvGemmPlan &p, const WArgs &a, cudaStream_t stream) {
+  const long long n = (long long)p.n_tiles * ((a.rows + 3) / 4) * (128 * p.mt);
+  const long long blocks = (n + 255) / 256, cap = 8ll * sm_count();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(blocks < cap ? blocks : cap));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, wgemm_fixup_kernel<EPI>, a, 128 * p.mt) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
 Phase make_phase(const SvGemmPlan &p, int M, int x_grouped, int epi, float *out, void *zout, const void *res,
                  const void *bias, int *counters, float *partial) {
@@ -112,8 +163,9 @@ int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, i
   if (map3(&maps[1], x, K, x_grouped ? G : 1, rows, 1, p.nt) != SPEC_OK) return SPEC_ERR_CUDA;
   maps[2] = maps[0];
   maps[3] = maps[1];
+  const bool defer = p.defer && epi != kEpiStats;
   for (int r0 = 0; r0 < rows; r0 += p.rows_per_launch) {
-    if (r0 > 0 || !counters_clear)
+    if (!defer && (r0 > 0 || !counters_clear))
       if (cudaMemsetAsync(counters, 0, p.counter_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
     WArgs a{};
     a.ph[0] = make_phase(p, M, x_grouped, epi, out, zout, res, bias, counters, partial);
@@ -130,9 +182,12 @@ int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, i
     a.inv_t = inv_t;
     a.stats = reinterpret_cast<float4 *>(stats);
     a.rec_stride = p.tiles_pg * 4;
-    const int rc = epi == kEpiF32     ? launch_f32(p, maps, a, dep, stream)
-                   : epi == kEpiStats ? launch_stats(p, maps, a, dep, stream)
-                                      : launch_silu(p, maps, a, dep, stream);
+    a.defer = defer ? 1 : 0;
+    int rc = epi == kEpiF32     ? launch_f32(p, maps, a, dep, stream)
+             : epi == kEpiStats ? launch_stats(p, maps, a, dep, stream)
+                                : launch_silu(p, maps, a, dep, stream);
+    if (rc == SPEC_OK && defer)
+      rc = epi == kEpiF32 ? launch_fixup<kEpiF32>(p, a, stream) : launch_fixup<kEpiSiluRes>(p, a, stream);
     if (rc != SPEC_OK) return rc;
   }
   return sv_launch_status();

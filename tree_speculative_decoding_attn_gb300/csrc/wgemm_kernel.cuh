@@ -24,7 +24,11 @@
 // tile's counter (one counter per epilogue warp, which owns 32 of every 128
 // W rows); the last to arrive sums all contributors' slots in CTA order (so
 // the result does not depend on arrival order) and runs the epilogue.  No
-// CTA or warp ever waits for another.
+// CTA or warp ever waits for another.  When the tiles are few against the
+// CTAs (a small weight matrix: every tile cut among several CTAs), that
+// last warp would read every partial of its tile alone; those launches
+// ("defer") only leave the partials, and wgemm_fixup_kernel, launched as a
+// programmatic dependent, sums them over the whole GPU in the same CTA order.
 //
 // Roles (192 threads):
 //   warp 0       TMA producer: W chunk (kM x 64) and X chunk (NT x 64) per
@@ -101,6 +105,7 @@ struct WArgs {
   float4 *stats;               // kEpiStats: [*, rec_stride] records (one per tile and epilogue warp)
   int rec_stride;              // kEpiStats: records per activation row (tiles * 4)
   int *xready;                 // chained phases: count of phase-0 (tile, quarter) results stored
+  int defer;                   // single phase: cut tiles only leave partials; wgemm_fixup_kernel sums them
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long units, long long ctas) {
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[buf]);
         bool stored = whole;
-        if (!whole) {
+        if (!whole && !a.defer) {
           // ticket per (tile, quarter): the warp that brings the last
           // contributor's rows of this quarter reduces them; no warp waits
           __threadfence();
