@@ -61,6 +61,19 @@ def measured_traffic(workload: str, stage: str):
         return ent[2] if hashlib.sha256(f.read()).hexdigest()[:16] == ent[1] else None
 
 
+def wgemm_launches(M: int, K: int, G: int, rows: int, sms: int) -> int:
+    """Kernel launches of one weight-streaming GEMM of rows <= 256: the GEMM,
+    plus the stream-K fixup when a tile's K chunks span two CTAs (the
+    library's plan: 16..128 activation rows use 256-row W tiles, 256 rows
+    128-row tiles; 64-wide K chunks; one contiguous unit range per CTA)."""
+    km = 256 if rows <= 128 else 128
+    nk, tiles = K // 64, -(-M // km) * G
+    units = tiles * nk
+    ctas = min(units, sms)
+    cta_of = lambda x: ((x + 1) * ctas - 1) // units
+    return 1 + any(cta_of(t * nk) != cta_of(t * nk + nk - 1) for t in range(tiles))
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -219,6 +232,10 @@ class GpuStep:
             self.logits = cu(lg, tdt)
             del lg
         self._attn_stage()
+        # the fused LM head + acceptance (statistics epilogue) is an entry point
+        # of its own; the step keeps the LM head and the acceptance apart,
+        # which measured faster at the Vicuna shape (see the design notes)
+        self.fused_accept = False
         if w.medusa:
             self._lm_head_stage(cu)
         self._accept_commit_stages()
@@ -243,7 +260,7 @@ class GpuStep:
         heads_bytes = 2 * K * d * d + 2 * K * V * d + 2 * B * d + 2 * B * K * d + 4 * B * K * V
         self.stages.append(("medusa_heads", lambda: sv.spec_medusa_heads(
             self.h, self.w1, None, self.w2, self.z, self.head_logits, workspace=self.heads_ws,
-            dev_status=self.status), 2, heads_bytes))
+            dev_status=self.status), 1, heads_bytes))  # W1 and W2 chained in one persistent launch
         self.stages.append(("topk", lambda: sv.spec_topk(self.head_logits, s, self.cand), 1, 4 * B * K * V))
         self.stages.append(("build_tree", lambda: sv.spec_build_tree(
             self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos, self.anc,
@@ -292,6 +309,21 @@ class GpuStep:
         self.eagle_round_bytes = 2 * (d * 2 * d + (hq + 2 * hkv) * D * d + d * hq * D + 2 * ffn * d + d * ffn + V * d) \
             + hkv * D * 2 * 2 * (int(self.prefix.sum()))
 
+    def eagle_launches(self):
+        """Kernels of the drafting rounds: per round the six GEMMs (+ their
+        fixups), nine row kernels, the tree build, attention + merge and the
+        two expansion kernels."""
+        w, sms = self.w, self.torch.cuda.get_device_properties(self.dev).multi_processor_count
+        hq, hkv, D, ffn, V = w.hq, w.hkv, w.head_dim, w.dynamic["draft"]["ffn"], w.vocab
+        d = hq * D
+        n = 0
+        for r in range(self.e_rounds):
+            R = w.batch * (1 if r == 0 else w.dynamic["frontier"])
+            n += sum(wgemm_launches(M, K, G, R, sms) for M, K, G in
+                     ((d, 2 * d, 1), ((hq + 2 * hkv) * D, d, 1), (d, hq * D, 1), (ffn, d, 2), (d, ffn, 1), (V, d, 1)))
+            n += 9 + 1 + 2 + 2
+        return n
+
     def _eagle_rounds(self):
         sv, w = self.sv, self.w
         par, tok, conf = self.pool
@@ -308,9 +340,7 @@ class GpuStep:
     def _static_or_dynamic_build(self, cu):
         sv, synth, w = self.sv, self.synth, self.w
         if w.tree == "dynamic" and w.dynamic.get("draft"):
-            # per round: 6 GEMMs, 4 stream-K fixups (the GEMMs of d-row weights), 9 row kernels,
-            # tree build, attention + merge, expansion (2)
-            self.stages.append(("eagle_draft", self._eagle_rounds, 24 * self.e_rounds,
+            self.stages.append(("eagle_draft", self._eagle_rounds, self.eagle_launches(),
                                 self.eagle_round_bytes * self.e_rounds))
         if w.tree == "dynamic":
             par, tok, conf = self.pool
@@ -338,10 +368,16 @@ class GpuStep:
         self.logits = torch.empty((B, N, V), dtype=torch.float32, device=self.dev)
         self.logits_bytes_row = V * 4
         self.h2d.append((self.hid.cpu().pin_memory(), self.hid))
+        if self.fused_accept:  # the LM head runs inside the lm_head_accept stage
+            self.lm_ws = torch.empty(max(sv.spec_lm_head_accept_workspace_bytes(B, N, d, V), 16),
+                                     dtype=torch.uint8, device=self.dev)
+            return
         self.lm_ws = torch.empty(max(sv.spec_lm_head_workspace_bytes(B * N, d, V), 16), dtype=torch.uint8,
                                  device=self.dev)
         self.stages.append(("lm_head", lambda: sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V),
-                                                               dev_status=self.status, workspace=self.lm_ws), 1,
+                                                               dev_status=self.status, workspace=self.lm_ws),
+                            wgemm_launches(V, d, 1, B * N, torch.cuda.get_device_properties(self.dev)
+                                           .multi_processor_count),
                             2 * V * d + 2 * B * N * d + 4 * B * N * V))
 
     def lm_head_logits(self):
@@ -357,12 +393,15 @@ class GpuStep:
         mode = {"greedy": sv.GREEDY, "typical": sv.TYPICAL, "reject": sv.REJECT}[w.accept]
         parents = self.par_out if w.tree == "dynamic" else self.parents_b
         self.step_counter = 0
-        if getattr(self, "fused_accept", False):
+        if self.fused_accept:
             B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
+            # the GEMM (+ its stream-K fixup) and the fold kernel
+            launches = wgemm_launches(V, d, 1, B * N, self.torch.cuda.get_device_properties(self.dev)
+                                      .multi_processor_count) + 1
             self.stages.append(("lm_head_accept", lambda: sv.spec_lm_head_accept(
                 mode, self.hid.view(B, N, d), self.wlm, self.tok, parents, self.fc, self.ns, self.acc_len,
                 self.acc_path, self.bonus, temperature=w.temperature, eps=w.eps, delta=w.delta,
-                dev_status=self.status, workspace=self.lm_ws), 2, 2 * V * d + 2 * B * N * d))
+                dev_status=self.status, workspace=self.lm_ws), launches, 2 * V * d + 2 * B * N * d))
         else:
             self.stages.append(("accept", lambda: sv.spec_accept(
             mode, self.logits, self.tok, parents, self.fc, self.ns, self.acc_len, self.acc_path, self.bonus,
@@ -390,7 +429,7 @@ class GpuStep:
         esz = 2 if self.tdt == self.torch.bfloat16 else 4
         rows = int((L + 1).sum())
         out = {}
-        if self.w.accept == "typical" or getattr(self, "fused_accept", False):
+        if self.w.accept == "typical" or self.fused_accept:
             out["accept"] = None
         else:
             out["accept"] = rows * self.logits_bytes_row

@@ -174,14 +174,6 @@ __device__ __forceinline__ Soft soft_merge(Soft a, Soft b) {
   if (m == -INFINITY) return Soft{m, 0.f};
   return Soft{m, (a.m == -INFINITY ? 0.f : a.s * expf(a.m - m)) + (b.m == -INFINITY ? 0.f : b.s * expf(b.m - m))};
 }
-__device__ __forceinline__ void soft_add(Soft &a, float z) {
-  if (z > a.m) {
-    a.s = (a.m == -INFINITY ? 0.f : a.s * expf(a.m - z)) + 1.f;
-    a.m = z;
-  } else if (z > -INFINITY) {
-    a.s += expf(z - a.m);
-  }
-}
 
 // A warp's top-k list: lane i < k holds the i-th largest key offered so far
 // (descending; 0 = empty), the other lanes 0.  warp_offer offers one key per
@@ -240,9 +232,28 @@ __global__ void __launch_bounds__(kThreads)
   WarpTop wt;
   Soft st{-INFINITY, 0.f};
   // every lane of a warp calls visit together (key 0 and z = -inf: no element)
-  auto visit = [&](bool in, int x, float v) {
-    warp_offer(wt, in ? sv::rank_key(v, (uint32_t)x) : 0ull, k);
-    if (in) soft_add(st, v * inv_t);
+  // The list's k-th value as a float prefilter (-inf while the list is not
+  // full): a lane's elements are offered only when one of them reaches it.
+  auto thr_value = [&]() { return wt.thr ? sv::key_value(wt.thr) : -INFINITY; };
+  // n values of one lane (warp-uniform call): the top-k offers, then the
+  // online statistics moved once to the group's max (fast exponentials: the
+  // normaliser is a sum of many positive terms)
+  auto visit_group = [&](bool in, int x, const float *v, int n) {
+    float mx = -INFINITY;
+    for (int e = 0; e < n; ++e) mx = fmaxf(mx, v[e]);
+    if (__any_sync(0xffffffffu, in && mx >= thr_value()))
+      for (int e = 0; e < n; ++e) {
+        const bool c = in && v[e] >= thr_value();
+        warp_offer(wt, c ? sv::rank_key(v[e], (uint32_t)(x + e)) : 0ull, k);
+      }
+    if (!in) return;
+    const float zmax = mx * inv_t;
+    if (zmax > st.m) {
+      st.s = st.m == -INFINITY ? 0.f : st.s * __expf(st.m - zmax);
+      st.m = zmax;
+    }
+    if (st.m == -INFINITY) return;  // every value so far is -inf
+    for (int e = 0; e < n; ++e) st.s += __expf(fmaf(v[e], inv_t, -st.m));
   };
   constexpr int kVec = 16 / sizeof(T);
   constexpr int kUnroll = sizeof(T) == 2 ? 2 : 4;
@@ -270,13 +281,14 @@ __global__ void __launch_bounds__(kThreads)
           v[2] = __uint_as_float(u[q].z);
           v[3] = __uint_as_float(u[q].w);
         }
-#pragma unroll
-        for (int e = 0; e < kVec; ++e) visit(x < vec_end, x + e, v[e]);
+        visit_group(x < vec_end, x, v, kVec);
       }
     }
   }
-  for (int x = vec_end + (int)threadIdx.x; __any_sync(0xffffffffu, x < hi); x += kThreads)
-    visit(x < hi, x, x < hi ? sv::to_f32(row[x]) : 0.f);
+  for (int x = vec_end + (int)threadIdx.x; __any_sync(0xffffffffu, x < hi); x += kThreads) {
+    const float v = x < hi ? sv::to_f32(row[x]) : 0.f;
+    visit_group(x < hi, x, &v, 1);
+  }
   // the CTA's statistics (warps in order) and its top-k (rank by counting)
 #pragma unroll
   for (int o = 16; o; o >>= 1) st = soft_merge(st, Soft{__shfl_xor_sync(0xffffffffu, st.m, o),

@@ -69,9 +69,13 @@ SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows) {
   const int sms = sm_count();
   p.n_ctas = (int)(p.units < sms ? p.units : sms);
   p.rows_per_launch = rl;
-  // at least two CTAs per tile on average: every tile is cut, and the
-  // partials are summed by the fixup launch
-  p.defer = (long long)p.n_tiles * 2 <= p.n_ctas;
+  // cut tiles are summed by the fixup launch in single-phase GEMMs (as fast
+  // as the last arriving warp or faster at every shape measured, by far
+  // when the tiles are few against the CTAs); none cut: no fixup launch
+  auto cta_of = [&](long long x) { return ((x + 1) * p.n_ctas - 1) / p.units; };  // the kernel's cta_of_unit
+  p.defer = false;
+  for (long long t = 0; p.units > 0 && t < p.n_tiles && !p.defer; ++t)
+    p.defer = cta_of(t * p.nk) != cta_of(t * p.nk + p.nk - 1);
   p.counter_bytes = align256((size_t)p.n_tiles * 16);
   p.partial_bytes = align256((size_t)2 * p.n_ctas * ((rl + 3) / 4 * 4) * km * 4);
   return p;
@@ -111,9 +115,64 @@ __global__ void __launch_bounds__(256) wgemm_fixup_kernel(const WArgs a, int kM)
   }
 }
 
+// The statistics epilogue's fixup: one warp per (cut tile, epilogue quarter,
+// 16 activation rows), lane = W row within the quarter, as in the kernel:
+// the contributors' partials are summed in CTA order, each lane merges its
+// MT W rows, and the transpose-reduction leaves one record per row.
+__global__ void __launch_bounds__(256) wgemm_fixup_stats_kernel(const WArgs a, int mt_n) {
+  grid_dep_wait();  // every contributor's partial is stored
+  const Phase &ph = a.ph[0];
+  const int kM = 128 * mt_n, rows4 = (a.rows + 3) >> 2, chunks = (a.rows + 15) >> 4;
+  const int lane = threadIdx.x & 31;
+  const long long n = (long long)ph.n_tiles * 4 * chunks;
+  const float4 *part = reinterpret_cast<const float4 *>(ph.partial);
+  for (long long wi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; wi < n;
+       wi += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int c0 = (int)(wi % chunks) * 16, quarter = (int)((wi / chunks) & 3), t = (int)(wi / chunks / 4);
+    const long long tu = (long long)t * a.nk;
+    const int c_first = cta_of_unit(tu, ph.units, a.n_ctas);
+    const int c_last = cta_of_unit(tu + a.nk - 1, ph.units, a.n_ctas);
+    if (c_first == c_last) continue;  // a whole tile: its records are the GEMM's own (warp-uniform)
+    const int slot_first = 2 * c_first + (range_start(c_first, ph.units, a.n_ctas) >= tu ? 0 : 1);
+    const int mt = t % ph.tiles_pg, ml = quarter * 32 + lane;
+    St e[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) e[i] = St{-INFINITY, 0.f, 0.f, 0ull};
+    for (int j = 0; j < mt_n; ++j) {
+      const int m = mt * kM + j * 128 + ml;
+      float4 sum[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = c_first; c <= c_last; ++c) {
+        const int sl = c == c_first ? slot_first : 2 * c;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = (c0 >> 2) + i;
+          if (q >= rows4) break;
+          const float4 v = __ldcg(part + ((long long)sl * rows4 + q) * kM + j * 128 + ml);
+          sum[i].x += v.x;
+          sum[i].y += v.y;
+          sum[i].z += v.z;
+          sum[i].w += v.w;
+        }
+      }
+      const bool vm = m < ph.M;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        e[4 * i] = st_merge(e[4 * i], st_one(sum[i].x, m, vm, a.inv_t));
+        e[4 * i + 1] = st_merge(e[4 * i + 1], st_one(sum[i].y, m, vm, a.inv_t));
+        e[4 * i + 2] = st_merge(e[4 * i + 2], st_one(sum[i].z, m, vm, a.inv_t));
+        e[4 * i + 3] = st_merge(e[4 * i + 3], st_one(sum[i].w, m, vm, a.inv_t));
+      }
+    }
+    put_record(a, mt * 4 + quarter, c0, st_transpose_reduce16(e));
+  }
+}
+
 template <int EPI>
 int launch_fixup(const SvGemmPlan &p, const WArgs &a, cudaStream_t stream) {
-  const long long n = (long long)p.n_tiles * ((a.rows + 3) / 4) * (128 * p.mt);
+  const long long n = EPI == kEpiStats ? (long long)p.n_tiles * 4 * ((a.rows + 15) / 16) * 32
+                                       : (long long)p.n_tiles * ((a.rows + 3) / 4) * (128 * p.mt);
   const long long blocks = (n + 255) / 256, cap = 8ll * sm_count();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(blocks < cap ? blocks : cap));
@@ -124,7 +183,13 @@ int launch_fixup(const SvGemmPlan &p, const WArgs &a, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wgemm_fixup_kernel<EPI>, a, 128 * p.mt) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  cudaError_t e;
+  if constexpr (EPI == kEpiStats) {
+    e = cudaLaunchKernelEx(&cfg, wgemm_fixup_stats_kernel, a, p.mt);
+  } else {
+    e = cudaLaunchKernelEx(&cfg, wgemm_fixup_kernel<EPI>, a, 128 * p.mt);
+  }
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 Phase make_phase(const SvGemmPlan &p, int M, int x_grouped, int epi, float *out, void *zout, const void *res,
@@ -163,7 +228,7 @@ int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, i
   if (map3(&maps[1], x, K, x_grouped ? G : 1, rows, 1, p.nt) != SPEC_OK) return SPEC_ERR_CUDA;
   maps[2] = maps[0];
   maps[3] = maps[1];
-  const bool defer = p.defer && epi != kEpiStats;
+  const bool defer = p.defer;
   for (int r0 = 0; r0 < rows; r0 += p.rows_per_launch) {
     if (!defer && (r0 > 0 || !counters_clear))
       if (cudaMemsetAsync(counters, 0, p.counter_bytes, stream) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -187,7 +252,9 @@ int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, i
              : epi == kEpiStats ? launch_stats(p, maps, a, dep, stream)
                                 : launch_silu(p, maps, a, dep, stream);
     if (rc == SPEC_OK && defer)
-      rc = epi == kEpiF32 ? launch_fixup<kEpiF32>(p, a, stream) : launch_fixup<kEpiSiluRes>(p, a, stream);
+      rc = epi == kEpiF32     ? launch_fixup<kEpiF32>(p, a, stream)
+           : epi == kEpiStats ? launch_fixup<kEpiStats>(p, a, stream)
+                              : launch_fixup<kEpiSiluRes>(p, a, stream);
     if (rc != SPEC_OK) return rc;
   }
   return sv_launch_status();

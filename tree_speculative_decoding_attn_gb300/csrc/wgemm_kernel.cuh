@@ -24,11 +24,13 @@
 // tile's counter (one counter per epilogue warp, which owns 32 of every 128
 // W rows); the last to arrive sums all contributors' slots in CTA order (so
 // the result does not depend on arrival order) and runs the epilogue.  No
-// CTA or warp ever waits for another.  When the tiles are few against the
-// CTAs (a small weight matrix: every tile cut among several CTAs), that
-// last warp would read every partial of its tile alone; those launches
-// ("defer") only leave the partials, and wgemm_fixup_kernel, launched as a
-// programmatic dependent, sums them over the whole GPU in the same CTA order.
+// CTA or warp ever waits for another.  Single-phase launches ("defer") only
+// leave the partials, and wgemm_fixup_kernel, launched as a programmatic
+// dependent, sums them over the whole GPU in the same CTA order: the last
+// warp alone reads every partial of its tile, which is slow when the tiles
+// are few against the CTAs (every tile cut among several).  The chained
+// Medusa launch keeps the in-kernel reduction (its second phase reads the
+// first phase's results inside the same launch).
 //
 // Roles (192 threads):
 //   warp 0       TMA producer: W chunk (kM x 64) and X chunk (NT x 64) per
