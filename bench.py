@@ -48,6 +48,10 @@ L2_BYTES = 129 * 1024 * 1024
 # source is the one the counters were taken on: (source, sha256 prefix,
 # bytes) keyed by (workload, stage).
 NCU_TRAFFIC = {
+    # attn_tc2_kernel, 70B shape at batch 16 (one quarter of the workload's
+    # sequences; traffic grows with the sequences): (286,152,448 read +
+    # 6,764,416 written, mean of two launches) x 4, from one ncu capture
+    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "533dabf1486075f4", 1171667456),
 }
 
 
