@@ -155,6 +155,7 @@ class GpuStep:
         w = self.w = synth.WORKLOADS[name]
         self.name = name
         dev = self.dev = device
+        self.sms = torch.cuda.get_device_properties(dev).multi_processor_count
         bf = torch.bfloat16
         tdt = self.tdt = bf if w.dtype == "bf16" else torch.float32
         cu = lambda x, dt=None: (torch.from_numpy(np.ascontiguousarray(x)).to(dt) if dt else
@@ -264,7 +265,8 @@ class GpuStep:
         heads_bytes = 2 * K * d * d + 2 * K * V * d + 2 * B * d + 2 * B * K * d + 4 * B * K * V
         self.stages.append(("medusa_heads", lambda: sv.spec_medusa_heads(
             self.h, self.w1, None, self.w2, self.z, self.head_logits, workspace=self.heads_ws,
-            dev_status=self.status), 1, heads_bytes))  # W1 and W2 chained in one persistent launch
+            dev_status=self.status), wgemm_launches(d, d, K, B, self.sms) + wgemm_launches(V, d, K, B, self.sms),
+            heads_bytes))  # W1 then W2, each with its fixup
         self.stages.append(("topk", lambda: sv.spec_topk(self.head_logits, s, self.cand), 1, 4 * B * K * V))
         self.stages.append(("build_tree", lambda: sv.spec_build_tree(
             self.parents, self.rank, self.cand, self.root, self.d_prefix, self.tok, self.depth, self.pos, self.anc,
@@ -317,7 +319,7 @@ class GpuStep:
         """Kernels of the drafting rounds: per round the six GEMMs (+ their
         fixups), nine row kernels, the tree build, attention + merge and the
         two expansion kernels."""
-        w, sms = self.w, self.torch.cuda.get_device_properties(self.dev).multi_processor_count
+        w, sms = self.w, self.sms
         hq, hkv, D, ffn, V = w.hq, w.hkv, w.head_dim, w.dynamic["draft"]["ffn"], w.vocab
         d = hq * D
         n = 0
@@ -380,8 +382,7 @@ class GpuStep:
                                  device=self.dev)
         self.stages.append(("lm_head", lambda: sv.spec_lm_head(self.hid, self.wlm, self.logits.view(B * N, V),
                                                                dev_status=self.status, workspace=self.lm_ws),
-                            wgemm_launches(V, d, 1, B * N, torch.cuda.get_device_properties(self.dev)
-                                           .multi_processor_count),
+                            wgemm_launches(V, d, 1, B * N, self.sms),
                             2 * V * d + 2 * B * N * d + 4 * B * N * V))
 
     def lm_head_logits(self):
@@ -400,8 +401,7 @@ class GpuStep:
         if self.fused_accept:
             B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
             # the GEMM (+ its stream-K fixup) and the fold kernel
-            launches = wgemm_launches(V, d, 1, B * N, self.torch.cuda.get_device_properties(self.dev)
-                                      .multi_processor_count) + 1
+            launches = wgemm_launches(V, d, 1, B * N, self.sms) + 1
             self.stages.append(("lm_head_accept", lambda: sv.spec_lm_head_accept(
                 mode, self.hid.view(B, N, d), self.wlm, self.tok, parents, self.fc, self.ns, self.acc_len,
                 self.acc_path, self.bonus, temperature=w.temperature, eps=w.eps, delta=w.delta,

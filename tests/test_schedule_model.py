@@ -5,10 +5,10 @@ The kernel splits the (tile, 64-wide K chunk) units of a GEMM into one
 contiguous range per CTA, range_start(c) = floor(c * units / ctas).  A tile
 whose chunks span several ranges is "cut": each contributor stores its
 partial accumulator in a slot (2c when the tile is the first segment of CTA
-c's range, 2c + 1 when it is a later one), and the last contributor to
-arrive sums the slots of CTAs cta_of_unit(first chunk) .. cta_of_unit(last
-chunk), where cta_of_unit(x) = floor(((x + 1) * ctas - 1) / units) and only
-the first contributor can have started before the tile.  These are the
+c's range, 2c + 1 when it is a later one), and the fixup kernel sums the
+slots of CTAs cta_of_unit(first chunk) .. cta_of_unit(last chunk), where
+cta_of_unit(x) = floor(((x + 1) * ctas - 1) / units) and only the first
+contributor can have started before the tile.  These are the
 formulas of the kernel's header, written out here; the checks below are the
 properties the schedule relies on, compared with brute force over every
 unit."""

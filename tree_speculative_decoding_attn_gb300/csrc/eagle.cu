@@ -378,7 +378,7 @@ Layout layout(int B, int F, int d, int hq, int hkv, int D, int ffn, int V, int s
                             {V, d, 1}};
   for (auto &sh : shapes) {
     const SvGemmPlan p = sv_wgemm_plan(sh[0], sh[1], sh[2], R);
-    const size_t need = p.counter_bytes + p.partial_bytes;
+    const size_t need = p.partial_bytes;
     g = need > g ? need : g;
   }
   l.gemm_bytes = g;
@@ -407,12 +407,11 @@ int sv_eagle_round(const SvEagleWeights &w, int batch, int hidden, int hq, int h
   auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16 *>(base + off); };
   auto f32 = [&](size_t off) { return reinterpret_cast<float *>(base + off); };
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t *>(base + off); };
-  int *gc = reinterpret_cast<int *>(at(l.gemm));
   // a GEMM whose output is float32 rows [R, G, M], the workspace share reused
   auto gemm = [&](const void *W, const void *X, int M, int K, int G, float *out) {
     const SvGemmPlan p = sv_wgemm_plan(M, K, G, R);
-    return sv_wgemm(p, W, X, 0, M, K, G, R, 0, out, nullptr, nullptr, nullptr, gc,
-                    reinterpret_cast<float *>(at(l.gemm) + p.counter_bytes), false, false, status, stream);
+    return sv_wgemm(p, W, X, 0, M, K, G, R, 0, out, nullptr, nullptr, nullptr, reinterpret_cast<float *>(at(l.gemm)),
+                    false, status, stream);
   };
   int rc;
   inputs_kernel<<<R, kThreads, 0, stream>>>(reinterpret_cast<const __nv_bfloat16 *>(feat),

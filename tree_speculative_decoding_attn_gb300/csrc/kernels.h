@@ -73,16 +73,16 @@ struct SvGemmPlan {
   int nt, mt;              // activation rows per MMA (N), 128-row MMAs per tile
   int nk, tiles_pg, n_tiles, n_ctas, rows_per_launch;
   long long units;         // (tile, 64-wide K chunk) pairs
-  size_t counter_bytes, partial_bytes;
-  bool defer;              // cut tiles summed by a dependent fixup launch (single-phase GEMMs)
+  size_t partial_bytes;
+  bool any_cut;            // some tile is cut: the fixup launch sums its partials
 };
 SvGemmPlan sv_wgemm_plan(int M, int K, int G, int rows);
 // One weight-streaming GEMM (all row blocks).  epi: 0 float32 logits, 1
 // bf16 SiLU + residual, 2 softmax statistics records (float4 per 32 W rows
 // and activation row: max logit, sum exp, first moment, argmax).
 int sv_wgemm(const SvGemmPlan &p, const void *w, const void *x, int x_grouped, int M, int K, int G, int rows,
-             int epi, float *out, void *zout, const void *res, const void *bias, int *counters, float *partial,
-             bool counters_clear, bool pdl, int32_t *status, cudaStream_t stream, float inv_t = 1.f,
+             int epi, float *out, void *zout, const void *res, const void *bias, float *partial, bool pdl,
+             int32_t *status, cudaStream_t stream, float inv_t = 1.f,
              void *stats = nullptr);
 size_t sv_medusa_heads_ws_bytes(int batch, int n_heads, int hidden, int vocab);
 int sv_medusa_heads(const void *h, const void *w1, const void *b1, const void *w2, int batch,

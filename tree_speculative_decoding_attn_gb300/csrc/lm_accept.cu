@@ -232,7 +232,7 @@ Layout layout(int batch, int n_nodes, int hidden, int vocab) {
   const int rows = batch * n_nodes;
   l.p = sv_wgemm_plan(vocab, hidden, 1, rows);
   const int rec = l.p.tiles_pg * 4;  // one record per (row, tile, epilogue warp)
-  l.fold_counters = l.p.counter_bytes;
+  l.fold_counters = 0;
   l.partial = l.fold_counters + align256((size_t)batch * 4);
   l.stats = l.partial + l.p.partial_bytes;
   l.rowstat = l.stats + align256((size_t)rows * rec * 16);
@@ -255,13 +255,11 @@ int sv_lm_head_accept(int mode, const void *hid, const void *w, int batch, int n
   const Layout l = layout(batch, n_nodes, hidden, vocab);
   uint8_t *base = reinterpret_cast<uint8_t *>(ws);
   const int rows = batch * n_nodes;
-  const bool single = rows <= l.p.rows_per_launch;
-  // one memset clears the GEMM's tile counters and the per-sequence tickets
+  // the per-sequence tickets start at zero
   if (cudaMemsetAsync(base, 0, l.partial, stream) != cudaSuccess) return SPEC_ERR_CUDA;
   const float inv_t = 1.f / temperature;
   int rc = sv_wgemm(l.p, w, hid, 0, vocab, hidden, 1, rows, 2, nullptr, nullptr, nullptr, nullptr,
-                    reinterpret_cast<int *>(base), reinterpret_cast<float *>(base + l.partial), single, false, status,
-                    stream, inv_t, base + l.stats);
+                    reinterpret_cast<float *>(base + l.partial), false, status, stream, inv_t, base + l.stats);
   if (rc != SPEC_OK) return rc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_nodes, batch);

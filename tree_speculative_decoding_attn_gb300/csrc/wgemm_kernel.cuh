@@ -19,18 +19,14 @@
 // of a persistent grid (one CTA per SM), so every SM streams the same number
 // of weight bytes whatever the tile count (stream-K).
 //
-// A tile whose chunks span several CTAs is "cut": each contributor writes its
-// float32 partial accumulator to a workspace slot and takes a ticket from the
-// tile's counter (one counter per epilogue warp, which owns 32 of every 128
-// W rows); the last to arrive sums all contributors' slots in CTA order (so
-// the result does not depend on arrival order) and runs the epilogue.  No
-// CTA or warp ever waits for another.  Single-phase launches ("defer") only
-// leave the partials, and wgemm_fixup_kernel, launched as a programmatic
-// dependent, sums them over the whole GPU in the same CTA order: the last
-// warp alone reads every partial of its tile, which is slow when the tiles
-// are few against the CTAs (every tile cut among several).  The chained
-// Medusa launch keeps the in-kernel reduction (its second phase reads the
-// first phase's results inside the same launch).
+// A tile whose chunks span several CTAs is "cut": each contributor writes
+// its float32 partial accumulator to a workspace slot (2c for the first
+// segment of CTA c's range, 2c + 1 for a later one) and the launch's
+// dependent, wgemm_fixup_kernel or wgemm_fixup_stats_kernel in wgemm.cu,
+// sums the slots of every cut tile in CTA order over the whole GPU and runs
+// the epilogue.  Whole tiles run it here.  No CTA or warp ever waits for
+// another.  (A reduction by the last contributor to arrive was measured
+// slower at every shape: one warp then reads every partial of its tile.)
 //
 // Roles (192 threads):
 //   warp 0       TMA producer: W chunk (kM x 64) and X chunk (NT x 64) per
@@ -79,24 +75,19 @@ struct Cfg {
   static constexpr uint32_t kSmem = kStages * kStage + 1024 + 256;
 };
 
-// One GEMM of a launch.  A launch runs one or two of them ("phases") over
-// the same activation rows and reduction length; with two, every CTA first
-// takes its share of phase 0, then its share of phase 1, and phase 1 reads
-// phase 0's bf16 output as its X operand (the Medusa W1 -> W2 chain).
+// The GEMM of a launch: its weight matrix, tiles, units and outputs.
 struct Phase {
-  int M, tiles_pg, n_tiles, x_grouped, epi;  // epi: the launched kernel's epilogue for this phase
+  int M, tiles_pg, n_tiles, x_grouped, epi;  // epi: the launched kernel's epilogue
   long long units;             // n_tiles * nk
   float *out;                  // kEpiF32: [*, G, M] float32
   __nv_bfloat16 *zout;         // kEpiSiluRes: [*, G, M] bf16
   const __nv_bfloat16 *res;    // kEpiSiluRes: [*, M]
   const __nv_bfloat16 *bias;   // kEpiSiluRes: [G, M] or null
   float *partial;              // [2 * n_ctas][ceil(rows / 4)][kM][4] float32
-  int *counters;               // [n_tiles * 4] (one per tile and epilogue warp), zero at launch
 };
 
 struct WArgs {
-  Phase ph[2];
-  int nphase;
+  Phase ph;
   int K, G;                    // reduction length, groups (heads)
   int rows;                    // valid activation rows of this launch (<= NT)
   int r0;                      // first activation row of this launch
@@ -106,8 +97,6 @@ struct WArgs {
   float inv_t;                 // kEpiStats: 1 / temperature
   float4 *stats;               // kEpiStats: [*, rec_stride] records (one per tile and epilogue warp)
   int rec_stride;              // kEpiStats: records per activation row (tiles * 4)
-  int *xready;                 // chained phases: count of phase-0 (tile, quarter) results stored
-  int defer;                   // single phase: cut tiles only leave partials; wgemm_fixup_kernel sums them
 };
 
 __device__ __forceinline__ long long range_start(long long c, long long units, long long ctas) {
@@ -196,17 +185,9 @@ __device__ __forceinline__ void store4(const WArgs &a, const Phase &ph, int g, i
   }
 }
 
-// The CTA's units of phase p: [lo, hi).
-__device__ __forceinline__ void phase_range(const WArgs &a, int p, int c, long long &lo, long long &hi) {
-  lo = range_start(c, a.ph[p].units, a.n_ctas);
-  hi = range_start(c + 1, a.ph[p].units, a.n_ctas);
-}
-
-// E0, E1: epilogues of phase 0 and phase 1 (E1 < 0: a single phase).
-template <int NT, int MT, int E0, int E1>
+template <int NT, int MT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    wgemm_kernel(const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_x0,
-                 const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_x1, const WArgs a) {
+    wgemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x, const WArgs a) {
   using C = Cfg<NT, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -220,10 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
-  long long lo0, hi0, lo1 = 0, hi1 = 0;
-  phase_range(a, 0, c, lo0, hi0);
-  if (a.nphase > 1) phase_range(a, 1, c, lo1, hi1);
-  const long long n0 = hi0 - lo0, n_it = n0 + (hi1 - lo1);
+  const Phase &ph = a.ph;
+  const long long lo = range_start(c, ph.units, a.n_ctas), hi = range_start(c + 1, ph.units, a.n_ctas);
+  const long long n_it = hi - lo;  // this CTA's units
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -237,12 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done, 1);
     *abort_flag = 0;
     mbar_fence_init();
-    tma_prefetch_desc(&tm_w0);
-    tma_prefetch_desc(&tm_x0);
-    if (a.nphase > 1) {
-      tma_prefetch_desc(&tm_w1);
-      tma_prefetch_desc(&tm_x1);
-    }
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_x);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::kTmemCols);
   tc_fence_before();
@@ -255,34 +231,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      // item i of this CTA: phase 0 units first, then phase 1
-      auto item = [&](long long i, int &p, int &t, int &k) {
-        p = i < n0 ? 0 : 1;
-        const long long u = p == 0 ? lo0 + i : lo1 + (i - n0);
+      // item i of this CTA: unit lo + i = (tile t, K chunk k)
+      auto item = [&](long long i, int &t, int &k) {
+        const long long u = lo + i;
         t = (int)(u / a.nk);
         k = (int)(u % a.nk);
       };
       auto load_w = [&](long long i) {
-        int p, t, k;
-        item(i, p, t, k);
+        int t, k;
+        item(i, t, k);
         const int s = (int)(i % C::kStages);
         mbar_expect_tx(&full[s], C::kStage);
-        tma_load_3d_hint(smem + s * C::kStage, p ? &tm_w1 : &tm_w0, k * kKC, (t % a.ph[p].tiles_pg) * C::kM,
-                         t / a.ph[p].tiles_pg, &full[s], pol);
+        tma_load_3d_hint(smem + s * C::kStage, &tm_w, k * kKC, (t % ph.tiles_pg) * C::kM, t / ph.tiles_pg, &full[s],
+                         pol);
       };
       auto load_x = [&](long long i) {
-        int p, t, k;
-        item(i, p, t, k);
+        int t, k;
+        item(i, t, k);
         const int s = (int)(i % C::kStages);
-        tma_load_3d(smem + s * C::kStage + C::kWBytes, p ? &tm_x1 : &tm_x0, k * kKC,
-                    a.ph[p].x_grouped ? t / a.ph[p].tiles_pg : 0, a.r0, &full[s]);
+        tma_load_3d(smem + s * C::kStage + C::kWBytes, &tm_x, k * kKC, ph.x_grouped ? t / ph.tiles_pg : 0, a.r0,
+                    &full[s]);
       };
       // the first ring's weight chunks do not depend on the previous kernel
       const long long pre = a.pdl_wait ? (n_it < C::kStages ? n_it : C::kStages) : 0;
       for (long long i = 0; i < pre; ++i) load_w(i);
       if (a.pdl_wait) grid_dep_wait();
       long long w_issued = pre, issued = 0;
-      bool x_ok = a.nphase < 2;  // phase 1's X is phase 0's output
       for (long long i = 0; i < n_it; ++i) {
         if (i >= w_issued) {
           const int s = (int)(i % C::kStages);
@@ -293,35 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           load_w(i);
           w_issued = i + 1;
-        }
-        if (i >= n0 && !x_ok) {
-          // first phase-1 chunk: wait (bounded) until every phase-0 result
-          // is stored, meanwhile keeping the weight stream going into every
-          // ring slot the MMAs free; then make those generic-proxy stores
-          // visible to TMA
-          const int target = a.ph[0].n_tiles * 4;
-          uint32_t spins = 0;
-          while (true) {
-            while (w_issued < n_it && w_issued < i + C::kStages) {
-              const long long j = w_issued;
-              if (j >= C::kStages && !mbar_test(&empty[j % C::kStages], (uint32_t)((j / C::kStages) & 1) ^ 1u))
-                break;
-              load_w(j);
-              w_issued = j + 1;
-            }
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.xready) : "memory");
-            if (v >= target || *abort_flag) break;
-            if (++spins > kWaitLimit) break;
-            __nanosleep(64);
-          }
-          if (spins > kWaitLimit || *abort_flag) {
-            *abort_flag = 1;
-            sv::report(a.status, SPEC_DEV_TIMEOUT);
-            break;
-          }
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          x_ok = true;
         }
         load_x(i);
         issued = i + 1;
@@ -342,38 +287,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     long long it = 0;
     int seg = 0;
-    for (int p = 0; p < a.nphase && ok; ++p) {
-      const long long ulo = p ? lo1 : lo0, uhi = p ? hi1 : hi0;
-      for (long long u = ulo; u < uhi && ok; ++seg) {
-        const int klo = (int)(u % a.nk);
-        const int khi = (int)((uhi - u) < (long long)(a.nk - klo) ? klo + (uhi - u) : a.nk);
-        const int buf = seg & 1;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, kWaitLimit)))) break;
+    for (long long u = lo; u < hi && ok; ++seg) {
+      const int klo = (int)(u % a.nk);
+      const int khi = (int)((hi - u) < (long long)(a.nk - klo) ? klo + (hi - u) : a.nk);
+      const int buf = seg & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&acc_empty[buf], ((seg >> 1) & 1) ^ 1, kWaitLimit)))) break;
+      tc_fence_after();
+      const uint32_t dacc = tmem + (uint32_t)(buf * C::kAccCols);
+      for (int k = klo; k < khi; ++k, ++it) {
+        const int s = (int)(it % C::kStages);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1), kWaitLimit)) &&
+                   !*abort_flag))
+          break;
         tc_fence_after();
-        const uint32_t dacc = tmem + (uint32_t)(buf * C::kAccCols);
-        for (int k = klo; k < khi; ++k, ++it) {
-          const int s = (int)(it % C::kStages);
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (uint32_t)((it / C::kStages) & 1), kWaitLimit)) &&
-                     !*abort_flag))
-            break;
-          tc_fence_after();
-          if (lane == 0) {
-            const uint32_t wa = base + (uint32_t)s * C::kStage, xa = wa + C::kWBytes;
+        if (lane == 0) {
+          const uint32_t wa = base + (uint32_t)s * C::kStage, xa = wa + C::kWBytes;
 #pragma unroll
-            for (int kk = 0; kk < kKC / 16; ++kk)
+          for (int kk = 0; kk < kKC / 16; ++kk)
 #pragma unroll
-              for (int j = 0; j < MT; ++j)
-                mma_ss(dacc + j * NT, smem_desc_sw128(wa + j * (128 * kKC * 2) + kk * 32, 16, 1024),
-                       smem_desc_sw128(xa + kk * 32, 16, 1024), idesc, (k > klo || kk > 0));
-            mma_commit(&empty[s]);
-          }
-          __syncwarp();
+            for (int j = 0; j < MT; ++j)
+              mma_ss(dacc + j * NT, smem_desc_sw128(wa + j * (128 * kKC * 2) + kk * 32, 16, 1024),
+                     smem_desc_sw128(xa + kk * 32, 16, 1024), idesc, (k > klo || kk > 0));
+          mma_commit(&empty[s]);
         }
-        if (!ok) break;
-        if (lane == 0) mma_commit(&acc_full[buf]);
         __syncwarp();
-        u += khi - klo;
       }
+      if (!ok) break;
+      if (lane == 0) mma_commit(&acc_full[buf]);
+      __syncwarp();
+      u += khi - klo;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -388,209 +330,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tq = tmem + ((uint32_t)(quarter * 32) << 16);
     const int rows4 = (a.rows + 3) >> 2;
     int seg = 0;
-    bool live = true;
-    auto run_phase = [&](auto epi_c, auto p_c) {
-      constexpr int EPI = decltype(epi_c)::value;
-      constexpr int p = decltype(p_c)::value;
-      const Phase &ph = a.ph[p];
-      const long long ulo = p ? lo1 : lo0, uhi = p ? hi1 : hi0;
-      // this quarter's results of phase 0 count toward phase 1's X readiness
-      const bool feeds = p == 0 && a.nphase > 1;
-      for (long long u = ulo; u < uhi; ++seg) {
-        const int t = (int)(u / a.nk), klo = (int)(u % a.nk);
-        const int khi = (int)((uhi - u) < (long long)(a.nk - klo) ? klo + (uhi - u) : a.nk);
-        const int g = t / ph.tiles_pg, mt = t % ph.tiles_pg;
-        const bool whole = klo == 0 && khi == a.nk;
-        const int buf = seg & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (seg >> 1) & 1, kWaitLimit)) ||
-            __any_sync(0xffffffffu, *abort_flag != 0)) {
-          *abort_flag = 1;
-          sv::report(a.status, SPEC_DEV_TIMEOUT);
-          live = false;
-          break;
-        }
-        tc_fence_after();
-        // partial slot layout: [rows / 4][kM][4] floats, so four rows of one
-        // W row are one 16-byte vector (for the reducer's loads)
-        float4 *slot = reinterpret_cast<float4 *>(ph.partial) + (long long)(2 * c + (u == ulo ? 0 : 1)) * rows4 * C::kM;
-        if constexpr (EPI == kEpiStats) {
-          if (whole) {
-            // 16 activation rows at a time: each lane merges its MT W rows
-            // of a row, then the transpose-reduction over the warp; one
-            // record per (row, tile, quarter) covering 32 * MT W rows
-#pragma unroll 1
-            for (int c0 = 0; c0 < a.rows && c0 < NT; c0 += 16) {
-              St e[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) e[i] = St{-INFINITY, 0.f, 0.f, 0ull};
-#pragma unroll
-              for (int j = 0; j < MT; ++j) {
-                const int m = mt * C::kM + j * 128 + ml;
-                uint32_t acc[16];
-                tmem_ld16(tq + (uint32_t)(buf * C::kAccCols + j * NT + c0), acc);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                  e[i] = st_merge(e[i], st_one(__uint_as_float(acc[i]), m, m < ph.M, a.inv_t));
-              }
-              put_record(a, mt * 4 + quarter, c0, st_transpose_reduce16(e));
-            }
-          }
-        }
-#pragma unroll 1
-        for (int j = 0; j < MT; ++j) {
-          if (EPI == kEpiStats && whole) break;
-#pragma unroll 1
-          for (int cc = 0; cc < NT / C::kCW; ++cc) {
-            if (cc * C::kCW >= a.rows) break;  // warp-uniform
-            const uint32_t ta = tq + (uint32_t)(buf * C::kAccCols + j * NT + cc * C::kCW);
-            uint32_t acc[32];
-            if constexpr (C::kCW == 32) {
-              tmem_ld32(ta, acc);
-            } else {
-              tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(acc));
-            }
-            tmem_wait_ld();
-            const int m = mt * C::kM + j * 128 + ml;
-            if constexpr (EPI != kEpiStats) {
-              if (whole) {
-                const int rec = 0;
-#pragma unroll
-                for (int i = 0; i < C::kCW; i += 4)
-                  store4<EPI>(a, ph, g, m, rec, cc * C::kCW + i,
-                         make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]),
-                                     __uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3])));
-                continue;
-              }
-            }
-            {
-#pragma unroll
-              for (int i = 0; i < C::kCW; i += 4) {
-                const int r = cc * C::kCW + i;
-                if (r < a.rows)
-                  slot[(long long)(r >> 2) * C::kM + j * 128 + ml] =
-                      make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]), __uint_as_float(acc[i + 2]),
-                                  __uint_as_float(acc[i + 3]));
-              }
-            }
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        bool stored = whole;
-        if (!whole && !a.defer) {
-          // ticket per (tile, quarter): the warp that brings the last
-          // contributor's rows of this quarter reduces them; no warp waits
-          __threadfence();
-          __syncwarp();
-          int ticket = 0;
-          if (lane == 0) ticket = atomicAdd(&ph.counters[4 * t + quarter], 1);
-          ticket = __shfl_sync(0xffffffffu, ticket, 0);
-          const long long tu = (long long)t * a.nk;
-          const int c_first = cta_of_unit(tu, ph.units, a.n_ctas);
-          const int c_last = cta_of_unit(tu + a.nk - 1, ph.units, a.n_ctas);
-          if (ticket == c_last - c_first) {
-            stored = true;
-            __threadfence();
-            // 8 entries (sub-tile j, 4 rows) per round, two contributors'
-            // 16-byte vectors in flight together; each entry's contributions
-            // are summed in CTA order.  Only the first contributor can have
-            // started before the tile (slot 2c + 1); the others start inside
-            // it (2c).
-            const float4 *part = reinterpret_cast<const float4 *>(ph.partial);
-            const int nc = c_last - c_first + 1;
-            const int slot_first = 2 * c_first + (range_start(c_first, ph.units, a.n_ctas) >= tu ? 0 : 1);
-            const int n_ent = MT * rows4;
-            auto src = [&](int cq, int e) {
-              const int sl = cq == 0 ? slot_first : 2 * (c_first + cq);
-              return part + ((long long)sl * rows4 + e % rows4) * C::kM + (e / rows4) * 128 + ml;
-            };
-            if constexpr (EPI == kEpiStats) {
-              // 16 activation rows (4 entries of 4) per round; the MT W rows
-              // of each lane are merged, then the transpose-reduction
-#pragma unroll 1
-              for (int c0 = 0; c0 < a.rows; c0 += 16) {
-                St e[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) e[i] = St{-INFINITY, 0.f, 0.f, 0ull};
-#pragma unroll 1
-                for (int j = 0; j < MT; ++j) {
-                  const int q0 = c0 >> 2, m = mt * C::kM + j * 128 + ml;
-                  float4 sum[4];
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-                  for (int cq = 0; cq < nc; cq += 2) {
-                    float4 v0[4], v1[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                      const bool in = q0 + i < rows4;
-                      const int en = j * rows4 + q0 + i;
-                      v0[i] = in ? __ldcg(src(cq, en)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                      v1[i] = in && cq + 1 < nc ? __ldcg(src(cq + 1, en)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                      sum[i].x += v0[i].x; sum[i].y += v0[i].y; sum[i].z += v0[i].z; sum[i].w += v0[i].w;
-                      sum[i].x += v1[i].x; sum[i].y += v1[i].y; sum[i].z += v1[i].z; sum[i].w += v1[i].w;
-                    }
-                  }
-                  const bool vm = m < ph.M;
-#pragma unroll
-                  for (int i = 0; i < 4; ++i) {
-                    e[4 * i] = st_merge(e[4 * i], st_one(sum[i].x, m, vm, a.inv_t));
-                    e[4 * i + 1] = st_merge(e[4 * i + 1], st_one(sum[i].y, m, vm, a.inv_t));
-                    e[4 * i + 2] = st_merge(e[4 * i + 2], st_one(sum[i].z, m, vm, a.inv_t));
-                    e[4 * i + 3] = st_merge(e[4 * i + 3], st_one(sum[i].w, m, vm, a.inv_t));
-                  }
-                }
-                put_record(a, mt * 4 + quarter, c0, st_transpose_reduce16(e));
-              }
-            } else {
-#pragma unroll 1
-            for (int e0 = 0; e0 < n_ent; e0 += 8) {
-              float4 sum[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-              for (int cq = 0; cq < nc; cq += 2) {
-                float4 v0[8], v1[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const bool in = e0 + i < n_ent;
-                  v0[i] = in ? __ldcg(src(cq, e0 + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                  v1[i] = in && cq + 1 < nc ? __ldcg(src(cq + 1, e0 + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  sum[i].x += v0[i].x; sum[i].y += v0[i].y; sum[i].z += v0[i].z; sum[i].w += v0[i].w;
-                  sum[i].x += v1[i].x; sum[i].y += v1[i].y; sum[i].z += v1[i].z; sum[i].w += v1[i].w;
-                }
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int e = e0 + i;
-                if (e >= n_ent) break;
-                const int j = e / rows4;
-                store4<EPI>(a, ph, g, mt * C::kM + j * 128 + ml, (mt * MT + j) * 4 + quarter, (e % rows4) * 4,
-                            sum[i]);
-              }
-            }
-            }
-          }
-        }
-        if (feeds && stored) {  // this (tile, quarter) of phase 0 is final
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) atomicAdd(a.xready, 1);
-        }
-        u += khi - klo;
+    for (long long u = lo; u < hi; ++seg) {
+      const int t = (int)(u / a.nk), klo = (int)(u % a.nk);
+      const int khi = (int)((hi - u) < (long long)(a.nk - klo) ? klo + (hi - u) : a.nk);
+      const int g = t / ph.tiles_pg, mt = t % ph.tiles_pg;
+      const bool whole = klo == 0 && khi == a.nk;
+      const int buf = seg & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (seg >> 1) & 1, kWaitLimit)) ||
+          __any_sync(0xffffffffu, *abort_flag != 0)) {
+        *abort_flag = 1;
+        sv::report(a.status, SPEC_DEV_TIMEOUT);
+        break;
       }
-    };
-    run_phase(std::integral_constant<int, E0>{}, std::integral_constant<int, 0>{});
-    if constexpr (E1 >= 0) {
-      if (live) run_phase(std::integral_constant<int, E1>{}, std::integral_constant<int, 1>{});
+      tc_fence_after();
+      // partial slot layout: [rows / 4][kM][4] floats, so four rows of one
+      // W row are one 16-byte vector (for the reducer's loads)
+      float4 *slot = reinterpret_cast<float4 *>(ph.partial) + (long long)(2 * c + (u == lo ? 0 : 1)) * rows4 * C::kM;
+      if constexpr (EPI == kEpiStats) {
+        if (whole) {
+          // 16 activation rows at a time: each lane merges its MT W rows
+          // of a row, then the transpose-reduction over the warp; one
+          // record per (row, tile, quarter) covering 32 * MT W rows
+#pragma unroll 1
+          for (int c0 = 0; c0 < a.rows && c0 < NT; c0 += 16) {
+            St e[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) e[i] = St{-INFINITY, 0.f, 0.f, 0ull};
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+              const int m = mt * C::kM + j * 128 + ml;
+              uint32_t acc[16];
+              tmem_ld16(tq + (uint32_t)(buf * C::kAccCols + j * NT + c0), acc);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                e[i] = st_merge(e[i], st_one(__uint_as_float(acc[i]), m, m < ph.M, a.inv_t));
+            }
+            put_record(a, mt * 4 + quarter, c0, st_transpose_reduce16(e));
+          }
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < MT; ++j) {
+        if (EPI == kEpiStats && whole) break;
+#pragma unroll 1
+        for (int cc = 0; cc < NT / C::kCW; ++cc) {
+          if (cc * C::kCW >= a.rows) break;  // warp-uniform
+          const uint32_t ta = tq + (uint32_t)(buf * C::kAccCols + j * NT + cc * C::kCW);
+          uint32_t acc[32];
+          if constexpr (C::kCW == 32) {
+            tmem_ld32(ta, acc);
+          } else {
+            tmem_ld16(ta, *reinterpret_cast<uint32_t(*)[16]>(acc));
+          }
+          tmem_wait_ld();
+          const int m = mt * C::kM + j * 128 + ml;
+          if constexpr (EPI != kEpiStats) {
+            if (whole) {
+              const int rec = 0;
+#pragma unroll
+              for (int i = 0; i < C::kCW; i += 4)
+                store4<EPI>(a, ph, g, m, rec, cc * C::kCW + i,
+                       make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]),
+                                   __uint_as_float(acc[i + 2]), __uint_as_float(acc[i + 3])));
+              continue;
+            }
+          }
+          {
+#pragma unroll
+            for (int i = 0; i < C::kCW; i += 4) {
+              const int r = cc * C::kCW + i;
+              if (r < a.rows)
+                slot[(long long)(r >> 2) * C::kM + j * 128 + ml] =
+                    make_float4(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1]), __uint_as_float(acc[i + 2]),
+                                __uint_as_float(acc[i + 3]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      u += khi - klo;
     }
   }
   tc_fence_before();
@@ -602,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Launch one kernel instance over p.n_ctas CTAs (PDL attribute when `pdl`).
-template <int NT, int MT, int E0, int E1>
+template <int NT, int MT, int EPI>
 int launch_t(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream) {
   using C = Cfg<NT, MT>;
-  auto kern = wgemm_kernel<NT, MT, E0, E1>;
+  auto kern = wgemm_kernel<NT, MT, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem) != cudaSuccess)
     return SPEC_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -618,25 +439,24 @@ int launch_t(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], a) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], a) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }
 
-template <int E0, int E1>
+template <int EPI>
 int launch_nt(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream) {
   switch (p.nt) {
-    case 16: return launch_t<16, 2, E0, E1>(p, maps, a, pdl, stream);
-    case 32: return launch_t<32, 2, E0, E1>(p, maps, a, pdl, stream);
-    case 64: return launch_t<64, 2, E0, E1>(p, maps, a, pdl, stream);
-    case 128: return launch_t<128, 2, E0, E1>(p, maps, a, pdl, stream);
-    default: return launch_t<256, 1, E0, E1>(p, maps, a, pdl, stream);
+    case 16: return launch_t<16, 2, EPI>(p, maps, a, pdl, stream);
+    case 32: return launch_t<32, 2, EPI>(p, maps, a, pdl, stream);
+    case 64: return launch_t<64, 2, EPI>(p, maps, a, pdl, stream);
+    case 128: return launch_t<128, 2, EPI>(p, maps, a, pdl, stream);
+    default: return launch_t<256, 1, EPI>(p, maps, a, pdl, stream);
   }
 }
 
 // One translation unit per epilogue family (compiled in parallel).
 int launch_f32(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream);
 int launch_silu(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream);
-int launch_silu_f32(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream);
 int launch_stats(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream);
 
 }  // namespace wg

@@ -5,7 +5,7 @@ namespace sv {
 namespace wg {
 
 int launch_stats(const SvGemmPlan &p, const CUtensorMap *maps, const WArgs &a, bool pdl, cudaStream_t stream) {
-  return launch_nt<kEpiStats, -1>(p, maps, a, pdl, stream);
+  return launch_nt<kEpiStats>(p, maps, a, pdl, stream);
 }
 
 }  // namespace wg
