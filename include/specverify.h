@@ -495,6 +495,10 @@ int spec_lm_head_accept(int mode, const void *hid, const void *w, int batch, int
  * Outputs: acc_len [batch] (accepted nodes, root excluded), acc_path
  * [batch, path_cap] (node ids root first, -1 after), bonus [batch].
  * path_cap must exceed the tree depth.  Decisions use float32.
+ * dev_status: SPEC_DEV_BAD_TOKEN (a child token outside [0, vocab): never
+ * accepted), SPEC_DEV_CAPACITY (path longer than path_cap), and in typical
+ * mode SPEC_DEV_BAD_PARENTS when parents[] disagrees with the child links
+ * (that sequence accepts the root alone).
  * ------------------------------------------------------------------ */
 int spec_accept(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
                 int n_nodes, int vocab,
