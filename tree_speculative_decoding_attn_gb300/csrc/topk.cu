@@ -11,6 +11,8 @@
 // comparison is a single integer max.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -189,6 +191,7 @@ __device__ __forceinline__ Soft soft_merge(Soft a, Soft b) {
 struct WarpTop {
   unsigned long long l = 0ull;   // this lane's entry
   unsigned long long thr = 0ull; // the k-th entry (warp-uniform)
+  float thr_v = -INFINITY;       // its value (-inf while the list is not full)
 };
 __device__ __forceinline__ unsigned long long u64max(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 __device__ __forceinline__ unsigned long long u64min(unsigned long long a, unsigned long long b) { return a > b ? b : a; }
@@ -214,6 +217,7 @@ __device__ __forceinline__ void warp_offer(WarpTop &w, unsigned long long key, i
     }
     w.l = c;
     w.thr = __shfl_sync(0xffffffffu, w.l, k - 1);
+    w.thr_v = w.thr ? sv::key_value(w.thr) : -INFINITY;
     return;
   }
   while (bal) {
@@ -226,6 +230,7 @@ __device__ __forceinline__ void warp_offer(WarpTop &w, unsigned long long key, i
     if (lane > pos && lane < 16) w.l = up;
     if (lane == pos) w.l = kk;
     w.thr = __shfl_sync(0xffffffffu, w.l, k - 1);
+    w.thr_v = w.thr ? sv::key_value(w.thr) : -INFINITY;
   }
 }
 
@@ -263,18 +268,21 @@ __global__ void __launch_bounds__(kThreads)
   // every lane of a warp calls visit together (key 0 and z = -inf: no element)
   // The list's k-th value as a float prefilter (-inf while the list is not
   // full): a lane's elements are offered only when one of them reaches it.
-  auto thr_value = [&]() { return wt.thr ? sv::key_value(wt.thr) : -INFINITY; };
   // n values of one lane (warp-uniform call): the top-k offers, then the
   // online statistics moved once to the group's max (fast exponentials: the
   // normaliser is a sum of many positive terms)
-  auto visit_group = [&](bool in, int x, const float *v, int n) {
+  auto visit_group = [&](bool in, int x, const float *v, auto n_c) {
+    constexpr int n = decltype(n_c)::value;
     float mx = -INFINITY;
+#pragma unroll
     for (int e = 0; e < n; ++e) mx = fmaxf(mx, v[e]);
-    if (__any_sync(0xffffffffu, in && mx >= thr_value()))
+    if (__any_sync(0xffffffffu, in && mx >= wt.thr_v)) {
+#pragma unroll
       for (int e = 0; e < n; ++e) {
-        const bool c = in && v[e] >= thr_value();
+        const bool c = in && v[e] >= wt.thr_v;
         warp_offer(wt, c ? sv::rank_key(v[e], (uint32_t)(x + e)) : 0ull, k);
       }
+    }
     if (!in) return;
     const float zmax = mx * inv_t;
     if (zmax > st.m) {
@@ -282,7 +290,10 @@ __global__ void __launch_bounds__(kThreads)
       st.m = zmax;
     }
     if (st.m == -INFINITY) return;  // every value so far is -inf
-    for (int e = 0; e < n; ++e) st.s += __expf(fmaf(v[e], inv_t, -st.m));
+    float add = 0.f;
+#pragma unroll
+    for (int e = 0; e < n; ++e) add += __expf(fmaf(v[e], inv_t, -st.m));
+    st.s += add;
   };
   constexpr int kVec = 16 / sizeof(T);
   constexpr int kUnroll = sizeof(T) == 2 ? 2 : 4;
@@ -310,13 +321,13 @@ __global__ void __launch_bounds__(kThreads)
           v[2] = __uint_as_float(u[q].z);
           v[3] = __uint_as_float(u[q].w);
         }
-        visit_group(x < vec_end, x, v, kVec);
+        visit_group(x < vec_end, x, v, std::integral_constant<int, kVec>{});
       }
     }
   }
   for (int x = vec_end + (int)threadIdx.x; __any_sync(0xffffffffu, x < hi); x += kThreads) {
     const float v = x < hi ? sv::to_f32(row[x]) : 0.f;
-    visit_group(x < hi, x, &v, 1);
+    visit_group(x < hi, x, &v, std::integral_constant<int, 1>{});
   }
   // the CTA's statistics (warps in order) and its top-k (rank by counting)
 #pragma unroll
