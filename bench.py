@@ -405,14 +405,15 @@ class GpuStep:
                 mode, self.hid.view(B, N, d), self.wlm, self.tok, parents, self.fc, self.ns, self.acc_len,
                 self.acc_path, self.bonus, temperature=w.temperature, eps=w.eps, delta=w.delta,
                 dev_status=self.status, workspace=self.lm_ws), launches, 2 * V * d + 2 * B * N * d))
+            self.stages.append(("kv_commit", lambda: sv.kv_commit(
+                self.kc, self.vc, self.kt, self.vt, self.acc_len, self.acc_path, self.d_prefix, self.new_prefix,
+                self.status), 1, None))
         else:
-            self.stages.append(("accept", lambda: sv.spec_accept(
-            mode, self.logits, self.tok, parents, self.fc, self.ns, self.acc_len, self.acc_path, self.bonus,
-                temperature=w.temperature, eps=w.eps, delta=w.delta, seed=w.seed, step=0, dev_status=self.status),
-                1, None))
-        self.stages.append(("kv_commit", lambda: sv.kv_commit(
-            self.kc, self.vc, self.kt, self.vt, self.acc_len, self.acc_path, self.d_prefix, self.new_prefix,
-            self.status), 1, None))
+            # acceptance and the commit of the accepted path in one launch
+            self.stages.append(("accept_commit", lambda: sv.spec_accept_commit(
+                mode, self.logits, self.tok, parents, self.fc, self.ns, self.acc_len, self.acc_path, self.bonus,
+                self.kc, self.vc, self.kt, self.vt, self.d_prefix, self.new_prefix, temperature=w.temperature,
+                eps=w.eps, delta=w.delta, seed=w.seed, step=0, dev_status=self.status), 1, None))
 
     def e2e_input(self, name):
         """A per-step input of the end-to-end leg: copied from pinned host
@@ -437,11 +438,13 @@ class GpuStep:
         esz = 2 if self.tdt == self.torch.bfloat16 else 4
         rows = int((L + 1).sum())
         out = {}
-        if self.w.accept == "typical" or self.fused_accept:
-            out["accept"] = None
+        commit = rows * self.w.hkv * self.w.head_dim * 2 * esz * 2
+        if self.fused_accept:
+            out["kv_commit"] = commit
+        elif self.w.accept == "typical":
+            out["accept_commit"] = None
         else:
-            out["accept"] = rows * self.logits_bytes_row
-        out["kv_commit"] = rows * self.w.hkv * self.w.head_dim * 2 * esz * 2
+            out["accept_commit"] = rows * self.logits_bytes_row + commit
         return out, float(L.mean())
 
 

@@ -508,6 +508,25 @@ int spec_accept(int mode, const void *logits, const void *draft_logits, int dtyp
                 int32_t *bonus, int32_t *dev_status, spec_stream_t stream);
 
 /* --------------------------------------------------------------------
+ * spec_accept_commit -- spec_accept and kv_commit (contiguous cache) in one
+ * launch: each sequence's cluster, once it has taken its path, copies that
+ * path's K/V rows into the cache and advances prefix_len.  The pages'
+ * steps 7 and 8 of "Medusa, explained" / section 3.2 of "5.3 Medusa、EAGLE
+ * 与 MTP"; the arguments, results and device errors are those of the two
+ * calls (acc_len and acc_path are still written).  prefix_len_out may equal
+ * prefix_len; a path that would pass s_max sets SPEC_DEV_CAPACITY and that
+ * sequence is neither copied nor advanced.
+ * ------------------------------------------------------------------ */
+int spec_accept_commit(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
+                       int n_nodes, int vocab, const int32_t *tok, const int32_t *parents,
+                       const int32_t *first_child, const int32_t *next_sibling, float temperature,
+                       float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
+                       int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *k_cache,
+                       void *v_cache, const void *k_tree, const void *v_tree, int elem_bytes,
+                       int n_layers, int hkv, int s_max, int head_dim, const int32_t *prefix_len,
+                       int32_t *prefix_len_out, int32_t *dev_status, spec_stream_t stream);
+
+/* --------------------------------------------------------------------
  * kv_commit -- append the accepted path's K/V rows to the cache and
  * discard the rest ("5.3 Medusa、EAGLE 与 MTP", section 3.2).
  *

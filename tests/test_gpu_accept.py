@@ -303,6 +303,50 @@ def test_reject_children_covering_the_vocabulary(V):
         assert _compare_decisions(got[:3], ref[:3], ref[3], rerun, "reject (whole vocabulary)") == 0
 
 
+@pytest.mark.parametrize("mode", [sv.GREEDY, sv.TYPICAL, sv.REJECT])
+@pytest.mark.parametrize("dtype,layers", [(torch.bfloat16, 1), (torch.float32, 3)])
+def test_accept_commit_fused_equals_the_two_calls(mode, dtype, layers):
+    """spec_accept_commit gives exactly spec_accept followed by kv_commit:
+    paths, bonus, every cache byte and the advanced prefix lengths (in
+    place), including a sequence whose path would pass s_max (reported,
+    neither copied nor advanced)."""
+    shape = SHAPES[2]
+    B, V, Hkv, D, S = 6, 5000, 2, 64, 96
+    t = _tree_batch(shape, B, V, 90 + mode)
+    bf16 = dtype == torch.bfloat16
+    lg = _logits(shape, t, B, V, 91 + mode, bf16)
+    cap = shape.n_levels + 1
+    N = shape.n
+    g = np.random.default_rng(92)
+    kc, vc = (g.standard_normal((layers, B, Hkv, S, D)).astype(np.float32) for _ in range(2))
+    kt, vt = (g.standard_normal((layers, B, Hkv, N, D)).astype(np.float32) for _ in range(2))
+    prefix = np.array([0, 5, 17, 40, S - 3, S - cap - 1], np.int32)   # sequence 4 cannot fit a long path
+    kw = dict(temperature=1.0, eps=0.3, delta=0.09, seed=7, step=3)
+    gg = t["gpu"]
+    lgd = dev(lg, dtype)
+    # the two calls
+    a_len, a_path, a_bon, st_a = zeros_i32(B), zeros_i32(B, cap), zeros_i32(B), zeros_i32(1)
+    sv.spec_accept(mode, lgd, gg["tok"], gg["parent"], gg["first_child"], gg["next_sibling"], a_len, a_path, a_bon,
+                   dev_status=st_a, **kw)
+    kc1, vc1 = dev(kc, dtype), dev(vc, dtype)
+    p1 = i32(prefix)
+    sv.kv_commit(kc1, vc1, dev(kt, dtype), dev(vt, dtype), a_len, a_path, p1, p1, st_a)
+    # fused
+    f_len, f_path, f_bon, st_f = zeros_i32(B), zeros_i32(B, cap), zeros_i32(B), zeros_i32(1)
+    kc2, vc2 = dev(kc, dtype), dev(vc, dtype)
+    p2 = i32(prefix)
+    sv.spec_accept_commit(mode, lgd, gg["tok"], gg["parent"], gg["first_child"], gg["next_sibling"], f_len, f_path,
+                          f_bon, kc2, vc2, dev(kt, dtype), dev(vt, dtype), p2, p2, dev_status=st_f, **kw)
+    torch.cuda.synchronize()
+    for a, f in ((a_len, f_len), (a_path, f_path), (a_bon, f_bon), (p1, p2)):
+        np.testing.assert_array_equal(host(f), host(a))
+    assert int(host(st_f)[0]) == int(host(st_a)[0])
+    for a, f in ((kc1, kc2), (vc1, vc2)):
+        assert torch.equal(a, f)
+    if int(host(a_len)[4]) + 1 > 3:   # the long path of sequence 4 did not fit
+        assert int(host(st_f)[0]) == sv.DEV_CAPACITY and int(host(p2)[4]) == prefix[4]
+
+
 def test_commit_bad_path_is_reported_and_skipped():
     B, Hkv, S, N, D = 3, 2, 32, 8, 64
     g = np.random.default_rng(9)

@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                   const int32_t *__restrict__ tok, const int32_t *__restrict__ parents,
                   const int32_t *__restrict__ first_child, const int32_t *__restrict__ next_sibling,
                   float temp, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
-                  int32_t *acc_len, int32_t *acc_path, int32_t *bonus_out, int32_t *status) {
+                  int32_t *acc_len, int32_t *acc_path, int32_t *bonus_out, int32_t *status, const SvCommit cm) {
   __shared__ Red red;
   __shared__ int s_path[kMaxNodes + 1];
   __shared__ int s_len, s_next, s_bonus;
@@ -626,7 +626,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = 0; j < path_cap; ++j) acc_path[(int64_t)b * path_cap + j] = j < len ? s_path[j] : -1;
     bonus_out[b] = s_bonus;
   }
-  cluster_barrier();  // partners' reads of this CTA's exchange slots are done
+  // the fused commit (kv_commit's copies): the cluster's CTAs share the
+  // accepted rows of every (K or V, layer, KV head), 16-byte vectors
+  int P = 0, len = 0;
+  bool fits = false;
+  if (cm.kc) {
+    P = cm.prefix_len[b];
+    len = min(s_len, path_cap);
+    fits = P >= 0 && P + len <= cm.s_max;
+    if (cta == 0 && threadIdx.x == 0 && !fits) sv::report(status, SPEC_DEV_CAPACITY);
+    if (fits) {
+      const int n = len * cm.vec_per_row;  // vectors of one (layer, head) for K or V
+      const int total = 2 * cm.n_layers * cm.hkv * n;
+      const int nb = (int)gridDim.y;
+#pragma unroll 4
+      for (int idx = (int)(cta * kThreads + threadIdx.x); idx < total; idx += nc * kThreads) {
+        const int it = idx / n, e = idx - it * n;
+        const int j = e / cm.vec_per_row, c = e - j * cm.vec_per_row;
+        const int lh = it >> 1;  // layer * hkv + head
+        const int layer = lh / cm.hkv, h = lh % cm.hkv;
+        const int64_t lb = ((int64_t)layer * nb + b) * cm.hkv + h;
+        const uint4 v = ((it & 1) ? cm.vt : cm.kt)[(lb * N + s_path[j]) * cm.vec_per_row + c];
+        ((it & 1) ? cm.vc : cm.kc)[(lb * cm.s_max + P + j) * cm.vec_per_row + c] = v;
+      }
+    }
+  }
+  cluster_barrier();  // partners' reads of this CTA's exchange slots (and of prefix_len) are done
+  if (cm.kc && cm.prefix_len_out && cta == 0 && threadIdx.x == 0) cm.prefix_len_out[b] = fits ? P + len : P;
 }
 
 // CTAs per sequence (the kernel reads it from gridDim.x): enough to fill
@@ -664,7 +690,8 @@ int launch_accept(int mode, const void *logits, const void *draft, int batch, in
                   const int32_t *tok,
                   const int32_t *parents, const int32_t *first_child, const int32_t *next_sibling,
                   float temperature, float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
-                  int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream) {
+                  int32_t *acc_len, int32_t *acc_path, int32_t *bonus, int32_t *status, cudaStream_t stream,
+                  const SvCommit &cm) {
   const int nc = cluster_size<T>(batch);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nc, batch);
@@ -680,7 +707,7 @@ int launch_accept(int mode, const void *logits, const void *draft, int batch, in
   return cudaLaunchKernelEx(&cfg, accept_kernel<T>, mode, (const T *)logits, (const T *)draft, n_nodes, vocab,
                             tok, parents,
                             first_child, next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
-                            acc_path, bonus, status) == cudaSuccess
+                            acc_path, bonus, status, cm) == cudaSuccess
              ? SPEC_OK
              : SPEC_ERR_CUDA;
 }
@@ -691,12 +718,12 @@ int sv_accept(int mode, const void *logits, const void *draft, int dtype, int ba
               const int32_t *tok, const int32_t *parents, const int32_t *first_child,
               const int32_t *next_sibling, float temperature, float eps, float delta,
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
-              int32_t *bonus, int32_t *status, cudaStream_t stream) {
+              int32_t *bonus, int32_t *status, cudaStream_t stream, SvCommit commit) {
   if (dtype == SPEC_BF16)
     return launch_accept<__nv_bfloat16>(mode, logits, draft, batch, n_nodes, vocab, tok, parents, first_child,
                                         next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len,
-                                        acc_path, bonus, status, stream);
+                                        acc_path, bonus, status, stream, commit);
   return launch_accept<float>(mode, logits, draft, batch, n_nodes, vocab, tok, parents, first_child, next_sibling,
                               temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus, status,
-                              stream);
+                              stream, commit);
 }

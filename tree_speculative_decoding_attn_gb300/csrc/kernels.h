@@ -113,11 +113,20 @@ int sv_tree_expand(const void *logits, int dtype, int batch, int n_front, int vo
                    int32_t *pool_tok, float *pool_conf, float *pool_val, int32_t *pool_count,
                    int pool_cap, int32_t *next_frontier, int n_next, int32_t *status,
                    cudaStream_t stream);
+// The commit fused into the acceptance launch (contiguous cache; kc null:
+// no commit).  Layouts as kv_commit; vec_per_row = head_dim * elem_bytes / 16.
+struct SvCommit {
+  uint4 *kc, *vc;
+  const uint4 *kt, *vt;
+  int n_layers, hkv, s_max, vec_per_row;
+  const int32_t *prefix_len;
+  int32_t *prefix_len_out;
+};
 int sv_accept(int mode, const void *logits, const void *draft, int dtype, int batch, int n_nodes, int vocab,
               const int32_t *tok, const int32_t *parents, const int32_t *first_child,
               const int32_t *next_sibling, float temperature, float eps, float delta,
               uint64_t seed, uint64_t step, int path_cap, int32_t *acc_len, int32_t *acc_path,
-              int32_t *bonus, int32_t *status, cudaStream_t stream);
+              int32_t *bonus, int32_t *status, cudaStream_t stream, SvCommit commit = SvCommit{});
 // kv_commit; `pages` (table null: contiguous) addresses a paged cache
 // [n_layers, num_blocks, hkv, block_size, D] with s_max = max_blocks *
 // block_size.

@@ -331,6 +331,49 @@ int spec_accept(int mode, const void *logits, const void *draft_logits, int dtyp
                    bonus, dev_status, cs(stream));
 }
 
+int spec_accept_commit(int mode, const void *logits, const void *draft_logits, int dtype, int batch,
+                       int n_nodes, int vocab, const int32_t *tok, const int32_t *parents,
+                       const int32_t *first_child, const int32_t *next_sibling, float temperature,
+                       float eps, float delta, uint64_t seed, uint64_t step, int path_cap,
+                       int32_t *acc_len, int32_t *acc_path, int32_t *bonus, void *k_cache,
+                       void *v_cache, const void *k_tree, const void *v_tree, int elem_bytes,
+                       int n_layers, int hkv, int s_max, int head_dim, const int32_t *prefix_len,
+                       int32_t *prefix_len_out, int32_t *dev_status, spec_stream_t stream) {
+  if (!logits || !tok || !parents || !first_child || !next_sibling || !acc_len || !acc_path || !bonus)
+    return SPEC_ERR_INVALID_ARG;
+  if (mode != SPEC_ACCEPT_GREEDY && mode != SPEC_ACCEPT_TYPICAL && mode != SPEC_ACCEPT_REJECT &&
+      mode != SPEC_ACCEPT_REJECT_STOCHASTIC)
+    return SPEC_ERR_INVALID_ARG;
+  if ((mode == SPEC_ACCEPT_REJECT_STOCHASTIC) != (draft_logits != nullptr)) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return SPEC_ERR_UNSUPPORTED;
+  if (batch < 1 || n_nodes < 1 || vocab < 1 || path_cap < 1) return SPEC_ERR_INVALID_ARG;
+  if (n_nodes > SPEC_MAX_NODES) return SPEC_ERR_UNSUPPORTED;
+  if (mode != SPEC_ACCEPT_GREEDY && !(temperature > 0.f)) return SPEC_ERR_INVALID_ARG;
+  if (mode == SPEC_ACCEPT_GREEDY) temperature = 1.f;
+  // the commit's arguments, as kv_commit
+  if (!k_cache || !v_cache || !k_tree || !v_tree || !prefix_len) return SPEC_ERR_INVALID_ARG;
+  if (elem_bytes != 2 && elem_bytes != 4) return SPEC_ERR_UNSUPPORTED;
+  if (n_layers < 1 || hkv < 1 || s_max < 1 || head_dim < 1) return SPEC_ERR_INVALID_ARG;
+  if (path_cap > SPEC_MAX_NODES + 1) return SPEC_ERR_UNSUPPORTED;
+  if ((head_dim * elem_bytes) % 16) return SPEC_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_tree) || !aligned16(v_tree))
+    return SPEC_ERR_INVALID_ARG;
+  SvCommit cm{};
+  cm.kc = static_cast<uint4 *>(k_cache);
+  cm.vc = static_cast<uint4 *>(v_cache);
+  cm.kt = static_cast<const uint4 *>(k_tree);
+  cm.vt = static_cast<const uint4 *>(v_tree);
+  cm.n_layers = n_layers;
+  cm.hkv = hkv;
+  cm.s_max = s_max;
+  cm.vec_per_row = head_dim * elem_bytes / 16;
+  cm.prefix_len = prefix_len;
+  cm.prefix_len_out = prefix_len_out;
+  return sv_accept(mode, logits, draft_logits, dtype, batch, n_nodes, vocab, tok, parents, first_child,
+                   next_sibling, temperature, eps, delta, seed, step, path_cap, acc_len, acc_path, bonus,
+                   dev_status, cs(stream), cm);
+}
+
 int spec_build_tree_batch(const int32_t *parents, const int32_t *n_valid, const int32_t *tok_in,
                           const int32_t *prefix_len, int batch, int n_nodes, int32_t *tok, int32_t *depth,
                           int32_t *pos_ids, uint64_t *anc_mask, int32_t *first_child, int32_t *next_sibling,

@@ -64,6 +64,8 @@ _SIGS = {
     "kv_commit_paged": ([_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp,
                          _vp], _i),
     "kv_commit": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp], _i),
+    "spec_accept_commit": ([_i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _f, _f, _u64, _u64, _i, _vp, _vp,
+                            _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
 }
 
 
@@ -373,6 +375,25 @@ def spec_accept(mode, logits, tok, parents, first_child, next_sibling, acc_len, 
         int(mode), _p(logits), _p(draft_logits), _DT[logits.dtype], B, N, V, _p(tok), _p(parents), _p(first_child),
         _p(next_sibling), float(temperature), float(eps), float(delta), int(seed), int(step),
         acc_path.shape[1], _p(acc_len), _p(acc_path), _p(bonus), _p(dev_status), _stream()))
+
+
+def spec_accept_commit(mode, logits, tok, parents, first_child, next_sibling, acc_len, acc_path, bonus, k_cache,
+                       v_cache, k_tree, v_tree, prefix_len, prefix_len_out=None, temperature=1.0, eps=0.0,
+                       delta=0.0, seed=0, step=0, dev_status=None, draft_logits=None):
+    """spec_accept and kv_commit (contiguous cache) in one launch."""
+    B, N, V = logits.shape
+    _want(logits, torch.float32, torch.bfloat16)
+    if draft_logits is not None and (draft_logits.dtype != logits.dtype or draft_logits.shape != logits.shape):
+        raise TypeError("draft_logits must match logits in dtype and shape")
+    if k_cache.dim() == 4:
+        L, (_, Hkv, S, D) = 1, k_cache.shape
+    else:
+        L, _, Hkv, S, D = k_cache.shape
+    _check("spec_accept_commit", load().spec_accept_commit(
+        int(mode), _p(logits), _p(draft_logits), _DT[logits.dtype], B, N, V, _p(tok), _p(parents), _p(first_child),
+        _p(next_sibling), float(temperature), float(eps), float(delta), int(seed), int(step), acc_path.shape[1],
+        _p(acc_len), _p(acc_path), _p(bonus), _p(k_cache), _p(v_cache), _p(k_tree), _p(v_tree),
+        k_cache.element_size(), L, Hkv, S, D, _p(prefix_len), _p(prefix_len_out), _p(dev_status), _stream()))
 
 
 def kv_commit(k_cache, v_cache, k_tree, v_tree, acc_len, acc_path, prefix_len, prefix_len_out=None,
