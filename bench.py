@@ -448,24 +448,116 @@ class GpuStep:
         return out, float(L.mean())
 
 
-def attention_only(name: str, device, steps: int, warmup: int):
+def _time_calls(call, steps: int, warmup: int, status=None, what: str = ""):
+    """Median CUDA-event time of `call` with an L2 flush before each launch
+    (the GPU idles while the host queues the events and the launch)."""
+    import torch
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        call()
+    times = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        torch.cuda._sleep(2_000_000)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); call(); e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    if status is not None and int(status.item()) != 0:
+        raise RuntimeError(f"{what}: device status {int(status.item())}")
+    return statistics.median(times)
+
+
+def row_timings(device, hbm: float):
+    """The rows built on top of the verify step, timed alone at the
+    workloads' shapes: the paged prefix cache (70B shape, 128-key blocks in
+    a shuffled pool), a 256-node tree (multi-word ancestor masks), rejection
+    with stochastic siblings (8B shape), and the LM head fused with greedy
+    acceptance against the LM head plus acceptance (Vicuna shape)."""
+    import torch
+    from tree_speculative_decoding_attn_gb300 import specverify as sv
+    from tree_speculative_decoding_attn_gb300 import synth
+    out = {}
+    r = attention_only("llama70b_serving", device, steps=10, warmup=3, paged=True)
+    r["frac_hbm"] = r["gbps"] / hbm
+    out["paged_attention_llama70b"] = r
+    r = attention_only("long_context", device, steps=10, warmup=3, n_nodes=256, prefix=4096)
+    r["frac_hbm"] = r["gbps"] / hbm
+    out["attention_256_nodes"] = r
+    # stochastic-sibling rejection, 8B shape: batch 8, 60 nodes, vocabulary 128256
+    w = synth.WORKLOADS["llama8b_eagle2"]
+    B, N, V = w.batch, w.n_nodes, w.vocab
+    shape = synth.random_tree(w.seed, N, (10, 4, 3, 2, 2))
+    gen = torch.Generator(device=device).manual_seed(w.seed + 5)
+    lg = (torch.randn(B, N, V, generator=gen, device=device) * 2).to(torch.bfloat16)
+    dq = (torch.randn(B, N, V, generator=gen, device=device) * 2).to(torch.bfloat16)
+    i32 = lambda *sh: torch.zeros(sh, dtype=torch.int32, device=device)
+    tok, fc, ns = i32(B, N), i32(B, N), i32(B, N)
+    cand = torch.from_numpy(synth.candidate_tokens(w.seed, B, shape.n_levels, 10, V)).to(device)
+    sv.spec_build_tree(torch.from_numpy(shape.parents).to(device), torch.from_numpy(shape.rank).to(device), cand,
+                       i32(B), i32(B), tok, i32(B, N), i32(B, N), torch.zeros((B, N), dtype=torch.int64, device=device),
+                       fc, ns)
+    par = torch.from_numpy(np.broadcast_to(shape.parents, (B, N)).copy()).to(device)
+    al, ap, bo, st = i32(B), i32(B, shape.n_levels + 1), i32(B), i32(1)
+    t = _time_calls(lambda: sv.spec_accept(sv.REJECT_STOCHASTIC, lg, tok, par, fc, ns, al, ap, bo, temperature=1.0,
+                                           seed=11, step=0, dev_status=st, draft_logits=dq), 10, 3, st, "stochastic")
+    out["stochastic_reject_llama8b"] = {"us": t * 1e6, "rows_read_per_visit": 2, "vocab": V, "batch": B}
+    del lg, dq
+    # LM head + greedy acceptance at the Vicuna shape: fused and as two calls
+    w = synth.WORKLOADS["vicuna7b_medusa"]
+    B, N, V, d = w.batch, w.n_nodes, w.vocab, w.medusa["hidden"]
+    shape = synth.tree_shape(w)
+    hid = (torch.randn(B, N, d, generator=gen, device=device)).to(torch.bfloat16)
+    wlm = (torch.randn(V, d, generator=gen, device=device) * 0.02).to(torch.bfloat16)
+    tok = torch.randint(0, V, (B, N), generator=gen, device=device, dtype=torch.int32)
+    fc, ns = i32(B, N), i32(B, N)
+    sv.spec_build_tree(torch.from_numpy(shape.parents).to(device), torch.from_numpy(shape.rank).to(device), None,
+                       None, i32(B), None, i32(B, N), i32(B, N), torch.zeros((B, N), dtype=torch.int64, device=device),
+                       fc, ns)
+    par = torch.from_numpy(np.broadcast_to(shape.parents, (B, N)).copy()).to(device)
+    al, ap, bo, st = i32(B), i32(B, shape.n_levels + 1), i32(B), i32(1)
+    logits = torch.empty(B * N, V, dtype=torch.float32, device=device)
+    ws_f = torch.empty(sv.spec_lm_head_accept_workspace_bytes(B, N, d, V), dtype=torch.uint8, device=device)
+    ws_l = torch.empty(max(sv.spec_lm_head_workspace_bytes(B * N, d, V), 16), dtype=torch.uint8, device=device)
+    t_f = _time_calls(lambda: sv.spec_lm_head_accept(sv.GREEDY, hid, wlm, tok, par, fc, ns, al, ap, bo, workspace=ws_f,
+                                                     dev_status=st), 10, 3, st, "fused")
+    t_u = _time_calls(lambda: (sv.spec_lm_head(hid.view(B * N, d), wlm, logits, workspace=ws_l, dev_status=st),
+                               sv.spec_accept(sv.GREEDY, logits.view(B, N, V), tok, par, fc, ns, al, ap, bo,
+                                              dev_status=st)), 10, 3, st, "unfused")
+    out["lm_head_accept_vicuna7b"] = {"fused_us": t_f * 1e6, "lm_head_then_accept_us": t_u * 1e6}
+    return out
+
+
+def attention_only(name: str, device, steps: int, warmup: int, paged: bool = False, n_nodes: int = 0,
+                   prefix: int = 0):
     """tree_attn_verify alone at a workload's full shape (inputs drawn on the
     device from a seeded torch generator; values do not affect the timing).
-    Per-launch CUDA-event times with an L2 flush between launches."""
+    Per-launch CUDA-event times with an L2 flush between launches.  `paged`:
+    the prefix cache as 128-key blocks of a shuffled pool; `n_nodes` /
+    `prefix`: another tree size (a dense tree) or a uniform prefix length."""
     import torch
     from tree_speculative_decoding_attn_gb300 import specverify as sv
     from tree_speculative_decoding_attn_gb300 import synth
     w = synth.WORKLOADS[name]
-    B, N, Hq, Hkv, D = w.batch, w.n_nodes, w.hq, w.hkv, w.head_dim
-    prefix = synth.prefix_lengths(w)
+    B, N, Hq, Hkv, D = w.batch, n_nodes or w.n_nodes, w.hq, w.hkv, w.head_dim
+    prefix = synth.prefix_lengths(w) if not prefix else np.full(B, prefix, np.int32)
     S = int(prefix.max()) + 64
     gen = torch.Generator(device=device).manual_seed(w.seed)
     bf = torch.bfloat16
     rnd = lambda *s: torch.randn(s, generator=gen, device=device, dtype=torch.float32).to(bf)
-    q, kc, vc, kt, vt = rnd(B, N, Hq, D), rnd(B, Hkv, S, D), rnd(B, Hkv, S, D), rnd(B, Hkv, N, D), rnd(B, Hkv, N, D)
-    shape = synth.random_tree(w.seed, N, w.caps if w.caps else (10, 4, 3, 2, 2))
+    q, kt, vt = rnd(B, N, Hq, D), rnd(B, Hkv, N, D), rnd(B, Hkv, N, D)
+    blk = 128
+    if paged:
+        max_blocks = -(-S // blk)
+        nb = B * max_blocks
+        kc, vc = rnd(nb, Hkv, blk, D), rnd(nb, Hkv, blk, D)
+        table = torch.randperm(nb, generator=gen, device=device).to(torch.int32).view(B, max_blocks)
+    else:
+        kc, vc = rnd(B, Hkv, S, D), rnd(B, Hkv, S, D)
+    shape = (synth.dense_tree((8, 4, 4, 2, 2), N) if n_nodes else
+             synth.random_tree(w.seed, N, w.caps if w.caps else (10, 4, 3, 2, 2)))
     i32 = lambda *s: torch.zeros(s, dtype=torch.int32, device=device)
-    anc = torch.zeros((B, N), dtype=torch.int64, device=device)
+    anc = torch.zeros((B, N, sv.mask_words(N)), dtype=torch.int64, device=device).squeeze(-1)
     d_prefix = torch.from_numpy(prefix).to(device)
     sv.spec_build_tree(torch.from_numpy(shape.parents).to(device), torch.from_numpy(shape.rank).to(device), None,
                        None, d_prefix, None, i32(B, N), i32(B, N), anc, i32(B, N), i32(B, N))
@@ -473,30 +565,19 @@ def attention_only(name: str, device, steps: int, warmup: int):
     splits = sv.tree_attn_plan_splits(bf, B, N, Hq, Hkv, D, prefix)
     wsb = sv.tree_attn_workspace_bytes(bf, B, N, Hq, Hkv, D, int(prefix.max()), splits)
     ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=device)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     status = torch.zeros(1, dtype=torch.int32, device=device)
-    call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()),
-                                       num_splits=splits, workspace=ws, dev_status=status)
-    for _ in range(warmup):
-        call()
-    times = []
-    for _ in range(steps):
-        flush.fill_(1.0)
-        # the GPU idles here while the host queues the events and launches,
-        # so the timed interval holds device work only
-        torch.cuda._sleep(2_000_000)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(); call(); e1.record()
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e-3)
-    if int(status.item()) != 0:
-        raise RuntimeError(f"{name}: device status {sv.spec_status_string(int(status.item()))} ({int(status.item())})")
-    t = statistics.median(times)
+    if paged:
+        call = lambda: sv.tree_attn_verify_paged(q, kc, vc, table, kt, vt, d_prefix, anc, out, int(prefix.max()),
+                                                 num_splits=splits, workspace=ws, dev_status=status)
+    else:
+        call = lambda: sv.tree_attn_verify(q, kc, vc, kt, vt, d_prefix, anc, out, int(prefix.max()),
+                                           num_splits=splits, workspace=ws, dev_status=status)
+    t = _time_calls(call, steps, warmup, status, name)
     nbytes = Hkv * D * 2 * 2 * (int(prefix.sum()) + B * N) + 2 * B * N * Hq * D * 2
     flops = 4 * N * (Hq // Hkv) * D * Hkv * (int(prefix.sum()) + B * N)
-    del q, kc, vc, kt, vt, flush
+    del q, kc, vc, kt, vt
     return {"us": t * 1e6, "gbps": nbytes / t / 1e9, "tflops": flops / t / 1e12, "bytes": nbytes,
-            "launches": 2 if wsb else 1, "splits": splits}
+            "launches": 2 if wsb else 1, "splits": splits, "n_nodes": N}
 
 
 # ----------------------------------------------------------------------------
@@ -924,7 +1005,7 @@ def main():
     del step
     torch.cuda.empty_cache()
 
-    extra, extra_attn = {}, {}
+    extra, extra_attn, rows = {}, {}, {}
     if rank == 0 and not args.no_extra:
         for nm in synth.WORKLOADS:
             if nm == args.workload:
@@ -941,6 +1022,8 @@ def main():
             r["frac_tensor"] = r["tflops"] / tc_peak
             extra_attn[nm] = r
             torch.cuda.empty_cache()
+        rows = row_timings(dev, hbm)
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
@@ -964,7 +1047,7 @@ def main():
                 "gpu_launches": launches * args.steps,
                 "stages_us": {k: v * 1e6 for k, v in stage_s.items()},
                 "mean_accepted": mean_acc, "attention": attention, "workloads": extra,
-                "attention_full_shapes": extra_attn, "clocks": clocks.summary()}
+                "attention_full_shapes": extra_attn, "rows": rows, "clocks": clocks.summary()}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
