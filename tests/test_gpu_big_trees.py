@@ -92,6 +92,9 @@ ATTN = [
     ("bf16", 2, 16, 8, 128, [129, 2048], DENSE256),        # GQA 2: 512 rows
     ("f32", 1, 4, 4, 64, [300], synth.random_tree(11, 200, (10, 8, 6, 4, 3))),
     ("bf16", 1, 32, 8, 128, [1000], synth.dense_tree((8, 8), 65)),  # 260 rows, one node in the second word
+    ("bf16", 1, 4, 4, 128, [333], synth.chain(130)),                 # 130 rows: the odd CTA mostly padding
+    ("bf16", 2, 2, 2, 128, [5, 129], synth.random_tree(12, 100, (10, 8, 6, 4, 3))),  # 100 rows, one CTA's worth
+    ("bf16", 3, 32, 4, 128, [6000, 1, 3000], DENSE256),             # 2048 rows per KV head: cut row groups
 ]
 
 

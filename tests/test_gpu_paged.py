@@ -119,7 +119,9 @@ CASES = [
     ("bf16", 4, 64, 8, 128, 128, [4096, 1000, 0, 2300], 32, [(4, 3, 2)]),       # SM pairs (256 rows)
     ("bf16", 3, 32, 32, 128, 256, [2048, 700, 129], 64, [(10, 10, 10, 10)]),   # single CTA, split KV
     ("f32", 2, 4, 4, 64, 128, [300, 129], 20, [(4, 3, 2)]),                     # CUDA cores
-    ("bf16", 2, 8, 8, 128, 128, [700, 1500], 130, [(6, 5, 4, 3)]),              # two mask words, CUDA cores
+    ("bf16", 2, 8, 8, 128, 128, [700, 1500], 130, [(6, 5, 4, 3)]),              # three mask words, SM pairs
+    ("bf16", 2, 32, 8, 128, 128, [3000, 129], 256, [(8, 6, 4, 3)]),             # two tree tiles, SM pairs
+    ("f32", 2, 4, 4, 64, 128, [300, 129], 200, [(6, 5, 4, 3)]),                 # four mask words, CUDA cores
 ]
 
 

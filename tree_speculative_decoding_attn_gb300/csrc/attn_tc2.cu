@@ -12,12 +12,16 @@
 // every K/V tile.  A row group is (sequence, KV head, pair of 128-row query
 // tiles): CTA k of a cluster owns rows [256 p + 128 k, +128) of pair p.
 //
-// Work.  The units of a row group are its tree tile (unit 0) and its prefix
-// tiles of 128 keys (units 1..).  All units of all row groups, in order
-// (sequence, KV head, pair, unit), form one sequence of U units, split into
-// C contiguous ranges of equal weight: a prefix tile weighs 1 and a tree
-// tile 1 + kSegW, the row group's fixed cost (pipeline drain, epilogue,
-// mask), so ranges with more row-group starts hold fewer tiles.  A row
+// Work.  The units of a row group are its tree tiles of 128 keys (units
+// 0 .. nt-1, nt = ceil(N / 128)) and its prefix tiles of 128 keys (units
+// nt ..).  All units of all row groups, in order (sequence, KV head, pair,
+// unit), form one sequence of U units, split into C contiguous ranges of
+// equal weight: a prefix tile weighs 1 and the tree tiles together
+// nt + kSegW, the row group's fixed cost (pipeline drain, epilogue, mask)
+// included, so ranges with more row-group starts hold fewer tiles.  No range
+// starts between two tree tiles, so the first tile of every part of a row
+// group (its first tree tile, holding the root, or a prefix tile) shows
+// every row at least one key.  A row
 // group that lies wholly inside one cluster's range is normalised and
 // written out; the parts of a row group cut by range ends leave partials
 // (unnormalised O in bf16, running max in log2 units and row sum in
@@ -117,24 +121,26 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(256, 128, 0, 1);  // V MN-major (di
 struct Sched {
   const int32_t *prefix_len;
   int batch, hkv, pairs, n_nodes, s_max, max_prefix, n_clusters;
+  int nt, mw;                                              // tree tiles; ancestor-mask words per node
   sv::KvPages pg;                                          // prefix cache addressing
   __device__ int gpb() const { return hkv * pairs; }  // row groups per sequence
 };
 
 // A row group's fixed cost (the pipeline drain and epilogue at its end, the
-// tree mask) in tile equivalents, carried by its tree tile in the balanced
+// tree mask) in tile equivalents, carried by its tree tiles in the balanced
 // split: a row group of n tiles weighs n + kSegW, and its unit t starts at
-// weight unit_start_w(t) within it.
+// weight unit_start_w(t) within it (all tree tiles at 0: no range starts
+// between them).
 constexpr int kSegW = 3;
-__device__ __forceinline__ int unit_start_w(int t) { return t == 0 ? 0 : kSegW + t; }
+__device__ __forceinline__ int unit_start_w(int t, int nt) { return t < nt ? 0 : kSegW + t; }
 
 // A prefix length out of bounds counts as 0 (the sequence is reported and
 // its output left unwritten).
 __device__ __forceinline__ bool prefix_ok(const Sched &s, int raw) {
   return raw >= 0 && raw <= s.max_prefix && raw <= s.s_max;
 }
-__device__ __forceinline__ int seq_tiles(int P) { return 1 + (P + kBN - 1) / kBN; }
-__device__ __forceinline__ int tiles_of(const Sched &s, int raw) { return seq_tiles(prefix_ok(s, raw) ? raw : 0); }
+__device__ __forceinline__ int seq_tiles(const Sched &s, int P) { return s.nt + (P + kBN - 1) / kBN; }
+__device__ __forceinline__ int tiles_of(const Sched &s, int raw) { return seq_tiles(s, prefix_ok(s, raw) ? raw : 0); }
 
 __device__ __forceinline__ long long warp_sum_ll(long long v) {
 #pragma unroll
@@ -228,7 +234,7 @@ __device__ void warp_seek2(const Sched &s, const SeqTab &tb, long long x0, long 
       const int nl = __shfl_sync(0xffffffffu, n, l);
       int gi = (int)((x - wb) / (nl + kSegW));
       const int r = (int)(x - wb - (long long)gi * (nl + kSegW));
-      int t = r == 0 ? 0 : max(1, r - kSegW);
+      int t = r == 0 ? 0 : max(s.nt, r - kSegW);
       int b = 32 * i + l;
       p->u = ub + (long long)gi * nl + t;
       p->wrg = wb + (long long)gi * (nl + kSegW);
@@ -261,10 +267,11 @@ __device__ void warp_seek2(const Sched &s, const SeqTab &tb, long long x0, long 
   }
 }
 
-// Clusters in use: each range is at least as wide as the heaviest unit, so
-// every range holds a unit's start.
+// Clusters in use: each range is at least as wide as the heaviest run of
+// units with one start weight (a row group's tree tiles), so every range
+// holds a unit's start.
 __device__ __forceinline__ long long clusters_used(const Sched &s, long long W) {
-  return max(1ll, min((long long)s.n_clusters, W / (1 + kSegW)));
+  return max(1ll, min((long long)s.n_clusters, W / (s.nt + kSegW)));
 }
 __device__ __forceinline__ long long range_start(long long c, long long W, long long C) { return c * W / C; }
 // Cluster whose range holds weight x (the largest c with range_start(c) <= x).
@@ -297,7 +304,7 @@ __device__ __forceinline__ int load_prefix(const Sched &s, int b) { return b < s
 __device__ __forceinline__ void cur_apply(Cur &c, const Sched &s, int raw) {
   c.ok = prefix_ok(s, raw);
   c.P = c.ok ? raw : 0;
-  c.n = seq_tiles(c.P);
+  c.n = seq_tiles(s, c.P);
 }
 __device__ __forceinline__ Cur cur_begin(const Bars *bars, const Sched &s) {
   Cur c;
@@ -319,8 +326,10 @@ __device__ __forceinline__ void cur_next(Cur &c, const Sched &s) {
     }
   }
 }
-// Valid keys of a prefix tile (t >= 1).
-__device__ __forceinline__ int tile_keys(const Cur &c) { return min(kBN, c.P - (c.t - 1) * kBN); }
+// Valid keys of tile t: a tree tile (t < nt) or a prefix tile.
+__device__ __forceinline__ int tile_keys(const Cur &c, const Sched &s) {
+  return c.t < s.nt ? min(kBN, s.n_nodes - c.t * kBN) : min(kBN, c.P - (c.t - s.nt) * kBN);
+}
 
 __device__ __forceinline__ void give_up(Bars *bars, int32_t *status) {
   bars->abort = 1;
@@ -351,12 +360,21 @@ __device__ __forceinline__ bool v_ready(Bars *bars, uint8_t *sV, int g, int nkey
   return true;
 }
 
+// MAXW: ancestor-mask words per node, rounded up to 1, 2 or 4 (trees of up
+// to 64, 128 or 256 nodes; one, one or two tree tiles).
+template <int MAXW>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                     const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_kt,
                     const __grid_constant__ CUtensorMap tm_vt, const __grid_constant__ CUtensorMap tm_o,
-                    const Sched s, const uint64_t *__restrict__ anc, void *__restrict__ ws, int Hq,
+                    const Sched s_in, const uint64_t *__restrict__ anc, void *__restrict__ ws, int Hq,
                     float scale_log2, int32_t *status) {
+  // the tree-tile count as a compile-time constant in every schedule step
+  const Sched s = [&] {
+    Sched t = s_in;
+    t.nt = (MAXW + 1) / 2;
+    return t;
+  }();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t *sQ = smem;
   uint8_t *sK = sQ + kQB * kQBytes;
@@ -409,7 +427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           d.usable = cluster_of(p0.wrg, W, C) == cluster - 1;
           d.b = p0.b;
           d.gi = p0.gi;
-          d.c_hi = cluster_of(p0.wrg + unit_start_w(tiles_of(s, raw0) - 1), W, C);
+          d.c_hi = cluster_of(p0.wrg + unit_start_w(tiles_of(s, raw0) - 1, s.nt), W, C);
         }
         cut_descs(ws, s.n_clusters)[cluster] = d;
       }
@@ -477,9 +495,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (kPrefetch > 0 && g + kPrefetch < T) {
           // warm L2 with this CTA's half of tile g + kPrefetch
           const int pbh = cpf.b * s.hkv + cpf.gi / pairs;
-          const bool ptree = cpf.t == 0;
-          const int prow = ptree ? pbh * N : sv::kv_row(s.pg, cpf.b, s.hkv, cpf.gi / pairs, s.s_max, (cpf.t - 1) * kBN,
-                                                        nullptr);
+          const bool ptree = cpf.t < s.nt;
+          const int prow = ptree ? pbh * N + cpf.t * kBN
+                                 : sv::kv_row(s.pg, cpf.b, s.hkv, cpf.gi / pairs, s.s_max, (cpf.t - s.nt) * kBN, nullptr);
           if (is_v) {
             tma_prefetch_2d(ptree ? &tm_vt : &tm_vc, 64 * (int)rank, prow);
           } else {
@@ -510,10 +528,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           give_up(bars, status);
           break;
         }
-        const bool tree = c.t == 0;
+        const bool tree = c.t < s.nt;
         // (a 128-key tile lies inside one cache block: block sizes are
         // multiples of 128; a bad block id gives row -1, read as zeros)
-        const int row0 = tree ? bh * N : sv::kv_row(s.pg, c.b, s.hkv, kvh, s.s_max, (c.t - 1) * kBN, status);
+        const int row0 =
+            tree ? bh * N + c.t * kBN : sv::kv_row(s.pg, c.b, s.hkv, kvh, s.s_max, (c.t - s.nt) * kBN, status);
         if (is_v) {
           mbar_expect_tx(land, kVBytes);
           tma_load_2d(sV + st * kVBytes, tree ? &tm_vt : &tm_vc, 64 * (int)rank, row0, land);
@@ -618,7 +637,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int g = 0; ok && g < T; ++g) {
         // O += P(g) V(g) once P of both CTAs is ready (which also covers both
         // V halves of tile g)
-        const int nkeys = cp.t == 0 ? N : tile_keys(cp);
+        const int nkeys = tile_keys(cp, s);
         if (!(ok = warp_wait(&bars->pfull[g % kSB], (g / kSB) & 1) && v_ready(bars, sV, g, nkeys))) break;
         tc_fence_after();
         const bool first = g == 0 || cp.t == 0;
@@ -656,7 +675,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t pfull_even0 = mapa_cluster(&bars->pfull[0], 0);  // pfull[i] at + 8 i
       Cur c = cur_begin(bars, s);
       for (int g = 0; g < T; ++g) {
-        if (!warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1) || !v_ready(bars, sV, g, c.t == 0 ? N : tile_keys(c)) ||
+        if (!warp_wait(&bars->sfull[g % kSB], (g / kSB) & 1) || !v_ready(bars, sV, g, tile_keys(c, s)) ||
             bars->abort) {
           give_up(bars, status);
           break;
@@ -687,15 +706,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool from_start = c.t == 0;
     float ma = NEG_INF, mb = NEG_INF;  // running max of rows ra, rb (log2 units)
     float la = 0.f, lb_sum = 0.f;      // this thread's part of their sums
-    // ancestor bits of a row in a row group (padding rows: all tree keys),
-    // loaded one row group ahead so the tree tile never waits
-    auto grow = [&](int gi, int lane_row) { return (gi % pairs) * kPairRows + (int)rank * 128 + lane_row; };
-    auto load_mask = [&](int b, int gi, int lane_row) -> uint64_t {
-      const int rr = grow(gi, lane_row);
-      return rr < R ? anc[(int64_t)b * N + rr / G] : ~0ull;
+    // Ancestor bits of a row for tree tile tt (words 2 tt and 2 tt + 1 of its
+    // node; padding rows: all tree keys): the first tree tile's loaded one
+    // row group ahead, a later tree tile's one tile ahead, so no tree tile
+    // waits for them.
+    constexpr int NT = (MAXW + 1) / 2;        // tree tiles
+    constexpr int MP = MAXW == 1 ? 1 : 2;     // mask words of one tree tile
+    const int MW = MAXW == 1 ? 1 : s.mw;
+    struct Mask {
+      uint64_t w[MP];
     };
-    uint64_t amask_a = c.t == 0 ? load_mask(c.b, c.gi, ra) : 0ull, amask_b = c.t == 0 ? load_mask(c.b, c.gi, rb) : 0ull;
-    uint64_t next_a = 0ull, next_b = 0ull;
+    auto grow = [&](int gi, int lane_row) { return (gi % pairs) * kPairRows + (int)rank * 128 + lane_row; };
+    auto load_mask = [&](int b, int gi, int lane_row, int tt) -> Mask {
+      Mask m;
+      const int rr = grow(gi, lane_row);
+      const uint64_t *p = anc + ((int64_t)b * N + rr / G) * MW + 2 * tt;
+#pragma unroll
+      for (int i = 0; i < MP; ++i) m.w[i] = rr >= R ? ~0ull : (MP == 1 || 2 * tt + i < MW) ? p[i] : 0ull;
+      return m;
+    };
+    Mask amask_a{}, amask_b{}, next_a{}, next_b{};
+    if (c.t < NT) {
+      amask_a = load_mask(c.b, c.gi, ra, c.t);
+      amask_b = load_mask(c.b, c.gi, rb, c.t);
+    }
     bool ok = true;
     bool s_ready = false;  // S(g) seen complete during tile g - 1
     // A failed wait (timeout) or an abort turns the rest into a no-op that
@@ -715,8 +749,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       la = lb_sum = 0.f;
       if (g + (c.n - 1 - c.t) + 1 < T) {  // the next segment's ancestor bits, a segment ahead
         const bool same_b = c.gi + 1 < s.gpb();
-        next_a = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, ra);
-        next_b = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, rb);
+        next_a = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, ra, 0);
+        next_b = load_mask(same_b ? c.b : c.b + 1, same_b ? c.gi + 1 : 0, rb, 0);
       }
       bool first = true;
       for (;;) {
@@ -732,16 +766,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 64; ++i) sv[i] = __float_as_uint(0.f);
         }
-        const bool tree = c.t == 0;
-        const int nvalid = tree ? N : tile_keys(c);
+        const bool tree = c.t < s.nt;
+        const int nvalid = tile_keys(c, s);
         // The tile body comes in two instances so that full prefix tiles, the
         // steady state, carry no masking code: the masked one serves the tree
-        // tile and the last, partial prefix tile.
+        // tiles and the last, partial prefix tile.
         auto tile = [&](auto masked) {
           if constexpr (decltype(masked)::value) {
             // Visibility of this thread's keys 8j + 2 tq + e as bits 2j + e: the
             // keys below nvalid are a prefix of these bits (they increase with
-            // the bit index); on the tree tile (N <= 64) also the ancestor bits.
+            // the bit index); on a tree tile also the ancestor bits (keys 0-63
+            // of the tile from its first mask word, 64-127 from its second).
             const int m8 = nvalid - 2 * tq;
             const int nb = m8 <= 0 ? 0 : min(32, 2 * (m8 >> 3) + min(2, m8 & 7));
             const uint32_t in = nb >= 32 ? 0xFFFFFFFFu : ((1u << nb) - 1u);
@@ -753,8 +788,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 x = (x | (x >> 12)) & 0x000000FF000000FFull;
                 return (uint32_t)((x | (x >> 24)) & 0xFFFFull);
               };
-              va &= mine(amask_a);
-              vb &= mine(amask_b);
+              if constexpr (MP == 1) {
+                va &= mine(amask_a.w[0]);
+                vb &= mine(amask_b.w[0]);
+              } else {
+                va &= mine(amask_a.w[0]) | (mine(amask_a.w[1]) << 16);
+                vb &= mine(amask_b.w[0]) | (mine(amask_b.w[1]) << 16);
+              }
+              if constexpr (NT > 1) {
+                if (c.t + 1 < NT) {  // the next tree tile's bits, a tile ahead
+                  amask_a = load_mask(c.b, c.gi, ra, c.t + 1);
+                  amask_b = load_mask(c.b, c.gi, rb, c.t + 1);
+                }
+              }
             }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {  // i = 2j + e: register 4j + e of row ra, 4j + 2 + e of row rb
@@ -800,8 +846,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bool exact = decltype(masked)::value || first;
           for (;;) {
             if (exact) {
-              // exact row max of the tile; every row sees a key in every tile
-              // (itself on the tree tile), so it is finite
+              // exact row max of the tile: finite on a part's first tile (the
+              // root, or prefix keys, are visible to every row); a later tree
+              // tile may hide all its keys from a row (max -inf: the running
+              // max stays, and its P is 0)
               float xa[2] = {NEG_INF, NEG_INF}, xb[2] = {NEG_INF, NEG_INF};
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -1026,7 +1074,7 @@ __global__ void __launch_bounds__(256, 4) attn_tc2_combine_kernel(void *__restri
     float Mb = M;
 #pragma unroll
     for (int i = 0; i < kCombBatch; ++i) Mb = fmaxf(Mb, ml[i].x);
-    // every part has a finite max (each tile holds a visible key)
+    // every part has a finite max (its first tile holds a key visible to every row)
     const float r = exp2f(M - Mb);  // 0 on the first batch
     L *= r;
 #pragma unroll
@@ -1103,7 +1151,7 @@ int tc2_clusters() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   int n = g_clusters[dev].load();
   if (n > 0) return n;
-  if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+  if (cudaFuncSetAttribute(attn_tc2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
       cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -1111,7 +1159,7 @@ int tc2_clusters() {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc2_kernel, &cfg) != cudaSuccess || clusters < 1) return 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, attn_tc2_kernel<1>, &cfg) != cudaSuccess || clusters < 1) return 0;
   g_clusters[dev].store(clusters);
   return clusters;
 }
@@ -1121,7 +1169,7 @@ int tc2_clusters() {
 bool sv_attn_tc2_supported(const SvAttnShape &s) {
   if (s.dtype != SPEC_BF16 || s.head_dim != kD || s.hkv < 1) return false;
   const int G = s.hq / s.hkv;
-  return s.n_nodes <= 64 && G <= 128 && (128 % G) == 0 && s.n_nodes * G > 128;
+  return s.n_nodes <= SPEC_MAX_NODES && G <= 128 && (128 % G) == 0 && (s.n_nodes * G > 128 || s.n_nodes > 64);
 }
 
 size_t sv_attn_tc2_ws_bytes() {
@@ -1180,12 +1228,16 @@ int sv_attn_tc2(const SvAttnShape &s, const void *q, const void *kc, const void 
   sc.s_max = s.s_max;
   sc.max_prefix = s.max_prefix;
   sc.n_clusters = C;
+  sc.nt = (s.n_nodes + kBN - 1) / kBN;
+  sc.mw = (s.n_nodes + 63) / 64;
   sc.pg = sv::KvPages{s.block_table, s.block_size, s.max_blocks, s.num_blocks};
-  if (cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-      cudaSuccess)
+  // (every instance has the same shared memory and one CTA per SM, so the
+  // cluster count looked up for one holds for all)
+  auto kern = sc.mw == 1 ? attn_tc2_kernel<1> : sc.mw == 2 ? attn_tc2_kernel<2> : attn_tc2_kernel<4>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  attn_tc2_kernel<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, mo, sc, anc,
-                                                          ws, s.hq, scale * 1.4426950408889634f, status);
+  kern<<<2 * C, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkt, mvt, mo, sc, anc, ws, s.hq,
+                                               scale * 1.4426950408889634f, status);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   if (C > 1) {
     // programmatic dependent launch: the merge blocks locate their row groups
