@@ -49,9 +49,9 @@ L2_BYTES = 129 * 1024 * 1024
 # bytes) keyed by (workload, stage).
 NCU_TRAFFIC = {
     # attn_tc2_kernel, 70B shape at batch 16 (one quarter of the workload's
-    # sequences; traffic grows with the sequences): (286,152,448 read +
-    # 6,764,416 written, mean of two launches) x 4, from one ncu capture
-    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "533dabf1486075f4", 1171667456),
+    # sequences; traffic grows with the sequences): (286,012,800 read +
+    # 6,767,488 written, mean of two launches) x 4, from one ncu capture
+    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "b5dc631715b2914d", 1171121152),
 }
 
 
@@ -863,6 +863,10 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling cases)")
     ap.add_argument("--attention-only", action="store_true",
                     help="time tree_attn_verify alone at the workload's shape (profiling runs)")
+    ap.add_argument("--nodes", type=int, default=0,
+                    help="with --attention-only: a dense tree of this many nodes instead of the workload's")
+    ap.add_argument("--prefix", type=int, default=0,
+                    help="with --attention-only: this prefix length for every sequence")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -880,7 +884,8 @@ def main():
         synth.WORKLOADS[args.workload] = dataclasses.replace(synth.WORKLOADS[args.workload], batch=args.batch)
     hbm, tc_peak, peak_kind = _peaks()
     if args.attention_only:
-        r = attention_only(args.workload, dev, steps=args.steps, warmup=args.warmup)
+        r = attention_only(args.workload, dev, steps=args.steps, warmup=args.warmup, n_nodes=args.nodes,
+                           prefix=args.prefix)
         r.update(workload=args.workload, frac_hbm=r["gbps"] / hbm, peak_kind=peak_kind)
         print(json.dumps({"attention_only": r}), flush=True)
         return

@@ -324,15 +324,16 @@ int spec_eagle_round(const spec_eagle_weights *w, int batch, int hidden, int hq,
  *               (may be NULL when that size is 0)
  * dtype SPEC_F32 or SPEC_BF16; head_dim 64 or 128; n_nodes <= 256;
  * hq % hkv == 0; (hq / hkv) * n_nodes <= 512 for trees of up to 64 nodes,
- * <= 2048 above (those run on the CUDA-core kernel).  Softmax and accumulation
- * are float32.  A prefix_len above max_prefix sets SPEC_DEV_CAPACITY and
- * that sequence's output is left unwritten.
- * bf16 with head_dim 128 and more than 128 query rows per KV head
- * ((hq / hkv) * n_nodes > 128, hq / hkv dividing 128) runs on pairs of
- * SMs with a persistent grid that balances its own work: num_splits is
- * ignored there (tree_attn_plan_splits returns 1) and the workspace holds
- * the partial rows of the row groups cut between SM pairs.  Calls that
- * may overlap on the GPU need separate workspaces.
+ * <= 2048 above.  Softmax and accumulation are float32.  A prefix_len above
+ * max_prefix sets SPEC_DEV_CAPACITY and that sequence's output is left
+ * unwritten.
+ * bf16 with head_dim 128 (hq / hkv dividing 128) and either more than 128
+ * query rows per KV head ((hq / hkv) * n_nodes > 128) or more than 64
+ * nodes runs on pairs of SMs with a persistent grid that balances its own
+ * work: num_splits is ignored there (tree_attn_plan_splits returns 1) and
+ * the workspace holds the partial rows of the row groups cut between SM
+ * pairs.  f32 and head_dim 64 run on CUDA cores.  Calls that may overlap
+ * on the GPU need separate workspaces.
  * ------------------------------------------------------------------ */
 size_t tree_attn_workspace_bytes(int dtype, int batch, int n_nodes, int hq, int hkv,
                                  int head_dim, int max_prefix, int num_splits);
