@@ -167,7 +167,6 @@ class GpuStep:
         self.s_max = self.max_prefix + 64
         self.stages = []          # (name, fn, launches, algorithmic bytes or None)
         self.h2d = []             # (pinned host copy, attribute name) copied each end-to-end step
-        self.d2h = []
         # tree
         if w.tree == "dynamic":
             dk = w.dynamic
@@ -211,7 +210,7 @@ class GpuStep:
         # the per-sequence scalars
         for nm in ("q", "kt", "vt", "d_prefix", "root"):
             self.e2e_input(nm)
-        self.d2h += [self.acc_len, self.acc_path, self.bonus, self.new_prefix]
+        self.d2h_names = ["acc_len", "acc_path", "bonus", "new_prefix"]  # results read back per step
 
         if w.medusa:
             self._medusa_stages(cu)
@@ -936,19 +935,31 @@ def main():
                 "bytes_per_launch": dom_bytes, "launch_us": stage_s[dom] * 1e6}
 
     # end-to-end leg through the public API: every step copies its inputs
-    # from pinned host memory and reads its results back.  The copies run on
-    # a stream of their own into two alternating device buffer sets, so step
-    # k + 1's inputs travel while step k computes (a set is rewritten only
-    # after the step that read it has finished).
+    # from pinned host memory and reads its results back.  Two alternating
+    # device buffer sets (inputs and results): the input copies run on a
+    # stream of their own, so step k + 1's inputs travel while step k
+    # computes, and the result read-back on a third, so the next step starts
+    # without waiting for it (a set is rewritten only after the step that
+    # read its inputs has finished and its results have been read back).
     names = [n for _, n in step.h2d]
     hosts = [h for h, _ in step.h2d]
     h2d_bytes = sum(h.numel() * h.element_size() for h in hosts)
     sets = [[getattr(step, n) for n in names], [torch.empty_like(getattr(step, n)) for n in names]]
-    outs_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.d2h]
-    d2h_bytes = sum(t.numel() * t.element_size() for t in outs_host)
-    main, copy_s = torch.cuda.current_stream(), torch.cuda.Stream()
+    onames = step.d2h_names
+    osets = [[getattr(step, n) for n in onames], [torch.empty_like(getattr(step, n)) for n in onames]]
+    outs_host = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in osets[0]] for _ in range(2)]
+    d2h_bytes = sum(t.numel() * t.element_size() for t in outs_host[0])
+    main, copy_s, back_s = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     freed = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def use_set(si):
+        for n, d in zip(names, sets[si]):
+            setattr(step, n, d)
+        for n, d in zip(onames, osets[si]):
+            setattr(step, n, d)
 
     def issue_copy(k):
         with torch.cuda.stream(copy_s):
@@ -963,8 +974,7 @@ def main():
     # the line reports the graph figure and keeps the eager one beside it
     graphs = []
     for si in range(2):
-        for n, d in zip(names, sets[si]):
-            setattr(step, n, d)
+        use_set(si)
         graphs.append(capture(step, 1, False)[0])
 
     def e2e_run(use_graphs):
@@ -977,30 +987,35 @@ def main():
             if k + 1 < args.steps:
                 issue_copy(k + 1)
             main.wait_event(copied[k % 2])
+            if k >= 2:
+                main.wait_event(read[k % 2])  # this set's previous results are back on the host
             if use_graphs:
                 graphs[k % 2].replay()
             else:
-                for n, d in zip(names, sets[k % 2]):
-                    setattr(step, n, d)
+                use_set(k % 2)
                 step.run()
             freed[k % 2].record(main)
-            for hdst, dsrc in zip(outs_host, step.d2h):
-                hdst.copy_(dsrc, non_blocking=True)
+            done[k % 2].record(main)
+            with torch.cuda.stream(back_s):
+                back_s.wait_event(done[k % 2])
+                for hdst, dsrc in zip(outs_host[k % 2], osets[k % 2]):
+                    hdst.copy_(dsrc, non_blocking=True)
+                read[k % 2].record(back_s)
         main.wait_stream(copy_s)
+        main.wait_stream(back_s)
         e1.record()
         torch.cuda.synchronize()
         return job_max(e0.elapsed_time(e1) * 1e-3, dist, dev)
 
     e2e_eager_s = e2e_run(False)
     e2e_s = e2e_run(True)
-    for n, d in zip(names, sets[0]):
-        setattr(step, n, d)
+    use_set(0)
     del graphs
     e2e = {"value": job_rate(args.steps, ws, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d_bytes,
            "d2h_bytes_per_step": d2h_bytes,
            "how": "per step: H2D of its inputs from pinned memory on a copy stream (double-buffered, "
                   "overlapping the previous step), the step's API calls replayed from a one-step CUDA graph, "
-                  "D2H of the accepted paths",
+                  "D2H of the accepted paths on a third stream (double-buffered results)",
            "eager_value": job_rate(args.steps, ws, e2e_eager_s)}
 
     launches = step.launches_per_step()
