@@ -90,3 +90,33 @@ def test_noalloc_rejects_work_beyond_its_scratch():
         sv.tree_attn_verify_noalloc(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], out,
                                     x["max_prefix"], num_splits=64)
     assert e.value.code == sv.ERR_CAPACITY
+
+
+def test_noalloc_256_node_tree_matches():
+    """A dense 256-node tree (two tree tiles, four ancestor words per node)
+    on the SM-pair kernel through the fixed array."""
+    B, hq, hkv, n = 2, 16, 4, 256
+    shape = synth.dense_tree((4, 4, 4, 4), n)
+    w = synth.Workload("noalloc256", 31, batch=B, hq=hq, hkv=hkv, head_dim=128, dtype="bf16", prefix=(700, 1900),
+                       n_nodes=n, n_levels=shape.n_levels, vocab=10, accept="greedy", tree="random")
+    prefix = synth.prefix_lengths(w)
+    q, kc, vc, kt, vt = synth.attention_inputs(w, prefix, q_scale=2.0)
+    W = sv.mask_words(n)
+    anc = np.broadcast_to(T.mask_words_multi(T.depth_and_mask(shape.parents)[1]), (B, n, W)).copy()
+    bf = torch.bfloat16
+    x = dict(q=dev(q, bf), kc=dev(kc, bf), vc=dev(vc, bf), kt=dev(kt, bf), vt=dev(vt, bf), prefix=i32(prefix),
+             anc=dev(anc.view(np.int64)), max_prefix=int(prefix.max()))
+    need = sv.tree_attn_workspace_bytes(bf, B, n, hq, hkv, 128, x["max_prefix"])
+    assert 0 < need <= sv.NOALLOC_SCRATCH_BYTES
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    ref = torch.empty_like(x["q"])
+    got = torch.full_like(x["q"], float("nan"))
+    st = zeros_i32(1)
+    sv.tree_attn_verify(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], ref, x["max_prefix"],
+                        workspace=ws, dev_status=st)
+    sv.tree_attn_verify_noalloc(x["q"], x["kc"], x["vc"], x["kt"], x["vt"], x["prefix"], x["anc"], got,
+                                x["max_prefix"], dev_status=st)
+    torch.cuda.synchronize()
+    assert int(host(st)[0]) == 0
+    ok, excess = within(host(got), host(ref), *TOL)
+    assert ok, f"max excess {excess}"
