@@ -91,7 +91,12 @@ constexpr uint32_t kVBytes = kBN * 64 * 2;   // 128 keys x 64 dims
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr int kSB = 3;                       // S/P buffers in TMEM (128 columns each)
 constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 in all)
-constexpr float kTau = 8.f;                  // running max moves only when a tile exceeds it by 2^8
+// The running max moves only when a tile exceeds it by more than kTau (log2
+// units): P = 2^(s - m) then stays below 2^16, far inside bf16's and float32's
+// exponent range, and its relative precision does not depend on its size.  A
+// small bound made the first prefix tile after a tree tile (whose rows see
+// only a few keys) move the max and rescale O in most row groups.
+constexpr float kTau = 16.f;
 constexpr uint16_t kBoth = 3;                // CTA mask of the pair
 constexpr int kStoreThread = 64;             // softmax thread that issues the output stores (warp 2, lane 0)
 // A partial row: 128 bf16 of unnormalised O (256 B), then the running max
