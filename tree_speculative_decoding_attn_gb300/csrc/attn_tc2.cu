@@ -97,6 +97,7 @@ constexpr uint32_t kColO = kSB * 128;        // O after them (128 columns; 512 i
 // small bound made the first prefix tile after a tree tile (whose rows see
 // only a few keys) move the max and rescale O in most row groups.
 constexpr float kTau = 16.f;
+constexpr float kSumBound = 65536.f;  // 2^kTau
 constexpr uint16_t kBoth = 3;                // CTA mask of the pair
 constexpr int kStoreThread = 64;             // softmax thread that issues the output stores (warp 2, lane 0)
 // A partial row: 128 bf16 of unnormalised O (256 B), then the running max
@@ -818,22 +819,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const bool next_done = ok && g + 1 < T && mbar_test(&bars->sfull[(g + 1) % kSB], ((g + 1) / kSB) & 1);
           // P = 2^(s * scale - m) as bf16 pairs: key pair 8j + 2 tq, +1 is P
           // column 4j + tq, written over the tile's first 64 S columns of this
-          // warp's lanes (all of them were read above); the row sums; and this
-          // thread's largest exponent s * scale - m.
+          // warp's lanes (all of them were read above); and the row sums.
           uint32_t pk[32];
           float2 sa2, sb2;
-          auto exps = [&]() -> float {
+          auto exps = [&]() {
             const float2 sc2 = make_float2(scale_log2, scale_log2);
             const float2 na2 = make_float2(-ma, -ma), nb2 = make_float2(-mb, -mb);
-            float mx0 = NEG_INF, mx1 = NEG_INF;
             sa2 = sb2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float2 xa2 = fma2(make_float2(__uint_as_float(sv[4 * j]), __uint_as_float(sv[4 * j + 1])), sc2, na2);
               const float2 xb2 =
                   fma2(make_float2(__uint_as_float(sv[4 * j + 2]), __uint_as_float(sv[4 * j + 3])), sc2, nb2);
-              mx0 = fmax3(mx0, xa2.x, xa2.y);
-              mx1 = fmax3(mx1, xb2.x, xb2.y);
               const float2 pa = make_float2(ex2(xa2.x), ex2(xa2.y));
               const float2 pb = make_float2(ex2(xb2.x), ex2(xb2.y));
               sa2 = add2(sa2, pa);
@@ -841,13 +838,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               pk[2 * j] = pack_bf16(pa.x, pa.y);
               pk[2 * j + 1] = pack_bf16(pb.x, pb.y);
             }
-            return fmaxf(mx0, mx1);
           };
           // Past a row group's first tile, P is computed in one pass with the
           // running max as it stands: the exact tile max matters only when some
-          // score exceeds the running max by more than kTau, and then the tile is
-          // read again and redone on the exact path (the tree and ragged tiles
-          // and a segment's first tile take the exact path at once).
+          // score exceeds the running max by more than kTau, which shows in the
+          // row sums (one P above 2^kTau puts its row's sum above it), and then
+          // the tile is read again and redone on the exact path (the tree and
+          // ragged tiles and a segment's first tile take the exact path at once).
           bool exact = decltype(masked)::value || first;
           for (;;) {
             if (exact) {
@@ -903,8 +900,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               }
             }
             if (!ok) break;
-            const float mx = exps();
-            if (exact || !__any_sync(0xffffffffu, mx > kTau)) break;
+            exps();
+            // some P above 2^kTau makes its row's partial sum exceed it too (a
+            // NaN or infinite sum fails the test as well)
+            if (exact || !__any_sync(0xffffffffu, !(fmaxf(sa2.x + sa2.y, sb2.x + sb2.y) <= kSumBound))) break;
             exact = true;
             tmem_ld_16x256b_x16(s_addr, sv);
             tmem_wait_ld();
