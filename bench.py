@@ -49,9 +49,9 @@ L2_BYTES = 129 * 1024 * 1024
 # bytes) keyed by (workload, stage).
 NCU_TRAFFIC = {
     # attn_tc2_kernel, 70B shape at batch 16 (one quarter of the workload's
-    # sequences; traffic grows with the sequences): (285,990,784 read +
-    # 6,717,824 written, mean of two launches) x 4, from one ncu capture
-    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "b9dc8338ec24f536", 1170834432),
+    # sequences; traffic grows with the sequences): (286,022,272 read +
+    # 6,765,184 written, mean of two launches) x 4, from one ncu capture
+    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "8aaeb11a88d32a4c", 1171149824),
 }
 
 
