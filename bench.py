@@ -51,7 +51,8 @@ NCU_TRAFFIC = {
     # attn_tc2_kernel, 70B shape at batch 16 (one quarter of the workload's
     # sequences; traffic grows with the sequences): (286,022,272 read +
     # 6,765,184 written, mean of two launches) x 4, from one ncu capture
-    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "8aaeb11a88d32a4c", 1171149824),
+    # (taken on this code; the source has changed since only in comments)
+    ("llama70b_serving", "tree_attn"): ("csrc/attn_tc2.cu", "178217b7f9f1ce91", 1171149824),
 }
 
 

@@ -1,7 +1,7 @@
-// Tree attention for GQA groups with more than 128 query rows per KV head
-// (bf16 in, float32 softmax and accumulation, head_dim 128), on pairs of
-// SMs: tcgen05.mma.cta_group::2 with M = 256, a persistent grid, and a
-// stream-K split of the work.
+// Tree attention for GQA groups with more than 128 query rows per KV head,
+// or trees of more than 64 nodes (up to 256), bf16 in, float32 softmax and
+// accumulation, head_dim 128, on pairs of SMs: tcgen05.mma.cta_group::2 with
+// M = 256, a persistent grid, and a stream-K split of the work.
 //
 // "5.3 Medusa、EAGLE 与 MTP" (infra-guide), sections 3.1 and 8: every node
 // attends to the shared prefix and to its ancestors-or-self; "Medusa,
@@ -21,9 +21,8 @@
 // included, so ranges with more row-group starts hold fewer tiles.  No range
 // starts between two tree tiles, so the first tile of every part of a row
 // group (its first tree tile, holding the root, or a prefix tile) shows
-// every row at least one key.  A row
-// group that lies wholly inside one cluster's range is normalised and
-// written out; the parts of a row group cut by range ends leave partials
+// every row at least one key.  A row group that lies wholly inside one
+// cluster's range is normalised and written out; the parts of a row group cut by range ends leave partials
 // (unnormalised O in bf16, running max in log2 units and row sum in
 // float32) in workspace slots (2c + 1 for the part cut at cluster c's range
 // end, 2c for the one cut at its start), merged by attn_tc2_combine_kernel.
@@ -51,7 +50,7 @@
 //            reads all 128 keys of a tile with the 16-lane load shape, so a
 //            row lives in 4 threads of one warp and its exact tile max is two
 //            shuffles away; the running max moves only when a tile exceeds
-//            it by 2^8 (then the sum and O are rescaled).  P = 2^(s - m) is
+//            it by 2^16 (then the sum and O are rescaled).  P = 2^(s - m) is
 //            written as bf16 pairs over the tile's first 64 S columns.
 //            V: before PV(g) the even CTA's PV issuer waits for its own V
 //            half to land and zeroes the V rows past the last key of a
