@@ -95,6 +95,25 @@ def test_growing_scores_force_rescaling():
         assert ok, f"max excess over tolerance {excess}"
 
 
+def test_jumping_scores_force_the_exact_redo_and_rescale_on_sm_pairs():
+    """Prefix keys scaled by 1.5 per 128-key tile on the SM-pair kernel (64
+    nodes x 4 heads = 256 rows per KV head): from about the sixth tile on,
+    each tile's scores exceed the running max by more than 2^16, so the
+    one-pass tile fails its row-sum test, is redone with the exact max and O
+    is rescaled, tile after tile."""
+    shape = synth.random_tree(5, 64, (4, 4, 4))
+    w, prefix, q, kc, vc, kt, vt = _small("bf16", 2, 16, 4, 128, [1200, 900], shape, q_scale=1.0, seed=23)
+    f = (1.5 ** (np.arange(kc.shape[2]) // 128)).astype(np.float32)
+    kc = synth.round_bf16(kc * f[None, None, :, None])
+    for splits in (1, 0):
+        got, status, _ = _run(w, shape, prefix, q, kc, vc, kt, vt, num_splits=splits)
+        assert status == 0
+        ref = A.tree_attention(q, kc, vc, kt, vt, prefix, T.depth_and_mask(shape.parents)[1])
+        ok, excess = within(got, ref, *TOL["bf16"])
+        assert ok, f"max excess over tolerance {excess}"
+        assert np.abs(ref).max() > 0.1
+
+
 def test_non_finite_stale_cache_rows_are_ignored():
     """Cache rows past the prefix hold NaN/Inf (never-written memory): the
     output must not see them."""
