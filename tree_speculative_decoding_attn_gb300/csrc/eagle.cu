@@ -55,6 +55,12 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
   return t;
 }
 
+// The row kernels that feed a GEMM let it launch at once (programmatic
+// dependent launch): the GEMM streams its first weights while the row
+// kernel runs and reads the row kernel's output only after
+// griddepcontrol.wait, which returns once this grid has completed.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // x[r] = [feat[b, parent(v)] ; emb[tok(v)]] for frontier node v = frontier[b, f];
 // the root's parent feature is slot pool_cap.
 __global__ void __launch_bounds__(kThreads)
@@ -62,6 +68,7 @@ __global__ void __launch_bounds__(kThreads)
                   const int32_t *__restrict__ pool_parent, const int32_t *__restrict__ pool_tok,
                   const int32_t *__restrict__ frontier, int F, int pool_cap, int d, int V,
                   __nv_bfloat16 *__restrict__ x, int32_t *status) {
+  pdl_trigger();
   const int r = blockIdx.x, b = r / F;
   const int v = frontier[r];
   const bool ok = v >= 0 && v < pool_cap;
@@ -88,6 +95,7 @@ __global__ void __launch_bounds__(kThreads)
                    const __nv_bfloat16 *__restrict__ w, int d, __nv_bfloat16 *__restrict__ y,
                    __nv_bfloat16 *__restrict__ feat_out, const int32_t *__restrict__ frontier, int F, int pool_cap) {
   __shared__ float red[kThreads / 32];
+  pdl_trigger();
   const int r = blockIdx.x;
   const float4 *xr = reinterpret_cast<const float4 *>(x + (int64_t)r * d);
   const float4 *ar = add ? reinterpret_cast<const float4 *>(add + (int64_t)r * d) : nullptr;
@@ -305,6 +313,7 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     gather_out_kernel(const __nv_bfloat16 *__restrict__ out, const int32_t *__restrict__ cidx, int F, int C, int hqd,
                       __nv_bfloat16 *__restrict__ a) {
+  pdl_trigger();
   const int r = blockIdx.x, b = r / F;
   const int ci = cidx[r];
   const uint4 *src = reinterpret_cast<const uint4 *>(out + ((int64_t)b * C + ci) * hqd);
@@ -316,6 +325,7 @@ __global__ void __launch_bounds__(kThreads)
 // (chunks of 4 * kThreads, R), f a multiple of 4.
 __global__ void __launch_bounds__(kThreads)
     swiglu_kernel(const float *__restrict__ gu, int f, __nv_bfloat16 *__restrict__ act) {
+  pdl_trigger();
   const int r = blockIdx.y, i = (int)(blockIdx.x * kThreads + threadIdx.x);
   if (4 * i >= f) return;
   const float4 g = reinterpret_cast<const float4 *>(gu + (int64_t)r * 2 * f)[i];
@@ -407,11 +417,12 @@ int sv_eagle_round(const SvEagleWeights &w, int batch, int hidden, int hq, int h
   auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16 *>(base + off); };
   auto f32 = [&](size_t off) { return reinterpret_cast<float *>(base + off); };
   auto i32 = [&](size_t off) { return reinterpret_cast<int32_t *>(base + off); };
-  // a GEMM whose output is float32 rows [R, G, M], the workspace share reused
+  // a GEMM whose output is float32 rows [R, G, M], the workspace share reused;
+  // launched as a programmatic dependent of the row kernel that feeds it
   auto gemm = [&](const void *W, const void *X, int M, int K, int G, float *out) {
     const SvGemmPlan p = sv_wgemm_plan(M, K, G, R);
     return sv_wgemm(p, W, X, 0, M, K, G, R, 0, out, nullptr, nullptr, nullptr, reinterpret_cast<float *>(at(l.gemm)),
-                    false, status, stream);
+                    true, status, stream);
   };
   int rc;
   inputs_kernel<<<R, kThreads, 0, stream>>>(reinterpret_cast<const __nv_bfloat16 *>(feat),
